@@ -1,0 +1,337 @@
+"""Pins for the CPU oracle: it is checked against what the pages and the
+mathematics fix, never against itself.
+
+* worked examples printed on the pages (tests/golden/*.json, each cited);
+* closed forms (softmax of two tokens, temperature scaling);
+* special cases that reduce to a library routine (greedy == numpy.argmax,
+  top_k=1 / top_p=1e-6 / tiny temperature == argmax);
+* invariants (sum q == 1, q proportional to exp(l/T) on the kept set, the
+  draw's measure equals q);
+* an independent O(V^2) brute force for V <= 16 (tests/brute_force.py).
+
+Each case is chosen so that a plausible slip in the oracle (top-p on the
+inclusive instead of the exclusive cumulative sum, no renormalisation after
+top-k, the draw in sorted instead of vocab order, multiplying by T instead of
+dividing, a wrong tie rule) fails at least one test.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import brute_force
+import oracle
+from paged_kv_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _row(values, dtype=torch.float32):
+    return torch.tensor([values], dtype=dtype)
+
+
+def _sample1(values, T, k=-1, p=1.0, u=0.5, dtype=torch.float32, probs=True):
+    res = oracle.sample(_row(values, dtype), torch.tensor([T]), torch.tensor([k], dtype=torch.int32),
+                        torch.tensor([p]), torch.tensor([u]), want_probs=probs)
+    return res
+
+
+# ---------------------------------------------------------------- golden: sampler
+
+
+def test_page_sampler_example_topk2():
+    g = _golden("sampler_filters.json")
+    row = g["rows"][0]
+    q0 = 1.0 / (1.0 + math.exp(-1.0))  # e^5 / (e^5 + e^4)
+    assert abs(q0 - row["q0_printed"]) < row["q0_printed_tol"]
+    res = _sample1(g["logits"], row["temperature"], row["top_k"], row["top_p"], 0.5)
+    q = res["probs"][0]
+    assert abs(q[0] - q0) < 1e-12
+    assert abs(q[1] - (1 - q0)) < 1e-12
+    assert set(np.nonzero(q)[0].tolist()) == set(row["support"])
+    # Inverse CDF in vocab order: u < q0 draws token 0, otherwise token 1.
+    for u, want in [(0.0, 0), (q0 - 1e-6, 0), (q0 + 1e-6, 1), (0.999999, 1)]:
+        assert _sample1(g["logits"], 1.0, 2, 1.0, u, probs=False)["tokens"][0] == want
+
+
+def test_page_sampler_example_topp05_and_greedy():
+    g = _golden("sampler_filters.json")
+    logits = torch.tensor([g["logits"]] * 3, dtype=torch.float32)
+    t = torch.tensor([r["temperature"] for r in g["rows"]])
+    k = torch.tensor([r["top_k"] for r in g["rows"]], dtype=torch.int32)
+    p = torch.tensor([r["top_p"] for r in g["rows"]])
+    for u in np.linspace(0.0, 0.999, 41):
+        res = oracle.sample(logits, t, k, p, torch.full((3,), float(u)), want_probs=True)
+        assert res["tokens"][0] in g["rows"][0]["support"]
+        assert res["tokens"][1] == 0 and res["kept"][1] == 1
+        assert res["tokens"][2] == 0
+    # The page says the top probability is "about 0.67"; exactly it is
+    # e^5 / (e^5 + e^4 + e^3 + 3), which is > 0.5, so top-p keeps only token 0.
+    q_top = math.exp(5) / (math.exp(5) + math.exp(4) + math.exp(3) + 3)
+    assert 0.6 < q_top < 0.7
+
+
+def test_all_greedy_batch_matches_numpy_argmax():
+    logits = workloads.random_rows(16, 1000, torch.float32, seed=1, discrete=True)
+    res = oracle.sample(logits)
+    np.testing.assert_array_equal(res["tokens"], np.argmax(logits.numpy(), axis=1))
+    bf = workloads.random_rows(16, 777, torch.bfloat16, seed=2)
+    res = oracle.sample(bf)
+    np.testing.assert_array_equal(res["tokens"], np.argmax(bf.float().numpy(), axis=1))
+
+
+def test_greedy_signed_zero_ties_and_nan():
+    # -0 and +0 are equal values: the lowest index wins.
+    res = oracle.sample(torch.tensor([[-1.0, -0.0, 0.0, -2.0]]))
+    assert res["tokens"][0] == 1
+    res = oracle.sample(torch.tensor([[1.0, float("nan"), 2.0]]))
+    assert res["tokens"][0] == -1 and res["row_status"][0] & 1
+
+
+# ---------------------------------------------------------------- closed forms
+
+
+def test_temperature_divides_logits():
+    # Two tokens: q0 = 1 / (1 + exp(-(l0 - l1) / T)).
+    for T in (0.25, 0.5, 2.0):
+        q = _sample1([2.0, 0.0], T)["probs"][0]
+        assert abs(q[0] - 1.0 / (1.0 + math.exp(-2.0 / T))) < 1e-12
+
+
+def test_topp_renormalises_after_topk():
+    # [5,4,3,0,0,0], k=2: renormalised q0 = 0.731 >= 0.7, so top_p=0.7 keeps only
+    # token 0.  Without renormalisation q0 would be 0.656 < 0.7 and token 1 kept.
+    res = _sample1([5.0, 4.0, 3.0, 0.0, 0.0, 0.0], 1.0, 2, 0.7)
+    assert res["kept"][0] == 1 and res["probs"][0][0] == 1.0
+
+
+def test_topp_uses_mass_before_token():
+    # Exclusive cumulative sum: the top token is always kept even when its own
+    # probability exceeds p.
+    res = _sample1([10.0, 0.0, 0.0], 1.0, -1, 0.01)
+    assert res["kept"][0] == 1
+    # p just above the top token's probability keeps exactly two tokens.
+    q0 = math.exp(10) / (math.exp(10) + 2)
+    res = _sample1([10.0, 0.0, 0.0], 1.0, -1, q0 + 1e-6)
+    assert res["kept"][0] == 2
+    res = _sample1([10.0, 0.0, 0.0], 1.0, -1, q0 - 1e-6)
+    assert res["kept"][0] == 1
+
+
+def test_draw_walks_vocab_order():
+    # The maximum sits at index 1; a small u must land on token 0, whose
+    # interval comes first in vocab order.
+    q0 = 1.0 / (1.0 + math.exp(5) + math.exp(4))
+    assert _sample1([0.0, 5.0, 4.0], 1.0, -1, 1.0, q0 * 0.5)["tokens"][0] == 0
+    assert _sample1([0.0, 5.0, 4.0], 1.0, -1, 1.0, q0 * 1.5)["tokens"][0] == 1
+    assert _sample1([0.0, 5.0, 4.0], 1.0, -1, 1.0, 0.99)["tokens"][0] == 2
+
+
+def test_topk_ties_take_lowest_index():
+    # Values 3 at indices 4, 1, 6 (ties); k=2 keeps the two lowest indices.
+    res = _sample1([0.0, 3.0, 0.0, 0.0, 3.0, 1.0, 3.0], 1.0, 2, 1.0)
+    assert set(np.nonzero(res["probs"][0])[0].tolist()) == {1, 4}
+
+
+# ---------------------------------------------------------------- reductions to argmax
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_degenerate_settings_reduce_to_argmax(seed):
+    logits = workloads.random_rows(8, 300, torch.float32, seed=seed)
+    want = np.argmax(logits.numpy(), axis=1)
+    B = logits.shape[0]
+    us = torch.linspace(0.0, 0.999, B)
+    ones = torch.ones(B)
+    res = oracle.sample(logits, ones, torch.ones(B, dtype=torch.int32), None, us)
+    np.testing.assert_array_equal(res["tokens"], want)  # top_k = 1
+    res = oracle.sample(logits, ones, None, torch.full((B,), 1e-6), us)
+    np.testing.assert_array_equal(res["tokens"], want)  # top_p = 1e-6
+    res = oracle.sample(logits, torch.full((B,), 1e-7), None, None, us)
+    np.testing.assert_array_equal(res["tokens"], want)  # T clamps to 1e-6
+
+
+# ---------------------------------------------------------------- invariants
+
+
+def test_probabilities_sum_to_one_and_follow_softmax():
+    logits = workloads.random_rows(12, 2000, torch.bfloat16, seed=5)
+    t, k, p, u = workloads.random_params(12, seed=6, greedy_frac=0.0)
+    res = oracle.sample(logits, t, k, p, u, want_probs=True)
+    lf = logits.double().numpy()
+    for b in range(12):
+        q = res["probs"][b]
+        assert abs(q.sum() - 1.0) < 1e-12
+        s = np.nonzero(q)[0]
+        assert len(s) == res["kept"][b]
+        # Ratio test: q_i / q_j == exp((l_i - l_j) / T) on the kept set.
+        i0 = s[np.argmax(lf[b, s])]
+        ratio = q[s] / q[i0]
+        want = np.exp((lf[b, s] - lf[b, i0]) / float(t[b]))
+        np.testing.assert_allclose(ratio, want, rtol=1e-12)
+        # The kept set is a prefix of the (logit desc, index asc) order.
+        order = sorted(range(lf.shape[1]), key=lambda i: (-lf[b, i], i))
+        assert set(order[:len(s)]) == set(s.tolist())
+
+
+def test_draw_measure_equals_probability():
+    rng = np.random.default_rng(7)
+    for trial in range(20):
+        V = int(rng.integers(2, 12))
+        l = rng.integers(-3, 4, V).astype(np.float32).tolist()
+        T, k, p = 0.7, int(rng.integers(0, V + 2)), float(rng.choice([1.0, 0.6, 0.9]))
+        q = _sample1(l, T, k, p)["probs"][0]
+        cuts = np.cumsum([q[i] for i in range(V)])
+        points = sorted({0.0} | {min(max(c + d, 0.0), 1 - 1e-12)
+                                  for c in cuts for d in (-1e-9, 1e-9)})
+        measure = np.zeros(V)
+        for a, bnd in zip(points[:-1], points[1:]):
+            tok = _sample1(l, T, k, p, (a + bnd) / 2, probs=False)["tokens"][0]
+            measure[tok] += bnd - a
+        measure[_sample1(l, T, k, p, points[-1], probs=False)["tokens"][0]] += 1 - points[-1]
+        np.testing.assert_allclose(measure, q, atol=1e-8)
+
+
+# ---------------------------------------------------------------- brute force
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_brute_force_tiny_vocab(seed):
+    rng = np.random.default_rng(100 + seed)
+    for _ in range(40):
+        V = int(rng.integers(1, 17))
+        if rng.random() < 0.5:
+            l = rng.integers(-3, 4, V).astype(np.float64)
+        else:
+            l = rng.normal(0, 2, V)
+        l = np.asarray(l, np.float32).astype(np.float64).tolist()
+        T = float(np.float32(rng.choice([0.3, 0.7, 1.0, 1.8])))
+        k = int(rng.choice([-1, 1, 2, 3, V - 1, V, V + 3]))
+        p = float(np.float32(rng.choice([1.0, 0.95, 0.6, 0.3, 1e-6])))
+        u = float(np.float32(rng.random()))
+        res = _sample1(l, T, k, p, u)
+        q_bf = brute_force.kept_probabilities(l, T, k, p)
+        q = res["probs"][0]
+        assert set(np.nonzero(q)[0].tolist()) == set(i for i in q_bf if q_bf[i] > 0)
+        for i, qi in q_bf.items():
+            assert abs(q[i] - qi) < 1e-12
+        if res["cdf_margin"][0] > 1e-9 and res["topp_margin"][0] > 1e-9:
+            assert res["tokens"][0] == brute_force.sample_row(l, T, k, p, u)
+
+
+def test_row_status_bits():
+    res = oracle.sample(torch.tensor([[float("-inf")] * 4, [1.0, float("inf"), 0.0, 0.0],
+                                      [0.0, 1.0, 2.0, 3.0]]),
+                        torch.tensor([1.0, 1.0, 1.0]), None, None,
+                        torch.tensor([0.5, 0.5, 1.5]))
+    assert res["tokens"][0] == -1 and res["row_status"][0] == 2
+    assert res["tokens"][1] == -1 and res["row_status"][1] == 1
+    assert res["row_status"][2] == 16 and res["tokens"][2] == 3  # u clamped below 1
+
+
+# ---------------------------------------------------------------- write-back
+
+
+def test_writeback_golden():
+    g = _golden("writeback_tuple.json")
+    pool = np.zeros(g["pool_shape"], np.int32)
+    st = oracle.writeback(g["tokens"], g["rows"], g["cols"], pool)
+    assert st == 0
+    np.testing.assert_array_equal(pool, np.array(g["expected_pool"], np.int32))
+    pool2 = np.zeros(g["pool_shape"], np.int32)
+    st = oracle.writeback([1, 2], [3, 0], [0, 5], pool2)
+    assert st == (4 | 8) and not pool2.any()
+
+
+# ---------------------------------------------------------------- pages
+
+
+def test_pages_selftest_example():
+    g = _golden("pages_selftest.json")
+    res = oracle.alloc_pages([g["cached_len"]], [g["device_len"]], g["page_size"], 100)
+    assert res["first_page"][0] == g["expected_first_page"]
+    assert res["num_pages"][0] == g["expected_num_pages"] and res["total"] == 1
+    pt = np.full((1, 16), -1, np.int32)
+    free = np.arange(10, dtype=np.int32) * 4 + 40
+    out = oracle.fill_page_table([6], [9], [0], 4, free, pt)
+    assert out["rc"] == 0 and out["total"] == 1
+    assert (np.nonzero(pt[0] >= 0)[0].tolist()) == g["expected_positions"]
+    assert pt[0, 8:12].tolist() == [40, 41, 42, 43]
+
+
+def test_pages_allocate_sequence():
+    g = _golden("pages_allocate_sequence.json")
+    ps, n = g["page_size"], g["num_pages"]
+    free = np.arange(n, dtype=np.int32) * ps
+    pt = np.zeros((4, 32), np.int32)
+    for step in g["steps"]:
+        out = oracle.fill_page_table([step["cached_len"]], [step["device_len"]],
+                                     [g["table_idx"]], ps, free, pt)
+        assert out["rc"] == 0
+        free = free[out["total"]:]
+        assert len(free) == step["free_after"]
+        if "row_prefix" in step:
+            assert pt[g["table_idx"], :8].tolist() == step["row_prefix"]
+        if "aligned_column" in step:
+            assert pt[g["table_idx"], step["aligned_column"]] % ps == 0
+            assert pt[g["table_idx"], 8:12].tolist() == [8, 9, 10, 11]
+
+
+def test_pages_trace_page_size_one():
+    g = _golden("pages_trace_ps1.json")
+    free = np.arange(g["num_pages"], dtype=np.int32)
+    lens = np.array(g["prompt_lens"], np.int32)
+    pt = np.zeros((5, 64), np.int32)
+    out = oracle.fill_page_table(np.zeros(4, np.int32), lens, np.arange(4), 1, free, pt)
+    free = free[out["total"]:]
+    assert len(free) == g["free_after_prefill"]
+    for want in g["free_after_each_decode"]:
+        out = oracle.fill_page_table(lens, lens + 1, np.arange(4), 1, free, pt)
+        free = free[out["total"]:]
+        lens = lens + 1
+        assert len(free) == want
+
+
+def test_pages_hand_example_and_invariants():
+    # ps=4, cached {0,6,3,10}, device {5,9,4,13}: pages [0,2), [2,3), none, [3,4).
+    w = workloads.pr1()
+    res = oracle.alloc_pages(w.cached_len, w.device_len, 4, 64)
+    assert res["num_pages"].tolist() == [2, 1, 0, 1] and res["total"] == 4
+    assert res["offset"].tolist() == [0, 2, 3, 3]
+    pt = np.full(w.pt_shape, -1, np.int32)
+    out = oracle.fill_page_table(w.cached_len, w.device_len, w.table_idx, 4,
+                                 w.free_slots, pt)
+    assert out["rc"] == 0
+    assert pt[0, :8].tolist() == list(range(8))
+    assert pt[1, 8:12].tolist() == [8, 9, 10, 11]
+    assert pt[3, 12:16].tolist() == [12, 13, 14, 15]
+    assert (pt[2] == -1).all()
+    assert (pt >= 0).sum() == 16
+
+
+def test_pages_disjoint_aligned_and_enospc():
+    w = workloads.mixed(B=32, V=64)
+    free = w.free_slots.numpy()
+    pt = np.full(w.pt_shape, -1, np.int32)
+    out = oracle.fill_page_table(w.cached_len, w.device_len, w.table_idx, w.page_size,
+                                 free, pt)
+    N = out["total"]
+    taken = pt[pt >= 0]
+    assert len(taken) == N * w.page_size
+    assert len(np.unique(taken)) == len(taken)  # no location handed out twice
+    starts = taken[taken % w.page_size == 0]
+    assert set(starts.tolist()) == set(free[:N].tolist())  # exactly the front of the list
+    # Not enough pages: nothing is written.
+    pt2 = np.full(w.pt_shape, -1, np.int32)
+    out = oracle.fill_page_table(w.cached_len, w.device_len, w.table_idx, w.page_size,
+                                 free[: N - 1], pt2)
+    assert out["rc"] == -2 and (pt2 == -1).all()
