@@ -1,0 +1,187 @@
+/*
+ * pkv.h -- C ABI of the decode-step tail: batched per-request sampling with
+ * fused token write-back, and paged-KV page allocation / page-table fill.
+ *
+ * The operations follow "mini-sglang from Scratch":
+ *   - sampling: page "The engine and the sampler", section "The sampler"
+ *     (Sampler.prepare, Sampler.sample, sample_torch);
+ *   - token write-back: page "The scheduler skeleton and the offline
+ *     interface", section "Preparing a batch" (_make_write_tuple,
+ *     Scheduler._forward);
+ *   - page allocation and page-table fill: page "CacheManager: allocation,
+ *     release and admission control", sections "The free-page list",
+ *     "Allocating pages for this step's tokens" (_allocate, allocate_paged,
+ *     _write_page_table).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller unless the comment says
+ *     "host".  The library never allocates, frees or copies caller memory and
+ *     never synchronises: every call is enqueued on `stream` and returns.
+ *   - Host-detectable errors return a negative pkv_status and launch nothing.
+ *     pkv_last_error() then describes the problem (per calling thread).
+ *   - Device-detectable problems set bits in the caller's int32 status word
+ *     (zeroed by the caller; bits are OR-ed in, never cleared), write -1 for
+ *     the affected token and skip the affected write.  No kernel traps.
+ *   - Integers are int32 except lengths of device buffers and pool / table
+ *     coordinates, which are int64.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_EINVAL = -1,       /* bad argument: NULL pointer, size, stride, dtype */
+  PKV_ENOSPC = -2,       /* not enough free pages (pkv_alloc_pages)          */
+  PKV_ECUDA = -3,        /* a CUDA call failed (launch or attribute)         */
+  PKV_EUNSUPPORTED = -4  /* valid but outside what the kernels handle        */
+} pkv_status;
+
+typedef enum { PKV_FP32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits of the device status word. */
+#define PKV_ST_NONFINITE 1     /* NaN in a row, or +inf in a sampled row       */
+#define PKV_ST_ALL_NEG_INF 2   /* sampled row whose logits are all -inf        */
+#define PKV_ST_ROW_OOB 4       /* write-back / page-table row out of range     */
+#define PKV_ST_COL_OOB 8       /* write-back / page-table column out of range  */
+#define PKV_ST_BAD_UNIFORM 16  /* uniform outside [0,1): clamped, still drawn  */
+#define PKV_ST_NOSPC 32        /* page fill: more pages needed than are free   */
+
+/* Largest vocabulary the sampler handles for each dtype. */
+#define PKV_MAX_VOCAB_BF16 524288
+#define PKV_MAX_VOCAB_FP32 262144
+/* Largest batch of pkv_fill_page_table (its per-request scan lives in shared memory). */
+#define PKV_MAX_FILL_BATCH 4096
+
+/* Text of the last host-side error on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* Library version, 100 * major + minor. */
+int pkv_version(void);
+
+/*
+ * Scratch bytes pkv_sample_batch needs for (B, V, dtype).  The kernels keep
+ * all intermediate state on chip, so this is 0; the argument pair stays in the
+ * ABI so that callers already pass a workspace.
+ */
+size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt);
+
+/*
+ * pkv_sample_batch -- one token per row of a [B, V] logits matrix.
+ *
+ * Follows Sampler.sample / sample_torch ("The engine and the sampler",
+ * section "The sampler") with torch.multinomial replaced by an inverse CDF
+ * against a caller-supplied uniform:
+ *   - temperature == NULL: the whole batch is greedy (torch.argmax);
+ *   - a row with temperature <= 0 is greedy and returns the exact argmax;
+ *   - otherwise T = max(temperature, 1e-6); top_k < 1 or >= V means no top-k;
+ *     top_p is clamped into [1e-6, 1] (NULL top_k / top_p: off for all rows);
+ *     the row is filtered top-k first, then top-p on the renormalised top-k
+ *     distribution (a token is kept while the mass before it is < top_p), and
+ *     the kept set is renormalised and walked in ascending vocab index: the
+ *     token is the first i with uniform < cumulative probability.
+ * Ties anywhere (argmax, the k-th and the top-p boundary) go to the lowest
+ * index.  Arithmetic is fp32 (bf16 logits are widened exactly).
+ *
+ *   logits      [B, row_stride] fp32 or bf16, row-major; only the first V
+ *               entries of each row are read.  16-byte-aligned rows (base and
+ *               row_stride * element size) take the vectorised path.
+ *   temperature [B] fp32 or NULL      top_k [B] int32 or NULL
+ *   top_p       [B] fp32 or NULL      uniform [B] fp32, required unless
+ *                                     temperature is NULL
+ *   out_tokens  [B] int32, written (-1 for a row with a device error)
+ *   token_pool  [pool_rows, pool_cols] int32 or NULL.  When given, the fused
+ *               write-back does token_pool[wb_rows[b], wb_cols[b]] = token for
+ *               every row with wb_cols[b] >= 0 and token >= 0 (the write
+ *               tuple's column -1 means "do not write").
+ *   wb_rows     [B] int32, wb_cols [B] int64 (required with token_pool)
+ *   probs_out   [B, V] fp32 or NULL: debug output of the kept-set
+ *               probabilities (one-hot for greedy rows); leave NULL when timing.
+ *   status      device int32 status word or NULL.
+ *   workspace   may be NULL (see pkv_sample_workspace_bytes).
+ * Errors: PKV_EINVAL (NULL required pointer, B < 1, B > 65535, V < 1,
+ * row_stride < V, bad dtype, pool sizes < 1), PKV_EUNSUPPORTED (V above
+ * PKV_MAX_VOCAB_*), PKV_ECUDA (launch failure).
+ */
+int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                     const float* temperature, const int32_t* top_k, const float* top_p,
+                     const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                     int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                     const int64_t* wb_cols, float* probs_out, int32_t* status,
+                     void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * pkv_writeback_tokens -- token_pool[rows[b], cols[b]] = tokens[b].
+ *
+ * The standalone form of the write-back in Scheduler._forward ("The scheduler
+ * skeleton and the offline interface", section "Preparing a batch").  Rows
+ * with cols[b] < 0 or tokens[b] < 0 are skipped; out-of-range rows / columns
+ * set PKV_ST_ROW_OOB / PKV_ST_COL_OOB and are skipped.
+ *   tokens [B] int32, rows [B] int32, cols [B] int64,
+ *   token_pool [pool_rows, pool_cols] int32, status device int32 or NULL.
+ * Errors: PKV_EINVAL (NULL pointer, B < 0, pool sizes < 1), PKV_ECUDA.
+ * B == 0 is a no-op.
+ */
+int pkv_writeback_tokens(const int32_t* tokens, const int32_t* rows, const int64_t* cols,
+                         int B, int32_t* token_pool, int64_t pool_rows, int64_t pool_cols,
+                         int32_t* status, pkv_stream_t stream);
+
+/*
+ * pkv_alloc_pages -- HOST computation of this step's page allocation
+ * (CacheManager.allocate_paged, "CacheManager: allocation, release and
+ * admission control", section "Allocating pages for this step's tokens").
+ *
+ * For request i: first_page[i] = ceil(cached_len[i] / page_size),
+ * num_pages[i] = max(0, ceil(device_len[i] / page_size) - first_page[i]),
+ * offset[i] = sum of num_pages[j] for j < i (pages are taken from the front of
+ * the free list in batch order), *total = sum of num_pages.
+ * All pointers are HOST pointers.  Returns PKV_ENOSPC when *total >
+ * free_count (outputs are still filled), PKV_EINVAL for NULL pointers, B < 0,
+ * page_size < 1 or a negative length.  The caller advances its free list by
+ * *total.
+ */
+int pkv_alloc_pages(const int32_t* cached_len, const int32_t* device_len, int B,
+                    int page_size, int64_t free_count, int32_t* first_page,
+                    int32_t* num_pages, int64_t* offset, int64_t* total);
+
+/*
+ * pkv_fill_page_table -- device page allocation plus page-table fill
+ * (_write_page_table with the page-to-token expansion, same section).
+ *
+ * On device: the per-request page counts of pkv_alloc_pages, their exclusive
+ * scan, and for j < num_pages[i], o < page_size:
+ *   page_table[table_idx[i], (first_page[i] + j) * page_size + o]
+ *       = free_slots[offset[i] + j] + o
+ * i.e. whole pages, even past device_len.  free_slots holds the first token
+ * location of each free page; pages are taken from its front.  Nothing else
+ * in page_table changes.  If the total exceeds free_count, PKV_ST_NOSPC is set,
+ * *total_out is 0 and nothing is written.  A request whose table row or last
+ * column is out of range sets PKV_ST_ROW_OOB / PKV_ST_COL_OOB and is skipped
+ * (its pages are still counted as taken).
+ *   cached_len, device_len, table_idx [B] int32; free_slots [free_count] int32;
+ *   page_table [pt_rows, pt_cols] int32; total_out device int64 or NULL
+ *   (receives the number of pages taken); status device int32 or NULL.
+ * Errors: PKV_EINVAL (NULL pointer, B < 0, B > PKV_MAX_FILL_BATCH,
+ * page_size < 1, free_count outside [0, 2^31), empty table), PKV_ECUDA.
+ * B == 0 writes *total_out = 0.
+ */
+int pkv_fill_page_table(const int32_t* cached_len, const int32_t* device_len,
+                        const int32_t* table_idx, int B, int page_size,
+                        const int32_t* free_slots, int64_t free_count, int32_t* page_table,
+                        int64_t pt_rows, int64_t pt_cols, int64_t* total_out,
+                        int32_t* status, pkv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

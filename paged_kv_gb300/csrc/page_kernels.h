@@ -1,0 +1,34 @@
+// Host-side declarations of the page-fill and write-back launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+constexpr int kMaxFillBatch = 4096;
+
+struct FillParams {
+  const int32_t* cached_len;   // [B]
+  const int32_t* device_len;   // [B]
+  const int32_t* table_idx;    // [B]
+  int B;
+  int page_size;
+  const int32_t* free_slots;   // [free_count] page-start token locations
+  int64_t free_count;
+  int32_t* page_table;         // [pt_rows, pt_cols]
+  int64_t pt_rows;
+  int64_t pt_cols;
+  int64_t* total_out;          // device, or nullptr
+  int32_t* status;             // device, or nullptr
+  bool vec4;                   // 16-byte stores are aligned (ps % 4 == 0, pt_cols % 4 == 0)
+};
+
+size_t fill_smem_bytes(int B);
+cudaError_t launch_fill_page_table(const FillParams& F, int num_sms, cudaStream_t stream);
+cudaError_t launch_writeback(const int32_t* tokens, const int32_t* rows, const int64_t* cols,
+                             int B, int32_t* pool, int64_t pool_rows, int64_t pool_cols,
+                             int32_t* status, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,221 @@
+// C ABI of the decode-step tail (declared in include/pkv.h): argument
+// validation, launch-shape choice and the kernel launches.  Host-only logic
+// (pkv_alloc_pages) is plain C++.  Nothing here allocates device memory or
+// synchronises a stream.
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/pkv.h"
+#include "launch_config.h"
+#include "page_kernels.h"
+#include "sample_params.h"
+
+namespace pkv {
+cudaError_t launch_sample_bf16(const SampleParams& P, const SampleConfig& c, bool all_greedy,
+                               cudaStream_t stream);
+cudaError_t launch_sample_fp32(const SampleParams& P, const SampleConfig& c, bool all_greedy,
+                               cudaStream_t stream);
+}  // namespace pkv
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_err[0] = '\0';
+  return PKV_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// SM count of the current device (cached per device).
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t div_ceil(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_last_error(void) { return g_err; }
+
+int pkv_version(void) { return 100; }
+
+size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt) {
+  (void)B;
+  (void)V;
+  (void)dt;
+  return 0;
+}
+
+int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                     const float* temperature, const int32_t* top_k, const float* top_p,
+                     const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                     int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                     const int64_t* wb_cols, float* probs_out, int32_t* status,
+                     void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (logits == nullptr) return fail(PKV_EINVAL, "logits is NULL");
+  if (out_tokens == nullptr) return fail(PKV_EINVAL, "out_tokens is NULL");
+  if (dt != PKV_FP32 && dt != PKV_BF16) return fail(PKV_EINVAL, "dtype %d is not fp32 or bf16", dt);
+  if (B < 1 || B > 65535) return fail(PKV_EINVAL, "B=%d outside [1, 65535]", B);
+  if (V < 1) return fail(PKV_EINVAL, "V=%d < 1", V);
+  if (row_stride < V) return fail(PKV_EINVAL, "row_stride=%lld < V=%d", (long long)row_stride, V);
+  if (temperature != nullptr && uniform == nullptr)
+    return fail(PKV_EINVAL, "uniform is required when temperature is given");
+  if (token_pool != nullptr) {
+    if (wb_rows == nullptr || wb_cols == nullptr)
+      return fail(PKV_EINVAL, "token_pool given without wb_rows / wb_cols");
+    if (pool_rows < 1 || pool_cols < 1)
+      return fail(PKV_EINVAL, "token pool shape [%lld, %lld] is empty", (long long)pool_rows,
+                  (long long)pool_cols);
+  }
+  const bool bf16 = dt == PKV_BF16;
+  const int max_v = bf16 ? PKV_MAX_VOCAB_BF16 : PKV_MAX_VOCAB_FP32;
+  if (V > max_v) return fail(PKV_EUNSUPPORTED, "V=%d above the maximum %d", V, max_v);
+  const size_t elt = bf16 ? 2 : 4;
+  const bool vec = aligned16(logits) && ((static_cast<uint64_t>(row_stride) * elt) % 16 == 0);
+  pkv::SampleConfig cfg;
+  if (!pkv::choose_sample_config(B, V, bf16, vec, num_sms(), &cfg))
+    return fail(PKV_EUNSUPPORTED, "no launch shape covers V=%d", V);
+
+  pkv::SampleParams P;
+  P.logits = logits;
+  P.row_stride = row_stride;
+  P.B = B;
+  P.V = V;
+  P.temperature = temperature;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.uniform = uniform;
+  P.out_tokens = out_tokens;
+  P.token_pool = token_pool;
+  P.pool_rows = pool_rows;
+  P.pool_cols = pool_cols;
+  P.wb_rows = wb_rows;
+  P.wb_cols = wb_cols;
+  P.probs_out = probs_out;
+  P.status = status;
+  P.cta_chunk = cfg.chunk;
+  const bool all_greedy = temperature == nullptr;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = bf16 ? pkv::launch_sample_bf16(P, cfg, all_greedy, s)
+                             : pkv::launch_sample_fp32(P, cfg, all_greedy, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
+  return ok();
+}
+
+int pkv_writeback_tokens(const int32_t* tokens, const int32_t* rows, const int64_t* cols, int B,
+                         int32_t* token_pool, int64_t pool_rows, int64_t pool_cols,
+                         int32_t* status, pkv_stream_t stream) {
+  if (B < 0) return fail(PKV_EINVAL, "B=%d < 0", B);
+  if (B == 0) return ok();
+  if (tokens == nullptr || rows == nullptr || cols == nullptr || token_pool == nullptr)
+    return fail(PKV_EINVAL, "NULL pointer argument");
+  if (pool_rows < 1 || pool_cols < 1) return fail(PKV_EINVAL, "empty token pool");
+  const cudaError_t e = pkv::launch_writeback(tokens, rows, cols, B, token_pool, pool_rows,
+                                              pool_cols, status,
+                                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "write-back launch");
+  return ok();
+}
+
+int pkv_alloc_pages(const int32_t* cached_len, const int32_t* device_len, int B, int page_size,
+                    int64_t free_count, int32_t* first_page, int32_t* num_pages,
+                    int64_t* offset, int64_t* total) {
+  if (B < 0) return fail(PKV_EINVAL, "B=%d < 0", B);
+  if (page_size < 1) return fail(PKV_EINVAL, "page_size=%d < 1", page_size);
+  if (total == nullptr) return fail(PKV_EINVAL, "total is NULL");
+  if (B > 0 && (cached_len == nullptr || device_len == nullptr || first_page == nullptr ||
+                num_pages == nullptr || offset == nullptr))
+    return fail(PKV_EINVAL, "NULL pointer argument");
+  for (int i = 0; i < B; ++i) {
+    if (cached_len[i] < 0 || device_len[i] < 0)
+      return fail(PKV_EINVAL, "request %d: negative length (cached_len=%d device_len=%d)", i,
+                  cached_len[i], device_len[i]);
+  }
+  int64_t acc = 0;
+  for (int i = 0; i < B; ++i) {
+    const int64_t first = div_ceil(cached_len[i], page_size);
+    const int64_t last = div_ceil(device_len[i], page_size);
+    const int64_t n = last > first ? last - first : 0;
+    first_page[i] = static_cast<int32_t>(first);
+    num_pages[i] = static_cast<int32_t>(n);
+    offset[i] = acc;
+    acc += n;
+  }
+  *total = acc;
+  if (acc > free_count)
+    return fail(PKV_ENOSPC, "%lld pages needed, %lld free", (long long)acc, (long long)free_count);
+  return ok();
+}
+
+int pkv_fill_page_table(const int32_t* cached_len, const int32_t* device_len,
+                        const int32_t* table_idx, int B, int page_size,
+                        const int32_t* free_slots, int64_t free_count, int32_t* page_table,
+                        int64_t pt_rows, int64_t pt_cols, int64_t* total_out, int32_t* status,
+                        pkv_stream_t stream) {
+  if (B < 0 || B > PKV_MAX_FILL_BATCH)
+    return fail(PKV_EINVAL, "B=%d outside [0, %d]", B, PKV_MAX_FILL_BATCH);
+  if (page_size < 1) return fail(PKV_EINVAL, "page_size=%d < 1", page_size);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0) {
+    if (total_out != nullptr) {
+      const cudaError_t e = cudaMemsetAsync(total_out, 0, sizeof(int64_t), s);
+      if (e != cudaSuccess) return cuda_fail(e, "total_out reset");
+    }
+    return ok();
+  }
+  if (cached_len == nullptr || device_len == nullptr || table_idx == nullptr ||
+      page_table == nullptr || (free_slots == nullptr && free_count > 0))
+    return fail(PKV_EINVAL, "NULL pointer argument");
+  if (free_count < 0 || free_count > INT32_MAX)
+    return fail(PKV_EINVAL, "free_count=%lld outside [0, 2^31)", (long long)free_count);
+  if (pt_rows < 1 || pt_cols < 1) return fail(PKV_EINVAL, "empty page table");
+  pkv::FillParams F;
+  F.cached_len = cached_len;
+  F.device_len = device_len;
+  F.table_idx = table_idx;
+  F.B = B;
+  F.page_size = page_size;
+  F.free_slots = free_slots;
+  F.free_count = free_count;
+  F.page_table = page_table;
+  F.pt_rows = pt_rows;
+  F.pt_cols = pt_cols;
+  F.total_out = total_out;
+  F.status = status;
+  F.vec4 = (page_size % 4 == 0) && (pt_cols % 4 == 0) && aligned16(page_table);
+  const cudaError_t e = pkv::launch_fill_page_table(F, num_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "page-fill launch");
+  return ok();
+}
+
+}  // extern "C"
