@@ -1,0 +1,199 @@
+"""Thin ctypes binding of ``libpkv.so`` (the C ABI in ``include/pkv.h``).
+
+Argument marshalling only: every step of the sampler, the write-back and the
+page fill runs in the library's CUDA kernels.  PyTorch supplies device memory
+and the current stream.  The functions keep the C names without the ``pkv_``
+prefix and raise ``PkvError`` on a negative status.  There is no CPU fallback:
+if ``libpkv.so`` has not been built (``__graft_entry__.build()``) every call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+
+PKV_OK, PKV_EINVAL, PKV_ENOSPC, PKV_ECUDA, PKV_EUNSUPPORTED = 0, -1, -2, -3, -4
+PKV_FP32, PKV_BF16 = 0, 1
+ST_NONFINITE, ST_ALL_NEG_INF, ST_ROW_OOB, ST_COL_OOB, ST_BAD_UNIFORM, ST_NOSPC = 1, 2, 4, 8, 16, 32
+
+_lock = threading.Lock()
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"pkv error {code}: {message}")
+        self.code = code
+
+
+def load() -> ctypes.CDLL:
+    """Load libpkv.so (raises if it is missing: there is no fallback path)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing; build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+            lib.pkv_last_error.restype = ctypes.c_char_p
+            lib.pkv_last_error.argtypes = []
+            lib.pkv_version.restype = i32
+            lib.pkv_version.argtypes = []
+            lib.pkv_sample_workspace_bytes.restype = sz
+            lib.pkv_sample_workspace_bytes.argtypes = [i32, i32, i32]
+            lib.pkv_sample_batch.restype = i32
+            lib.pkv_sample_batch.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp,
+                                             i64, i64, vp, vp, vp, vp, vp, sz, vp]
+            lib.pkv_writeback_tokens.restype = i32
+            lib.pkv_writeback_tokens.argtypes = [vp, vp, vp, i32, vp, i64, i64, vp, vp]
+            lib.pkv_alloc_pages.restype = i32
+            lib.pkv_alloc_pages.argtypes = [vp, vp, i32, i32, i64, vp, vp, vp, vp]
+            lib.pkv_fill_page_table.restype = i32
+            lib.pkv_fill_page_table.argtypes = [vp, vp, vp, i32, i32, vp, i64, vp, i64, i64,
+                                                vp, vp, vp]
+            _lib = lib
+    return _lib
+
+
+def last_error() -> str:
+    return load().pkv_last_error().decode()
+
+
+def version() -> int:
+    return load().pkv_version()
+
+
+def _check(rc: int) -> None:
+    if rc != PKV_OK:
+        raise PkvError(rc, last_error())
+
+
+def _dev(t: Optional[torch.Tensor], dtype: torch.dtype, name: str, n: Optional[int] = None):
+    """Device pointer of a contiguous CUDA tensor of the given dtype (or None)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if n is not None and t.numel() < n:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {n}")
+    return t.data_ptr()
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def sample_workspace_bytes(B: int, V: int, dtype: torch.dtype) -> int:
+    return int(load().pkv_sample_workspace_bytes(B, V, PKV_BF16 if dtype == torch.bfloat16 else PKV_FP32))
+
+
+def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = None,
+                 top_k: Optional[torch.Tensor] = None, top_p: Optional[torch.Tensor] = None,
+                 uniform: Optional[torch.Tensor] = None,
+                 out_tokens: Optional[torch.Tensor] = None,
+                 token_pool: Optional[torch.Tensor] = None,
+                 wb_rows: Optional[torch.Tensor] = None, wb_cols: Optional[torch.Tensor] = None,
+                 probs_out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """pkv_sample_batch: one int32 token per row of ``logits`` [B, V].
+
+    ``logits`` is fp32 or bf16 with unit column stride (any row stride).
+    Returns ``out_tokens`` (allocated here if not given).  See include/pkv.h.
+    """
+    lib = load()
+    if logits.dim() != 2 or not logits.is_cuda:
+        raise ValueError("logits must be a 2-D CUDA tensor")
+    if logits.stride(1) != 1:
+        raise ValueError("logits must have unit column stride")
+    if logits.dtype == torch.bfloat16:
+        dcode = PKV_BF16
+    elif logits.dtype == torch.float32:
+        dcode = PKV_FP32
+    else:
+        raise TypeError(f"logits dtype {logits.dtype} is not fp32 or bf16")
+    B, V = logits.shape
+    if out_tokens is None:
+        out_tokens = torch.empty(B, dtype=torch.int32, device=logits.device)
+    pool_rows = pool_cols = 0
+    if token_pool is not None:
+        if token_pool.dim() != 2:
+            raise ValueError("token_pool must be 2-D")
+        pool_rows, pool_cols = token_pool.shape
+    rc = lib.pkv_sample_batch(
+        logits.data_ptr(), dcode, B, V, logits.stride(0),
+        _dev(temperature, torch.float32, "temperature", B),
+        _dev(top_k, torch.int32, "top_k", B), _dev(top_p, torch.float32, "top_p", B),
+        _dev(uniform, torch.float32, "uniform", B), _dev(out_tokens, torch.int32, "out_tokens", B),
+        _dev(token_pool, torch.int32, "token_pool"), pool_rows, pool_cols,
+        _dev(wb_rows, torch.int32, "wb_rows", B), _dev(wb_cols, torch.int64, "wb_cols", B),
+        _dev(probs_out, torch.float32, "probs_out", B * V), _dev(status, torch.int32, "status", 1),
+        None, 0, _stream(stream, logits.device))
+    _check(rc)
+    return out_tokens
+
+
+def writeback_tokens(tokens: torch.Tensor, rows: torch.Tensor, cols: torch.Tensor,
+                     token_pool: torch.Tensor, status: Optional[torch.Tensor] = None,
+                     stream=None) -> None:
+    """pkv_writeback_tokens: token_pool[rows[b], cols[b]] = tokens[b] (cols < 0 skipped)."""
+    lib = load()
+    B = tokens.numel()
+    R, C = token_pool.shape
+    rc = lib.pkv_writeback_tokens(
+        _dev(tokens, torch.int32, "tokens"), _dev(rows, torch.int32, "rows", B),
+        _dev(cols, torch.int64, "cols", B), B, _dev(token_pool, torch.int32, "token_pool"),
+        R, C, _dev(status, torch.int32, "status", 1), _stream(stream, token_pool.device))
+    _check(rc)
+
+
+def alloc_pages(cached_len, device_len, page_size: int, free_count: int) -> dict:
+    """pkv_alloc_pages on host int32 arrays; returns first_page, num_pages, offset, total.
+
+    Raises PkvError(PKV_ENOSPC) when the total exceeds free_count.
+    """
+    lib = load()
+    c = torch.as_tensor(cached_len, dtype=torch.int32).contiguous().cpu()
+    d = torch.as_tensor(device_len, dtype=torch.int32).contiguous().cpu()
+    B = c.numel()
+    first = torch.empty(B, dtype=torch.int32)
+    num = torch.empty(B, dtype=torch.int32)
+    off = torch.empty(B, dtype=torch.int64)
+    total = torch.zeros(1, dtype=torch.int64)
+    rc = lib.pkv_alloc_pages(c.data_ptr(), d.data_ptr(), B, int(page_size), int(free_count),
+                             first.data_ptr(), num.data_ptr(), off.data_ptr(), total.data_ptr())
+    out = {"first_page": first, "num_pages": num, "offset": off, "total": int(total[0])}
+    _check(rc)
+    return out
+
+
+def fill_page_table(cached_len: torch.Tensor, device_len: torch.Tensor, table_idx: torch.Tensor,
+                    page_size: int, free_slots: torch.Tensor, page_table: torch.Tensor,
+                    total_out: Optional[torch.Tensor] = None,
+                    status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pkv_fill_page_table: allocate from the front of ``free_slots`` and fill ``page_table``."""
+    lib = load()
+    B = cached_len.numel()
+    R, C = page_table.shape
+    rc = lib.pkv_fill_page_table(
+        _dev(cached_len, torch.int32, "cached_len", B), _dev(device_len, torch.int32, "device_len", B),
+        _dev(table_idx, torch.int32, "table_idx", B), B, int(page_size),
+        _dev(free_slots, torch.int32, "free_slots"), free_slots.numel(),
+        _dev(page_table, torch.int32, "page_table"), R, C,
+        _dev(total_out, torch.int64, "total_out", 1), _dev(status, torch.int32, "status", 1),
+        _stream(stream, page_table.device))
+    _check(rc)

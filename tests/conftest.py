@@ -14,6 +14,12 @@ if HERE not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+    # Build (or reuse) the CUDA library and the oracle before collection.
+    from paged_kv_gb300 import build as _build
+    import oracle as _oracle
+
+    _build.build()
+    _oracle.build()
 
 
 def pytest_collection_modifyitems(config, items):

@@ -1,0 +1,103 @@
+"""CPU tests of the C ABI: the library loads, exports every symbol that
+include/pkv.h declares, rejects bad arguments on the host before any launch,
+and its host-side page allocation matches the oracle."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_gb300 import pkv, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = pkv.load()
+    names = declared_functions()
+    assert "pkv_sample_batch" in names and "pkv_fill_page_table" in names
+    for name in names:
+        assert hasattr(lib, name), f"{name} is declared in pkv.h but not exported"
+
+
+def test_version_and_workspace():
+    assert pkv.version() == 100
+    assert pkv.load().pkv_sample_workspace_bytes(256, 151936, 1) == 0
+
+
+def test_host_validation_launches_nothing():
+    lib = pkv.load()
+    # NULL logits / out_tokens, bad sizes: rejected before any CUDA call.
+    rc = lib.pkv_sample_batch(None, 1, 4, 100, 100, None, None, None, None, 1, None, 0, 0,
+                              None, None, None, None, None, 0, None)
+    assert rc == pkv.PKV_EINVAL and "logits" in pkv.last_error()
+    dummy = ctypes.c_void_p(16)
+    rc = lib.pkv_sample_batch(dummy, 1, 0, 100, 100, None, None, None, None, dummy, None, 0,
+                              0, None, None, None, None, None, 0, None)
+    assert rc == pkv.PKV_EINVAL
+    rc = lib.pkv_sample_batch(dummy, 1, 4, 100, 99, None, None, None, None, dummy, None, 0, 0,
+                              None, None, None, None, None, 0, None)
+    assert rc == pkv.PKV_EINVAL and "row_stride" in pkv.last_error()
+    rc = lib.pkv_sample_batch(dummy, 7, 4, 100, 100, None, None, None, None, dummy, None, 0,
+                              0, None, None, None, None, None, 0, None)
+    assert rc == pkv.PKV_EINVAL
+    rc = lib.pkv_sample_batch(dummy, 1, 4, 100, 100, dummy, None, None, None, dummy, None, 0,
+                              0, None, None, None, None, None, 0, None)
+    assert rc == pkv.PKV_EINVAL and "uniform" in pkv.last_error()
+    rc = lib.pkv_sample_batch(dummy, 1, 4, 100, 100, None, None, None, None, dummy, dummy, 4,
+                              8, None, None, None, None, None, 0, None)
+    assert rc == pkv.PKV_EINVAL and "wb_rows" in pkv.last_error()
+    rc = lib.pkv_sample_batch(dummy, 0, 4, 300000, 300000, None, None, None, None, dummy,
+                              None, 0, 0, None, None, None, None, None, 0, None)
+    assert rc == pkv.PKV_EUNSUPPORTED
+    rc = lib.pkv_fill_page_table(dummy, dummy, dummy, 5000, 4, dummy, 10, dummy, 4, 4, None,
+                                 None, None)
+    assert rc == pkv.PKV_EINVAL
+    rc = lib.pkv_fill_page_table(dummy, dummy, dummy, 4, 0, dummy, 10, dummy, 4, 4, None,
+                                 None, None)
+    assert rc == pkv.PKV_EINVAL and "page_size" in pkv.last_error()
+    rc = lib.pkv_writeback_tokens(None, dummy, dummy, 3, dummy, 2, 2, None, None)
+    assert rc == pkv.PKV_EINVAL
+
+
+@pytest.mark.parametrize("name", ["pr1", "mixed", "nucleus", "large"])
+def test_host_alloc_pages_matches_oracle(name):
+    w = workloads.make(name) if name in ("pr1",) else workloads.make(name, B=64, V=64)
+    host = pkv.alloc_pages(w.cached_len, w.device_len, w.page_size, len(w.free_slots))
+    ref = oracle.alloc_pages(w.cached_len, w.device_len, w.page_size, len(w.free_slots))
+    assert ref["rc"] == 0
+    np.testing.assert_array_equal(host["first_page"].numpy(), ref["first_page"])
+    np.testing.assert_array_equal(host["num_pages"].numpy(), ref["num_pages"])
+    np.testing.assert_array_equal(host["offset"].numpy(), ref["offset"])
+    assert host["total"] == ref["total"]
+
+
+def test_host_alloc_pages_pins_and_errors():
+    res = pkv.alloc_pages([6], [9], 4, 10)  # one page: logical page 2
+    assert res["first_page"].tolist() == [2] and res["num_pages"].tolist() == [1]
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.alloc_pages([0, 0], [9, 9], 4, 5)
+    assert e.value.code == pkv.PKV_ENOSPC
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.alloc_pages([-1], [3], 4, 5)
+    assert e.value.code == pkv.PKV_EINVAL
+    with pytest.raises(pkv.PkvError):
+        pkv.alloc_pages([0], [3], 0, 5)
+    assert pkv.alloc_pages([], [], 4, 0)["total"] == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+
+    with pytest.raises(ValueError):
+        pkv.sample_batch(torch.zeros(2, 8))
