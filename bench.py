@@ -1,0 +1,463 @@
+"""Benchmark of the decode-step tail on GB300.
+
+One step = one pass of the whole hot path over one batch: pkv_sample_batch
+(temperature / top-k / top-p / inverse-CDF sampling with the fused token
+write-back) followed by pkv_fill_page_table (page allocation + page-table
+fill).  Workload: the mixed batch B=256, V=151936, bf16 logits N(0, 3^2),
+every 3rd row greedy, pages of 16 tokens.  Logits rotate over enough
+buffers to exceed twice the L2 size, so every step reads them from HBM.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica of the batch on its own GPU (rows are independent; no collective on
+the data path), the timed region is bracketed by a barrier and a device
+synchronise, and the step time is the maximum over ranks.
+
+--impl reference times the CPU oracle instead (the plain fp64 definition),
+on this host's cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sampled tokens/s and logits GB/s vs GB300 HBM peak at B=256, V=151936 bf16"
+UNIT = "tokens/s"
+WORKLOAD = "mixed"
+KERNEL_SOURCES = ("paged_kv_gb300/csrc/sample_kernel.cuh", "paged_kv_gb300/csrc/device_common.cuh",
+                  "paged_kv_gb300/csrc/launch_config.h", "paged_kv_gb300/csrc/sample_launch.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sampler_mixed_traffic.json")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- distributed harness
+
+
+def dist_env():
+    """(rank, world, local_rank) from the torchrun environment (defaults: 0, 1, 0)."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return dist if world > 1 else None
+
+
+def barrier(dist_mod, device=None):
+    if dist_mod is not None:
+        if device is not None and device.type == "cuda":
+            dist_mod.barrier(device_ids=[device.index])
+        else:
+            dist_mod.barrier()
+
+
+def max_over_ranks(value: float, dist_mod, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity on one rank)."""
+    if dist_mod is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if device is not None and device.type == "cuda" else "cpu")
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, dist_mod, device=None) -> float:
+    if dist_mod is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if device is not None and device.type == "cuda" else "cpu")
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.SUM)
+    return float(t.item())
+
+
+def timed_steps(step, steps: int, warmup: int, dist_mod=None, device=None) -> float:
+    """Runs `warmup` untimed steps, then times exactly `steps` steps; returns
+    milliseconds (max over ranks).  On CUDA the region is timed with events on
+    the current stream, bracketed by a barrier and a synchronise."""
+    import torch
+
+    cuda = device is not None and device.type == "cuda"
+    for i in range(warmup):
+        step(i)
+    if cuda:
+        torch.cuda.synchronize(device)
+    barrier(dist_mod, device)
+    if cuda:
+        torch.cuda.synchronize(device)
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record()
+        for i in range(steps):
+            step(i)
+        end.record()
+        torch.cuda.synchronize(device)
+        ms = start.elapsed_time(end)
+    else:
+        t0 = time.perf_counter()
+        for i in range(steps):
+            step(i)
+        ms = (time.perf_counter() - t0) * 1e3
+    barrier(dist_mod, device)
+    return max_over_ranks(ms, dist_mod, device)
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sms.sort()
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def physical_gpu_index(local_rank: int) -> int:
+    """nvidia-smi index of this rank's GPU (CUDA_VISIBLE_DEVICES maps them)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    items = [v.strip() for v in vis.split(",") if v.strip()]
+    if local_rank < len(items) and items[local_rank].isdigit():
+        return int(items[local_rank])
+    return local_rank
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per sampler launch from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes one sampler launch must move: one read of the logits plus the
+    per-row parameters, tokens and write-back (T, k, p, u, row, col, token,
+    pool write)."""
+    return w.B * w.V * w.elt + w.B * (4 + 4 + 4 + 4 + 4 + 8 + 4 + 4)
+
+
+# ----------------------------------------------------------------- our arm
+
+
+def run_ours(args):
+    import torch
+
+    from paged_kv_gb300 import pkv, workloads
+
+    rank, world, local_rank = dist_env()
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_mod = init_dist("nccl")
+
+    w = workloads.make(WORKLOAD)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    logit_bytes = w.B * w.V * w.elt
+    nbuf = max(4, -(-2 * l2 // logit_bytes) + 1)
+    base = w.logits.to(device)
+    bufs = [base] + [base.clone() for _ in range(nbuf - 1)]
+    d = lambda x: None if x is None else x.to(device)  # noqa: E731
+    t, k, p, u = d(w.temperature), d(w.top_k), d(w.top_p), d(w.uniform)
+    rows, cols = d(w.wb_rows), d(w.wb_cols)
+    pool = torch.zeros(w.pool_shape, dtype=torch.int32, device=device)
+    cached, dev_len, tidx = d(w.cached_len), d(w.device_len), d(w.table_idx)
+    free = d(w.free_slots)
+    pt = torch.zeros(w.pt_shape, dtype=torch.int32, device=device)
+    total = torch.zeros(1, dtype=torch.int64, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    out = torch.empty(w.B, dtype=torch.int32, device=device)
+
+    def step(i):
+        pkv.sample_batch(bufs[i % nbuf], t, k, p, u, out_tokens=out, token_pool=pool,
+                         wb_rows=rows, wb_cols=cols, status=status)
+        pkv.fill_page_table(cached, dev_len, tidx, w.page_size, free, pt, total, status)
+
+    with ClockSampler(physical_gpu_index(local_rank)) as clocks:
+        ms = timed_steps(step, args.steps, args.warmup, dist_mod, device)
+    torch.cuda.synchronize(device)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status word {int(status.item())} after the timed run")
+    ms_per_step = ms / args.steps
+    value = world * w.B / (ms_per_step * 1e-3)
+
+    # Dominant kernel (the sampler) alone, timed with events on the stream it
+    # is launched on (torch's current stream).
+    n_k = max(200, min(args.steps, 5000))
+    ms_k = timed_steps(lambda i: pkv.sample_batch(bufs[i % nbuf], t, k, p, u, out_tokens=out,
+                                                  token_pool=pool, wb_rows=rows, wb_cols=cols,
+                                                  status=status),
+                       n_k, args.warmup, dist_mod, device)
+    us_k = ms_k / n_k * 1e3
+    alg = algorithmic_bytes(w)
+    achieved = alg / (us_k * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+    ms_f = timed_steps(lambda i: pkv.fill_page_table(cached, dev_len, tidx, w.page_size, free,
+                                                     pt, total, status),
+                       n_k, args.warmup, dist_mod, device)
+
+    # End to end through the public API from pinned host buffers: H2D of the
+    # step's inputs, the two calls, D2H of the tokens and the page total.
+    host = {name: getattr(w, name) for name in ("temperature", "top_k", "top_p", "uniform",
+                                                "wb_rows", "wb_cols", "cached_len",
+                                                "device_len", "table_idx")}
+    h_logits = w.logits.pin_memory()
+    h_in = {n: v.pin_memory() for n, v in host.items()}
+    h_tok = torch.empty(w.B, dtype=torch.int32).pin_memory()
+    h_total = torch.empty(1, dtype=torch.int64).pin_memory()
+    d_in = {n: torch.empty_like(v, device=device) for n, v in host.items()}
+    d_logits = torch.empty_like(base)
+    h2d = h_logits.numel() * h_logits.element_size() + sum(
+        v.numel() * v.element_size() for v in h_in.values())
+    d2h = h_tok.numel() * 4 + 8
+
+    def e2e_step(i):
+        d_logits.copy_(h_logits, non_blocking=True)
+        for n in d_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        pkv.sample_batch(d_logits, d_in["temperature"], d_in["top_k"], d_in["top_p"],
+                         d_in["uniform"], out_tokens=out, token_pool=pool,
+                         wb_rows=d_in["wb_rows"], wb_cols=d_in["wb_cols"], status=status)
+        pkv.fill_page_table(d_in["cached_len"], d_in["device_len"], d_in["table_idx"],
+                            w.page_size, free, pt, total, status)
+        h_tok.copy_(out, non_blocking=True)
+        h_total.copy_(total, non_blocking=True)
+
+    ms_e2e = timed_steps(e2e_step, args.e2e_steps, 3, dist_mod, device)
+    e2e_value = world * w.B / (ms_e2e / args.e2e_steps * 1e-3)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = cpu_baseline(w, budget_s=12.0)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "mixed decode batch: B=256, V=151936 bf16 logits N(0,3^2), "
+                                   "1/3 greedy, T~U[0.5,1.5], top_k in {off,20,50}, "
+                                   "top_p in {1,0.9,0.95}; pages of 16",
+                       "B": w.B, "V": w.V, "page_size": w.page_size,
+                       "parallelism": f"replicas x{world}",
+                       "l2": f"logits rotate over {nbuf} buffers ({nbuf * logit_bytes >> 20} MiB > 2x L2)"},
+            "logits_gbs": round(world * logit_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+            "page_fill_us": round(ms_f / n_k * 1e3, 3),
+            "roofline": {"bound": "hbm", "kernel": "sample_kernel", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
+                         "algorithmic_bytes": alg, "us_per_launch": round(us_k, 3)},
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist_mod is not None:
+        dist_mod.destroy_process_group()
+
+
+# ----------------------------------------------------------------- oracle arm
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, budget_s: float = 12.0, rows: int = 64) -> dict:
+    """The oracle as it stands, on this host's cores, on a bounded sample:
+    the first `rows` rows of the batch (sampling) plus the whole page fill,
+    repeated until about `budget_s` seconds have passed."""
+    import numpy as np
+
+    import oracle
+
+    cores = host_cores()
+    sub = slice(0, rows)
+    s = lambda x: None if x is None else x[sub]  # noqa: E731
+    logits = w.logits[sub].contiguous()
+    args = (s(w.temperature), s(w.top_k), s(w.top_p), s(w.uniform))
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.sample(logits, *args, threads=cores)
+        pt = np.zeros(w.pt_shape, np.int32)
+        oracle.fill_page_table(w.cached_len, w.device_len, w.table_idx, w.page_size,
+                               w.free_slots, pt)
+        done += rows
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} rows of the mixed batch ({rows} per pass, with the full page fill) "
+                      f"in {dt:.1f} s, fp64, {cores} threads"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_kv_gb300 import workloads
+
+    w = workloads.make(WORKLOAD)
+    cores = host_cores()
+    import numpy as np
+
+    import oracle
+
+    rows = 16
+    sub = slice(0, rows)
+    s = lambda x: None if x is None else x[sub]  # noqa: E731
+    logits = w.logits[sub].contiguous()
+    params = (s(w.temperature), s(w.top_k), s(w.top_p), s(w.uniform))
+
+    def step(i):
+        oracle.sample(logits, *params, threads=cores)
+        pt = np.zeros(w.pt_shape, np.int32)
+        oracle.fill_page_table(w.cached_len, w.device_len, w.table_idx, w.page_size,
+                               w.free_slots, pt)
+
+    steps = min(args.steps, 20)
+    warm = min(args.warmup, 3)
+    ms = timed_steps(step, steps, warm)
+    value = rows / (ms / steps * 1e-3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": steps, "warmup": warm, "ms_per_step": round(ms / steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "mixed decode batch: B=256, V=151936 bf16 (oracle on a "
+                               f"{rows}-row sample per step)", "B": w.B, "V": w.V,
+                   "page_size": w.page_size},
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows of the mixed batch per step plus the full page "
+                                   f"fill, {steps} steps"},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -605,6 +605,9 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
       const float tpv = tp;
       cp = tie_cutoff<BF16>(d, lane_base, [&](float x, int e) { return x == tpv && in_k(x, e); },
                             rp, sm, s_slice, ph, crank, csize, tid, lane, warp);
+      // The cut counted only K members; when both thresholds fall in the same
+      // tie group, members past the top-k cutoff are outside K and stay out.
+      if (tp == tk && ck < cp) cp = ck;
     }
     auto in_s = [&](float x, int e) { return x > tp || (x == tp && e < cp); };
 
