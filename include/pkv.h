@@ -55,6 +55,9 @@ typedef enum { PKV_FP32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_ST_COL_OOB 8       /* write-back / page-table column out of range  */
 #define PKV_ST_BAD_UNIFORM 16  /* uniform outside [0,1): clamped, still drawn  */
 #define PKV_ST_NOSPC 32        /* page fill: more pages needed than are free   */
+#define PKV_ST_TIMEOUT 64      /* a bulk copy into shared memory did not complete
+                                  within the kernel's bounded wait; the token of
+                                  that row is unreliable                        */
 
 /* Largest vocabulary the sampler handles for each dtype. */
 #define PKV_MAX_VOCAB_BF16 524288
@@ -93,8 +96,10 @@ size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt);
  * index.  Arithmetic is fp32 (bf16 logits are widened exactly).
  *
  *   logits      [B, row_stride] fp32 or bf16, row-major; only the first V
- *               entries of each row are read.  16-byte-aligned rows (base and
- *               row_stride * element size) take the vectorised path.
+ *               entries of each row are read.  Rows whose start and length
+ *               are 16-byte aligned (base, row_stride * element size and
+ *               V * element size) are fetched with bulk copies; others with
+ *               element loads.
  *   temperature [B] fp32 or NULL      top_k [B] int32 or NULL
  *   top_p       [B] fp32 or NULL      uniform [B] fp32, required unless
  *                                     temperature is NULL

@@ -101,7 +101,9 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
   const int max_v = bf16 ? PKV_MAX_VOCAB_BF16 : PKV_MAX_VOCAB_FP32;
   if (V > max_v) return fail(PKV_EUNSUPPORTED, "V=%d above the maximum %d", V, max_v);
   const size_t elt = bf16 ? 2 : 4;
-  const bool vec = aligned16(logits) && ((static_cast<uint64_t>(row_stride) * elt) % 16 == 0);
+  // The TMA bulk-copy path needs 16-byte-aligned row starts and row lengths.
+  const bool vec = aligned16(logits) && ((static_cast<uint64_t>(row_stride) * elt) % 16 == 0) &&
+                   ((static_cast<uint64_t>(V) * elt) % 16 == 0);
   pkv::SampleConfig cfg;
   if (!pkv::choose_sample_config(B, V, bf16, vec, num_sms(), &cfg))
     return fail(PKV_EUNSUPPORTED, "no launch shape covers V=%d", V);
@@ -124,6 +126,7 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
   P.probs_out = probs_out;
   P.status = status;
   P.cta_chunk = cfg.chunk;
+  P.list_cap = 0;  // set by the launcher for the chosen kernel
   const bool all_greedy = temperature == nullptr;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = bf16 ? pkv::launch_sample_bf16(P, cfg, all_greedy, s)

@@ -9,27 +9,33 @@
 // Order between equal logits is by ascending index everywhere.
 //
 // GB300 design:
-//   * One thread-block cluster of C CTAs per row (grid = C x B).  CTA r of the
-//     cluster owns the contiguous slice [r*chunk, (r+1)*chunk) of the row and
-//     keeps it in REGISTERS for the whole kernel: the logits are read from HBM
-//     exactly once, with 16-byte streaming loads, each warp reading 512
-//     contiguous bytes per instruction.  Within a CTA every warp owns a
-//     contiguous sub-slice, so index order is (warp, vector j, lane, element).
-//   * Every cross-CTA step is a cluster barrier plus reads of the other CTAs'
-//     shared memory (DSMEM): row maximum / argmax, radix-select histograms,
-//     tie counts and the partial sums of the inverse-CDF scan.  No global
-//     scratch memory is used and nothing is sorted.
-//   * top-k: radix select (8-bit digits, 2 levels for bf16, 4 for fp32) on an
-//     order-preserving integer key with exact integer counts, then the tied
-//     elements at the threshold are cut by index (lowest first).
-//   * top-p: the same radix select weighted by probability mass.  Masses are
-//     accumulated as 2^-40 fixed-point integers, so bucket sums are exact and
-//     independent of the order of the shared-memory atomics (deterministic).
-//   * inverse CDF: per-warp partial sums -> per-CTA sums exchanged across the
+//   * One thread-block cluster of C CTAs per row (grid = C x B, not
+//     persistent, so rows never wait for each other).  CTA r owns the
+//     contiguous slice [r*chunk, (r+1)*chunk) of the row.  Its first thread
+//     issues one TMA bulk copy (cp.async.bulk + mbarrier) of the slice into
+//     shared memory, so a CTA holds no registers while its bytes are in flight
+//     and several CTAs per SM keep HBM busy.  Every logit is read from HBM
+//     exactly once; all later passes read shared memory.
+//   * Cross-CTA steps are cluster barriers.  Scalars are PUSHED into every
+//     CTA's shared memory before a barrier (DSMEM stores), so each CTA reads
+//     only its own shared memory afterwards and can exit right after its last
+//     barrier.
+//   * Fast selection (no per-element atomics): a guaranteed lower bound theta of
+//     the final threshold comes from the warps' per-thread maxima -- by count
+//     for top-k (each warp has >= k_w elements >= its k_w-th largest thread
+//     maximum), by probability mass for top-p (the warp's thread maxima that
+//     carry >= p of the warp's mass).  The few elements >= theta are compacted,
+//     in index order, into a list in the leader CTA's shared memory; the
+//     leader finishes top-k, top-p and the inverse CDF exactly on that list
+//     (radix selects with 256-bucket histograms over the list only).
+//   * Fallback (lists that would overflow, dense top-p rows): the same
+//     selections as radix selects over the whole row held on chip, with
+//     cluster-wide histogram exchanges.  Masses are 2^-40 fixed-point
+//     integers accumulated with pairs of 32-bit atomics, so every sum is exact
+//     and independent of atomic order (deterministic).
+//   * The draw: per-warp partial sums -> per-CTA sums exchanged across the
 //     cluster -> the CTA, warp, 256-element slab, lane and element where the
-//     cumulative mass first exceeds u * Z_S.  The one warp that searches copies
-//     its slice to shared memory and walks it with runtime loops, which keeps
-//     the register budget of the other phases intact.
+//     cumulative mass first exceeds u * Z_S (or a block scan over the list).
 //   * No tensor cores (nothing here is a contraction); exp is MUFU.EX2.
 #pragma once
 
@@ -44,46 +50,59 @@ namespace pkv {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;
+constexpr int kMaxClusterCtas = 16;
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
+constexpr uint32_t kWaitIters = 1u << 22;       // bound on mbarrier polls
 
 constexpr int kStNonFinite = 1;
 constexpr int kStAllNegInf = 2;
 constexpr int kStRowOOB = 4;
 constexpr int kStColOOB = 8;
 constexpr int kStBadUniform = 16;
+constexpr int kStTimeout = 64;
 
-// Values one CTA publishes for the others to read through DSMEM.  Two copies
-// alternate between consecutive cluster phases: a copy is rewritten only after
-// the next cluster barrier, which every CTA reaches after finishing its reads.
-struct Exchange {
-  float f;
-  int32_t i;
-  uint32_t u;
-  uint32_t pad;
-  union {
-    uint32_t cnt[kBuckets];
-    unsigned long long mass[kBuckets];
-  } hist;
+// One CTA's values for one exchange phase, pushed into every CTA.
+struct Slot {
+  float f0;
+  float f1;
+  int32_t i0;
+  uint32_t u0;
+  unsigned long long l0;
+  uint32_t pad0;
+  uint32_t pad1;
+};
+static_assert(sizeof(Slot) == 32, "Slot is pushed as two 16-byte stores");
+
+// Histogram a CTA publishes for the others to read (fallback radix select).
+struct PullBuf {
+  uint32_t lo[kBuckets];  // counts, or low words of fixed-point masses
+  uint32_t hi[kBuckets];  // high words of fixed-point masses
 };
 
 struct SampleSmem {
-  Exchange ex[2];
+  Slot push[2][kMaxClusterCtas];
+  PullBuf pull[2];
   unsigned long long scan[kBuckets];
+  uint32_t hlo[kBuckets];  // CTA-local histogram (list selects)
+  uint32_t hhi[kBuckets];
   unsigned long long wl[kWarps];
   float wf[kWarps];
   uint32_t wu[kWarps];
   int32_t wi[kWarps];
+  float wt[kWarps];
   float bf[4];
   int32_t bi[4];
   uint32_t bu[4];
-  unsigned long long bl[2];
+  unsigned long long bl[4];
+  uint64_t mbar;
 };
 
 // ----------------------------------------------------------------- element access
 //
-// Thread storage: d[j][c] is 32-bit word c of the thread's j-th 16-byte vector.
-// fp32: one element per word; bf16: two per word (low half first).  Element
-// index of (j, c, h) = lane_base + j*32*VW + c*EPW + h.
+// The slice is an array of 16-byte vectors.  Thread (warp w, lane l) owns the
+// vectors (w*NV + j)*32 + l, j < NV, so every warp owns a contiguous
+// sub-slice.  Element c of the thread's vector j has row index
+// lane_base + j*32*VW + c.
 
 template <bool BF16>
 struct Layout {
@@ -101,22 +120,6 @@ __device__ __forceinline__ float elem(uint32_t word, int h) {
   }
 }
 
-// f(x, e) for every element held by the thread, in ascending index order.
-template <bool BF16, int NV, typename F>
-__device__ __forceinline__ void for_each(const uint32_t (&d)[NV][4], int lane_base, F&& f) {
-  using L = Layout<BF16>;
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int h = 0; h < L::EPW; ++h) {
-        f(elem<BF16>(d[j][c], h), lane_base + j * 32 * L::VW + c * L::EPW + h);
-      }
-    }
-  }
-}
-
 // f(x, e) for the elements of one 16-byte vector whose first index is e0.
 template <bool BF16, typename F>
 __device__ __forceinline__ void for_vector(const uint4& v, int e0, F&& f) {
@@ -129,46 +132,34 @@ __device__ __forceinline__ void for_vector(const uint4& v, int e0, F&& f) {
   }
 }
 
-// Copies the warp's register slice to shared memory (slab j, lane l at
-// s[j*32 + l]) so that one warp can search it with runtime loops.
-template <int NV>
-__device__ __forceinline__ void dump_slice(const uint32_t (&d)[NV][4], uint4* s, int lane) {
-#pragma unroll
-  for (int j = 0; j < NV; ++j) s[j * 32 + lane] = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
-  __syncwarp();
+// NaN-propagating maximum of one 16-byte vector.
+template <bool BF16>
+__device__ __forceinline__ float vector_max(const uint4& v) {
+  if constexpr (BF16) {
+    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
+    return fmax_nan(elem<true>(m2, 0), elem<true>(m2, 1));
+  } else {
+    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
 }
 
-template <bool BF16, int NV, bool VEC>
-__device__ __forceinline__ void load_slice(const SampleParams& P, int row, int lane_base,
-                                           uint32_t (&d)[NV][4]) {
+struct Ctx {
+  int tid, lane, warp;
+  uint32_t crank, csize;
+  int row, V;
+  int lane_base;  // row index of the thread's first element
+  const uint4* sv;
+};
+
+// f(x, e) for every element the thread owns, in ascending index order.
+template <bool BF16, int NV, typename F>
+__device__ __forceinline__ void for_each(const Ctx& c, F&& f) {
   using L = Layout<BF16>;
-  const char* rp = static_cast<const char*>(P.logits) +
-                   static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) * L::ELT;
-  const int V = P.V;
-#pragma unroll
+#pragma unroll 2
   for (int j = 0; j < NV; ++j) {
-    const int e0 = lane_base + j * 32 * L::VW;
-    if (VEC && e0 + L::VW <= V) {
-      const uint4 v = ld_stream_v4(rp + static_cast<size_t>(e0) * L::ELT);
-      d[j][0] = v.x;
-      d[j][1] = v.y;
-      d[j][2] = v.z;
-      d[j][3] = v.w;
-    } else {
-      // Row tail or unaligned row: element loads, -inf past the end.
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if constexpr (BF16) {
-          const int e = e0 + 2 * c;
-          const uint32_t lo = e < V ? reinterpret_cast<const uint16_t*>(rp)[e] : 0xff80u;
-          const uint32_t hi = e + 1 < V ? reinterpret_cast<const uint16_t*>(rp)[e + 1] : 0xff80u;
-          d[j][c] = lo | (hi << 16);
-        } else {
-          const int e = e0 + c;
-          d[j][c] = e < V ? reinterpret_cast<const uint32_t*>(rp)[e] : 0xff800000u;
-        }
-      }
-    }
+    const uint4 v = c.sv[(c.warp * NV + j) * 32 + c.lane];
+    for_vector<BF16>(v, c.lane_base + j * 32 * L::VW, f);
   }
 }
 
@@ -185,6 +176,22 @@ __device__ __forceinline__ T block_suffix_scan(T v, T* s_w, int lane, int warp) 
   return v + add;
 }
 
+// Exclusive prefix over threads in tid order; *total receives the block sum.
+template <typename T>
+__device__ __forceinline__ T block_exclusive_scan(T v, T* s_w, int lane, int warp, T* total) {
+  const T incl = warp_inclusive_scan(v, lane);
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  T before = 0, all = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) before += s_w[w];
+    all += s_w[w];
+  }
+  __syncthreads();
+  *total = all;
+  return before + incl - v;
+}
+
 __device__ __forceinline__ int block_max_int(int v, int32_t* s_w, int lane, int warp) {
   v = __reduce_max_sync(kFull, v);
   if (lane == 0) s_w[warp] = v;
@@ -196,19 +203,62 @@ __device__ __forceinline__ int block_max_int(int v, int32_t* s_w, int lane, int 
   return r;
 }
 
-// Radix-select step: thread t holds the cluster-wide weight `tot` of bucket t.
+__device__ __forceinline__ int block_min_int(int v, int32_t* s_w, int lane, int warp) {
+  v = __reduce_min_sync(kFull, v);
+  if (lane == 0) s_w[warp] = v;
+  __syncthreads();
+  int r = s_w[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) r = min(r, s_w[w]);
+  __syncthreads();
+  return r;
+}
+
+// Radix-select step: thread t holds the weight `tot` of bucket t (t < 256).
 // Returns the highest bucket b whose suffix weight S(b) = sum_{t >= b} tot_t
 // reaches `rem`, and S(b + 1) (the weight strictly above it) in *above.
-template <typename T>
-__device__ __forceinline__ int select_bucket(T tot, T rem, SampleSmem& sm, T* above, int tid,
-                                             int lane, int warp) {
+__device__ __forceinline__ int select_bucket(unsigned long long tot, unsigned long long rem,
+                                             SampleSmem& sm, unsigned long long* above,
+                                             int tid, int lane, int warp) {
   const unsigned long long S = block_suffix_scan<unsigned long long>(tot, sm.wl, lane, warp);
   sm.scan[tid] = S;
   int b = block_max_int(S >= rem ? tid : -1, sm.wi, lane, warp);
-  if (b < 0) b = 0;  // unreachable: the caller keeps rem <= S(0)
-  *above = (b + 1 < kBuckets) ? static_cast<T>(sm.scan[b + 1]) : T(0);
+  if (b < 0) b = 0;  // unreachable: callers keep rem <= S(0)
+  *above = (b + 1 < kBuckets) ? sm.scan[b + 1] : 0ull;
   __syncthreads();
   return b;
+}
+
+// Adds a 64-bit fixed-point value to a (lo, hi) pair of 32-bit counters.
+__device__ __forceinline__ void atomic_add_u64_split(uint32_t* lo, uint32_t* hi,
+                                                     unsigned long long v) {
+  const uint32_t vlo = static_cast<uint32_t>(v);
+  const uint32_t vhi = static_cast<uint32_t>(v >> 32);
+  const uint32_t old = atomicAdd(lo, vlo);
+  const uint32_t carry = (old + vlo < old) ? 1u : 0u;
+  if (vhi + carry != 0u) atomicAdd(hi, vhi + carry);
+}
+
+__device__ __forceinline__ unsigned long long mass_fx(float w) {
+  return static_cast<unsigned long long>(__float2ull_rz(w * kMassScale));
+}
+
+// ----------------------------------------------------------------- exchange
+
+// Pushes this CTA's slot into slot[crank] of every CTA, then waits at the
+// cluster barrier.  Returns the buffer to read locally.
+__device__ __forceinline__ const Slot* push_exchange(SampleSmem& sm, int& ph, const Ctx& c,
+                                                     const Slot& mine) {
+  Slot* buf = sm.push[ph & 1];
+  if (c.tid < static_cast<int>(c.csize)) {
+    const uint32_t a = dsmem(&buf[c.crank], static_cast<uint32_t>(c.tid));
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(&mine);
+    st_dsmem_v4(a, w[0], w[1], w[2], w[3]);
+    st_dsmem_v4(a + 16, w[4], w[5], w[6], w[7]);
+  }
+  cluster_sync();
+  ++ph;
+  return buf;
 }
 
 // ----------------------------------------------------------------- output
@@ -231,209 +281,371 @@ __device__ __forceinline__ void emit_token(const SampleParams& P, int row, int t
   if (st != 0 && P.status != nullptr) atomicOr(P.status, st);
 }
 
-// ----------------------------------------------------------------- tie cutoff
+// ----------------------------------------------------------------- warp helpers
+
+// 32 floats sorted descending across the warp (bitonic network).
+__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float o = __shfl_xor_sync(kFull, v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_max ? fmaxf(v, o) : fminf(v, o);
+    }
+  }
+  return v;
+}
+
+// ----------------------------------------------------------------- list selects
 //
-// Among the elements satisfying `member` across the whole cluster, the first
-// r in index order are kept.  Returns this CTA's cutoff: its members with
-// index < cutoff are the kept ones.  One cluster phase.
-template <bool BF16, int NV, typename M>
-__device__ __forceinline__ int tie_cutoff(const uint32_t (&d)[NV][4], int lane_base, M&& member,
-                                          unsigned long long r, SampleSmem& sm, uint4* s_slice,
-                                          int& ph, uint32_t crank, uint32_t csize, int tid,
-                                          int lane, int warp) {
-  using L = Layout<BF16>;
-  uint32_t cnt = 0;
-  for_each<BF16>(d, lane_base, [&](float x, int e) { cnt += member(x, e) ? 1u : 0u; });
-  const uint32_t wc = __reduce_add_sync(kFull, cnt);
-  if (lane == 0) sm.wu[warp] = wc;
-  __syncthreads();
-  Exchange& ex = sm.ex[ph & 1];
-  if (tid == 0) {
-    uint32_t s = 0;
-    for (int w = 0; w < kWarps; ++w) s += sm.wu[w];
-    ex.u = s;
-  }
-  cluster_sync();
-  ++ph;
-  if (warp == 0) {
-    const uint32_t c = lane < static_cast<int>(csize) ? ld_dsmem_u32(dsmem(&ex.u, lane)) : 0u;
-    const uint32_t incl = warp_inclusive_scan(c, lane);
-    const uint32_t before = __shfl_sync(kFull, incl - c, crank);
-    const uint32_t mine = __shfl_sync(kFull, c, crank);
-    if (lane == 0) {
-      unsigned long long rl = r > before ? r - before : 0ull;
-      if (rl > mine) rl = mine;
-      sm.bu[0] = static_cast<uint32_t>(rl);
-      sm.bu[1] = mine;
+// The leader's list holds n entries (value, row index) in ascending index
+// order.  These run in one CTA with __syncthreads only.
+
+// Smallest and largest key of the list entries satisfying `keep`.
+template <typename K>
+__device__ __forceinline__ void list_key_range(const float* val, int n, K&& keep, SampleSmem& sm,
+                                               const Ctx& c, uint32_t* kmin, uint32_t* kmax) {
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for (int i = c.tid; i < n; i += kThreads) {
+    if (keep(i)) {
+      const uint32_t k = float_key(val[i]);
+      lo = min(lo, k);
+      hi = max(hi, k);
     }
   }
+  lo = __reduce_min_sync(kFull, lo);
+  hi = __reduce_max_sync(kFull, hi);
+  if (c.lane == 0) {
+    sm.wu[c.warp] = lo;
+    sm.wi[c.warp] = static_cast<int32_t>(hi);
+  }
   __syncthreads();
-  const uint32_t rl = sm.bu[0];
-  const uint32_t mine = sm.bu[1];
-  int cut;
-  if (rl == 0) {
-    cut = INT_MIN;
-  } else if (rl >= mine) {
-    cut = INT_MAX;
-  } else {
-    // The warp holding the rl-th member of this CTA.
-    uint32_t cum = 0;
-    int wstar = kWarps - 1;
-    uint32_t rw = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      if (cum + sm.wu[w] >= rl) {
-        wstar = w;
-        rw = rl - cum;
-        break;
+  uint32_t a = 0xffffffffu, b = 0u;
+  for (int w = 0; w < kWarps; ++w) {
+    a = min(a, sm.wu[w]);
+    b = max(b, static_cast<uint32_t>(sm.wi[w]));
+  }
+  __syncthreads();
+  *kmin = a;
+  *kmax = b;
+}
+
+// Radix select over the list: the key t such that the weight of entries with
+// key > t is < target <= the weight with key >= t.  weight(i) is 1 (count) or
+// a fixed-point mass; entries with keep(i) false weigh nothing.  Returns t and
+// the weight still needed from the entries equal to t in *rem.
+template <bool MASS, typename K, typename W>
+__device__ __forceinline__ float list_select(const float* val, int n, K&& keep, W&& weight,
+                                             unsigned long long target, SampleSmem& sm,
+                                             const Ctx& c, unsigned long long* rem_out) {
+  uint32_t kmin, kmax;
+  list_key_range(val, n, keep, sm, c, &kmin, &kmax);
+  unsigned long long rem = target;
+  if (kmin == kmax) {
+    *rem_out = rem;
+    return key_float(kmin);
+  }
+  const int top = 31 - __clz(kmin ^ kmax);
+  uint32_t prefix = static_cast<uint32_t>(
+      static_cast<unsigned long long>(kmin) & ~((2ull << top) - 1ull));
+  for (int hi = top; hi >= 0; hi -= 8) {
+    const int lo = hi >= 7 ? hi - 7 : 0;
+    const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;
+    const uint32_t amask =
+        static_cast<uint32_t>(~((2ull << hi) - 1ull));  // bits above the digit
+    sm.hlo[c.tid] = 0u;
+    sm.hhi[c.tid] = 0u;
+    __syncthreads();
+    for (int i = c.tid; i < n; i += kThreads) {
+      if (!keep(i)) continue;
+      const uint32_t key = float_key(val[i]);
+      if ((key & amask) != (prefix & amask)) continue;
+      const uint32_t d = (key >> lo) & dmask;
+      if constexpr (MASS) {
+        atomic_add_u64_split(&sm.hlo[d], &sm.hhi[d], weight(i));
+      } else {
+        atomicAdd(&sm.hlo[d], 1u);
       }
-      cum += sm.wu[w];
-    }
-    if (warp == wstar) {
-      dump_slice(d, s_slice, lane);
-      uint32_t acc = 0;
-      int found = INT_MAX;
-#pragma unroll 1
-      for (int j = 0; j < NV; ++j) {
-        const uint4 v = s_slice[j * 32 + lane];
-        const int e0 = lane_base + j * 32 * L::VW;
-        uint32_t cj = 0;
-        for_vector<BF16>(v, e0, [&](float x, int e) { cj += member(x, e) ? 1u : 0u; });
-        const uint32_t incl = warp_inclusive_scan(cj, lane);
-        const uint32_t stot = __shfl_sync(kFull, incl, 31);
-        if (acc + stot >= rw) {
-          const unsigned bal = __ballot_sync(kFull, acc + incl >= rw);
-          const int lx = __ffs(bal) - 1;
-          int sel = INT_MAX;
-          if (lane == lx) {
-            uint32_t need = rw - (acc + incl - cj);  // 1-based rank inside this lane's vector
-            for_vector<BF16>(v, e0, [&](float x, int e) {
-              if (member(x, e)) {
-                if (need == 1 && sel == INT_MAX) sel = e;
-                --need;
-              }
-            });
-          }
-          found = __shfl_sync(kFull, sel, lx);
-          break;
-        }
-        acc += stot;
-      }
-      if (lane == 0) sm.bi[0] = found == INT_MAX ? INT_MAX : found + 1;
     }
     __syncthreads();
-    cut = sm.bi[0];
+    const unsigned long long tot =
+        MASS ? ((static_cast<unsigned long long>(sm.hhi[c.tid]) << 32) | sm.hlo[c.tid])
+             : static_cast<unsigned long long>(sm.hlo[c.tid]);
+    unsigned long long above;
+    const int b = select_bucket(tot, rem, sm, &above, c.tid, c.lane, c.warp);
+    rem -= above;
+    prefix |= static_cast<uint32_t>(b) << lo;
   }
+  *rem_out = rem;
+  return key_float(prefix);
+}
+
+// Position cut for ties in the list: among entries with member(i), the first
+// r (list order = index order) are kept.  Returns the position after the r-th
+// member (n if there are fewer than r).
+template <typename M>
+__device__ __forceinline__ int list_tie_cut(int n, M&& member, unsigned long long r,
+                                            SampleSmem& sm, const Ctx& c) {
+  const int per = (n + kThreads - 1) / kThreads;
+  const int i0 = min(n, c.tid * per);
+  const int i1 = min(n, i0 + per);
+  uint32_t cnt = 0;
+  for (int i = i0; i < i1; ++i) cnt += member(i) ? 1u : 0u;
+  uint32_t total;
+  const uint32_t before = block_exclusive_scan<uint32_t>(cnt, sm.wu, c.lane, c.warp, &total);
+  if (c.tid == 0) sm.bi[3] = n;
+  __syncthreads();
+  if (r <= total && before < r && r <= before + cnt) {
+    uint32_t need = static_cast<uint32_t>(r - before);
+    for (int i = i0; i < i1; ++i) {
+      if (member(i) && --need == 0) {
+        sm.bi[3] = i + 1;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  const int cut = sm.bi[3];
   __syncthreads();
   return cut;
 }
 
-// ----------------------------------------------------------------- the kernel
-
-template <bool BF16, int NV, bool VEC, bool ALL_GREEDY>
-__global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams P) {
-  using L = Layout<BF16>;
-  constexpr int NLEV = BF16 ? 2 : 4;  // 8-bit radix levels covering the key
-  __shared__ SampleSmem sm;
-  __shared__ uint4 s_slice[NV * 32];
-
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const uint32_t crank = cluster_rank();
-  const uint32_t csize = cluster_size();
-  const int row = blockIdx.y;
-  const int V = P.V;
-  const int cta_begin = static_cast<int>(crank) * P.cta_chunk;
-  const int lane_base = cta_begin + warp * (32 * NV * L::VW) + lane * L::VW;
-
-  uint32_t d[NV][4];
-  load_slice<BF16, NV, VEC>(P, row, lane_base, d);
-
-  const bool greedy = ALL_GREEDY || !(P.temperature[row] > 0.0f);
-
-  // ---- phase 1: row maximum (NaN-propagating), argmax for greedy rows.
-  float tmax;
-  if constexpr (BF16) {
-    uint32_t a0 = d[0][0], a1 = d[0][1], a2 = d[0][2], a3 = d[0][3];
-#pragma unroll
-    for (int j = 1; j < NV; ++j) {
-      a0 = bf16x2_max_nan(a0, d[j][0]);
-      a1 = bf16x2_max_nan(a1, d[j][1]);
-      a2 = bf16x2_max_nan(a2, d[j][2]);
-      a3 = bf16x2_max_nan(a3, d[j][3]);
+// Inverse CDF over the list entries with in_s(i): the first entry (list
+// order) whose cumulative weight exceeds u * Z_S; else the last with weight.
+// Writes Z_S to *zs.  Returns the row index of the token (-1 if none).
+template <typename S, typename W>
+__device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&& w_of, float u,
+                                         SampleSmem& sm, const Ctx& c, float* zs) {
+  const int per = (n + kThreads - 1) / kThreads;
+  const int i0 = min(n, c.tid * per);
+  const int i1 = min(n, i0 + per);
+  float seg = 0.0f;
+  int last = -1;
+  for (int i = i0; i < i1; ++i) {
+    if (in_s(i)) {
+      const float w = w_of(i);
+      seg += w;
+      if (w > 0.0f) last = i;
     }
-    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(a0, a1), bf16x2_max_nan(a2, a3));
-    tmax = fmax_nan(elem<true>(m2, 0), elem<true>(m2, 1));
-  } else {
-    float a0 = elem<false>(d[0][0], 0), a1 = elem<false>(d[0][1], 0);
-    float a2 = elem<false>(d[0][2], 0), a3 = elem<false>(d[0][3], 0);
-#pragma unroll
-    for (int j = 1; j < NV; ++j) {
-      a0 = fmax_nan(a0, elem<false>(d[j][0], 0));
-      a1 = fmax_nan(a1, elem<false>(d[j][1], 0));
-      a2 = fmax_nan(a2, elem<false>(d[j][2], 0));
-      a3 = fmax_nan(a3, elem<false>(d[j][3], 0));
-    }
-    tmax = fmax_nan(fmax_nan(a0, a1), fmax_nan(a2, a3));
   }
-  int tidx = INT_MAX;
-  if (greedy) {
-    // Lowest index holding the thread maximum: walk downwards, keep the last hit.
-#pragma unroll
-    for (int j = NV - 1; j >= 0; --j) {
-#pragma unroll
-      for (int c = 3; c >= 0; --c) {
-#pragma unroll
-        for (int h = L::EPW - 1; h >= 0; --h) {
-          if (elem<BF16>(d[j][c], h) == tmax) tidx = lane_base + j * 32 * L::VW + c * L::EPW + h;
+  float total;
+  const float before = block_exclusive_scan<float>(seg, sm.wt, c.lane, c.warp, &total);
+  const float target = u * total;
+  const int cand = block_min_int((target < before + seg && seg > 0.0f) ? c.tid : INT_MAX, sm.wi,
+                                 c.lane, c.warp);
+  const int lastpos = block_max_int(last, sm.wi, c.lane, c.warp);
+  if (c.tid == 0) sm.bi[2] = lastpos;
+  __syncthreads();
+  if (cand != INT_MAX && c.tid == cand) {
+    float run = before;
+    int sel = -1;
+    for (int i = i0; i < i1; ++i) {
+      if (in_s(i)) {
+        run += w_of(i);
+        if (target < run) {
+          sel = i;
+          break;
         }
       }
     }
+    sm.bi[2] = sel >= 0 ? sel : last;
   }
-  const int nan_any = __any_sync(kFull, tmax != tmax);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(kFull, tmax, o);
-    const int oi = __shfl_xor_sync(kFull, tidx, o);
-    if (ov > tmax || (ov == tmax && oi < tidx)) {
-      tmax = ov;
-      tidx = oi;
+  __syncthreads();
+  const int pos = sm.bi[2];
+  *zs = total;
+  __syncthreads();
+  return pos >= 0 ? idx[pos] : -1;
+}
+
+// ----------------------------------------------------------------- the kernel
+
+template <bool BF16, int NV, bool TMA, bool ALL_GREEDY>
+__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams P) {
+  using L = Layout<BF16>;
+  constexpr int CHUNK = kThreads * NV * L::VW;  // elements per CTA
+  constexpr int NLEV = BF16 ? 2 : 4;            // 8-bit radix levels (fallback)
+  __shared__ SampleSmem sm;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  uint4* s_vec = reinterpret_cast<uint4*>(dyn);
+  float* l_val = reinterpret_cast<float*>(dyn + CHUNK * L::ELT);
+  int32_t* l_idx = reinterpret_cast<int32_t*>(l_val + P.list_cap);
+
+  Ctx c;
+  c.tid = threadIdx.x;
+  c.lane = c.tid & 31;
+  c.warp = c.tid >> 5;
+  c.crank = cluster_rank();
+  c.csize = cluster_size();
+  c.row = blockIdx.y;
+  c.V = P.V;
+  c.sv = s_vec;
+  const int V = P.V;
+  const int row = c.row;
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  const int cta_begin = static_cast<int>(c.crank) * CHUNK;
+  c.lane_base = cta_begin + ((warp * NV) * 32 + lane) * L::VW;
+  const int nvalid = max(0, min(CHUNK, V - cta_begin));
+
+  // ---- bring the slice into shared memory
+  const char* gsrc = static_cast<const char*>(P.logits) +
+                     (static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) +
+                      static_cast<size_t>(cta_begin)) * L::ELT;
+  if constexpr (TMA) {
+    if (tid == 0) {
+      mbar_init(&sm.mbar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t bytes = static_cast<uint32_t>(nvalid) * L::ELT;
+      mbar_arrive_expect_tx(&sm.mbar, bytes);
+      for (uint32_t off = 0; off < bytes; off += 16384u) {
+        bulk_copy_g2s(dyn + off, gsrc + off, min(16384u, bytes - off), &sm.mbar);
+      }
+    }
+  } else {
+    for (int e = tid; e < nvalid; e += kThreads) {
+      if constexpr (BF16) {
+        reinterpret_cast<uint16_t*>(dyn)[e] = reinterpret_cast<const uint16_t*>(gsrc)[e];
+      } else {
+        reinterpret_cast<uint32_t*>(dyn)[e] = reinterpret_cast<const uint32_t*>(gsrc)[e];
+      }
     }
   }
-  if (lane == 0) {
-    sm.wf[warp] = tmax;
-    sm.wi[warp] = tidx;
-    sm.wu[warp] = nan_any;
+  for (int e = nvalid + tid; e < CHUNK; e += kThreads) {  // padding: -inf
+    if constexpr (BF16) {
+      reinterpret_cast<uint16_t*>(dyn)[e] = 0xff80u;
+    } else {
+      reinterpret_cast<uint32_t*>(dyn)[e] = 0xff800000u;
+    }
+  }
+
+  // Row parameters (Sampler.prepare's normalisation), read while the copy runs.
+  const bool greedy = ALL_GREEDY || !(P.temperature[row] > 0.0f);
+  float T = 1.0f, p = 1.0f, u = 0.0f;
+  int k = V;
+  int st = 0;
+  if (!greedy) {
+    T = fmaxf(P.temperature[row], 1e-6f);
+    k = P.top_k != nullptr ? P.top_k[row] : -1;
+    if (k < 1 || k >= V) k = V;
+    p = P.top_p != nullptr ? fminf(fmaxf(P.top_p[row], 1e-6f), 1.0f) : 1.0f;
+    u = P.uniform[row];
+    if (!(u >= 0.0f && u < 1.0f)) {
+      st |= kStBadUniform;
+      u = (u != u) ? 0.0f : fminf(fmaxf(u, 0.0f), 0x1.fffffep-1f);
+    }
+  }
+  const float c2 = 1.4426950408889634f / T;  // log2(e) / T
+  bool copy_ok = true;
+  if constexpr (TMA) copy_ok = mbar_wait_bounded(&sm.mbar, 0, kWaitIters);
+  const bool timed_out = __syncthreads_or(!copy_ok) != 0;
+  if (timed_out) st |= kStTimeout;
+  // On a timeout the kernel still runs every barrier (with whatever the slice
+  // holds) and waits once more for its copy before the CTA exits.
+  auto leave = [&]() {
+    if constexpr (TMA) {
+      if (timed_out && tid == 0) mbar_wait_bounded(&sm.mbar, 0, kWaitIters);
+    }
+  };
+
+  // ---- phase 1: thread maxima, row maximum (NaN-propagating), argmax.
+  float tmax = -INFINITY;
+  int tidx = INT_MAX;
+  bool nan = false;
+#pragma unroll 2
+  for (int j = 0; j < NV; ++j) {
+    const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
+    const float vm = vector_max<BF16>(v);
+    if (vm != vm) {
+      nan = true;
+    } else if (vm > tmax || tidx == INT_MAX) {
+      tmax = vm;
+      if (greedy) {
+        int first = INT_MAX;
+        for_vector<BF16>(v, c.lane_base + j * 32 * L::VW, [&](float x, int e) {
+          if (x == vm && e < first) first = e;
+        });
+        tidx = first;
+      } else {
+        tidx = 0;
+      }
+    }
+  }
+  const float thread_max = tmax;
+  // theta from thread maxima for top-k rows: the k_w-th largest thread
+  // maximum of every warp whose elements all lie inside the row (W_full such
+  // warps, k_w = ceil(k / W_full)), so at least k elements are >= theta.
+  // Warps that reach past the row end do not constrain theta.
+  constexpr int kWarpSpan = 32 * NV * L::VW;
+  float theta_w = -INFINITY;
+  const bool topk_row = !greedy && k < V;
+  if (topk_row) {
+    const int w_full = V / kWarpSpan;
+    const int kw = w_full > 0 ? (k + w_full - 1) / w_full : INT_MAX;
+    const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
+    if (kw <= 32) {
+      const float sorted = warp_sort_desc(thread_max, lane);
+      theta_w = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
+    }
+  }
+  {
+    const int nan_any = __any_sync(kFull, nan);
+    float v = tmax;
+    int i = tidx;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(kFull, v, o);
+      const int oi = __shfl_xor_sync(kFull, i, o);
+      if (ov > v || (ov == v && oi < i)) {
+        v = ov;
+        i = oi;
+      }
+    }
+    if (lane == 0) {
+      sm.wf[warp] = v;
+      sm.wi[warp] = i;
+      sm.wu[warp] = static_cast<uint32_t>(nan_any);
+      sm.wt[warp] = theta_w;
+    }
   }
   __syncthreads();
   int ph = 0;
+  Slot mine = {};
   {
-    Exchange& ex = sm.ex[ph & 1];
-    if (tid == 0) {
-      float v = sm.wf[0];
-      int i = sm.wi[0];
-      uint32_t n = sm.wu[0];
-      for (int w = 1; w < kWarps; ++w) {
-        if (sm.wf[w] > v || (sm.wf[w] == v && sm.wi[w] < i)) {
-          v = sm.wf[w];
-          i = sm.wi[w];
-        }
-        n |= sm.wu[w];
+    float v = sm.wf[0];
+    int i = sm.wi[0];
+    uint32_t n = sm.wu[0];
+    float th = sm.wt[0];
+    for (int w = 1; w < kWarps; ++w) {
+      if (sm.wf[w] > v || (sm.wf[w] == v && sm.wi[w] < i)) {
+        v = sm.wf[w];
+        i = sm.wi[w];
       }
-      ex.f = v;
-      ex.i = i;
-      ex.u = n;
+      n |= sm.wu[w];
+      th = fminf(th, sm.wt[w]);
     }
-    cluster_sync();
-    ++ph;
+    mine.f0 = v;
+    mine.f1 = th;
+    mine.i0 = i;
+    mine.u0 = n;
+  }
+  __syncthreads();
+  float m, theta;
+  int gidx;
+  bool nan_row;
+  {
+    const Slot* s = push_exchange(sm, ph, c, mine);
     if (warp == 0) {
-      float v = -INFINITY;
+      float v = -INFINITY, th = INFINITY;
       int i = INT_MAX;
       uint32_t n = 0;
-      if (lane < static_cast<int>(csize)) {
-        v = ld_dsmem_f32(dsmem(&ex.f, lane));
-        i = static_cast<int>(ld_dsmem_u32(dsmem(&ex.i, lane)));
-        n = ld_dsmem_u32(dsmem(&ex.u, lane));
+      if (lane < static_cast<int>(c.csize)) {
+        v = s[lane].f0;
+        th = s[lane].f1;
+        i = s[lane].i0;
+        n = s[lane].u0;
       }
       n = __reduce_or_sync(kFull, n);
 #pragma unroll
@@ -444,219 +656,481 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
           v = ov;
           i = oi;
         }
+        th = fminf(th, __shfl_xor_sync(kFull, th, o));
       }
       if (lane == 0) {
         sm.bf[0] = v;
+        sm.bf[1] = th;
         sm.bi[0] = i;
         sm.bu[0] = n;
       }
     }
     __syncthreads();
+    m = sm.bf[0];
+    theta = sm.bf[1];
+    gidx = sm.bi[0];
+    nan_row = sm.bu[0] != 0;
+    __syncthreads();
   }
-  const float m = sm.bf[0];
-  const int gidx = sm.bi[0];
-  const bool nan_row = sm.bu[0] != 0;
-  __syncthreads();
+
+  float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
+  auto write_zero_probs = [&]() {
+    if (q_row != nullptr) {
+      for_each<BF16, NV>(c, [&](float, int e) {
+        if (e < V) q_row[e] = 0.0f;
+      });
+    }
+  };
 
   if (greedy) {
     const int tok = nan_row ? -1 : gidx;
-    if (crank == 0 && tid == 0) emit_token(P, row, tok, nan_row ? kStNonFinite : 0);
-    if (P.probs_out != nullptr) {
-      float* q = P.probs_out + static_cast<size_t>(row) * V;
-      for_each<BF16>(d, lane_base, [&](float, int e) {
-        if (e < V) q[e] = (e == tok) ? 1.0f : 0.0f;
+    if (c.crank == 0 && tid == 0) emit_token(P, row, tok, (nan_row ? kStNonFinite : 0) | st);
+    if (q_row != nullptr) {
+      for_each<BF16, NV>(c, [&](float, int e) {
+        if (e < V) q_row[e] = (e == tok) ? 1.0f : 0.0f;
       });
     }
-    cluster_sync();
+    leave();
     return;
   }
 
   if constexpr (!ALL_GREEDY) {
-    // ---- parameters (Sampler.prepare's normalisation, applied per row).
-    const float T = fmaxf(P.temperature[row], 1e-6f);
-    int k = P.top_k != nullptr ? P.top_k[row] : -1;
-    if (k < 1 || k >= V) k = V;
-    const float p = P.top_p != nullptr ? fminf(fmaxf(P.top_p[row], 1e-6f), 1.0f) : 1.0f;
-    float u = P.uniform[row];
-    int st = 0;
-    if (!(u >= 0.0f && u < 1.0f)) {
-      st |= kStBadUniform;
-      u = (u != u) ? 0.0f : fminf(fmaxf(u, 0.0f), 0x1.fffffep-1f);
-    }
     if (nan_row || m == INFINITY || m == -INFINITY) {
-      st = (m == -INFINITY && !nan_row) ? kStAllNegInf : kStNonFinite;
-      if (crank == 0 && tid == 0) emit_token(P, row, -1, st);
-      if (P.probs_out != nullptr) {
-        float* q = P.probs_out + static_cast<size_t>(row) * V;
-        for_each<BF16>(d, lane_base, [&](float, int e) {
-          if (e < V) q[e] = 0.0f;
-        });
-      }
-      cluster_sync();
+      const int est = (m == -INFINITY && !nan_row) ? kStAllNegInf : kStNonFinite;
+      if (c.crank == 0 && tid == 0) emit_token(P, row, -1, est | st);
+      write_zero_probs();
+      leave();
       return;
     }
-    const float c2 = 1.4426950408889634f / T;  // log2(e) / T
+    const bool use_p = p < 1.0f;
+    const int R = P.list_cap / static_cast<int>(c.csize);  // list entries per CTA region
 
-    // ---- top-k: radix select of the k-th key, then the index cutoff of ties.
+    // ---- top-p rows: Z and a mass-based theta from the warps' thread maxima.
+    float zrow = 0.0f;
+    if (!topk_row && use_p) {
+      float zt = 0.0f;
+      for_each<BF16, NV>(c, [&](float x, int) { zt += ex2((x - m) * c2); });
+      const float zw = warp_sum(zt);
+      // Largest theta_w whose thread maxima above it carry >= p' of the
+      // warp's mass; p' is p raised by 1e-4 so that rounding rarely forces
+      // the fallback (the leader checks the list's mass exactly).
+      const float sorted = warp_sort_desc(thread_max, lane);
+      const float ws = ex2((sorted - m) * c2);
+      const float cum = warp_inclusive_scan(ws, lane);
+      const float need = fminf(1.0f, p * 1.0001f) * zw;
+      const unsigned hit = __ballot_sync(kFull, cum >= need);
+      // A warp with no mass (all padding) does not constrain theta.
+      const float tw = zw > 0.0f ? (hit ? __shfl_sync(kFull, sorted, __ffs(hit) - 1) : -INFINITY)
+                                 : INFINITY;
+      if (lane == 0) {
+        sm.wf[warp] = zw;
+        sm.wt[warp] = tw;
+      }
+      __syncthreads();
+      Slot z = {};
+      float zsum = 0.0f, th = INFINITY;
+      for (int w = 0; w < kWarps; ++w) {
+        zsum += sm.wf[w];
+        th = fminf(th, sm.wt[w]);
+      }
+      z.f0 = zsum;
+      z.f1 = th;
+      __syncthreads();
+      const Slot* s = push_exchange(sm, ph, c, z);
+      if (warp == 0) {
+        float zz = lane < static_cast<int>(c.csize) ? s[lane].f0 : 0.0f;
+        float tt = lane < static_cast<int>(c.csize) ? s[lane].f1 : INFINITY;
+        zz = warp_sum(zz);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tt = fminf(tt, __shfl_xor_sync(kFull, tt, o));
+        if (lane == 0) {
+          sm.bf[0] = zz;
+          sm.bf[1] = tt;
+        }
+      }
+      __syncthreads();
+      zrow = sm.bf[0];
+      theta = sm.bf[1];
+      __syncthreads();
+    }
+
+    // ---- fast path: candidates >= theta into the leader's list.
+    const bool fast = (topk_row || use_p) && theta > -INFINITY;
+    if (fast) {
+      uint32_t cnt = 0;
+      unsigned long long mfx = 0;
+      for_each<BF16, NV>(c, [&](float x, int e) {
+        if (x >= theta && e < V) {
+          ++cnt;
+          if (!topk_row) mfx += mass_fx(ex2((x - m) * c2));
+        }
+      });
+      const uint32_t wc = __reduce_add_sync(kFull, cnt);
+      mfx = warp_sum(mfx);
+      if (lane == 0) {
+        sm.wu[warp] = wc;
+        sm.wl[warp] = mfx;
+      }
+      __syncthreads();
+      uint32_t woff = 0, ncta = 0;
+      unsigned long long mcta = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) woff += sm.wu[w];
+        ncta += sm.wu[w];
+        mcta += sm.wl[w];
+      }
+      if (static_cast<int>(ncta) <= R) {
+        // Ordered write: warp region, then vector by vector in lane order.
+        const uint32_t base = static_cast<uint32_t>(c.crank) * R + woff;
+        const uint32_t a_val = dsmem(l_val, 0);
+        const uint32_t a_idx = dsmem(l_idx, 0);
+        uint32_t acc = 0;
+        for (int j = 0; j < NV; ++j) {
+          const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
+          const int e0 = c.lane_base + j * 32 * L::VW;
+          uint32_t cj = 0;
+          for_vector<BF16>(v, e0, [&](float x, int e) { cj += (x >= theta && e < V) ? 1u : 0u; });
+          if (__ballot_sync(kFull, cj != 0) == 0) continue;
+          const uint32_t incl = warp_inclusive_scan(cj, lane);
+          uint32_t pos = base + acc + incl - cj;
+          for_vector<BF16>(v, e0, [&](float x, int e) {
+            if (x >= theta && e < V) {
+              st_dsmem_f32(a_val + 4u * pos, x);
+              st_dsmem_u32(a_idx + 4u * pos, static_cast<uint32_t>(e));
+              ++pos;
+            }
+          });
+          acc += __shfl_sync(kFull, incl, 31);
+        }
+      }
+      write_zero_probs();
+      Slot cs = {};
+      cs.u0 = ncta;
+      cs.l0 = mcta;
+      __syncthreads();
+      const Slot* s = push_exchange(sm, ph, c, cs);
+      // Uniform decision: every region fits, and (top-p rows) the list holds
+      // enough mass that no element below theta can be kept.
+      uint32_t over = 0;
+      unsigned long long lmass = 0;
+      for (uint32_t r = 0; r < c.csize; ++r) {
+        if (static_cast<int>(s[r].u0) > R) over = 1;
+        lmass += s[r].l0;
+      }
+      unsigned long long target_fx = 0;
+      if (!topk_row) {
+        const double t = static_cast<double>(p) * static_cast<double>(zrow) * 1099511627776.0;
+        target_fx = static_cast<unsigned long long>(ceil(t));
+        if (target_fx < 1) target_fx = 1;
+        if (lmass < target_fx) over = 1;
+      }
+      if (over == 0) {
+        if (c.crank != 0) {
+          leave();
+          return;
+        }
+        // ---- leader: pack the regions, then select and draw on the list.
+        int n = 0;
+        for (uint32_t r = 0; r < c.csize; ++r) n += static_cast<int>(s[r].u0);
+        {
+          // Packed index i comes from region r at offset i - (sum of earlier
+          // counts), never from a position below i: read, barrier, write.
+          constexpr int kMovePer = 16;
+          float mv[kMovePer];
+          int mi[kMovePer];
+          for (int b0 = 0; b0 < n; b0 += kThreads * kMovePer) {
+#pragma unroll
+            for (int q = 0; q < kMovePer; ++q) {
+              const int i = b0 + q * kThreads + tid;
+              if (i < n) {
+                int r = 0, off = i;
+                while (off >= static_cast<int>(s[r].u0)) {
+                  off -= static_cast<int>(s[r].u0);
+                  ++r;
+                }
+                mv[q] = l_val[r * R + off];
+                mi[q] = l_idx[r * R + off];
+              }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < kMovePer; ++q) {
+              const int i = b0 + q * kThreads + tid;
+              if (i < n) {
+                l_val[i] = mv[q];
+                l_idx[i] = mi[q];
+              }
+            }
+            __syncthreads();
+          }
+        }
+        // top-k: count select; ties go by index = list order.
+        int cut_k = n;
+        float tk = -INFINITY;
+        if (topk_row) {
+          unsigned long long rk;
+          tk = list_select<false>(l_val, n, [](int) { return true; }, [](int) { return 1ull; },
+                                  static_cast<unsigned long long>(k), sm, c, &rk);
+          const float tkv = tk;
+          cut_k = list_tie_cut(n, [&](int i) { return l_val[i] == tkv; }, rk, sm, c);
+        }
+        const float tkv = tk;
+        const int ckv = cut_k;
+        auto in_k = [&](int i) { return l_val[i] > tkv || (l_val[i] == tkv && i < ckv); };
+        auto w_of = [&](int i) { return ex2((l_val[i] - m) * c2); };
+        float tp = tk;
+        int cut_p = cut_k;
+        if (use_p) {
+          if (topk_row) {
+            unsigned long long zfx = 0;
+            for (int i = tid; i < n; i += kThreads) {
+              if (in_k(i)) zfx += mass_fx(w_of(i));
+            }
+            zfx = warp_sum(zfx);
+            if (lane == 0) sm.wl[warp] = zfx;
+            __syncthreads();
+            unsigned long long z = 0;
+            for (int w = 0; w < kWarps; ++w) z += sm.wl[w];
+            __syncthreads();
+            const double t = static_cast<double>(z) * static_cast<double>(p);
+            target_fx = static_cast<unsigned long long>(ceil(t));
+            if (target_fx < 1) target_fx = 1;
+            if (target_fx > z) target_fx = z;
+          }
+          unsigned long long rem;
+          tp = list_select<true>(l_val, n, in_k, [&](int i) { return mass_fx(w_of(i)); },
+                                 target_fx, sm, c, &rem);
+          // Members of the threshold group share one weight wt: member j
+          // (index order) is kept iff above + j * wt < target, i.e.
+          // j < ceil(rem / wt).
+          const unsigned long long wt = mass_fx(ex2((tp - m) * c2));
+          const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
+          const float tpv = tp;
+          cut_p = list_tie_cut(n, [&](int i) { return l_val[i] == tpv && in_k(i); }, rp, sm, c);
+        }
+        const float tpv = tp;
+        const int cpv = cut_p;
+        auto in_s = [&](int i) {
+          return in_k(i) && (l_val[i] > tpv || (l_val[i] == tpv && i < cpv));
+        };
+        float zs;
+        const int tok = list_draw(l_idx, n, in_s, w_of, u, sm, c, &zs);
+        if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
+        if (q_row != nullptr) {
+          const float inv = 1.0f / zs;
+          for (int i = tid; i < n; i += kThreads) {
+            if (in_s(i)) q_row[l_idx[i]] = w_of(i) * inv;
+          }
+        }
+        leave();
+        return;
+      }
+      // Over capacity: every CTA falls through to the on-chip fallback.
+    }
+
+    // ---- fallback / plain rows: whole-row passes over the on-chip slices.
     float tk = -INFINITY;
     int ck = INT_MAX;
-    if (k < V) {
+    bool pulled = false;  // other CTAs read this CTA's histograms: final barrier due
+    auto tie_cutoff = [&](auto member, unsigned long long r) -> int {
+      // First r members (index order) across the cluster; returns this
+      // CTA's index cutoff.
+      uint32_t cnt = 0;
+      for_each<BF16, NV>(c, [&](float x, int e) { cnt += member(x, e) ? 1u : 0u; });
+      const uint32_t wc = __reduce_add_sync(kFull, cnt);
+      if (lane == 0) sm.wu[warp] = wc;
+      __syncthreads();
+      Slot cs = {};
+      for (int w = 0; w < kWarps; ++w) cs.u0 += sm.wu[w];
+      const Slot* s = push_exchange(sm, ph, c, cs);
+      unsigned long long before = 0;
+      for (uint32_t r2 = 0; r2 < c.crank; ++r2) before += s[r2].u0;
+      const uint32_t mine_cnt = s[c.crank].u0;
+      unsigned long long rl = r > before ? r - before : 0ull;
+      if (rl > mine_cnt) rl = mine_cnt;
+      int cut;
+      if (rl == 0) {
+        cut = INT_MIN;
+      } else if (rl >= mine_cnt) {
+        cut = INT_MAX;
+      } else {
+        uint32_t cum = 0, rw = 0;
+        int wstar = kWarps - 1;
+        for (int w = 0; w < kWarps; ++w) {
+          if (cum + sm.wu[w] >= rl) {
+            wstar = w;
+            rw = static_cast<uint32_t>(rl) - cum;
+            break;
+          }
+          cum += sm.wu[w];
+        }
+        if (warp == wstar) {
+          uint32_t acc = 0;
+          int found = INT_MAX;
+          for (int j = 0; j < NV; ++j) {
+            const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
+            const int e0 = c.lane_base + j * 32 * L::VW;
+            uint32_t cj = 0;
+            for_vector<BF16>(v, e0, [&](float x, int e) { cj += member(x, e) ? 1u : 0u; });
+            const uint32_t incl = warp_inclusive_scan(cj, lane);
+            const uint32_t stot = __shfl_sync(kFull, incl, 31);
+            if (acc + stot >= rw) {
+              const unsigned bal = __ballot_sync(kFull, acc + incl >= rw);
+              const int lx = __ffs(bal) - 1;
+              int sel = INT_MAX;
+              if (lane == lx) {
+                uint32_t need = rw - (acc + incl - cj);
+                for_vector<BF16>(v, e0, [&](float x, int e) {
+                  if (member(x, e)) {
+                    if (need == 1 && sel == INT_MAX) sel = e;
+                    --need;
+                  }
+                });
+              }
+              found = __shfl_sync(kFull, sel, lx);
+              break;
+            }
+            acc += stot;
+          }
+          if (lane == 0) sm.bi[1] = found == INT_MAX ? INT_MAX : found + 1;
+        }
+        __syncthreads();
+        cut = sm.bi[1];
+      }
+      __syncthreads();
+      return cut;
+    };
+
+    if (topk_row) {
+      // Count radix select of the k-th key over the whole row.
       uint32_t prefix = 0, pmask = 0;
-      uint32_t rem = static_cast<uint32_t>(k);
-#pragma unroll 1
+      unsigned long long rem = static_cast<unsigned long long>(k);
       for (int lvl = 0; lvl < NLEV; ++lvl) {
         const int shift = 24 - 8 * lvl;
-        Exchange& ex = sm.ex[ph & 1];
-        ex.hist.cnt[tid] = 0u;
+        PullBuf& pb = sm.pull[ph & 1];
+        pb.lo[tid] = 0u;
         __syncthreads();
-        for_each<BF16>(d, lane_base, [&](float x, int) {
+        for_each<BF16, NV>(c, [&](float x, int) {
           const uint32_t key = float_key(x);
-          if ((key & pmask) == prefix) atomicAdd(&ex.hist.cnt[(key >> shift) & 0xffu], 1u);
+          if ((key & pmask) == prefix) atomicAdd(&pb.lo[(key >> shift) & 0xffu], 1u);
         });
         cluster_sync();
         ++ph;
-        uint32_t tot = 0;
-        for (uint32_t r = 0; r < csize; ++r) tot += ld_dsmem_u32(dsmem(&ex.hist.cnt[tid], r));
-        uint32_t above;
-        const int b = select_bucket<uint32_t>(tot, rem, sm, &above, tid, lane, warp);
+        pulled = true;
+        unsigned long long tot = 0;
+        for (uint32_t r = 0; r < c.csize; ++r) tot += ld_dsmem_u32(dsmem(&pb.lo[tid], r));
+        unsigned long long above;
+        const int b = select_bucket(tot, rem, sm, &above, tid, lane, warp);
         rem -= above;
         prefix |= static_cast<uint32_t>(b) << shift;
         pmask |= 0xffu << shift;
       }
-      if (BF16 && !(prefix & 0x80000000u)) prefix |= 0xffffu;  // bf16 negatives: low bits all ones
+      if (BF16 && !(prefix & 0x80000000u)) prefix |= 0xffffu;  // bf16 negatives: low bits ones
       tk = key_float(prefix);
       const float tkv = tk;
-      ck = tie_cutoff<BF16>(d, lane_base, [&](float x, int) { return x == tkv; },
-                            static_cast<unsigned long long>(rem), sm, s_slice, ph, crank, csize,
-                            tid, lane, warp);
+      ck = tie_cutoff([&](float x, int) { return x == tkv; }, rem);
     }
-    auto in_k = [&](float x, int e) { return x > tk || (x == tk && e < ck); };
+    const float tkf = tk;
+    const int ckf = ck;
+    auto in_k = [&](float x, int e) { return x > tkf || (x == tkf && e < ckf); };
 
-    // ---- top-p, first mass-histogram level over K (digit = key bits 31..24).
-    const bool use_p = p < 1.0f;
-    if (use_p) {
-      Exchange& ex = sm.ex[ph & 1];
-      ex.hist.mass[tid] = 0ull;
-      __syncthreads();
-      for_each<BF16>(d, lane_base, [&](float x, int e) {
-        if (in_k(x, e)) {
-          const float w = ex2((x - m) * c2);
-          atomicAdd(&ex.hist.mass[float_key(x) >> 24],
-                    static_cast<unsigned long long>(__float2ull_rz(w * kMassScale)));
-        }
-      });
-      cluster_sync();
-      ++ph;
-    }
-
-    // ---- top-p: mass-weighted radix select inside K, then the tie cutoff.
     float tp = tk;
     int cp = ck;
     if (use_p) {
       uint32_t prefix = 0, pmask = 0;
       unsigned long long rem = 0;
-#pragma unroll 1
       for (int lvl = 0; lvl < NLEV; ++lvl) {
         const int shift = 24 - 8 * lvl;
-        Exchange* hx = &sm.ex[(ph - 1) & 1];  // level 0 was filled above
-        if (lvl > 0) {
-          Exchange& ex = sm.ex[ph & 1];
-          ex.hist.mass[tid] = 0ull;
-          __syncthreads();
-          for_each<BF16>(d, lane_base, [&](float x, int e) {
-            const uint32_t key = float_key(x);
-            if ((key & pmask) == prefix && in_k(x, e)) {
-              const float w = ex2((x - m) * c2);
-              atomicAdd(&ex.hist.mass[(key >> shift) & 0xffu],
-                        static_cast<unsigned long long>(__float2ull_rz(w * kMassScale)));
-            }
-          });
-          cluster_sync();
-          ++ph;
-          hx = &ex;
-        }
+        PullBuf& pb = sm.pull[ph & 1];
+        pb.lo[tid] = 0u;
+        pb.hi[tid] = 0u;
+        __syncthreads();
+        for_each<BF16, NV>(c, [&](float x, int e) {
+          const uint32_t key = float_key(x);
+          if ((key & pmask) == prefix && in_k(x, e)) {
+            const uint32_t d = (key >> shift) & 0xffu;
+            atomic_add_u64_split(&pb.lo[d], &pb.hi[d], mass_fx(ex2((x - m) * c2)));
+          }
+        });
+        cluster_sync();
+        ++ph;
+        pulled = true;
         unsigned long long tot = 0;
-        for (uint32_t r = 0; r < csize; ++r) tot += ld_dsmem_u64(dsmem(&hx->hist.mass[tid], r));
+        for (uint32_t r = 0; r < c.csize; ++r) {
+          tot += (static_cast<unsigned long long>(ld_dsmem_u32(dsmem(&pb.hi[tid], r))) << 32) +
+                 ld_dsmem_u32(dsmem(&pb.lo[tid], r));
+        }
         if (lvl == 0) {
-          // Target: keep while (mass before) < p * Z, Z the exact fixed-point total.
+          // Target: keep while (mass before) < p * Z_k, Z_k the exact total.
           const unsigned long long z_fx =
               block_suffix_scan<unsigned long long>(tot, sm.wl, lane, warp);
           if (tid == 0) sm.bl[0] = z_fx;
           __syncthreads();
-          const double target = static_cast<double>(sm.bl[0]) * static_cast<double>(p);
-          rem = static_cast<unsigned long long>(ceil(target));
+          const unsigned long long zt = sm.bl[0];
+          rem = static_cast<unsigned long long>(
+              ceil(static_cast<double>(zt) * static_cast<double>(p)));
           if (rem < 1) rem = 1;
-          if (rem > sm.bl[0]) rem = sm.bl[0];
+          if (rem > zt) rem = zt;
           __syncthreads();
         }
         unsigned long long above;
-        const int b = select_bucket<unsigned long long>(tot, rem, sm, &above, tid, lane, warp);
+        const int b = select_bucket(tot, rem, sm, &above, tid, lane, warp);
         rem -= above;
         prefix |= static_cast<uint32_t>(b) << shift;
         pmask |= 0xffu << shift;
       }
       if (BF16 && !(prefix & 0x80000000u)) prefix |= 0xffffu;
       tp = key_float(prefix);
-      // Members of the threshold group share one weight wt: member j (index
-      // order) is kept iff above + j * wt < target, i.e. j < ceil(rem / wt).
-      const unsigned long long wt =
-          static_cast<unsigned long long>(__float2ull_rz(ex2((tp - m) * c2) * kMassScale));
+      const unsigned long long wt = mass_fx(ex2((tp - m) * c2));
       const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
       const float tpv = tp;
-      cp = tie_cutoff<BF16>(d, lane_base, [&](float x, int e) { return x == tpv && in_k(x, e); },
-                            rp, sm, s_slice, ph, crank, csize, tid, lane, warp);
-      // The cut counted only K members; when both thresholds fall in the same
-      // tie group, members past the top-k cutoff are outside K and stay out.
-      if (tp == tk && ck < cp) cp = ck;
+      cp = tie_cutoff([&](float x, int e) { return x == tpv && in_k(x, e); }, rp);
+      if (tp == tk && ck < cp) cp = ck;  // the cut counted only K members
     }
-    auto in_s = [&](float x, int e) { return x > tp || (x == tp && e < cp); };
+    const float tpf = tp;
+    const int cpf = cp;
+    auto in_s = [&](float x, int e) {
+      return in_k(x, e) && (x > tpf || (x == tpf && e < cpf));
+    };
 
     // ---- inverse CDF over S in vocab order.
     float ts = 0.0f;
-    for_each<BF16>(d, lane_base, [&](float x, int e) {
+    for_each<BF16, NV>(c, [&](float x, int e) {
       if (in_s(x, e)) ts += ex2((x - m) * c2);
     });
     const float wsum = warp_sum(ts);
     if (lane == 0) sm.wf[warp] = wsum;
     __syncthreads();
-    {
-      Exchange& ex = sm.ex[ph & 1];
-      if (tid == 0) {
-        float s = 0.0f;
-        for (int w = 0; w < kWarps; ++w) s += sm.wf[w];
-        ex.f = s;
+    Slot cs = {};
+    for (int w = 0; w < kWarps; ++w) cs.f0 += sm.wf[w];
+    const Slot* s = push_exchange(sm, ph, c, cs);
+    if (warp == 0) {
+      const float t = lane < static_cast<int>(c.csize) ? s[lane].f0 : 0.0f;
+      const float cum = warp_inclusive_scan(t, lane);
+      const float Z = __shfl_sync(kFull, cum, 31);
+      const float target = u * Z;
+      const unsigned hit = __ballot_sync(kFull, lane < static_cast<int>(c.csize) && target < cum);
+      int rstar;
+      float tloc;
+      if (hit != 0) {
+        rstar = __ffs(hit) - 1;
+        tloc = target - __shfl_sync(kFull, cum - t, rstar);
+      } else {
+        const unsigned pos = __ballot_sync(kFull, lane < static_cast<int>(c.csize) && t > 0.0f);
+        rstar = pos ? 31 - __clz(pos) : 0;
+        tloc = INFINITY;  // take the last kept token with mass
       }
-      cluster_sync();
-      ++ph;
-      if (warp == 0) {
-        const float t = lane < static_cast<int>(csize) ? ld_dsmem_f32(dsmem(&ex.f, lane)) : 0.0f;
-        const float cum = warp_inclusive_scan(t, lane);
-        const float Z = __shfl_sync(kFull, cum, 31);
-        const float target = u * Z;
-        const unsigned hit = __ballot_sync(kFull, lane < static_cast<int>(csize) && target < cum);
-        int rstar;
-        float tloc;
-        if (hit != 0) {
-          rstar = __ffs(hit) - 1;
-          tloc = target - __shfl_sync(kFull, cum - t, rstar);
-        } else {
-          const unsigned pos = __ballot_sync(kFull, lane < static_cast<int>(csize) && t > 0.0f);
-          rstar = pos ? 31 - __clz(pos) : 0;
-          tloc = INFINITY;  // take the last kept token with mass
-        }
-        if (lane == 0) {
-          sm.bi[0] = rstar;
-          sm.bf[0] = tloc;
-          sm.bf[1] = Z;
-        }
+      if (lane == 0) {
+        sm.bi[0] = rstar;
+        sm.bf[0] = tloc;
+        sm.bf[1] = Z;
       }
-      __syncthreads();
     }
+    __syncthreads();
     const int rstar = sm.bi[0];
     const float tloc = sm.bf[0];
     const float zs_all = sm.bf[1];
-    if (crank == static_cast<uint32_t>(rstar)) {
-      // Warp holding the crossing (sequential cumulative over warp sums).
+    if (c.crank == static_cast<uint32_t>(rstar)) {
       int wstar = -1;
       float tw = INFINITY;
       float cw = 0.0f;
@@ -675,14 +1149,12 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
         tw = INFINITY;
       }
       if (warp == wstar) {
-        dump_slice(d, s_slice, lane);
         float acc = 0.0f;
         int found = -1;
         int lastpos = -1;
-#pragma unroll 1
         for (int j = 0; j < NV; ++j) {
-          const uint4 v = s_slice[j * 32 + lane];
-          const int e0 = lane_base + j * 32 * L::VW;
+          const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
+          const int e0 = c.lane_base + j * 32 * L::VW;
           float lj = 0.0f;
           int llast = -1;
           for_vector<BF16>(v, e0, [&](float x, int e) {
@@ -720,14 +1192,16 @@ __global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams 
         if (lane == 0) emit_token(P, row, found, found < 0 ? (st | kStNonFinite) : st);
       }
     }
-    if (P.probs_out != nullptr) {
-      float* q = P.probs_out + static_cast<size_t>(row) * V;
+    if (q_row != nullptr) {
       const float inv = 1.0f / zs_all;
-      for_each<BF16>(d, lane_base, [&](float x, int e) {
-        if (e < V) q[e] = in_s(x, e) ? ex2((x - m) * c2) * inv : 0.0f;
+      for_each<BF16, NV>(c, [&](float x, int e) {
+        if (e < V) q_row[e] = in_s(x, e) ? ex2((x - m) * c2) * inv : 0.0f;
       });
     }
-    cluster_sync();
+    // Other CTAs read this CTA's histograms after the barriers above; stay
+    // until everyone is past them.
+    if (pulled) cluster_sync();
+    leave();
   }
 }
 

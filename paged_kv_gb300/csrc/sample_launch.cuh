@@ -10,23 +10,44 @@
 
 namespace pkv {
 
-template <bool BF16, int NV, bool VEC, bool AG>
-cudaError_t launch_one(const SampleParams& P, int C, cudaStream_t stream) {
-  auto kern = sample_kernel<BF16, NV, VEC, AG>;
-  if (C > 8) {
-    // Clusters of 9..16 CTAs are a non-portable size; opt in once per kernel.
-    static bool enabled = false;
-    if (!enabled) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-      enabled = true;
-    }
+// Candidate-list capacity: as large as fits next to the slice while keeping
+// three (else two, else one) CTAs per SM, at most 4096 entries.
+inline int list_capacity(size_t slice_bytes) {
+  constexpr size_t kSmPerSm = 228 * 1024;
+  constexpr size_t kPerCtaReserved = 1024;
+  for (int per_sm = 3; per_sm >= 1; --per_sm) {
+    const size_t budget = kSmPerSm / per_sm;
+    const size_t used = kPerCtaReserved + sizeof(SampleSmem) + slice_bytes;
+    if (budget <= used) continue;
+    size_t cap = (budget - used) / 8;
+    if (cap > 4096) cap = 4096;
+    cap = cap / 256 * 256;
+    if (cap >= 1024) return static_cast<int>(cap);
   }
+  return 1024;
+}
+
+template <bool BF16, int NV, bool TMA, bool AG>
+cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
+  auto kern = sample_kernel<BF16, NV, TMA, AG>;
+  constexpr size_t kSliceBytes = static_cast<size_t>(kThreads) * NV * 16;
+  static const int cap = list_capacity(kSliceBytes);
+  const size_t dyn = kSliceBytes + static_cast<size_t>(cap) * 8;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(dyn));
+    if (e != cudaSuccess) return e;
+    // Clusters of 9..16 CTAs are a non-portable size; opt in once per kernel.
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  P.list_cap = cap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(C), static_cast<unsigned>(P.B), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -23,6 +23,7 @@ struct SampleParams {
   float* probs_out;          // [B, V] or nullptr
   int32_t* status;           // device status word or nullptr
   int cta_chunk;             // elements owned by one CTA of a row's cluster
+  int list_cap;              // candidate-list entries in the leader's shared memory
 };
 
 }  // namespace pkv
