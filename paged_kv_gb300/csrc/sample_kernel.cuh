@@ -460,72 +460,37 @@ __device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&
 
 // ----------------------------------------------------------------- the kernel
 
-template <bool BF16, int NV, bool TMA, bool ALL_GREEDY>
-__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams P) {
+// One row of the batch; this CTA's slice of the row is in shared memory at
+// s_vec.  Every exit is uniform across the cluster and comes after the row's
+// last cluster barrier.  The CTA that collects and finishes the candidate
+// list ("leader") rotates with the row.
+template <bool BF16, int NV, bool ALL_GREEDY>
+__device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm,
+                                           const uint4* s_vec, float* l_val, int32_t* l_idx,
+                                           int row, int& ph, int st) {
   using L = Layout<BF16>;
   constexpr int CHUNK = kThreads * NV * L::VW;  // elements per CTA
   constexpr int NLEV = BF16 ? 2 : 4;            // 8-bit radix levels (fallback)
-  __shared__ SampleSmem sm;
-  extern __shared__ __align__(128) unsigned char dyn[];
-  uint4* s_vec = reinterpret_cast<uint4*>(dyn);
-  float* l_val = reinterpret_cast<float*>(dyn + CHUNK * L::ELT);
-  int32_t* l_idx = reinterpret_cast<int32_t*>(l_val + P.list_cap);
-
   Ctx c;
   c.tid = threadIdx.x;
   c.lane = c.tid & 31;
   c.warp = c.tid >> 5;
   c.crank = cluster_rank();
   c.csize = cluster_size();
-  c.row = blockIdx.y;
+  c.row = row;
   c.V = P.V;
   c.sv = s_vec;
   const int V = P.V;
-  const int row = c.row;
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   const int cta_begin = static_cast<int>(c.crank) * CHUNK;
   c.lane_base = cta_begin + ((warp * NV) * 32 + lane) * L::VW;
-  const int nvalid = max(0, min(CHUNK, V - cta_begin));
+  const bool has_pad = cta_begin + CHUNK > V;  // this slice reaches past the row end
+  const uint32_t leader = static_cast<uint32_t>(row) % c.csize;
 
-  // ---- bring the slice into shared memory
-  const char* gsrc = static_cast<const char*>(P.logits) +
-                     (static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) +
-                      static_cast<size_t>(cta_begin)) * L::ELT;
-  if constexpr (TMA) {
-    if (tid == 0) {
-      mbar_init(&sm.mbar, 1);
-      fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const uint32_t bytes = static_cast<uint32_t>(nvalid) * L::ELT;
-      mbar_arrive_expect_tx(&sm.mbar, bytes);
-      for (uint32_t off = 0; off < bytes; off += 16384u) {
-        bulk_copy_g2s(dyn + off, gsrc + off, min(16384u, bytes - off), &sm.mbar);
-      }
-    }
-  } else {
-    for (int e = tid; e < nvalid; e += kThreads) {
-      if constexpr (BF16) {
-        reinterpret_cast<uint16_t*>(dyn)[e] = reinterpret_cast<const uint16_t*>(gsrc)[e];
-      } else {
-        reinterpret_cast<uint32_t*>(dyn)[e] = reinterpret_cast<const uint32_t*>(gsrc)[e];
-      }
-    }
-  }
-  for (int e = nvalid + tid; e < CHUNK; e += kThreads) {  // padding: -inf
-    if constexpr (BF16) {
-      reinterpret_cast<uint16_t*>(dyn)[e] = 0xff80u;
-    } else {
-      reinterpret_cast<uint32_t*>(dyn)[e] = 0xff800000u;
-    }
-  }
-
-  // Row parameters (Sampler.prepare's normalisation), read while the copy runs.
+  // Row parameters (Sampler.prepare's normalisation).
   const bool greedy = ALL_GREEDY || !(P.temperature[row] > 0.0f);
   float T = 1.0f, p = 1.0f, u = 0.0f;
   int k = V;
-  int st = 0;
   if (!greedy) {
     T = fmaxf(P.temperature[row], 1e-6f);
     k = P.top_k != nullptr ? P.top_k[row] : -1;
@@ -538,17 +503,6 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
     }
   }
   const float c2 = 1.4426950408889634f / T;  // log2(e) / T
-  bool copy_ok = true;
-  if constexpr (TMA) copy_ok = mbar_wait_bounded(&sm.mbar, 0, kWaitIters);
-  const bool timed_out = __syncthreads_or(!copy_ok) != 0;
-  if (timed_out) st |= kStTimeout;
-  // On a timeout the kernel still runs every barrier (with whatever the slice
-  // holds) and waits once more for its copy before the CTA exits.
-  auto leave = [&]() {
-    if constexpr (TMA) {
-      if (timed_out && tid == 0) mbar_wait_bounded(&sm.mbar, 0, kWaitIters);
-    }
-  };
 
   // ---- phase 1: thread maxima, row maximum (NaN-propagating), argmax.
   float tmax = -INFINITY;
@@ -611,7 +565,6 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
     }
   }
   __syncthreads();
-  int ph = 0;
   Slot mine = {};
   {
     float v = sm.wf[0];
@@ -684,22 +637,20 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
 
   if (greedy) {
     const int tok = nan_row ? -1 : gidx;
-    if (c.crank == 0 && tid == 0) emit_token(P, row, tok, (nan_row ? kStNonFinite : 0) | st);
+    if (c.crank == leader && tid == 0) emit_token(P, row, tok, (nan_row ? kStNonFinite : 0) | st);
     if (q_row != nullptr) {
       for_each<BF16, NV>(c, [&](float, int e) {
         if (e < V) q_row[e] = (e == tok) ? 1.0f : 0.0f;
       });
     }
-    leave();
     return;
   }
 
   if constexpr (!ALL_GREEDY) {
     if (nan_row || m == INFINITY || m == -INFINITY) {
       const int est = (m == -INFINITY && !nan_row) ? kStAllNegInf : kStNonFinite;
-      if (c.crank == 0 && tid == 0) emit_token(P, row, -1, est | st);
+      if (c.crank == leader && tid == 0) emit_token(P, row, -1, est | st);
       write_zero_probs();
-      leave();
       return;
     }
     const bool use_p = p < 1.0f;
@@ -760,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
       uint32_t cnt = 0;
       unsigned long long mfx = 0;
       for_each<BF16, NV>(c, [&](float x, int e) {
-        if (x >= theta && e < V) {
+        if (x >= theta && (!has_pad || e < V)) {
           ++cnt;
           if (!topk_row) mfx += mass_fx(ex2((x - m) * c2));
         }
@@ -782,19 +733,19 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
       if (static_cast<int>(ncta) <= R) {
         // Ordered write: warp region, then vector by vector in lane order.
         const uint32_t base = static_cast<uint32_t>(c.crank) * R + woff;
-        const uint32_t a_val = dsmem(l_val, 0);
-        const uint32_t a_idx = dsmem(l_idx, 0);
+        const uint32_t a_val = dsmem(l_val, leader);
+        const uint32_t a_idx = dsmem(l_idx, leader);
         uint32_t acc = 0;
         for (int j = 0; j < NV; ++j) {
           const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
           const int e0 = c.lane_base + j * 32 * L::VW;
           uint32_t cj = 0;
-          for_vector<BF16>(v, e0, [&](float x, int e) { cj += (x >= theta && e < V) ? 1u : 0u; });
+          for_vector<BF16>(v, e0, [&](float x, int e) { cj += (x >= theta && (!has_pad || e < V)) ? 1u : 0u; });
           if (__ballot_sync(kFull, cj != 0) == 0) continue;
           const uint32_t incl = warp_inclusive_scan(cj, lane);
           uint32_t pos = base + acc + incl - cj;
           for_vector<BF16>(v, e0, [&](float x, int e) {
-            if (x >= theta && e < V) {
+            if (x >= theta && (!has_pad || e < V)) {
               st_dsmem_f32(a_val + 4u * pos, x);
               st_dsmem_u32(a_idx + 4u * pos, static_cast<uint32_t>(e));
               ++pos;
@@ -825,10 +776,7 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
         if (lmass < target_fx) over = 1;
       }
       if (over == 0) {
-        if (c.crank != 0) {
-          leave();
-          return;
-        }
+        if (c.crank != leader) return;
         // ---- leader: pack the regions, then select and draw on the list.
         int n = 0;
         for (uint32_t r = 0; r < c.csize; ++r) n += static_cast<int>(s[r].u0);
@@ -922,7 +870,6 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
             if (in_s(i)) q_row[l_idx[i]] = w_of(i) * inv;
           }
         }
-        leave();
         return;
       }
       // Over capacity: every CTA falls through to the on-chip fallback.
@@ -1198,10 +1145,117 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
         if (e < V) q_row[e] = in_s(x, e) ? ex2((x - m) * c2) * inv : 0.0f;
       });
     }
-    // Other CTAs read this CTA's histograms after the barriers above; stay
-    // until everyone is past them.
-    if (pulled) cluster_sync();
-    leave();
+    // Histograms other CTAs pulled from this one are not rewritten before the
+    // next row's first barrier, which they reach only after their reads.
+    (void)pulled;
+  }
+}
+
+
+// Persistent kernel: cluster g (blockIdx.y) handles rows g, g + G, g + 2G, ...
+// Each CTA streams its slice of successive rows through a two-stage ring in
+// shared memory: while one row is processed, the bulk copy of the row after
+// next lands in the other stage, so HBM reads continue across the cluster
+// barriers.  One thread waits on each stage's mbarrier (bounded); the others
+// wait at a CTA barrier.
+template <bool BF16, int NV, bool TMA, bool ALL_GREEDY>
+__global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams P) {
+  using L = Layout<BF16>;
+  constexpr int CHUNK = kThreads * NV * L::VW;
+  constexpr uint32_t kSliceBytes = static_cast<uint32_t>(CHUNK) * L::ELT;
+  __shared__ SampleSmem sm;
+  __shared__ uint64_t full[2];
+  extern __shared__ __align__(128) unsigned char dyn[];
+  unsigned char* stage0 = dyn;
+  unsigned char* stage1 = dyn + kSliceBytes;
+  float* l_val = reinterpret_cast<float*>(dyn + 2 * kSliceBytes);
+  int32_t* l_idx = reinterpret_cast<int32_t*>(l_val + P.list_cap);
+  const int tid = threadIdx.x;
+  const int V = P.V;
+  const int G = static_cast<int>(gridDim.y);
+  const int cta_begin = static_cast<int>(cluster_rank()) * CHUNK;
+  const int nvalid = max(0, min(CHUNK, V - cta_begin));
+  const uint32_t bytes = static_cast<uint32_t>(nvalid) * L::ELT;
+  auto src_of = [&](int row) {
+    return static_cast<const char*>(P.logits) +
+           (static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) +
+            static_cast<size_t>(cta_begin)) * L::ELT;
+  };
+  // Padding past the row end is -inf in both stages (copies never touch it).
+  for (int e = nvalid + tid; e < CHUNK; e += kThreads) {
+    if constexpr (BF16) {
+      reinterpret_cast<uint16_t*>(stage0)[e] = 0xff80u;
+      reinterpret_cast<uint16_t*>(stage1)[e] = 0xff80u;
+    } else {
+      reinterpret_cast<uint32_t*>(stage0)[e] = 0xff800000u;
+      reinterpret_cast<uint32_t*>(stage1)[e] = 0xff800000u;
+    }
+  }
+  auto issue = [&](int s, int row) {
+    unsigned char* dst = s == 0 ? stage0 : stage1;
+    const char* g = src_of(row);
+    mbar_arrive_expect_tx(&full[s], bytes);
+    for (uint32_t off = 0; off < bytes; off += 16384u) {
+      bulk_copy_g2s(dst + off, g + off, min(16384u, bytes - off), &full[s]);
+    }
+  };
+  bool pending0 = false, pending1 = false;  // thread 0: a copy whose wait timed out
+  if constexpr (TMA) {
+    if (tid == 0) {
+      mbar_init(&full[0], 1);
+      mbar_init(&full[1], 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      if (static_cast<int>(blockIdx.y) < P.B) issue(0, blockIdx.y);
+      if (static_cast<int>(blockIdx.y) + G < P.B) issue(1, blockIdx.y + G);
+    }
+  }
+  int ph = 0;
+  for (int it = 0;; ++it) {
+    const int row = static_cast<int>(blockIdx.y) + it * G;
+    if (row >= P.B) break;
+    const int s = it & 1;
+    unsigned char* cur = s == 0 ? stage0 : stage1;
+    int st = 0;
+    if constexpr (TMA) {
+      if (tid == 0) {
+        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(it >> 1) & 1u, kWaitIters);
+        if (s == 0) pending0 = !ok; else pending1 = !ok;
+        sm.bu[3] = ok ? 0u : 1u;
+      }
+      __syncthreads();
+      if (sm.bu[3] != 0u) st |= kStTimeout;
+    } else {
+      const char* g = src_of(row);
+      for (int e = tid; e < nvalid; e += kThreads) {
+        if constexpr (BF16) {
+          reinterpret_cast<uint16_t*>(cur)[e] = reinterpret_cast<const uint16_t*>(g)[e];
+        } else {
+          reinterpret_cast<uint32_t*>(cur)[e] = reinterpret_cast<const uint32_t*>(g)[e];
+        }
+      }
+      __syncthreads();
+    }
+    sample_row<BF16, NV, ALL_GREEDY>(P, sm, reinterpret_cast<const uint4*>(cur), l_val, l_idx,
+                                     row, ph, st);
+    __syncthreads();  // the whole CTA is done with this stage
+    if constexpr (TMA) {
+      const int next = row + 2 * G;
+      if (tid == 0 && next < P.B) {
+        fence_proxy_async_smem();
+        issue(s, next);
+      }
+    }
+  }
+  // No CTA leaves while another may still read its shared memory.
+  cluster_sync();
+  if constexpr (TMA) {
+    if (tid == 0) {
+      if (pending0) mbar_wait_bounded(&full[0], 0u, kWaitIters);
+      if (pending1) mbar_wait_bounded(&full[1], 0u, kWaitIters);
+    }
   }
 }
 
