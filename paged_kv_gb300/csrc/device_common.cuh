@@ -33,6 +33,17 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split form of the cluster barrier: arrive (release) now, wait (acquire)
+// later.  A CTA that has arrived may exit without waiting; waiting CTAs then
+// see everything it wrote before arriving.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Shared-window address of `p` (a __shared__ object of this CTA) as seen in
 // CTA `rank` of the same cluster.
 __device__ __forceinline__ uint32_t dsmem(const void* p, uint32_t rank) {

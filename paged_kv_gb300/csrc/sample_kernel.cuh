@@ -52,14 +52,12 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;
 constexpr int kMaxClusterCtas = 16;
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
-constexpr uint32_t kWaitIters = 1u << 22;       // bound on mbarrier polls
 
 constexpr int kStNonFinite = 1;
 constexpr int kStAllNegInf = 2;
 constexpr int kStRowOOB = 4;
 constexpr int kStColOOB = 8;
 constexpr int kStBadUniform = 16;
-constexpr int kStTimeout = 64;
 
 // One CTA's values for one exchange phase, pushed into every CTA.
 struct Slot {
@@ -81,6 +79,8 @@ struct PullBuf {
 
 struct SampleSmem {
   Slot push[2][kMaxClusterCtas];
+  Slot gather[kMaxClusterCtas];  // collected by the leader only
+  uint32_t cnt[kMaxClusterCtas];
   PullBuf pull[2];
   unsigned long long scan[kBuckets];
   uint32_t hlo[kBuckets];  // CTA-local histogram (list selects)
@@ -90,11 +90,11 @@ struct SampleSmem {
   uint32_t wu[kWarps];
   int32_t wi[kWarps];
   float wt[kWarps];
+  float wz[kWarps];
   float bf[4];
   int32_t bi[4];
   uint32_t bu[4];
   unsigned long long bl[4];
-  uint64_t mbar;
 };
 
 // ----------------------------------------------------------------- element access
@@ -460,37 +460,310 @@ __device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&
 
 // ----------------------------------------------------------------- the kernel
 
-// One row of the batch; this CTA's slice of the row is in shared memory at
-// s_vec.  Every exit is uniform across the cluster and comes after the row's
-// last cluster barrier.  The CTA that collects and finishes the candidate
-// list ("leader") rotates with the row.
-template <bool BF16, int NV, bool ALL_GREEDY>
-__device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm,
-                                           const uint4* s_vec, float* l_val, int32_t* l_idx,
-                                           int row, int& ph, int st) {
+// ----------------------------------------------------------------- leader finish
+
+// The leader CTA holds every candidate of the row in its list, region r
+// (entries r*R .. r*R + cnt[r]) coming from CTA r, each region in index
+// order.  Packs the regions, then finishes exactly on the list: top-k (count
+// select, ties by index), top-p inside K (mass select on 2^-40 fixed-point
+// weights; target_fx is given for rows without top-k), renormalisation and
+// the inverse-CDF draw.  Emits the token and, if asked, the probabilities.
+__device__ __forceinline__ void leader_finish(const SampleParams& P, SampleSmem& sm, const Ctx& c,
+                                              float* l_val, int32_t* l_idx, int R, int row,
+                                              bool topk_row, int k, bool use_p, float p,
+                                              unsigned long long target_fx, float m, float c2,
+                                              float u, int st, float* q_row) {
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  int n = 0;
+  for (uint32_t r = 0; r < c.csize; ++r) n += static_cast<int>(sm.cnt[r]);
+  {
+    // Packed index i comes from region r at offset i - (earlier counts),
+    // never from a position below i: read, barrier, write.
+    constexpr int kMovePer = 16;
+    float mv[kMovePer];
+    int mi[kMovePer];
+    for (int b0 = 0; b0 < n; b0 += kThreads * kMovePer) {
+#pragma unroll
+      for (int q = 0; q < kMovePer; ++q) {
+        const int i = b0 + q * kThreads + tid;
+        if (i < n) {
+          int r = 0, off = i;
+          while (off >= static_cast<int>(sm.cnt[r])) {
+            off -= static_cast<int>(sm.cnt[r]);
+            ++r;
+          }
+          mv[q] = l_val[r * R + off];
+          mi[q] = l_idx[r * R + off];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < kMovePer; ++q) {
+        const int i = b0 + q * kThreads + tid;
+        if (i < n) {
+          l_val[i] = mv[q];
+          l_idx[i] = mi[q];
+        }
+      }
+      __syncthreads();
+    }
+  }
+  int cut_k = n;
+  float tk = -INFINITY;
+  if (topk_row) {
+    unsigned long long rk;
+    tk = list_select<false>(l_val, n, [](int) { return true; }, [](int) { return 1ull; },
+                            static_cast<unsigned long long>(k), sm, c, &rk);
+    const float tkv = tk;
+    cut_k = list_tie_cut(n, [&](int i) { return l_val[i] == tkv; }, rk, sm, c);
+  }
+  const float tkv = tk;
+  const int ckv = cut_k;
+  auto in_k = [&](int i) { return l_val[i] > tkv || (l_val[i] == tkv && i < ckv); };
+  auto w_of = [&](int i) { return ex2((l_val[i] - m) * c2); };
+  float tp = tk;
+  int cut_p = cut_k;
+  if (use_p) {
+    if (topk_row) {
+      unsigned long long zfx = 0;
+      for (int i = tid; i < n; i += kThreads) {
+        if (in_k(i)) zfx += mass_fx(w_of(i));
+      }
+      zfx = warp_sum(zfx);
+      if (lane == 0) sm.wl[warp] = zfx;
+      __syncthreads();
+      unsigned long long z = 0;
+      for (int w = 0; w < kWarps; ++w) z += sm.wl[w];
+      __syncthreads();
+      const double t = static_cast<double>(z) * static_cast<double>(p);
+      target_fx = static_cast<unsigned long long>(ceil(t));
+      if (target_fx < 1) target_fx = 1;
+      if (target_fx > z) target_fx = z;
+    }
+    unsigned long long rem;
+    tp = list_select<true>(l_val, n, in_k, [&](int i) { return mass_fx(w_of(i)); }, target_fx, sm,
+                           c, &rem);
+    // Members of the threshold group share one weight wt: member j (index
+    // order) is kept iff above + j * wt < target, i.e. j < ceil(rem / wt).
+    const unsigned long long wt = mass_fx(ex2((tp - m) * c2));
+    const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
+    const float tpv = tp;
+    cut_p = list_tie_cut(n, [&](int i) { return l_val[i] == tpv && in_k(i); }, rp, sm, c);
+  }
+  const float tpv = tp;
+  const int cpv = cut_p;
+  auto in_s = [&](int i) { return in_k(i) && (l_val[i] > tpv || (l_val[i] == tpv && i < cpv)); };
+  float zs;
+  const int tok = list_draw(l_idx, n, in_s, w_of, u, sm, c, &zs);
+  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
+  if (q_row != nullptr) {
+    const float inv = 1.0f / zs;
+    for (int i = tid; i < n; i += kThreads) {
+      if (in_s(i)) q_row[l_idx[i]] = w_of(i) * inv;
+    }
+  }
+}
+
+// ----------------------------------------------------------------- CTA-local selects
+
+// Among this CTA's elements with member(x, e), the first r in index order:
+// returns the element-index cutoff (members with e < cutoff), INT_MAX if there
+// are no more than r members.  CTA barriers only.
+template <bool BF16, int NV, typename M>
+__device__ __forceinline__ int cta_tie_cut(const Ctx& c, SampleSmem& sm, M&& member,
+                                           unsigned long long r) {
+  using L = Layout<BF16>;
+  const int lane = c.lane, warp = c.warp;
+  uint32_t cnt = 0;
+  for_each<BF16, NV>(c, [&](float x, int e) { cnt += member(x, e) ? 1u : 0u; });
+  const uint32_t wc = __reduce_add_sync(kFull, cnt);
+  if (lane == 0) sm.wu[warp] = wc;
+  __syncthreads();
+  unsigned long long cum = 0;
+  int wstar = -1;
+  uint32_t rw = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (wstar < 0 && cum + sm.wu[w] >= r) {
+      wstar = w;
+      rw = static_cast<uint32_t>(r - cum);
+    }
+    cum += sm.wu[w];
+  }
+  if (r == 0) wstar = -2;
+  if (c.tid == 0) sm.bi[1] = wstar == -2 ? INT_MIN : INT_MAX;
+  __syncthreads();
+  if (warp == wstar) {
+    uint32_t acc = 0;
+    int found = INT_MAX;
+    for (int j = 0; j < NV; ++j) {
+      const uint4 v = c.sv[(warp * NV + j) * 32 + lane];
+      const int e0 = c.lane_base + j * 32 * L::VW;
+      uint32_t cj = 0;
+      for_vector<BF16>(v, e0, [&](float x, int e) { cj += member(x, e) ? 1u : 0u; });
+      const uint32_t incl = warp_inclusive_scan(cj, lane);
+      const uint32_t stot = __shfl_sync(kFull, incl, 31);
+      if (acc + stot >= rw) {
+        const unsigned bal = __ballot_sync(kFull, acc + incl >= rw);
+        const int lx = __ffs(bal) - 1;
+        int sel = INT_MAX;
+        if (lane == lx) {
+          uint32_t need = rw - (acc + incl - cj);
+          for_vector<BF16>(v, e0, [&](float x, int e) {
+            if (member(x, e)) {
+              if (need == 1 && sel == INT_MAX) sel = e;
+              --need;
+            }
+          });
+        }
+        found = __shfl_sync(kFull, sel, lx);
+        break;
+      }
+      acc += stot;
+    }
+    if (lane == 0) sm.bi[1] = found == INT_MAX ? INT_MAX : found + 1;
+  }
+  __syncthreads();
+  const int cut = sm.bi[1];
+  __syncthreads();
+  return cut;
+}
+
+// Exact top-k of this CTA's elements with keep(x, e), by (value desc, index
+// asc): returns t and *cut such that the top-k are {keep, x > t} and
+// {keep, x == t, e < cut}.  Radix select over keys with 32-bit shared atomics.
+template <bool BF16, int NV, typename K>
+__device__ __forceinline__ float cta_select_topk(const Ctx& c, SampleSmem& sm, K&& keep,
+                                                 unsigned long long k, int* cut) {
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  for_each<BF16, NV>(c, [&](float x, int e) {
+    if (keep(x, e)) {
+      const uint32_t key = float_key(x);
+      lo = min(lo, key);
+      hi = max(hi, key);
+    }
+  });
+  lo = __reduce_min_sync(kFull, lo);
+  hi = __reduce_max_sync(kFull, hi);
+  if (c.lane == 0) {
+    sm.wu[c.warp] = lo;
+    sm.wi[c.warp] = static_cast<int32_t>(hi);
+  }
+  __syncthreads();
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int w = 0; w < kWarps; ++w) {
+    kmin = min(kmin, sm.wu[w]);
+    kmax = max(kmax, static_cast<uint32_t>(sm.wi[w]));
+  }
+  __syncthreads();
+  unsigned long long rem = k;
+  uint32_t prefix = kmin;
+  if (kmin != kmax) {
+    const int top = 31 - __clz(kmin ^ kmax);
+    prefix = static_cast<uint32_t>(static_cast<unsigned long long>(kmin) & ~((2ull << top) - 1ull));
+    for (int hb = top; hb >= 0; hb -= 8) {
+      const int lb = hb >= 7 ? hb - 7 : 0;
+      const uint32_t dmask = (1u << (hb - lb + 1)) - 1u;
+      const uint32_t amask = static_cast<uint32_t>(~((2ull << hb) - 1ull));
+      sm.hlo[c.tid] = 0u;
+      __syncthreads();
+      for_each<BF16, NV>(c, [&](float x, int e) {
+        if (!keep(x, e)) return;
+        const uint32_t key = float_key(x);
+        if ((key & amask) == (prefix & amask)) atomicAdd(&sm.hlo[(key >> lb) & dmask], 1u);
+      });
+      __syncthreads();
+      unsigned long long above;
+      const int b = select_bucket(sm.hlo[c.tid], rem, sm, &above, c.tid, c.lane, c.warp);
+      rem -= above;
+      prefix |= static_cast<uint32_t>(b) << lb;
+    }
+  }
+  const float t = key_float(prefix);
+  *cut = cta_tie_cut<BF16, NV>(c, sm, [&](float x, int e) { return keep(x, e) && x == t; }, rem);
+  return t;
+}
+
+// ----------------------------------------------------------------- the kernel
+
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ void load_slice(const SampleParams& P, int row, int lane_base,
+                                           uint32_t (&d)[NV][4]) {
+  using L = Layout<BF16>;
+  const char* rp = static_cast<const char*>(P.logits) +
+                   static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) * L::ELT;
+  const int V = P.V;
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    const int e0 = lane_base + j * 32 * L::VW;
+    if (VEC && e0 + L::VW <= V) {
+      const uint4 v = ld_stream_v4(rp + static_cast<size_t>(e0) * L::ELT);
+      d[j][0] = v.x;
+      d[j][1] = v.y;
+      d[j][2] = v.z;
+      d[j][3] = v.w;
+    } else {
+      // Row tail or unaligned row: element loads, -inf past the end.
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (BF16) {
+          const int e = e0 + 2 * q;
+          const uint32_t lo = e < V ? reinterpret_cast<const uint16_t*>(rp)[e] : 0xff80u;
+          const uint32_t hi = e + 1 < V ? reinterpret_cast<const uint16_t*>(rp)[e + 1] : 0xff80u;
+          d[j][q] = lo | (hi << 16);
+        } else {
+          const int e = e0 + q;
+          d[j][q] = e < V ? reinterpret_cast<const uint32_t*>(rp)[e] : 0xff800000u;
+        }
+      }
+    }
+  }
+}
+
+// One cluster of C CTAs per row (grid C x B).  CTA r holds elements
+// [r*chunk, (r+1)*chunk) of its row: 16-byte loads into registers, copied
+// to shared memory when later passes need them.  Cross-CTA traffic is pushed
+// into the receiving CTA's shared memory.  The leader (rank 0) is the only
+// CTA that waits when it merely collects: the others arrive at the cluster
+// barrier and exit.
+template <bool BF16, int NV, bool VEC, bool ALL_GREEDY>
+__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams P) {
   using L = Layout<BF16>;
   constexpr int CHUNK = kThreads * NV * L::VW;  // elements per CTA
   constexpr int NLEV = BF16 ? 2 : 4;            // 8-bit radix levels (fallback)
+  constexpr int kWarpSpan = 32 * NV * L::VW;    // elements per warp
+  __shared__ SampleSmem sm;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  uint4* s_vec = reinterpret_cast<uint4*>(dyn);
+  float* l_val = reinterpret_cast<float*>(dyn + CHUNK * L::ELT);
+  int32_t* l_idx = reinterpret_cast<int32_t*>(l_val + P.list_cap);
+
+  // Every CTA of the cluster must have started before anyone stores into its
+  // shared memory: arrive now, wait just before the first remote store.
+  cluster_arrive();
+
   Ctx c;
   c.tid = threadIdx.x;
   c.lane = c.tid & 31;
   c.warp = c.tid >> 5;
   c.crank = cluster_rank();
   c.csize = cluster_size();
-  c.row = row;
+  c.row = blockIdx.y;
   c.V = P.V;
   c.sv = s_vec;
   const int V = P.V;
+  const int row = c.row;
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   const int cta_begin = static_cast<int>(c.crank) * CHUNK;
   c.lane_base = cta_begin + ((warp * NV) * 32 + lane) * L::VW;
   const bool has_pad = cta_begin + CHUNK > V;  // this slice reaches past the row end
-  const uint32_t leader = static_cast<uint32_t>(row) % c.csize;
+  constexpr uint32_t leader = 0;
+  const int R = P.list_cap / static_cast<int>(c.csize);  // list entries per CTA region
 
   // Row parameters (Sampler.prepare's normalisation).
   const bool greedy = ALL_GREEDY || !(P.temperature[row] > 0.0f);
   float T = 1.0f, p = 1.0f, u = 0.0f;
   int k = V;
+  int st = 0;
   if (!greedy) {
     T = fmaxf(P.temperature[row], 1e-6f);
     k = P.top_k != nullptr ? P.top_k[row] : -1;
@@ -503,14 +776,17 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
     }
   }
   const float c2 = 1.4426950408889634f / T;  // log2(e) / T
+  float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
 
-  // ---- phase 1: thread maxima, row maximum (NaN-propagating), argmax.
+  // ---- load the slice and take thread maxima (NaN-propagating).
+  uint32_t d[NV][4];
+  load_slice<BF16, NV, VEC>(P, row, c.lane_base, d);
   float tmax = -INFINITY;
   int tidx = INT_MAX;
   bool nan = false;
-#pragma unroll 2
+#pragma unroll
   for (int j = 0; j < NV; ++j) {
-    const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
+    const uint4 v = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
     const float vm = vector_max<BF16>(v);
     if (vm != vm) {
       nan = true;
@@ -527,24 +803,18 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
       }
     }
   }
-  const float thread_max = tmax;
-  // theta from thread maxima for top-k rows: the k_w-th largest thread
-  // maximum of every warp whose elements all lie inside the row (W_full such
-  // warps, k_w = ceil(k / W_full)), so at least k elements are >= theta.
-  // Warps that reach past the row end do not constrain theta.
-  constexpr int kWarpSpan = 32 * NV * L::VW;
-  float theta_w = -INFINITY;
-  const bool topk_row = !greedy && k < V;
-  if (topk_row) {
-    const int w_full = V / kWarpSpan;
-    const int kw = w_full > 0 ? (k + w_full - 1) / w_full : INT_MAX;
-    const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
-    if (kw <= 32) {
-      const float sorted = warp_sort_desc(thread_max, lane);
-      theta_w = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
+  if (q_row != nullptr) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      const uint4 v = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
+      for_vector<BF16>(v, c.lane_base + j * 32 * L::VW, [&](float, int e) {
+        if (e < V) q_row[e] = 0.0f;
+      });
     }
   }
-  {
+
+  if (greedy) {
+    // ---- greedy rows: (max, first index) to the leader, which alone waits.
     const int nan_any = __any_sync(kFull, nan);
     float v = tmax;
     int i = tidx;
@@ -561,157 +831,352 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
       sm.wf[warp] = v;
       sm.wi[warp] = i;
       sm.wu[warp] = static_cast<uint32_t>(nan_any);
-      sm.wt[warp] = theta_w;
     }
-  }
-  __syncthreads();
-  Slot mine = {};
-  {
-    float v = sm.wf[0];
-    int i = sm.wi[0];
-    uint32_t n = sm.wu[0];
-    float th = sm.wt[0];
-    for (int w = 1; w < kWarps; ++w) {
-      if (sm.wf[w] > v || (sm.wf[w] == v && sm.wi[w] < i)) {
-        v = sm.wf[w];
-        i = sm.wi[w];
-      }
-      n |= sm.wu[w];
-      th = fminf(th, sm.wt[w]);
-    }
-    mine.f0 = v;
-    mine.f1 = th;
-    mine.i0 = i;
-    mine.u0 = n;
-  }
-  __syncthreads();
-  float m, theta;
-  int gidx;
-  bool nan_row;
-  {
-    const Slot* s = push_exchange(sm, ph, c, mine);
-    if (warp == 0) {
-      float v = -INFINITY, th = INFINITY;
-      int i = INT_MAX;
-      uint32_t n = 0;
-      if (lane < static_cast<int>(c.csize)) {
-        v = s[lane].f0;
-        th = s[lane].f1;
-        i = s[lane].i0;
-        n = s[lane].u0;
-      }
-      n = __reduce_or_sync(kFull, n);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, v, o);
-        const int oi = __shfl_xor_sync(kFull, i, o);
-        if (ov > v || (ov == v && oi < i)) {
-          v = ov;
-          i = oi;
+    __syncthreads();
+    cluster_wait();
+    if (tid == 0) {
+      float bv = sm.wf[0];
+      int bi = sm.wi[0];
+      uint32_t bn = sm.wu[0];
+      for (int w = 1; w < kWarps; ++w) {
+        if (sm.wf[w] > bv || (sm.wf[w] == bv && sm.wi[w] < bi)) {
+          bv = sm.wf[w];
+          bi = sm.wi[w];
         }
-        th = fminf(th, __shfl_xor_sync(kFull, th, o));
+        bn |= sm.wu[w];
       }
-      if (lane == 0) {
-        sm.bf[0] = v;
-        sm.bf[1] = th;
-        sm.bi[0] = i;
-        sm.bu[0] = n;
-      }
+      const uint32_t a = dsmem(&sm.gather[c.crank], leader);
+      st_dsmem_v4(a, __float_as_uint(bv), 0u, static_cast<uint32_t>(bi), bn);
     }
     __syncthreads();
-    m = sm.bf[0];
-    theta = sm.bf[1];
-    gidx = sm.bi[0];
-    nan_row = sm.bu[0] != 0;
-    __syncthreads();
-  }
-
-  float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
-  auto write_zero_probs = [&]() {
-    if (q_row != nullptr) {
-      for_each<BF16, NV>(c, [&](float, int e) {
-        if (e < V) q_row[e] = 0.0f;
-      });
-    }
-  };
-
-  if (greedy) {
-    const int tok = nan_row ? -1 : gidx;
-    if (c.crank == leader && tid == 0) emit_token(P, row, tok, (nan_row ? kStNonFinite : 0) | st);
-    if (q_row != nullptr) {
-      for_each<BF16, NV>(c, [&](float, int e) {
-        if (e < V) q_row[e] = (e == tok) ? 1.0f : 0.0f;
-      });
+    cluster_arrive();
+    if (c.crank != leader) return;
+    cluster_wait();
+    if (tid == 0) {
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+      uint32_t bn = 0;
+      for (uint32_t r = 0; r < c.csize; ++r) {
+        const float gv = sm.gather[r].f0;
+        const int gi = sm.gather[r].i0;
+        if (gv > bv || (gv == bv && gi < bi)) {
+          bv = gv;
+          bi = gi;
+        }
+        bn |= sm.gather[r].u0;
+      }
+      const int tok = bn ? -1 : bi;
+      emit_token(P, row, tok, (bn ? kStNonFinite : 0) | st);
+      if (q_row != nullptr && tok >= 0) q_row[tok] = 1.0f;
     }
     return;
   }
 
   if constexpr (!ALL_GREEDY) {
-    if (nan_row || m == INFINITY || m == -INFINITY) {
-      const int est = (m == -INFINITY && !nan_row) ? kStAllNegInf : kStNonFinite;
-      if (c.crank == leader && tid == 0) emit_token(P, row, -1, est | st);
-      write_zero_probs();
-      return;
+    // ---- sampled rows: later passes read the slice from shared memory.
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      s_vec[(warp * NV + j) * 32 + lane] = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
     }
     const bool use_p = p < 1.0f;
-    const int R = P.list_cap / static_cast<int>(c.csize);  // list entries per CTA region
+    const int nan_any = __any_sync(kFull, nan);
 
-    // ---- top-p rows: Z and a mass-based theta from the warps' thread maxima.
-    float zrow = 0.0f;
-    if (!topk_row && use_p) {
-      float zt = 0.0f;
-      for_each<BF16, NV>(c, [&](float x, int) { zt += ex2((x - m) * c2); });
-      const float zw = warp_sum(zt);
-      // Largest theta_w whose thread maxima above it carry >= p' of the
-      // warp's mass; p' is p raised by 1e-4 so that rounding rarely forces
-      // the fallback (the leader checks the list's mass exactly).
-      const float sorted = warp_sort_desc(thread_max, lane);
-      const float ws = ex2((sorted - m) * c2);
-      const float cum = warp_inclusive_scan(ws, lane);
-      const float need = fminf(1.0f, p * 1.0001f) * zw;
-      const unsigned hit = __ballot_sync(kFull, cum >= need);
-      // A warp with no mass (all padding) does not constrain theta.
-      const float tw = zw > 0.0f ? (hit ? __shfl_sync(kFull, sorted, __ffs(hit) - 1) : -INFINITY)
-                                 : INFINITY;
-      if (lane == 0) {
-        sm.wf[warp] = zw;
-        sm.wt[warp] = tw;
-      }
-      __syncthreads();
-      Slot z = {};
-      float zsum = 0.0f, th = INFINITY;
-      for (int w = 0; w < kWarps; ++w) {
-        zsum += sm.wf[w];
-        th = fminf(th, sm.wt[w]);
-      }
-      z.f0 = zsum;
-      z.f1 = th;
-      __syncthreads();
-      const Slot* s = push_exchange(sm, ph, c, z);
-      if (warp == 0) {
-        float zz = lane < static_cast<int>(c.csize) ? s[lane].f0 : 0.0f;
-        float tt = lane < static_cast<int>(c.csize) ? s[lane].f1 : INFINITY;
-        zz = warp_sum(zz);
+    // Chunk-local top-k: if this chunk has >= k elements >= theta_c, every
+    // element of the row's top-k that lies in this chunk is >= theta_c (k
+    // elements > the row's k-th value cannot exist), so each CTA can pick its
+    // candidates with no information from the others.  theta_c is the min over
+    // the chunk's full warps of their kw-th largest thread maximum,
+    // kw = ceil(k / full warps).  Uniform eligibility: k <= 256, k <= R, and
+    // the last CTA (fewest full warps) still has kw <= 32.
+    const int nfull_cta = max(0, min(kWarps, (V - cta_begin) / kWarpSpan));
+    const int nfull_min =
+        max(0, min(kWarps, (V - static_cast<int>(c.csize - 1) * CHUNK) / kWarpSpan));
+    const bool local_topk = k < V && k <= 256 && k <= R && nfull_min >= 1 &&
+                            (k + nfull_min - 1) / nfull_min <= 32;
+    if (local_topk) {
+      const int kw = (k + nfull_cta - 1) / nfull_cta;
+      const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
+      const float sorted = warp_sort_desc(tmax, lane);
+      const float tw = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
+      float wmax = tmax;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tt = fminf(tt, __shfl_xor_sync(kFull, tt, o));
-        if (lane == 0) {
-          sm.bf[0] = zz;
-          sm.bf[1] = tt;
+      for (int o = 16; o > 0; o >>= 1) wmax = fmax_nan(wmax, __shfl_xor_sync(kFull, wmax, o));
+      if (lane == 0) {
+        sm.wt[warp] = tw;
+        sm.wf[warp] = wmax;
+        sm.wu[warp] = static_cast<uint32_t>(nan_any);
+      }
+      __syncthreads();
+      float theta = INFINITY, cmax = -INFINITY;
+      uint32_t cnan = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        theta = fminf(theta, sm.wt[w]);
+        cmax = fmax_nan(cmax, sm.wf[w]);
+        cnan |= sm.wu[w];
+      }
+      __syncthreads();
+      auto cand = [&](float x, int e) { return x >= theta && (!has_pad || e < V); };
+      uint32_t cnt = 0;
+      for_each<BF16, NV>(c, [&](float x, int e) { cnt += cand(x, e) ? 1u : 0u; });
+      const uint32_t wc = __reduce_add_sync(kFull, cnt);
+      if (lane == 0) sm.wu[warp] = wc;
+      __syncthreads();
+      uint32_t ncta = 0;
+      for (int w = 0; w < kWarps; ++w) ncta += sm.wu[w];
+      __syncthreads();
+      // Ties can push the count past the region: keep exactly the chunk's top-k.
+      float tloc = -INFINITY;
+      int cloc = INT_MAX;
+      if (static_cast<int>(ncta) > R) {
+        tloc = cta_select_topk<BF16, NV>(c, sm, cand, static_cast<unsigned long long>(k), &cloc);
+      }
+      const float tlv = tloc;
+      const int clv = cloc;
+      auto keep = [&](float x, int e) {
+        return cand(x, e) && (x > tlv || (x == tlv && e < clv));
+      };
+      cnt = 0;
+      for_each<BF16, NV>(c, [&](float x, int e) { cnt += keep(x, e) ? 1u : 0u; });
+      const uint32_t wk = __reduce_add_sync(kFull, cnt);
+      if (lane == 0) sm.wu[warp] = wk;
+      __syncthreads();
+      uint32_t woff = 0, nkeep = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) woff += sm.wu[w];
+        nkeep += sm.wu[w];
+      }
+      cluster_wait();
+      {
+        const uint32_t base = static_cast<uint32_t>(c.crank) * R + woff;
+        const uint32_t a_val = dsmem(l_val, leader);
+        const uint32_t a_idx = dsmem(l_idx, leader);
+        uint32_t acc = 0;
+        for (int j = 0; j < NV; ++j) {
+          const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
+          const int e0 = c.lane_base + j * 32 * L::VW;
+          uint32_t cj = 0;
+          for_vector<BF16>(v, e0, [&](float x, int e) { cj += keep(x, e) ? 1u : 0u; });
+          if (__ballot_sync(kFull, cj != 0) == 0) continue;
+          const uint32_t incl = warp_inclusive_scan(cj, lane);
+          uint32_t pos = base + acc + incl - cj;
+          for_vector<BF16>(v, e0, [&](float x, int e) {
+            if (keep(x, e)) {
+              st_dsmem_f32(a_val + 4u * pos, x);
+              st_dsmem_u32(a_idx + 4u * pos, static_cast<uint32_t>(e));
+              ++pos;
+            }
+          });
+          acc += __shfl_sync(kFull, incl, 31);
         }
       }
+      if (tid == 0) {
+        const uint32_t a = dsmem(&sm.gather[c.crank], leader);
+        st_dsmem_v4(a, __float_as_uint(cmax), 0u, 0u, cnan);
+        st_dsmem_u32(dsmem(&sm.cnt[c.crank], leader), nkeep);
+      }
       __syncthreads();
-      zrow = sm.bf[0];
-      theta = sm.bf[1];
-      __syncthreads();
+      cluster_arrive();
+      if (c.crank != leader) return;
+      cluster_wait();
+      float m = -INFINITY;
+      uint32_t rn = 0;
+      for (uint32_t r = 0; r < c.csize; ++r) {
+        m = fmax_nan(m, sm.gather[r].f0);
+        rn |= sm.gather[r].u0;
+      }
+      if (rn != 0 || m != m || m == INFINITY || m == -INFINITY) {
+        const int est = (m == -INFINITY && rn == 0) ? kStAllNegInf : kStNonFinite;
+        if (tid == 0) emit_token(P, row, -1, est | st);
+        return;
+      }
+      leader_finish(P, sm, c, l_val, l_idx, R, row, true, k, use_p, p, 0ull, m, c2, u, st,
+                    q_row);
+      return;
     }
 
-    // ---- fast path: candidates >= theta into the leader's list.
-    const bool fast = (topk_row || use_p) && theta > -INFINITY;
+    // ---- other sampled rows: one all-to-all exchange of the chunk maximum,
+    // the chunk mass (relative to the chunk maximum) and a bound theta_c.
+    const bool topk_row = k < V;
+    const bool need_z = !topk_row;
+    float zt = 0.0f;
+    if (need_z && tmax > -INFINITY) {
+      for_each<BF16, NV>(c, [&](float x, int) { zt += ex2((x - tmax) * c2); });
+    }
+    float wmax = tmax;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wmax = fmax_nan(wmax, __shfl_xor_sync(kFull, wmax, o));
+    const float zw = warp_sum(tmax > -INFINITY ? zt * ex2((tmax - wmax) * c2) : 0.0f);
+    float tw = -INFINITY;
+    if (topk_row) {
+      // kw-th largest thread maximum of every warp fully inside the row.
+      const int w_full = V / kWarpSpan;
+      const int kw = w_full > 0 ? (k + w_full - 1) / w_full : INT_MAX;
+      const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
+      if (kw <= 32) {
+        const float sorted = warp_sort_desc(tmax, lane);
+        tw = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
+      }
+    } else if (use_p) {
+      // Largest theta_w whose thread maxima above it carry >= p' of the
+      // warp's mass (p' = p raised by 1e-3, so that rounding rarely forces
+      // the fallback; the decision below is exact).  A warp without mass
+      // does not constrain theta.
+      const float sorted = warp_sort_desc(tmax, lane);
+      const float ws = sorted > -INFINITY ? ex2((sorted - wmax) * c2) : 0.0f;
+      const float cum = warp_inclusive_scan(ws, lane);
+      const float need = fminf(1.0f, p * 1.001f) * zw;
+      const unsigned hit = __ballot_sync(kFull, cum >= need);
+      tw = zw > 0.0f ? (hit ? __shfl_sync(kFull, sorted, __ffs(hit) - 1) : -INFINITY) : INFINITY;
+    }
+    if (lane == 0) {
+      sm.wt[warp] = tw;
+      sm.wf[warp] = wmax;
+      sm.wz[warp] = zw;
+      sm.wu[warp] = static_cast<uint32_t>(nan_any);
+    }
+    __syncthreads();
+    Slot mine = {};
+    {
+      float cm = -INFINITY, th = INFINITY, cz = 0.0f;
+      uint32_t cn = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        cm = fmax_nan(cm, sm.wf[w]);
+        th = fminf(th, sm.wt[w]);
+        cn |= sm.wu[w];
+      }
+      if (cm > -INFINITY) {
+        for (int w = 0; w < kWarps; ++w) {
+          if (sm.wf[w] > -INFINITY) cz += sm.wz[w] * ex2((sm.wf[w] - cm) * c2);
+        }
+      }
+      mine.f0 = cm;
+      mine.f1 = th;
+      mine.u0 = cn;
+      mine.pad0 = __float_as_uint(cz);
+    }
+    __syncthreads();
+    cluster_wait();
+    int ph = 0;
+    float m, theta, zrow, before_cta;
+    bool nan_row;
+    {
+      const Slot* s = push_exchange(sm, ph, c, mine);
+      float mm = -INFINITY, th = INFINITY;
+      uint32_t nn = 0;
+      for (uint32_t r = 0; r < c.csize; ++r) {
+        mm = fmax_nan(mm, s[r].f0);
+        th = fminf(th, s[r].f1);
+        nn |= s[r].u0;
+      }
+      float zz = 0.0f;
+      if (mm > -INFINITY && mm == mm) {
+        for (uint32_t r = 0; r < c.csize; ++r) {
+          if (s[r].f0 > -INFINITY) zz += __uint_as_float(s[r].pad0) * ex2((s[r].f0 - mm) * c2);
+        }
+      }
+      m = mm;
+      theta = th;
+      zrow = zz;
+      nan_row = nn != 0;
+      // CTA prefix of the masses, for the plain rows' draw (same summation
+      // order as zrow, so the CTA intervals tile [0, zrow) exactly).
+      float before = 0.0f;
+      for (uint32_t r = 0; r < c.crank; ++r) {
+        if (s[r].f0 > -INFINITY) before += __uint_as_float(s[r].pad0) * ex2((s[r].f0 - mm) * c2);
+      }
+      before_cta = before;
+    }
+    if (nan_row || m != m || m == INFINITY || m == -INFINITY) {
+      const int est = (m == -INFINITY && !nan_row) ? kStAllNegInf : kStNonFinite;
+      if (c.crank == leader && tid == 0) emit_token(P, row, -1, est | st);
+      return;
+    }
+
+    if (!topk_row && !use_p) {
+      // ---- plain rows: draw over the whole row; the CTA holding the
+      // crossing finds the token.
+      // Keep the target strictly below zrow so that it falls in the interval
+      // of a CTA that holds mass.
+      float target = u * zrow;
+      if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
+      const float before = before_cta;
+      const float mine_z =
+          mine.f0 > -INFINITY ? __uint_as_float(mine.pad0) * ex2((mine.f0 - m) * c2) : 0.0f;
+      if (target >= before && target < before + mine_z) {
+        // Warp holding the crossing (sequential over warps).
+        const float tloc = target - before;
+        int wstar = -1;
+        float tw2 = INFINITY, cw = 0.0f;
+        int wlast = -1;
+        for (int w = 0; w < kWarps; ++w) {
+          const float ww = sm.wf[w] > -INFINITY ? sm.wz[w] * ex2((sm.wf[w] - m) * c2) : 0.0f;
+          if (wstar < 0 && tloc < cw + ww) {
+            wstar = w;
+            tw2 = tloc - cw;
+          }
+          if (ww > 0.0f) wlast = w;
+          cw += ww;
+        }
+        if (wstar < 0) {
+          wstar = wlast < 0 ? 0 : wlast;
+          tw2 = INFINITY;
+        }
+        if (warp == wstar) {
+          float acc = 0.0f;
+          int found = -1, lastpos = -1;
+          for (int j = 0; j < NV; ++j) {
+            const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
+            const int e0 = c.lane_base + j * 32 * L::VW;
+            float lj = 0.0f;
+            int llast = -1;
+            for_vector<BF16>(v, e0, [&](float x, int e) {
+              const float w = ex2((x - m) * c2);
+              lj += w;
+              if (w > 0.0f) llast = e;
+            });
+            const unsigned has = __ballot_sync(kFull, llast >= 0);
+            if (has != 0) lastpos = __shfl_sync(kFull, llast, 31 - __clz(has));
+            const float incl = warp_inclusive_scan(lj, lane);
+            const float stot = __shfl_sync(kFull, incl, 31);
+            if (tw2 < acc + stot) {
+              const unsigned bal = __ballot_sync(kFull, tw2 < acc + incl);
+              const int lx = bal ? __ffs(bal) - 1 : 31;
+              int sel = -1;
+              if (lane == lx) {
+                float run = acc + (incl - lj);
+                for_vector<BF16>(v, e0, [&](float x, int e) {
+                  run += ex2((x - m) * c2);
+                  if (sel < 0 && tw2 < run) sel = e;
+                });
+                if (sel < 0) sel = llast;
+              }
+              found = __shfl_sync(kFull, sel, lx);
+              if (found < 0) found = lastpos;
+              break;
+            }
+            acc += stot;
+          }
+          if (found < 0) found = lastpos;
+          if (lane == 0 && found >= 0) emit_token(P, row, found, st);
+        }
+      }
+      if (q_row != nullptr) {
+        const float inv = 1.0f / zrow;
+        for_each<BF16, NV>(c, [&](float x, int e) {
+          if (e < V) q_row[e] = ex2((x - m) * c2) * inv;
+        });
+      }
+      return;
+    }
+
+    // ---- global theta: candidates >= theta into the leader's list.
+    const bool fast = theta > -INFINITY;
     if (fast) {
+      auto cand = [&](float x, int e) { return x >= theta && (!has_pad || e < V); };
       uint32_t cnt = 0;
       unsigned long long mfx = 0;
       for_each<BF16, NV>(c, [&](float x, int e) {
-        if (x >= theta && (!has_pad || e < V)) {
+        if (cand(x, e)) {
           ++cnt;
           if (!topk_row) mfx += mass_fx(ex2((x - m) * c2));
         }
@@ -731,7 +1196,6 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
         mcta += sm.wl[w];
       }
       if (static_cast<int>(ncta) <= R) {
-        // Ordered write: warp region, then vector by vector in lane order.
         const uint32_t base = static_cast<uint32_t>(c.crank) * R + woff;
         const uint32_t a_val = dsmem(l_val, leader);
         const uint32_t a_idx = dsmem(l_idx, leader);
@@ -740,12 +1204,12 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
           const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
           const int e0 = c.lane_base + j * 32 * L::VW;
           uint32_t cj = 0;
-          for_vector<BF16>(v, e0, [&](float x, int e) { cj += (x >= theta && (!has_pad || e < V)) ? 1u : 0u; });
+          for_vector<BF16>(v, e0, [&](float x, int e) { cj += cand(x, e) ? 1u : 0u; });
           if (__ballot_sync(kFull, cj != 0) == 0) continue;
           const uint32_t incl = warp_inclusive_scan(cj, lane);
           uint32_t pos = base + acc + incl - cj;
           for_vector<BF16>(v, e0, [&](float x, int e) {
-            if (x >= theta && (!has_pad || e < V)) {
+            if (cand(x, e)) {
               st_dsmem_f32(a_val + 4u * pos, x);
               st_dsmem_u32(a_idx + 4u * pos, static_cast<uint32_t>(e));
               ++pos;
@@ -754,7 +1218,6 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
           acc += __shfl_sync(kFull, incl, 31);
         }
       }
-      write_zero_probs();
       Slot cs = {};
       cs.u0 = ncta;
       cs.l0 = mcta;
@@ -777,99 +1240,10 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
       }
       if (over == 0) {
         if (c.crank != leader) return;
-        // ---- leader: pack the regions, then select and draw on the list.
-        int n = 0;
-        for (uint32_t r = 0; r < c.csize; ++r) n += static_cast<int>(s[r].u0);
-        {
-          // Packed index i comes from region r at offset i - (sum of earlier
-          // counts), never from a position below i: read, barrier, write.
-          constexpr int kMovePer = 16;
-          float mv[kMovePer];
-          int mi[kMovePer];
-          for (int b0 = 0; b0 < n; b0 += kThreads * kMovePer) {
-#pragma unroll
-            for (int q = 0; q < kMovePer; ++q) {
-              const int i = b0 + q * kThreads + tid;
-              if (i < n) {
-                int r = 0, off = i;
-                while (off >= static_cast<int>(s[r].u0)) {
-                  off -= static_cast<int>(s[r].u0);
-                  ++r;
-                }
-                mv[q] = l_val[r * R + off];
-                mi[q] = l_idx[r * R + off];
-              }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int q = 0; q < kMovePer; ++q) {
-              const int i = b0 + q * kThreads + tid;
-              if (i < n) {
-                l_val[i] = mv[q];
-                l_idx[i] = mi[q];
-              }
-            }
-            __syncthreads();
-          }
-        }
-        // top-k: count select; ties go by index = list order.
-        int cut_k = n;
-        float tk = -INFINITY;
-        if (topk_row) {
-          unsigned long long rk;
-          tk = list_select<false>(l_val, n, [](int) { return true; }, [](int) { return 1ull; },
-                                  static_cast<unsigned long long>(k), sm, c, &rk);
-          const float tkv = tk;
-          cut_k = list_tie_cut(n, [&](int i) { return l_val[i] == tkv; }, rk, sm, c);
-        }
-        const float tkv = tk;
-        const int ckv = cut_k;
-        auto in_k = [&](int i) { return l_val[i] > tkv || (l_val[i] == tkv && i < ckv); };
-        auto w_of = [&](int i) { return ex2((l_val[i] - m) * c2); };
-        float tp = tk;
-        int cut_p = cut_k;
-        if (use_p) {
-          if (topk_row) {
-            unsigned long long zfx = 0;
-            for (int i = tid; i < n; i += kThreads) {
-              if (in_k(i)) zfx += mass_fx(w_of(i));
-            }
-            zfx = warp_sum(zfx);
-            if (lane == 0) sm.wl[warp] = zfx;
-            __syncthreads();
-            unsigned long long z = 0;
-            for (int w = 0; w < kWarps; ++w) z += sm.wl[w];
-            __syncthreads();
-            const double t = static_cast<double>(z) * static_cast<double>(p);
-            target_fx = static_cast<unsigned long long>(ceil(t));
-            if (target_fx < 1) target_fx = 1;
-            if (target_fx > z) target_fx = z;
-          }
-          unsigned long long rem;
-          tp = list_select<true>(l_val, n, in_k, [&](int i) { return mass_fx(w_of(i)); },
-                                 target_fx, sm, c, &rem);
-          // Members of the threshold group share one weight wt: member j
-          // (index order) is kept iff above + j * wt < target, i.e.
-          // j < ceil(rem / wt).
-          const unsigned long long wt = mass_fx(ex2((tp - m) * c2));
-          const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
-          const float tpv = tp;
-          cut_p = list_tie_cut(n, [&](int i) { return l_val[i] == tpv && in_k(i); }, rp, sm, c);
-        }
-        const float tpv = tp;
-        const int cpv = cut_p;
-        auto in_s = [&](int i) {
-          return in_k(i) && (l_val[i] > tpv || (l_val[i] == tpv && i < cpv));
-        };
-        float zs;
-        const int tok = list_draw(l_idx, n, in_s, w_of, u, sm, c, &zs);
-        if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
-        if (q_row != nullptr) {
-          const float inv = 1.0f / zs;
-          for (int i = tid; i < n; i += kThreads) {
-            if (in_s(i)) q_row[l_idx[i]] = w_of(i) * inv;
-          }
-        }
+        if (tid < static_cast<int>(c.csize)) sm.cnt[tid] = s[tid].u0;
+        __syncthreads();
+        leader_finish(P, sm, c, l_val, l_idx, R, row, topk_row, k, use_p, p, target_fx, m, c2, u,
+                      st, q_row);
         return;
       }
       // Over capacity: every CTA falls through to the on-chip fallback.
@@ -1145,117 +1519,10 @@ __device__ __forceinline__ void sample_row(const SampleParams& P, SampleSmem& sm
         if (e < V) q_row[e] = in_s(x, e) ? ex2((x - m) * c2) * inv : 0.0f;
       });
     }
-    // Histograms other CTAs pulled from this one are not rewritten before the
-    // next row's first barrier, which they reach only after their reads.
-    (void)pulled;
-  }
-}
+    // Other CTAs read this CTA's histograms after the barriers above; stay
+    // until every CTA is past them.
+    if (pulled) cluster_sync();
 
-
-// Persistent kernel: cluster g (blockIdx.y) handles rows g, g + G, g + 2G, ...
-// Each CTA streams its slice of successive rows through a two-stage ring in
-// shared memory: while one row is processed, the bulk copy of the row after
-// next lands in the other stage, so HBM reads continue across the cluster
-// barriers.  One thread waits on each stage's mbarrier (bounded); the others
-// wait at a CTA barrier.
-template <bool BF16, int NV, bool TMA, bool ALL_GREEDY>
-__global__ void __launch_bounds__(kThreads, 2) sample_kernel(const SampleParams P) {
-  using L = Layout<BF16>;
-  constexpr int CHUNK = kThreads * NV * L::VW;
-  constexpr uint32_t kSliceBytes = static_cast<uint32_t>(CHUNK) * L::ELT;
-  __shared__ SampleSmem sm;
-  __shared__ uint64_t full[2];
-  extern __shared__ __align__(128) unsigned char dyn[];
-  unsigned char* stage0 = dyn;
-  unsigned char* stage1 = dyn + kSliceBytes;
-  float* l_val = reinterpret_cast<float*>(dyn + 2 * kSliceBytes);
-  int32_t* l_idx = reinterpret_cast<int32_t*>(l_val + P.list_cap);
-  const int tid = threadIdx.x;
-  const int V = P.V;
-  const int G = static_cast<int>(gridDim.y);
-  const int cta_begin = static_cast<int>(cluster_rank()) * CHUNK;
-  const int nvalid = max(0, min(CHUNK, V - cta_begin));
-  const uint32_t bytes = static_cast<uint32_t>(nvalid) * L::ELT;
-  auto src_of = [&](int row) {
-    return static_cast<const char*>(P.logits) +
-           (static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) +
-            static_cast<size_t>(cta_begin)) * L::ELT;
-  };
-  // Padding past the row end is -inf in both stages (copies never touch it).
-  for (int e = nvalid + tid; e < CHUNK; e += kThreads) {
-    if constexpr (BF16) {
-      reinterpret_cast<uint16_t*>(stage0)[e] = 0xff80u;
-      reinterpret_cast<uint16_t*>(stage1)[e] = 0xff80u;
-    } else {
-      reinterpret_cast<uint32_t*>(stage0)[e] = 0xff800000u;
-      reinterpret_cast<uint32_t*>(stage1)[e] = 0xff800000u;
-    }
-  }
-  auto issue = [&](int s, int row) {
-    unsigned char* dst = s == 0 ? stage0 : stage1;
-    const char* g = src_of(row);
-    mbar_arrive_expect_tx(&full[s], bytes);
-    for (uint32_t off = 0; off < bytes; off += 16384u) {
-      bulk_copy_g2s(dst + off, g + off, min(16384u, bytes - off), &full[s]);
-    }
-  };
-  bool pending0 = false, pending1 = false;  // thread 0: a copy whose wait timed out
-  if constexpr (TMA) {
-    if (tid == 0) {
-      mbar_init(&full[0], 1);
-      mbar_init(&full[1], 1);
-      fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-      if (static_cast<int>(blockIdx.y) < P.B) issue(0, blockIdx.y);
-      if (static_cast<int>(blockIdx.y) + G < P.B) issue(1, blockIdx.y + G);
-    }
-  }
-  int ph = 0;
-  for (int it = 0;; ++it) {
-    const int row = static_cast<int>(blockIdx.y) + it * G;
-    if (row >= P.B) break;
-    const int s = it & 1;
-    unsigned char* cur = s == 0 ? stage0 : stage1;
-    int st = 0;
-    if constexpr (TMA) {
-      if (tid == 0) {
-        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(it >> 1) & 1u, kWaitIters);
-        if (s == 0) pending0 = !ok; else pending1 = !ok;
-        sm.bu[3] = ok ? 0u : 1u;
-      }
-      __syncthreads();
-      if (sm.bu[3] != 0u) st |= kStTimeout;
-    } else {
-      const char* g = src_of(row);
-      for (int e = tid; e < nvalid; e += kThreads) {
-        if constexpr (BF16) {
-          reinterpret_cast<uint16_t*>(cur)[e] = reinterpret_cast<const uint16_t*>(g)[e];
-        } else {
-          reinterpret_cast<uint32_t*>(cur)[e] = reinterpret_cast<const uint32_t*>(g)[e];
-        }
-      }
-      __syncthreads();
-    }
-    sample_row<BF16, NV, ALL_GREEDY>(P, sm, reinterpret_cast<const uint4*>(cur), l_val, l_idx,
-                                     row, ph, st);
-    __syncthreads();  // the whole CTA is done with this stage
-    if constexpr (TMA) {
-      const int next = row + 2 * G;
-      if (tid == 0 && next < P.B) {
-        fence_proxy_async_smem();
-        issue(s, next);
-      }
-    }
-  }
-  // No CTA leaves while another may still read its shared memory.
-  cluster_sync();
-  if constexpr (TMA) {
-    if (tid == 0) {
-      if (pending0) mbar_wait_bounded(&full[0], 0u, kWaitIters);
-      if (pending1) mbar_wait_bounded(&full[1], 0u, kWaitIters);
-    }
   }
 }
 

@@ -10,15 +10,15 @@
 
 namespace pkv {
 
-// Candidate-list capacity: as large as fits next to the two-stage ring while
-// keeping two CTAs per SM (else one), at most 4096 entries.
-inline int list_capacity(size_t ring_bytes) {
+// Candidate-list capacity: as large as fits next to the slice while keeping
+// three CTAs per SM (else two, else one), at most 4096 entries.
+inline int list_capacity(size_t slice_bytes) {
   constexpr size_t kSmemPerSm = 228 * 1024;
   constexpr size_t kPerCtaReserved = 1024;
-  constexpr size_t kStatic = sizeof(SampleSmem) + 2 * sizeof(uint64_t) + 256;
-  for (int per_sm = 2; per_sm >= 1; --per_sm) {
+  constexpr size_t kStatic = sizeof(SampleSmem) + 256;
+  for (int per_sm = 3; per_sm >= 1; --per_sm) {
     const size_t budget = kSmemPerSm / per_sm;
-    const size_t used = kPerCtaReserved + kStatic + ring_bytes;
+    const size_t used = kPerCtaReserved + kStatic + slice_bytes;
     if (budget <= used) continue;
     size_t cap = (budget - used) / 8;
     if (cap > 4096) cap = 4096;
@@ -28,17 +28,21 @@ inline int list_capacity(size_t ring_bytes) {
   return 1024;
 }
 
-template <bool BF16, int NV, bool TMA, bool AG>
+template <bool BF16, int NV, bool VEC, bool AG>
 cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
-  auto kern = sample_kernel<BF16, NV, TMA, AG>;
-  constexpr size_t kRingBytes = 2 * static_cast<size_t>(kThreads) * NV * 16;
-  static const int cap = list_capacity(kRingBytes);
-  const size_t dyn = kRingBytes + static_cast<size_t>(cap) * 8;
+  auto kern = sample_kernel<BF16, NV, VEC, AG>;
+  constexpr size_t kSliceBytes = static_cast<size_t>(kThreads) * NV * 16;
+  static const int cap = list_capacity(kSliceBytes);
+  // An all-greedy batch uses neither the slice copy nor the list.
+  const size_t dyn = AG ? 0 : kSliceBytes + static_cast<size_t>(cap) * 8;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(dyn));
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (dyn > 0) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(dyn));
+      if (e != cudaSuccess) return e;
+    }
     // Clusters of 9..16 CTAs are a non-portable size; opt in once per kernel.
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -46,6 +50,7 @@ cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
   }
   P.list_cap = cap;
   cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C), static_cast<unsigned>(P.B), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
@@ -56,23 +61,6 @@ cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Persistent grid: as many clusters as can be resident at once (per device
-  // and cluster size, queried once), never more than there are rows.
-  static int cached_active[64][17] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int active = (dev >= 0 && dev < 64) ? cached_active[dev][C] : 0;
-  if (active <= 0) {
-    cfg.gridDim = dim3(static_cast<unsigned>(C), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active <= 0) {
-      cudaGetLastError();  // clear the query's error; fall back to one cluster per row
-      active = P.B;
-    } else if (dev >= 0 && dev < 64) {
-      cached_active[dev][C] = active;
-    }
-  }
-  const int G = active < P.B ? active : P.B;
-  cfg.gridDim = dim3(static_cast<unsigned>(C), static_cast<unsigned>(G), 1);
   return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
