@@ -55,6 +55,8 @@ typedef enum { PKV_FP32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_ST_COL_OOB 8       /* write-back / page-table column out of range  */
 #define PKV_ST_BAD_UNIFORM 16  /* uniform outside [0,1): clamped, still drawn  */
 #define PKV_ST_NOSPC 32        /* page fill: more pages needed than are free   */
+#define PKV_ST_TIMEOUT 64      /* a row's CTAs did not report in time (internal
+                                  error; the row's token is -1)                */
 
 /* Largest vocabulary the sampler handles for each dtype. */
 #define PKV_MAX_VOCAB_BF16 524288

@@ -44,6 +44,12 @@ __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Arrive without memory ordering (a start-up barrier that only says "this
+// CTA is running"; orderings it needs come from a fence before it).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
 // Shared-window address of `p` (a __shared__ object of this CTA) as seen in
 // CTA `rank` of the same cluster.
 __device__ __forceinline__ uint32_t dsmem(const void* p, uint32_t rank) {
@@ -85,7 +91,7 @@ __device__ __forceinline__ void st_dsmem_v4(uint32_t addr, uint32_t a, uint32_t 
                :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// ----------------------------------------------------------------- mbarrier + TMA bulk copy
+// ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -96,48 +102,37 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                : "memory");
 }
 
-// Makes barrier initialisation visible to the asynchronous (TMA) proxy.
+// Orders mbarrier initialisation before later cluster-scope arrivals on it.
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
-               :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+// Arrives (count 1) on an mbarrier of another CTA of the cluster, given its
+// shared::cluster address (dsmem).  Release at cluster scope: this thread's
+// earlier writes, and those ordered before them by a CTA barrier, are
+// visible to a thread that observes the phase with an acquire wait.
+__device__ __forceinline__ void mbar_remote_arrive(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+               :: "r"(cluster_addr) : "memory");
 }
 
-// One-dimensional bulk copy global -> this CTA's shared memory, completing
-// `bytes` transaction bytes on `bar`.  dst, src and bytes are multiples of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
-                                              uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
-
-// Orders this thread's earlier generic-proxy shared-memory accesses before
-// later asynchronous-proxy (bulk copy) writes to the same memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Tests phase `parity` of this CTA's mbarrier with acquire at cluster scope
+// (pairs with mbar_remote_arrive).  May suspend briefly; true once complete.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
   return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` with an iteration limit; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t max_iters) {
-  for (uint32_t it = 0; it < max_iters; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-  }
-  return false;
+// Global nanosecond timer (bounds every wait).
+__device__ __forceinline__ long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return static_cast<long long>(t);
 }
 
 // ----------------------------------------------------------------- loads

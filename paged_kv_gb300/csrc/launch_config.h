@@ -7,7 +7,7 @@
 namespace pkv {
 
 constexpr int kSampleThreads = 256;
-constexpr int kNvScalar = 16;     // vectors per thread on the unaligned (scalar-load) path
+constexpr int kNvScalar = 16;     // largest vectors-per-thread on the unaligned (element-load) path
 constexpr int kMaxCluster = 16;   // 9..16 are non-portable cluster sizes
 
 struct SampleConfig {
@@ -26,14 +26,18 @@ inline bool choose_sample_config(int B, int V, bool bf16, bool vec, int num_sms,
   const int per_nv = kSampleThreads * (bf16 ? 8 : 4);  // elements per unit of nv
   static const int kNvs[] = {4, 8, 10, 16};
   if (!vec) {
-    const int64_t cap = static_cast<int64_t>(per_nv) * kNvScalar;
-    const int64_t c = (V + cap - 1) / cap;
-    if (c > kMaxCluster) return false;
-    out->cluster = static_cast<int>(c);
-    out->nv = kNvScalar;
-    out->vec = false;
-    out->chunk = static_cast<int>(cap);
-    return true;
+    // Element loads: 10 vectors per thread while that covers V, else 16.
+    for (int nv : {10, kNvScalar}) {
+      const int64_t cap = static_cast<int64_t>(per_nv) * nv;
+      const int64_t c = (V + cap - 1) / cap;
+      if (c > kMaxCluster) continue;
+      out->cluster = static_cast<int>(c);
+      out->nv = nv;
+      out->vec = false;
+      out->chunk = static_cast<int>(cap);
+      return true;
+    }
+    return false;
   }
   int best_c = 0, best_nv = 0;
   int64_t best_cost = INT64_MAX;

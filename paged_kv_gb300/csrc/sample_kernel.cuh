@@ -9,37 +9,40 @@
 // Order between equal logits is by ascending index everywhere.
 //
 // GB300 design:
-//   * One thread-block cluster of C CTAs per row (grid = C x B, not
-//     persistent, so rows never wait for each other).  CTA r owns the
-//     contiguous slice [r*chunk, (r+1)*chunk) of the row.  Its first thread
-//     issues one TMA bulk copy (cp.async.bulk + mbarrier) of the slice into
-//     shared memory, so a CTA holds no registers while its bytes are in flight
-//     and several CTAs per SM keep HBM busy.  Every logit is read from HBM
-//     exactly once; all later passes read shared memory.
-//   * Cross-CTA steps are cluster barriers.  Scalars are PUSHED into every
-//     CTA's shared memory before a barrier (DSMEM stores), so each CTA reads
-//     only its own shared memory afterwards and can exit right after its last
-//     barrier.
-//   * Fast selection (no per-element atomics): a guaranteed lower bound theta of
-//     the final threshold comes from the warps' per-thread maxima -- by count
-//     for top-k (each warp has >= k_w elements >= its k_w-th largest thread
-//     maximum), by probability mass for top-p (the warp's thread maxima that
-//     carry >= p of the warp's mass).  The few elements >= theta are compacted,
-//     in index order, into a list in the leader CTA's shared memory; the
-//     leader finishes top-k, top-p and the inverse CDF exactly on that list
-//     (radix selects with 256-bucket histograms over the list only).
-//   * Fallback (lists that would overflow, dense top-p rows): the same
-//     selections as radix selects over the whole row held on chip, with
-//     cluster-wide histogram exchanges.  Masses are 2^-40 fixed-point
-//     integers accumulated with pairs of 32-bit atomics, so every sum is exact
-//     and independent of atomic order (deterministic).
-//   * The draw: per-warp partial sums -> per-CTA sums exchanged across the
-//     cluster -> the CTA, warp, 256-element slab, lane and element where the
-//     cumulative mass first exceeds u * Z_S (or a block scan over the list).
+//   * One thread-block cluster of C CTAs per row (grid C x B).  CTA r owns
+//     the contiguous slice [r*chunk, (r+1)*chunk) of the row and keeps it in
+//     registers (16-byte loads, every logit read from HBM once).  Warp w of
+//     a CTA owns a contiguous sub-slice; its vector j covers 32 consecutive
+//     16-byte groups, one per lane.
+//   * No all-to-all exchange.  Every CTA reduces its slice to a small
+//     summary (plus candidates or a histogram), pushes it into the leader
+//     CTA's shared memory, signals the leader's mbarrier with one
+//     release-arrive and exits.  Only the leader waits.  The one cluster
+//     barrier, at the start (relaxed arrive; waited on only by the CTAs that
+//     push), guarantees that the leader runs before anyone writes into it.
+//   * Row kinds, each finished by the leader:
+//       G  greedy: (max, first index) per CTA.
+//       K  top-k with k <= 256: a chunk-local lower bound theta_c on the
+//          row's k-th value (a chunk holding k elements >= theta_c cannot
+//          miss any of the row's top-k) selects candidates with no global
+//          information; the leader selects exactly on the candidate list.
+//       P  plain (no filter): chunk max and mass; the leader picks the
+//          chunk of the draw and re-reads that chunk (an L2 hit) to find the
+//          token.
+//       H  top-p, or top-k with k > 256, on bf16 rows: all elements with one
+//          bf16 value share one weight, so exact counts per value give exact
+//          masses.  Each CTA counts its elements per value over a window of
+//          1024 values below its maximum; the leader merges the counts,
+//          settles the top-k and top-p cuts exactly (2^-40 fixed-point
+//          masses), picks the chunk of the draw and re-reads it.
+//       F  whatever the above cannot settle (a cut below the window; fp32
+//          rows with top-p or k > 256): the leader selects exactly by radix
+//          passes over the row in global memory.
 //   * No tensor cores (nothing here is a contraction); exp is MUFU.EX2.
 #pragma once
 
 #include <climits>
+#include <cstddef>
 #include <cstdint>
 
 #include "device_common.cuh"
@@ -51,39 +54,50 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBuckets = 256;
 constexpr int kMaxClusterCtas = 16;
+constexpr int kHistKeys = 1024;                // values counted below a CTA's maximum (H rows)
+constexpr int kHistWords = kHistKeys / 2;      // two 16-bit counts per word
+constexpr int kListCap = 4096;                 // candidate entries in the leader (K rows)
+constexpr int kSampleDynBytes = kListCap * 8;  // the list, or C histograms
+
+// Dynamic shared memory of a sampled launch: the list or the histograms,
+// later (leader only) one staged chunk of kThreads * NV 16-byte vectors.
+template <int NV>
+constexpr int sample_dyn_bytes() {
+  return kThreads * NV * 16 > kSampleDynBytes ? kThreads * NV * 16 : kSampleDynBytes;
+}
+static_assert(kMaxClusterCtas * kHistWords * 4 == kSampleDynBytes, "dynamic shared memory");
+static_assert(kHistKeys == 4 * kThreads, "four merged histogram keys per leader thread");
+static_assert(kHistWords == 2 * kThreads, "two histogram words per thread");
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
+constexpr double kMassScaleD = 1099511627776.0;
+constexpr long long kWaitNs = 2000000000ll;     // the leader's wait for the other CTAs (2 s)
 
 constexpr int kStNonFinite = 1;
 constexpr int kStAllNegInf = 2;
 constexpr int kStRowOOB = 4;
 constexpr int kStColOOB = 8;
 constexpr int kStBadUniform = 16;
+constexpr int kStTimeout = 64;
 
-// One CTA's values for one exchange phase, pushed into every CTA.
-struct Slot {
-  float f0;
-  float f1;
-  int32_t i0;
-  uint32_t u0;
-  unsigned long long l0;
-  uint32_t pad0;
-  uint32_t pad1;
-};
-static_assert(sizeof(Slot) == 32, "Slot is pushed as two 16-byte stores");
+enum RowKind { kKindG = 0, kKindK = 1, kKindP = 2, kKindH = 3, kKindF = 4 };
 
-// Histogram a CTA publishes for the others to read (fallback radix select).
-struct PullBuf {
-  uint32_t lo[kBuckets];  // counts, or low words of fixed-point masses
-  uint32_t hi[kBuckets];  // high words of fixed-point masses
+// One CTA's summary, pushed into the leader's gather[rank] with one 16-byte
+// store (hence the alignment).
+struct __align__(16) Summary {
+  float f0;     // G: CTA max; others: chunk max (NaN if the chunk has a NaN)
+  float f1;     // P, and H without top-k: chunk mass relative to f0
+  int32_t i0;   // G: first index of the max; K: candidate count; H: 16-bit key of f0
+  uint32_t u0;  // NaN seen
 };
 
 struct SampleSmem {
-  Slot push[2][kMaxClusterCtas];
-  Slot gather[kMaxClusterCtas];  // collected by the leader only
+  unsigned long long bar;  // the leader's gather mbarrier
+  Summary gather[kMaxClusterCtas];
   uint32_t cnt[kMaxClusterCtas];
-  PullBuf pull[2];
+  uint32_t ties[kMaxClusterCtas];
+  unsigned long long cmass[kMaxClusterCtas][kWarps];
   unsigned long long scan[kBuckets];
-  uint32_t hlo[kBuckets];  // CTA-local histogram (list selects)
+  uint32_t hlo[kBuckets];  // histograms of the list and fallback selects
   uint32_t hhi[kBuckets];
   unsigned long long wl[kWarps];
   float wf[kWarps];
@@ -91,18 +105,14 @@ struct SampleSmem {
   int32_t wi[kWarps];
   float wt[kWarps];
   float wz[kWarps];
-  float bf[4];
-  int32_t bi[4];
-  uint32_t bu[4];
-  unsigned long long bl[4];
+  int32_t bi[8];
+  unsigned long long bl[8];
 };
 
+static_assert(sizeof(Summary) == 16, "one 16-byte store per summary");
+static_assert(offsetof(SampleSmem, gather) % 16 == 0, "16-byte stores into gather");
+
 // ----------------------------------------------------------------- element access
-//
-// The slice is an array of 16-byte vectors.  Thread (warp w, lane l) owns the
-// vectors (w*NV + j)*32 + l, j < NV, so every warp owns a contiguous
-// sub-slice.  Element c of the thread's vector j has row index
-// lane_base + j*32*VW + c.
 
 template <bool BF16>
 struct Layout {
@@ -122,45 +132,115 @@ __device__ __forceinline__ float elem(uint32_t word, int h) {
 
 // f(x, e) for the elements of one 16-byte vector whose first index is e0.
 template <bool BF16, typename F>
-__device__ __forceinline__ void for_vector(const uint4& v, int e0, F&& f) {
+__device__ __forceinline__ void for_vec(const uint32_t (&w)[4], int e0, F&& f) {
   using L = Layout<BF16>;
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int q = 0; q < 4; ++q) {
 #pragma unroll
-    for (int h = 0; h < L::EPW; ++h) f(elem<BF16>(w[c], h), e0 + c * L::EPW + h);
-  }
-}
-
-// NaN-propagating maximum of one 16-byte vector.
-template <bool BF16>
-__device__ __forceinline__ float vector_max(const uint4& v) {
-  if constexpr (BF16) {
-    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
-    return fmax_nan(elem<true>(m2, 0), elem<true>(m2, 1));
-  } else {
-    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
-                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+    for (int h = 0; h < L::EPW; ++h) f(elem<BF16>(w[q], h), e0 + q * L::EPW + h);
   }
 }
 
 struct Ctx {
   int tid, lane, warp;
   uint32_t crank, csize;
-  int row, V;
-  int lane_base;  // row index of the thread's first element
-  const uint4* sv;
 };
 
-// f(x, e) for every element the thread owns, in ascending index order.
-template <bool BF16, int NV, typename F>
-__device__ __forceinline__ void for_each(const Ctx& c, F&& f) {
+// Row index of the first element of vector j of (warp, lane) in chunk `chunk`.
+template <bool BF16, int NV>
+__device__ __forceinline__ int vec_base(int chunk, int warp, int lane, int j) {
   using L = Layout<BF16>;
-#pragma unroll 2
+  return chunk * (kThreads * NV * L::VW) + ((warp * NV + j) * 32 + lane) * L::VW;
+}
+
+// f(x, e) for every element of the thread's registers (chunk `chunk`).
+template <bool BF16, int NV, typename F>
+__device__ __forceinline__ void for_regs(const uint32_t (&d)[NV][4], int chunk, int warp,
+                                         int lane, F&& f) {
+#pragma unroll
+  for (int j = 0; j < NV; ++j) for_vec<BF16>(d[j], vec_base<BF16, NV>(chunk, warp, lane, j), f);
+}
+
+// Loads the thread's NV vectors of chunk `chunk` of `row`.  Elements past V
+// read as -inf.  VEC: the row start and V * elt are 16-byte aligned, so a
+// whole vector loads with one instruction; otherwise (and for the vector that
+// straddles V) elements load one by one.
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ void load_chunk(const SampleParams& P, int row, int chunk, int warp,
+                                           int lane, uint32_t (&d)[NV][4]) {
+  using L = Layout<BF16>;
+  const char* rp = static_cast<const char*>(P.logits) +
+                   static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) * L::ELT;
+  const int V = P.V;
+#pragma unroll
   for (int j = 0; j < NV; ++j) {
-    const uint4 v = c.sv[(c.warp * NV + j) * 32 + c.lane];
-    for_vector<BF16>(v, c.lane_base + j * 32 * L::VW, f);
+    const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+    if (VEC && e0 + L::VW <= V) {
+      const uint4 v = ld_stream_v4(rp + static_cast<size_t>(e0) * L::ELT);
+      d[j][0] = v.x;
+      d[j][1] = v.y;
+      d[j][2] = v.z;
+      d[j][3] = v.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (BF16) {
+          const int e = e0 + 2 * q;
+          const uint32_t lo = e < V ? reinterpret_cast<const uint16_t*>(rp)[e] : 0xff80u;
+          const uint32_t hi = e + 1 < V ? reinterpret_cast<const uint16_t*>(rp)[e + 1] : 0xff80u;
+          d[j][q] = lo | (hi << 16);
+        } else {
+          const int e = e0 + q;
+          d[j][q] = e < V ? reinterpret_cast<const uint32_t*>(rp)[e] : 0xff800000u;
+        }
+      }
+    }
   }
+}
+
+// NaN-propagating maximum of the thread's registers.
+template <bool BF16, int NV>
+__device__ __forceinline__ float regs_max(const uint32_t (&d)[NV][4]) {
+  if constexpr (BF16) {
+    uint32_t m2 = d[0][0];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (j != 0 || q != 0) m2 = bf16x2_max_nan(m2, d[j][q]);
+      }
+    }
+    return fmax_nan(elem<true>(m2, 0), elem<true>(m2, 1));
+  } else {
+    float m = __uint_as_float(d[0][0]);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (j != 0 || q != 0) m = fmax_nan(m, __uint_as_float(d[j][q]));
+      }
+    }
+    return m;
+  }
+}
+
+// 16-bit order-preserving key of a bf16 value held as a float (-0 folded).
+__device__ __forceinline__ uint32_t key16(float x) { return float_key(x) >> 16; }
+
+__device__ __forceinline__ float key16_float(uint32_t k) { return key_float(k << 16); }
+
+// Weight of logit x relative to the row maximum m: 2^((x - m) * log2(e) / T).
+// The one formula used wherever two results must agree to the last bit.
+__device__ __forceinline__ float weight(float x, float m, float c2) {
+  return ex2(__fmul_rn(__fsub_rn(x, m), c2));
+}
+
+__device__ __forceinline__ unsigned long long mass_fx(float w) {
+  return static_cast<unsigned long long>(__float2ull_rz(w * kMassScale));
+}
+
+__device__ __forceinline__ unsigned long long pick4(const unsigned long long (&a)[4], int j) {
+  return j == 0 ? a[0] : (j == 1 ? a[1] : (j == 2 ? a[2] : a[3]));
 }
 
 // ----------------------------------------------------------------- block helpers
@@ -192,6 +272,17 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* s_w, int lane, int war
   return before + incl - v;
 }
 
+template <typename T>
+__device__ __forceinline__ T block_sum(T v, T* s_w, int lane, int warp) {
+  v = warp_sum(v);
+  if (lane == 0) s_w[warp] = v;
+  __syncthreads();
+  T r = 0;
+  for (int w = 0; w < kWarps; ++w) r += s_w[w];
+  __syncthreads();
+  return r;
+}
+
 __device__ __forceinline__ int block_max_int(int v, int32_t* s_w, int lane, int warp) {
   v = __reduce_max_sync(kFull, v);
   if (lane == 0) s_w[warp] = v;
@@ -212,6 +303,12 @@ __device__ __forceinline__ int block_min_int(int v, int32_t* s_w, int lane, int 
   for (int w = 1; w < kWarps; ++w) r = min(r, s_w[w]);
   __syncthreads();
   return r;
+}
+
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(kFull, v, o));
+  return v;
 }
 
 // Radix-select step: thread t holds the weight `tot` of bucket t (t < 256).
@@ -237,28 +334,6 @@ __device__ __forceinline__ void atomic_add_u64_split(uint32_t* lo, uint32_t* hi,
   const uint32_t old = atomicAdd(lo, vlo);
   const uint32_t carry = (old + vlo < old) ? 1u : 0u;
   if (vhi + carry != 0u) atomicAdd(hi, vhi + carry);
-}
-
-__device__ __forceinline__ unsigned long long mass_fx(float w) {
-  return static_cast<unsigned long long>(__float2ull_rz(w * kMassScale));
-}
-
-// ----------------------------------------------------------------- exchange
-
-// Pushes this CTA's slot into slot[crank] of every CTA, then waits at the
-// cluster barrier.  Returns the buffer to read locally.
-__device__ __forceinline__ const Slot* push_exchange(SampleSmem& sm, int& ph, const Ctx& c,
-                                                     const Slot& mine) {
-  Slot* buf = sm.push[ph & 1];
-  if (c.tid < static_cast<int>(c.csize)) {
-    const uint32_t a = dsmem(&buf[c.crank], static_cast<uint32_t>(c.tid));
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&mine);
-    st_dsmem_v4(a, w[0], w[1], w[2], w[3]);
-    st_dsmem_v4(a + 16, w[4], w[5], w[6], w[7]);
-  }
-  cluster_sync();
-  ++ph;
-  return buf;
 }
 
 // ----------------------------------------------------------------- output
@@ -297,86 +372,339 @@ __device__ __forceinline__ float warp_sort_desc(float v, int lane) {
   return v;
 }
 
+// ----------------------------------------------------------------- chunk search
+//
+// These re-read a chunk from global memory (an L2 hit: the chunk was just
+// streamed) one vector at a time, so they hold no register copy of it.
+
+// Loads vector j of (warp, lane) in chunk `chunk` of `row` (see load_chunk).
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ void load_vec(const SampleParams& P, int row, int e0,
+                                         uint32_t (&w)[4]) {
+  using L = Layout<BF16>;
+  const char* rp = static_cast<const char*>(P.logits) +
+                   static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) * L::ELT;
+  const int V = P.V;
+  if (VEC && e0 + L::VW <= V) {
+    const uint4 v = *reinterpret_cast<const uint4*>(rp + static_cast<size_t>(e0) * L::ELT);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if constexpr (BF16) {
+        const int e = e0 + 2 * q;
+        const uint32_t lo = e < V ? reinterpret_cast<const uint16_t*>(rp)[e] : 0xff80u;
+        const uint32_t hi = e + 1 < V ? reinterpret_cast<const uint16_t*>(rp)[e + 1] : 0xff80u;
+        w[q] = lo | (hi << 16);
+      } else {
+        const int e = e0 + q;
+        w[q] = e < V ? reinterpret_cast<const uint32_t*>(rp)[e] : 0xff800000u;
+      }
+    }
+  }
+}
+
+// f(x, e) for every element the thread owns in chunk `chunk`, index order
+// within the thread.
+template <bool BF16, int NV, bool VEC, typename F>
+__device__ __forceinline__ void for_chunk(const SampleParams& P, int row, int chunk, int warp,
+                                          int lane, F&& f) {
+#pragma unroll 1
+  for (int j = 0; j < NV; ++j) {
+    const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+    uint32_t w[4];
+    load_vec<BF16, NV, VEC>(P, row, e0, w);
+    for_vec<BF16>(w, e0, f);
+  }
+}
+
+// The first element, in index order, of chunk `chunk` of `row` at which the
+// running sum of f(x, e) exceeds tau.  Returns its row index; when rounding
+// leaves tau at or above the running sum where it was expected to cross, the
+// last element with f > 0 before that point; -1 if the chunk has no element
+// with f > 0.  T is unsigned long long (exact: counts or fixed-point masses)
+// or float.  Index order is (warp, vector j, lane, element): the search
+// narrows warp -> vector -> lane -> element.
+template <bool BF16, int NV, bool VEC, typename T, typename F>
+__device__ __forceinline__ int chunk_search(const SampleParams& P, int row, int chunk, F&& f,
+                                            T tau, SampleSmem& sm, int tid, int lane, int warp) {
+  T tt = 0;
+  int last = -1;
+  for_chunk<BF16, NV, VEC>(P, row, chunk, warp, lane, [&](float x, int e) {
+    const T w = f(x, e);
+    tt += w;
+    if (w > T(0)) last = e;
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(kFull, tt, o);
+  const int wl = __reduce_max_sync(kFull, last);
+  if (lane == 0) {
+    if constexpr (sizeof(T) == 8) {
+      sm.wl[warp] = static_cast<unsigned long long>(tt);
+    } else {
+      sm.wf[warp] = static_cast<float>(tt);
+    }
+    sm.wi[warp] = wl;
+  }
+  __syncthreads();
+  int wstar = -1, lastpos = -1;
+  T tw = 0, acc = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    T ww;
+    if constexpr (sizeof(T) == 8) {
+      ww = static_cast<T>(sm.wl[w]);
+    } else {
+      ww = static_cast<T>(sm.wf[w]);
+    }
+    if (wstar < 0 && ww > T(0) && tau < acc + ww) {
+      wstar = w;
+      tw = tau - acc;
+    }
+    lastpos = max(lastpos, sm.wi[w]);
+    acc += ww;
+  }
+  if (warp == wstar) {
+    int found = -1;
+    T a = 0;
+#pragma unroll 1
+    for (int j = 0; j < NV && found < 0; ++j) {
+      const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+      uint32_t v[4];
+      load_vec<BF16, NV, VEC>(P, row, e0, v);
+      T sj = 0;
+      for_vec<BF16>(v, e0, [&](float x, int e) { sj += f(x, e); });
+      const T incl = warp_inclusive_scan(sj, lane);
+      const T tot = __shfl_sync(kFull, incl, 31);
+      if (tw < a + tot) {
+        const unsigned bal = __ballot_sync(kFull, tw < a + incl);
+        const int lx = bal ? __ffs(bal) - 1 : 31;
+        int sel = -1, lpos = -1;
+        if (lane == lx) {
+          T run = a + incl - sj;
+          for_vec<BF16>(v, e0, [&](float x, int e) {
+            const T w = f(x, e);
+            run += w;
+            if (w > T(0)) {
+              lpos = e;
+              if (sel < 0 && tw < run) sel = e;
+            }
+          });
+          if (sel < 0) sel = lpos;
+        }
+        found = __shfl_sync(kFull, sel, lx);
+        if (found < 0) found = INT_MAX;  // nothing found where expected: rounding
+      }
+      a += tot;
+    }
+    if (lane == 0) sm.bi[6] = found;
+  }
+  __syncthreads();
+  int res = lastpos;
+  if (wstar >= 0) {
+    res = sm.bi[6];
+    if (res < 0 || res == INT_MAX) res = sm.wi[wstar];
+  }
+  __syncthreads();
+  return res;
+}
+
+// The leader's copy of one chunk in shared memory, same layout as the
+// registers: vector j of (warp, lane) at sv[(warp * NV + j) * 32 + lane].
+// All NV loads of a thread are issued together (one L2 round trip); each
+// thread reads back only its own vectors, so no barrier is needed.
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ void stage_chunk(const SampleParams& P, int row, int chunk, uint4* sv,
+                                            int warp, int lane) {
+  uint32_t d[NV][4];
+  load_chunk<BF16, NV, VEC>(P, row, chunk, warp, lane, d);
+#pragma unroll
+  for (int j = 0; j < NV; ++j) {
+    sv[(warp * NV + j) * 32 + lane] = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
+  }
+}
+
+template <bool BF16, int NV, typename F>
+__device__ __forceinline__ void for_staged(const uint4* sv, int chunk, int warp, int lane, F&& f) {
+#pragma unroll 2
+  for (int j = 0; j < NV; ++j) {
+    const uint4 v = sv[(warp * NV + j) * 32 + lane];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    for_vec<BF16>(w, vec_base<BF16, NV>(chunk, warp, lane, j), f);
+  }
+}
+
+// chunk_search over a staged chunk (same contract as chunk_search).
+template <bool BF16, int NV, typename T, typename F>
+__device__ __forceinline__ int staged_search(const uint4* sv, int chunk, F&& f, T tau,
+                                             SampleSmem& sm, int tid, int lane, int warp) {
+  T tt = 0;
+  int last = -1;
+  for_staged<BF16, NV>(sv, chunk, warp, lane, [&](float x, int e) {
+    const T w = f(x, e);
+    tt += w;
+    if (w > T(0)) last = e;
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(kFull, tt, o);
+  const int wl = __reduce_max_sync(kFull, last);
+  if (lane == 0) {
+    if constexpr (sizeof(T) == 8) {
+      sm.wl[warp] = static_cast<unsigned long long>(tt);
+    } else {
+      sm.wf[warp] = static_cast<float>(tt);
+    }
+    sm.wi[warp] = wl;
+  }
+  __syncthreads();
+  int wstar = -1, lastpos = -1;
+  T tw = 0, acc = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    T ww;
+    if constexpr (sizeof(T) == 8) {
+      ww = static_cast<T>(sm.wl[w]);
+    } else {
+      ww = static_cast<T>(sm.wf[w]);
+    }
+    if (wstar < 0 && ww > T(0) && tau < acc + ww) {
+      wstar = w;
+      tw = tau - acc;
+    }
+    lastpos = max(lastpos, sm.wi[w]);
+    acc += ww;
+  }
+  if (warp == wstar) {
+    int found = -1;
+    T a = 0;
+#pragma unroll 1
+    for (int j = 0; j < NV && found < 0; ++j) {
+      const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+      const uint4 v4 = sv[(warp * NV + j) * 32 + lane];
+      const uint32_t v[4] = {v4.x, v4.y, v4.z, v4.w};
+      T sj = 0;
+      for_vec<BF16>(v, e0, [&](float x, int e) { sj += f(x, e); });
+      const T incl = warp_inclusive_scan(sj, lane);
+      const T tot = __shfl_sync(kFull, incl, 31);
+      if (tw < a + tot) {
+        const unsigned bal = __ballot_sync(kFull, tw < a + incl);
+        const int lx = bal ? __ffs(bal) - 1 : 31;
+        int sel = -1, lpos = -1;
+        if (lane == lx) {
+          T run = a + incl - sj;
+          for_vec<BF16>(v, e0, [&](float x, int e) {
+            const T w = f(x, e);
+            run += w;
+            if (w > T(0)) {
+              lpos = e;
+              if (sel < 0 && tw < run) sel = e;
+            }
+          });
+          if (sel < 0) sel = lpos;
+        }
+        found = __shfl_sync(kFull, sel, lx);
+        if (found < 0) found = INT_MAX;  // nothing found where expected: rounding
+      }
+      a += tot;
+    }
+    if (lane == 0) sm.bi[6] = found;
+  }
+  __syncthreads();
+  int res = lastpos;
+  if (wstar >= 0) {
+    res = sm.bi[6];
+    if (res < 0 || res == INT_MAX) res = sm.wi[wstar];
+  }
+  __syncthreads();
+  return res;
+}
+
 // ----------------------------------------------------------------- list selects
 //
 // The leader's list holds n entries (value, row index) in ascending index
 // order.  These run in one CTA with __syncthreads only.
 
-// Smallest and largest key of the list entries satisfying `keep`.
-template <typename K>
-__device__ __forceinline__ void list_key_range(const float* val, int n, K&& keep, SampleSmem& sm,
-                                               const Ctx& c, uint32_t* kmin, uint32_t* kmax) {
-  uint32_t lo = 0xffffffffu, hi = 0u;
+// Radix select over the list: the key t such that the weight of entries with
+// key > t is < target <= the weight with key >= t.  weight_of(i) is 1 (count)
+// or a fixed-point mass; entries with keep(i) false weigh nothing.  Returns t
+// and the weight still needed from the entries equal to t in *rem.  Only the
+// key bits on which the kept entries differ are examined, 8 at a time.
+template <bool MASS, typename K, typename W>
+__device__ __forceinline__ float list_select(const float* val, int n, K&& keep, W&& weight_of,
+                                             unsigned long long target, SampleSmem& sm,
+                                             const Ctx& c, unsigned long long* rem_out) {
+  uint32_t kand = 0xffffffffu, kor = 0u;
   for (int i = c.tid; i < n; i += kThreads) {
     if (keep(i)) {
       const uint32_t k = float_key(val[i]);
-      lo = min(lo, k);
-      hi = max(hi, k);
+      kand &= k;
+      kor |= k;
     }
   }
-  lo = __reduce_min_sync(kFull, lo);
-  hi = __reduce_max_sync(kFull, hi);
+  kand = __reduce_and_sync(kFull, kand);
+  kor = __reduce_or_sync(kFull, kor);
   if (c.lane == 0) {
-    sm.wu[c.warp] = lo;
-    sm.wi[c.warp] = static_cast<int32_t>(hi);
+    sm.wu[c.warp] = kand;
+    sm.wi[c.warp] = static_cast<int32_t>(kor);
   }
   __syncthreads();
-  uint32_t a = 0xffffffffu, b = 0u;
+  uint32_t a = 0xffffffffu, o = 0u;
+#pragma unroll
   for (int w = 0; w < kWarps; ++w) {
-    a = min(a, sm.wu[w]);
-    b = max(b, static_cast<uint32_t>(sm.wi[w]));
+    a &= sm.wu[w];
+    o |= static_cast<uint32_t>(sm.wi[w]);
   }
-  __syncthreads();
-  *kmin = a;
-  *kmax = b;
-}
-
-// Radix select over the list: the key t such that the weight of entries with
-// key > t is < target <= the weight with key >= t.  weight(i) is 1 (count) or
-// a fixed-point mass; entries with keep(i) false weigh nothing.  Returns t and
-// the weight still needed from the entries equal to t in *rem.
-template <bool MASS, typename K, typename W>
-__device__ __forceinline__ float list_select(const float* val, int n, K&& keep, W&& weight,
-                                             unsigned long long target, SampleSmem& sm,
-                                             const Ctx& c, unsigned long long* rem_out) {
-  uint32_t kmin, kmax;
-  list_key_range(val, n, keep, sm, c, &kmin, &kmax);
   unsigned long long rem = target;
-  if (kmin == kmax) {
+  const uint32_t diff = a ^ o;  // bits on which the kept keys differ
+  if (diff == 0u) {
+    __syncthreads();
     *rem_out = rem;
-    return key_float(kmin);
+    return key_float(a);
   }
-  const int top = 31 - __clz(kmin ^ kmax);
-  uint32_t prefix = static_cast<uint32_t>(
-      static_cast<unsigned long long>(kmin) & ~((2ull << top) - 1ull));
-  for (int hi = top; hi >= 0; hi -= 8) {
-    const int lo = hi >= 7 ? hi - 7 : 0;
+  const int top = 31 - __clz(diff);
+  const int bottom = __ffs(diff) - 1;
+  // Bits above `top` and below `bottom` are the same in every kept key.
+  uint32_t prefix = a & (top == 31 ? 0u : (0xffffffffu << (top + 1)));
+  prefix |= a & ((1u << bottom) - 1u);
+  for (int hi = top; hi >= bottom; hi -= 8) {
+    const int lo = max(hi - 7, bottom);
     const uint32_t dmask = (1u << (hi - lo + 1)) - 1u;
-    const uint32_t amask =
-        static_cast<uint32_t>(~((2ull << hi) - 1ull));  // bits above the digit
+    const uint32_t amask = hi == 31 ? 0u : (0xffffffffu << (hi + 1));  // bits above the digit
     sm.hlo[c.tid] = 0u;
-    sm.hhi[c.tid] = 0u;
+    if constexpr (MASS) sm.hhi[c.tid] = 0u;
     __syncthreads();
     for (int i = c.tid; i < n; i += kThreads) {
       if (!keep(i)) continue;
       const uint32_t key = float_key(val[i]);
       if ((key & amask) != (prefix & amask)) continue;
-      const uint32_t d = (key >> lo) & dmask;
+      const uint32_t dg = (key >> lo) & dmask;
       if constexpr (MASS) {
-        atomic_add_u64_split(&sm.hlo[d], &sm.hhi[d], weight(i));
+        atomic_add_u64_split(&sm.hlo[dg], &sm.hhi[dg], weight_of(i));
       } else {
-        atomicAdd(&sm.hlo[d], 1u);
+        atomicAdd(&sm.hlo[dg], 1u);
       }
     }
     __syncthreads();
     const unsigned long long tot =
         MASS ? ((static_cast<unsigned long long>(sm.hhi[c.tid]) << 32) | sm.hlo[c.tid])
              : static_cast<unsigned long long>(sm.hlo[c.tid]);
-    unsigned long long above;
-    const int b = select_bucket(tot, rem, sm, &above, c.tid, c.lane, c.warp);
-    rem -= above;
+    // Suffix sums S(t) over buckets; the bucket b with S(b + 1) < rem <= S(b).
+    const unsigned long long sw = warp_suffix_scan(tot, c.lane);
+    if (c.lane == 0) sm.wl[c.warp] = sw;
+    __syncthreads();
+    unsigned long long S = sw;
+    for (int w = c.warp + 1; w < kWarps; ++w) S += sm.wl[w];
+    if (S >= rem && S - tot < rem) {
+      sm.bi[4] = c.tid;
+      sm.bl[6] = S - tot;
+    }
+    __syncthreads();
+    const int b = sm.bi[4];
+    rem -= sm.bl[6];
     prefix |= static_cast<uint32_t>(b) << lo;
   }
+  __syncthreads();
   *rem_out = rem;
   return key_float(prefix);
 }
@@ -458,21 +786,16 @@ __device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&
   return pos >= 0 ? idx[pos] : -1;
 }
 
-// ----------------------------------------------------------------- the kernel
-
-// ----------------------------------------------------------------- leader finish
-
-// The leader CTA holds every candidate of the row in its list, region r
+// K rows.  The leader holds every candidate of the row in its list, region r
 // (entries r*R .. r*R + cnt[r]) coming from CTA r, each region in index
 // order.  Packs the regions, then finishes exactly on the list: top-k (count
 // select, ties by index), top-p inside K (mass select on 2^-40 fixed-point
-// weights; target_fx is given for rows without top-k), renormalisation and
-// the inverse-CDF draw.  Emits the token and, if asked, the probabilities.
-__device__ __forceinline__ void leader_finish(const SampleParams& P, SampleSmem& sm, const Ctx& c,
-                                              float* l_val, int32_t* l_idx, int R, int row,
-                                              bool topk_row, int k, bool use_p, float p,
-                                              unsigned long long target_fx, float m, float c2,
-                                              float u, int st, float* q_row) {
+// weights), renormalisation and the inverse-CDF draw.  Emits the token and,
+// if asked, the probabilities of the kept tokens.
+static __device__ __noinline__ void leader_finish_list(const SampleParams& P, SampleSmem& sm,
+                                                const Ctx& c, float* l_val, int32_t* l_idx, int R,
+                                                int row, int k, bool use_p, float p, float m,
+                                                float c2, float u, int st, float* q_row) {
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   int n = 0;
   for (uint32_t r = 0; r < c.csize; ++r) n += static_cast<int>(sm.cnt[r]);
@@ -508,44 +831,31 @@ __device__ __forceinline__ void leader_finish(const SampleParams& P, SampleSmem&
       __syncthreads();
     }
   }
-  int cut_k = n;
-  float tk = -INFINITY;
-  if (topk_row) {
-    unsigned long long rk;
-    tk = list_select<false>(l_val, n, [](int) { return true; }, [](int) { return 1ull; },
-                            static_cast<unsigned long long>(k), sm, c, &rk);
-    const float tkv = tk;
-    cut_k = list_tie_cut(n, [&](int i) { return l_val[i] == tkv; }, rk, sm, c);
-  }
-  const float tkv = tk;
-  const int ckv = cut_k;
-  auto in_k = [&](int i) { return l_val[i] > tkv || (l_val[i] == tkv && i < ckv); };
-  auto w_of = [&](int i) { return ex2((l_val[i] - m) * c2); };
+  unsigned long long rk;
+  const float tk = list_select<false>(l_val, n, [](int) { return true; },
+                                      [](int) { return 1ull; },
+                                      static_cast<unsigned long long>(k), sm, c, &rk);
+  const int cut_k = list_tie_cut(n, [&](int i) { return l_val[i] == tk; }, rk, sm, c);
+  auto in_k = [&](int i) { return l_val[i] > tk || (l_val[i] == tk && i < cut_k); };
+  auto w_of = [&](int i) { return weight(l_val[i], m, c2); };
   float tp = tk;
   int cut_p = cut_k;
   if (use_p) {
-    if (topk_row) {
-      unsigned long long zfx = 0;
-      for (int i = tid; i < n; i += kThreads) {
-        if (in_k(i)) zfx += mass_fx(w_of(i));
-      }
-      zfx = warp_sum(zfx);
-      if (lane == 0) sm.wl[warp] = zfx;
-      __syncthreads();
-      unsigned long long z = 0;
-      for (int w = 0; w < kWarps; ++w) z += sm.wl[w];
-      __syncthreads();
-      const double t = static_cast<double>(z) * static_cast<double>(p);
-      target_fx = static_cast<unsigned long long>(ceil(t));
-      if (target_fx < 1) target_fx = 1;
-      if (target_fx > z) target_fx = z;
+    unsigned long long zfx = 0;
+    for (int i = tid; i < n; i += kThreads) {
+      if (in_k(i)) zfx += mass_fx(w_of(i));
     }
+    const unsigned long long z = block_sum<unsigned long long>(zfx, sm.wl, lane, warp);
+    unsigned long long target_fx =
+        static_cast<unsigned long long>(ceil(static_cast<double>(z) * static_cast<double>(p)));
+    if (target_fx < 1) target_fx = 1;
+    if (target_fx > z) target_fx = z;
     unsigned long long rem;
     tp = list_select<true>(l_val, n, in_k, [&](int i) { return mass_fx(w_of(i)); }, target_fx, sm,
                            c, &rem);
     // Members of the threshold group share one weight wt: member j (index
     // order) is kept iff above + j * wt < target, i.e. j < ceil(rem / wt).
-    const unsigned long long wt = mass_fx(ex2((tp - m) * c2));
+    const unsigned long long wt = mass_fx(weight(tp, m, c2));
     const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
     const float tpv = tp;
     cut_p = list_tie_cut(n, [&](int i) { return l_val[i] == tpv && in_k(i); }, rp, sm, c);
@@ -564,78 +874,22 @@ __device__ __forceinline__ void leader_finish(const SampleParams& P, SampleSmem&
   }
 }
 
-// ----------------------------------------------------------------- CTA-local selects
+// ----------------------------------------------------------------- CTA-local top-k
 
-// Among this CTA's elements with member(x, e), the first r in index order:
-// returns the element-index cutoff (members with e < cutoff), INT_MAX if there
-// are no more than r members.  CTA barriers only.
-template <bool BF16, int NV, typename M>
-__device__ __forceinline__ int cta_tie_cut(const Ctx& c, SampleSmem& sm, M&& member,
-                                           unsigned long long r) {
-  using L = Layout<BF16>;
-  const int lane = c.lane, warp = c.warp;
-  uint32_t cnt = 0;
-  for_each<BF16, NV>(c, [&](float x, int e) { cnt += member(x, e) ? 1u : 0u; });
-  const uint32_t wc = __reduce_add_sync(kFull, cnt);
-  if (lane == 0) sm.wu[warp] = wc;
-  __syncthreads();
-  unsigned long long cum = 0;
-  int wstar = -1;
-  uint32_t rw = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (wstar < 0 && cum + sm.wu[w] >= r) {
-      wstar = w;
-      rw = static_cast<uint32_t>(r - cum);
-    }
-    cum += sm.wu[w];
-  }
-  if (r == 0) wstar = -2;
-  if (c.tid == 0) sm.bi[1] = wstar == -2 ? INT_MIN : INT_MAX;
-  __syncthreads();
-  if (warp == wstar) {
-    uint32_t acc = 0;
-    int found = INT_MAX;
-    for (int j = 0; j < NV; ++j) {
-      const uint4 v = c.sv[(warp * NV + j) * 32 + lane];
-      const int e0 = c.lane_base + j * 32 * L::VW;
-      uint32_t cj = 0;
-      for_vector<BF16>(v, e0, [&](float x, int e) { cj += member(x, e) ? 1u : 0u; });
-      const uint32_t incl = warp_inclusive_scan(cj, lane);
-      const uint32_t stot = __shfl_sync(kFull, incl, 31);
-      if (acc + stot >= rw) {
-        const unsigned bal = __ballot_sync(kFull, acc + incl >= rw);
-        const int lx = __ffs(bal) - 1;
-        int sel = INT_MAX;
-        if (lane == lx) {
-          uint32_t need = rw - (acc + incl - cj);
-          for_vector<BF16>(v, e0, [&](float x, int e) {
-            if (member(x, e)) {
-              if (need == 1 && sel == INT_MAX) sel = e;
-              --need;
-            }
-          });
-        }
-        found = __shfl_sync(kFull, sel, lx);
-        break;
-      }
-      acc += stot;
-    }
-    if (lane == 0) sm.bi[1] = found == INT_MAX ? INT_MAX : found + 1;
-  }
-  __syncthreads();
-  const int cut = sm.bi[1];
-  __syncthreads();
-  return cut;
-}
-
-// Exact top-k of this CTA's elements with keep(x, e), by (value desc, index
-// asc): returns t and *cut such that the top-k are {keep, x > t} and
-// {keep, x == t, e < cut}.  Radix select over keys with 32-bit shared atomics.
-template <bool BF16, int NV, typename K>
-__device__ __forceinline__ float cta_select_topk(const Ctx& c, SampleSmem& sm, K&& keep,
-                                                 unsigned long long k, int* cut) {
+// Exact top-k of this CTA's elements x >= theta (e < V), by (value desc,
+// index asc): returns t and *cut such that they are {x > t} and {x == t,
+// e < cut}.  Radix select over keys with 32-bit shared atomics, re-reading
+// the chunk from global memory; used only when ties overflow a K row's list
+// region.
+template <bool BF16, int NV, bool VEC>
+__device__ __noinline__ float cta_select_topk(const SampleParams& P, SampleSmem& sm, const Ctx& c,
+                                              int row, float theta, unsigned long long k,
+                                              int* cut) {
+  const int chunk = static_cast<int>(c.crank);
+  const int V = P.V;
+  auto keep = [&](float x, int e) { return x >= theta && e < V; };
   uint32_t lo = 0xffffffffu, hi = 0u;
-  for_each<BF16, NV>(c, [&](float x, int e) {
+  for_chunk<BF16, NV, VEC>(P, row, chunk, c.warp, c.lane, [&](float x, int e) {
     if (keep(x, e)) {
       const uint32_t key = float_key(x);
       lo = min(lo, key);
@@ -666,7 +920,7 @@ __device__ __forceinline__ float cta_select_topk(const Ctx& c, SampleSmem& sm, K
       const uint32_t amask = static_cast<uint32_t>(~((2ull << hb) - 1ull));
       sm.hlo[c.tid] = 0u;
       __syncthreads();
-      for_each<BF16, NV>(c, [&](float x, int e) {
+      for_chunk<BF16, NV, VEC>(P, row, chunk, c.warp, c.lane, [&](float x, int e) {
         if (!keep(x, e)) return;
         const uint32_t key = float_key(x);
         if ((key & amask) == (prefix & amask)) atomicAdd(&sm.hlo[(key >> lb) & dmask], 1u);
@@ -679,67 +933,471 @@ __device__ __forceinline__ float cta_select_topk(const Ctx& c, SampleSmem& sm, K
     }
   }
   const float t = key_float(prefix);
-  *cut = cta_tie_cut<BF16, NV>(c, sm, [&](float x, int e) { return keep(x, e) && x == t; }, rem);
+  // Cut after the rem-th member equal to t (index order).
+  const int pos = chunk_search<BF16, NV, VEC, unsigned long long>(
+      P, row, chunk, [&](float x, int e) { return (keep(x, e) && x == t) ? 1ull : 0ull; },
+      rem - 1ull, sm, c.tid, c.lane, c.warp);
+  *cut = pos >= 0 ? pos + 1 : INT_MAX;
   return t;
 }
 
-// ----------------------------------------------------------------- the kernel
+// ----------------------------------------------------------------- exact fallback (F)
+//
+// The leader alone settles the row by radix passes over the row in global
+// memory (elements read one by one; used only when the fast kinds cannot).
+// Same decisions as the list and histogram paths: 2^-40 fixed-point masses,
+// ties by index.
 
-template <bool BF16, int NV, bool VEC>
-__device__ __forceinline__ void load_slice(const SampleParams& P, int row, int lane_base,
-                                           uint32_t (&d)[NV][4]) {
-  using L = Layout<BF16>;
+template <bool BF16>
+__device__ __forceinline__ float load_elem(const SampleParams& P, int row, int e) {
   const char* rp = static_cast<const char*>(P.logits) +
-                   static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) * L::ELT;
+                   static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) * (BF16 ? 2 : 4);
+  if constexpr (BF16) {
+    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(rp)[e]) << 16);
+  } else {
+    return reinterpret_cast<const float*>(rp)[e];
+  }
+}
+
+// Among the elements of the row with member(x, e), the position after the
+// r-th in index order (INT_MAX if there are fewer than r; r >= 1).
+template <bool BF16, typename M>
+__device__ __forceinline__ int row_tie_cut(const SampleParams& P, int row, M&& member,
+                                           unsigned long long r, SampleSmem& sm, const Ctx& c) {
   const int V = P.V;
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int e0 = lane_base + j * 32 * L::VW;
-    if (VEC && e0 + L::VW <= V) {
-      const uint4 v = ld_stream_v4(rp + static_cast<size_t>(e0) * L::ELT);
-      d[j][0] = v.x;
-      d[j][1] = v.y;
-      d[j][2] = v.z;
-      d[j][3] = v.w;
-    } else {
-      // Row tail or unaligned row: element loads, -inf past the end.
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if constexpr (BF16) {
-          const int e = e0 + 2 * q;
-          const uint32_t lo = e < V ? reinterpret_cast<const uint16_t*>(rp)[e] : 0xff80u;
-          const uint32_t hi = e + 1 < V ? reinterpret_cast<const uint16_t*>(rp)[e + 1] : 0xff80u;
-          d[j][q] = lo | (hi << 16);
-        } else {
-          const int e = e0 + q;
-          d[j][q] = e < V ? reinterpret_cast<const uint32_t*>(rp)[e] : 0xff800000u;
+  const int per = (V + kThreads - 1) / kThreads;
+  const int i0 = min(V, c.tid * per);
+  const int i1 = min(V, i0 + per);
+  unsigned long long cnt = 0;
+  for (int e = i0; e < i1; ++e) cnt += member(load_elem<BF16>(P, row, e), e) ? 1ull : 0ull;
+  unsigned long long total;
+  const unsigned long long before =
+      block_exclusive_scan<unsigned long long>(cnt, sm.wl, c.lane, c.warp, &total);
+  if (c.tid == 0) sm.bi[3] = INT_MAX;
+  __syncthreads();
+  if (r <= total && before < r && r <= before + cnt) {
+    unsigned long long need = r - before;
+    for (int e = i0; e < i1; ++e) {
+      if (member(load_elem<BF16>(P, row, e), e) && --need == 0) {
+        sm.bi[3] = e + 1;
+        break;
+      }
+    }
+  }
+  __syncthreads();
+  const int cut = sm.bi[3];
+  __syncthreads();
+  return cut;
+}
+
+// Radix select over the row: the key t with W(key > t) < target <= W(key >= t),
+// W the sum of wfx(x, e) over elements with keep(x, e).  *rem receives target
+// - W(key > t).
+template <bool BF16, bool MASS, typename K, typename W>
+__device__ __forceinline__ float row_select(const SampleParams& P, int row, K&& keep, W&& wfx,
+                                            unsigned long long target, SampleSmem& sm,
+                                            const Ctx& c, unsigned long long* rem_out) {
+  const int V = P.V;
+  uint32_t prefix = 0, pmask = 0;
+  unsigned long long rem = target;
+  for (int lvl = 0; lvl < 4; ++lvl) {
+    const int shift = 24 - 8 * lvl;
+    sm.hlo[c.tid] = 0u;
+    sm.hhi[c.tid] = 0u;
+    __syncthreads();
+    for (int e = c.tid; e < V; e += kThreads) {
+      const float x = load_elem<BF16>(P, row, e);
+      if (!keep(x, e)) continue;
+      const uint32_t key = float_key(x);
+      if ((key & pmask) != prefix) continue;
+      const uint32_t dg = (key >> shift) & 0xffu;
+      if constexpr (MASS) {
+        atomic_add_u64_split(&sm.hlo[dg], &sm.hhi[dg], wfx(x, e));
+      } else {
+        atomicAdd(&sm.hlo[dg], 1u);
+      }
+    }
+    __syncthreads();
+    const unsigned long long tot =
+        MASS ? ((static_cast<unsigned long long>(sm.hhi[c.tid]) << 32) | sm.hlo[c.tid])
+             : static_cast<unsigned long long>(sm.hlo[c.tid]);
+    unsigned long long above;
+    const int b = select_bucket(tot, rem, sm, &above, c.tid, c.lane, c.warp);
+    rem -= above;
+    prefix |= static_cast<uint32_t>(b) << shift;
+    pmask |= 0xffu << shift;
+  }
+  *rem_out = rem;
+  return key_float(prefix);
+}
+
+template <bool BF16>
+__device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& sm, const Ctx& c,
+                                             int row, int k, bool use_p, float p, float u,
+                                             float m, float c2, int st, float* q_row) {
+  const int V = P.V;
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  // ---- top-k: the k-th key by count, ties cut by index.
+  float tk = -INFINITY;
+  int ck = INT_MAX;
+  if (k < V) {
+    unsigned long long rk;
+    tk = row_select<BF16, false>(P, row, [](float, int) { return true; },
+                                 [](float, int) { return 1ull; },
+                                 static_cast<unsigned long long>(k), sm, c, &rk);
+    const float tkv = tk;
+    ck = row_tie_cut<BF16>(P, row, [&](float x, int) { return x == tkv; }, rk, sm, c);
+  }
+  const float tkf = tk;
+  const int ckf = ck;
+  auto in_k = [&](float x, int e) { return x > tkf || (x == tkf && e < ckf); };
+  auto wfx = [&](float x, int) { return mass_fx(weight(x, m, c2)); };
+  // ---- top-p inside K: mass select on fixed-point weights.
+  float tp = tk;
+  int cp = ck;
+  if (use_p) {
+    unsigned long long z = 0;
+    for (int e = tid; e < V; e += kThreads) {
+      const float x = load_elem<BF16>(P, row, e);
+      if (in_k(x, e)) z += wfx(x, e);
+    }
+    z = block_sum<unsigned long long>(z, sm.wl, lane, warp);
+    unsigned long long target =
+        static_cast<unsigned long long>(ceil(static_cast<double>(z) * static_cast<double>(p)));
+    if (target < 1) target = 1;
+    if (target > z) target = z;
+    unsigned long long rem;
+    tp = row_select<BF16, true>(P, row, in_k, wfx, target, sm, c, &rem);
+    const unsigned long long wt = mass_fx(weight(tp, m, c2));
+    const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
+    const float tpv = tp;
+    cp = row_tie_cut<BF16>(P, row, [&](float x, int e) { return x == tpv && in_k(x, e); }, rp, sm,
+                           c);
+    if (tp == tk && ck < cp) cp = ck;
+  }
+  const float tpf = tp;
+  const int cpf = cp;
+  auto in_s = [&](float x, int e) { return in_k(x, e) && (x > tpf || (x == tpf && e < cpf)); };
+  // ---- draw in index order over contiguous segments.
+  const int per = (V + kThreads - 1) / kThreads;
+  const int i0 = min(V, tid * per);
+  const int i1 = min(V, i0 + per);
+  unsigned long long seg = 0;
+  int last = -1;
+  for (int e = i0; e < i1; ++e) {
+    const float x = load_elem<BF16>(P, row, e);
+    if (in_s(x, e)) {
+      const unsigned long long w = wfx(x, e);
+      seg += w;
+      if (w > 0) last = e;
+    }
+  }
+  unsigned long long zs;
+  const unsigned long long before =
+      block_exclusive_scan<unsigned long long>(seg, sm.wl, lane, warp, &zs);
+  const unsigned long long tdraw =
+      static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(zs));
+  const int lastpos = block_max_int(last, sm.wi, lane, warp);
+  if (tid == 0) sm.bi[2] = lastpos;
+  __syncthreads();
+  if (seg > 0 && tdraw >= before && tdraw < before + seg) {
+    unsigned long long run = before;
+    int sel = last;
+    for (int e = i0; e < i1; ++e) {
+      const float x = load_elem<BF16>(P, row, e);
+      if (in_s(x, e)) {
+        run += wfx(x, e);
+        if (tdraw < run) {
+          sel = e;
+          break;
         }
       }
+    }
+    sm.bi[2] = sel;
+  }
+  __syncthreads();
+  const int tok = sm.bi[2];
+  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
+  if (q_row != nullptr) {
+    const float inv = 1.0f / (static_cast<float>(zs) / kMassScale);
+    for (int e = tid; e < V; e += kThreads) {
+      const float x = load_elem<BF16>(P, row, e);
+      q_row[e] = in_s(x, e) ? weight(x, m, c2) * inv : 0.0f;
     }
   }
 }
 
-// One cluster of C CTAs per row (grid C x B).  CTA r holds elements
-// [r*chunk, (r+1)*chunk) of its row: 16-byte loads into registers, copied
-// to shared memory when later passes need them.  Cross-CTA traffic is pushed
-// into the receiving CTA's shared memory.  The leader (rank 0) is the only
-// CTA that waits when it merely collects: the others arrive at the cluster
-// barrier and exit.
+// ----------------------------------------------------------------- histogram finish (H)
+
+// The leader merges the C count histograms (CTA r counted its elements per
+// 16-bit key over the kHistKeys keys below a_r = gather[r].i0, the key of its
+// maximum), settles top-k and top-p exactly, picks the chunk holding the draw,
+// re-reads it and finds the token.  Returns false, having emitted nothing,
+// when a cut lies below the merged window; the caller then runs the exact
+// fallback.
+template <int NV, bool VEC>
+__device__ __noinline__ bool leader_finish_hist(const SampleParams& P, SampleSmem& sm,
+                                                const Ctx& c, const uint32_t* hist, uint4* stage,
+                                                int row,
+                                                int k, bool use_p, float p, float u, float m,
+                                                float zrow, float c2, int st, float* q_row) {
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  const int C = static_cast<int>(c.csize);
+  const int V = P.V;
+  const bool topk = k < V;
+  const uint32_t A = key16(m);
+  // Count of CTA r at merged key i (key A - i); 0 above the CTA's maximum.
+  auto count_at = [&](int r, uint32_t i) -> uint32_t {
+    const uint32_t delta = A - static_cast<uint32_t>(sm.gather[r].i0);
+    if (i > A || i < delta) return 0u;
+    const uint32_t idx = i - delta;
+    return (hist[r * kHistWords + (idx >> 1)] >> ((idx & 1u) * 16u)) & 0xffffu;
+  };
+  // Merged key i (0 = the row maximum); thread t holds keys 4t .. 4t + 3.
+  uint32_t cnt[4];
+  unsigned long long wfx[4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const uint32_t i = static_cast<uint32_t>(4 * tid + jj);
+    uint32_t n = 0;
+    for (int r = 0; r < C; ++r) n += count_at(r, i);
+    cnt[jj] = n;
+    wfx[jj] = n ? mass_fx(weight(key16_float(A - i), m, c2)) : 0ull;
+  }
+  // ---- top-k by count: keys i < ik are wholly in K, key ik keeps rk members.
+  int ik = kHistKeys;
+  unsigned long long rk = 0;
+  if (topk) {
+    const uint32_t local = cnt[0] + cnt[1] + cnt[2] + cnt[3];
+    uint32_t total;
+    const uint32_t before = block_exclusive_scan<uint32_t>(local, sm.wu, lane, warp, &total);
+    if (total < static_cast<uint32_t>(k)) return false;  // k-th value below the window
+    int cand = INT_MAX;
+    uint32_t run = before;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      if (run < static_cast<uint32_t>(k) && run + cnt[jj] >= static_cast<uint32_t>(k)) {
+        cand = 4 * tid + jj;
+        sm.bl[0] = static_cast<unsigned long long>(k) - run;  // one owner
+      }
+      run += cnt[jj];
+    }
+    ik = block_min_int(cand, sm.wi, lane, warp);
+    rk = sm.bl[0];
+    __syncthreads();
+  }
+  unsigned long long mk[4];  // mass of K at each key
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int i = 4 * tid + jj;
+    mk[jj] = i < ik ? cnt[jj] * wfx[jj] : (i == ik ? rk * wfx[jj] : 0ull);
+  }
+  // ---- top-p inside K by mass: keys i < is wholly in S, key is keeps rs.
+  int is = ik;
+  unsigned long long rs = rk;
+  if (use_p) {
+    const unsigned long long local = mk[0] + mk[1] + mk[2] + mk[3];
+    unsigned long long zk;
+    const unsigned long long before =
+        block_exclusive_scan<unsigned long long>(local, sm.wl, lane, warp, &zk);
+    unsigned long long target;
+    if (topk) {
+      target =
+          static_cast<unsigned long long>(ceil(static_cast<double>(zk) * static_cast<double>(p)));
+      if (target > zk) target = zk;
+    } else {
+      target = static_cast<unsigned long long>(
+          ceil(static_cast<double>(zrow) * kMassScaleD * static_cast<double>(p)));
+      if (zk < target) return false;  // the top-p cut lies below the window
+    }
+    if (target < 1) target = 1;
+    int cand = INT_MAX;
+    unsigned long long run = before;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      if (run < target && run + mk[jj] >= target) {
+        cand = 4 * tid + jj;
+        // Members j of the cut key are kept iff run + j * w < target.
+        const unsigned long long rem = target - run;
+        unsigned long long rp = wfx[jj] == 0 ? ~0ull : (rem + wfx[jj] - 1) / wfx[jj];
+        if (cand == ik && rp > rk) rp = rk;
+        sm.bl[1] = rp;  // one owner
+      }
+      run += mk[jj];
+    }
+    is = block_min_int(cand, sm.wi, lane, warp);
+    rs = sm.bl[1];
+    __syncthreads();
+  }
+  if (is >= kHistKeys) return false;  // unreachable when the masses add up
+  // ---- per-chunk masses of S: keys above the cut wholly, then the cut key's
+  // members in chunk order (chunks are in index order).
+  for (int r = 0; r < C; ++r) {
+    unsigned long long part = 0;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int i = 4 * tid + jj;
+      if (i < is) part += count_at(r, static_cast<uint32_t>(i)) * wfx[jj];
+    }
+    part = warp_sum(part);
+    if (lane == 0) sm.cmass[r][warp] = part;
+  }
+  if ((is >> 2) == tid) sm.bl[2] = pick4(wfx, is & 3);
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned long long wcut = sm.bl[2];
+    unsigned long long zs = 0, ties_before = 0;
+    for (int r = 0; r < C; ++r) {
+      unsigned long long mr = 0;
+      for (int w = 0; w < kWarps; ++w) mr += sm.cmass[r][w];
+      const uint32_t ties = count_at(r, static_cast<uint32_t>(is));
+      unsigned long long kept = 0;
+      if (ties_before < rs) kept = min(static_cast<unsigned long long>(ties), rs - ties_before);
+      ties_before += ties;
+      sm.cnt[r] = static_cast<uint32_t>(kept);
+      sm.ties[r] = ties;
+      mr += kept * wcut;
+      sm.cmass[r][0] = mr;
+      zs += mr;
+    }
+    const unsigned long long tdraw =
+        static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(zs));
+    unsigned long long cum = 0, tau = 0;
+    int cstar = -1, clast = -1;
+    for (int r = 0; r < C; ++r) {
+      const unsigned long long mr = sm.cmass[r][0];
+      if (cstar < 0 && mr > 0 && tdraw < cum + mr) {
+        cstar = r;
+        tau = tdraw - cum;
+      }
+      if (mr > 0) clast = r;
+      cum += mr;
+    }
+    if (cstar < 0) {
+      cstar = clast;
+      tau = ~0ull;  // the chunk's last token with mass
+    }
+    sm.bi[0] = cstar;
+    sm.bl[3] = tau;
+    sm.bl[5] = zs;
+  }
+  __syncthreads();
+  const int cstar = sm.bi[0];
+  const unsigned long long tau = sm.bl[3];
+  const unsigned long long zs = sm.bl[5];
+  const uint32_t ks = A - static_cast<uint32_t>(is);  // the cut key
+  __syncthreads();
+  // The histograms are consumed: the staging area may overwrite them.
+  // Members of the cut key kept in chunk r (staged): all, none, or those
+  // with index below the returned cut (the first sm.cnt[r]).
+  auto chunk_cut = [&](int r) -> int {
+    const uint32_t kept = sm.cnt[r];
+    if (kept >= sm.ties[r]) return INT_MAX;
+    if (kept == 0) return INT_MIN;
+    return staged_search<true, NV, unsigned long long>(
+               stage, r,
+               [&](float x, int e) { return (e < V && key16(x) == ks) ? 1ull : 0ull; },
+               static_cast<unsigned long long>(kept) - 1ull, sm, tid, lane, warp) + 1;
+  };
+  int tok = -1;
+  if (cstar >= 0) {
+    stage_chunk<true, NV, VEC>(P, row, cstar, stage, warp, lane);
+    const int ecut = chunk_cut(cstar);
+    tok = staged_search<true, NV, unsigned long long>(
+        stage, cstar,
+        [&](float x, int e) {
+          const uint32_t kx = key16(x);
+          const bool in = e < V && (kx > ks || (kx == ks && e < ecut));
+          return in ? mass_fx(weight(x, m, c2)) : 0ull;
+        },
+        tau, sm, tid, lane, warp);
+  }
+  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
+  if (q_row != nullptr) {
+    const float inv = 1.0f / (static_cast<float>(zs) / kMassScale);
+    for (int r = 0; r < C; ++r) {
+      __syncthreads();
+      stage_chunk<true, NV, VEC>(P, row, r, stage, warp, lane);
+      const int ecut = chunk_cut(r);
+      for_staged<true, NV>(stage, r, warp, lane, [&](float x, int e) {
+        if (e < V) {
+          const uint32_t kx = key16(x);
+          const bool in = kx > ks || (kx == ks && e < ecut);
+          q_row[e] = in ? weight(x, m, c2) * inv : 0.0f;
+        }
+      });
+    }
+  }
+  return true;
+}
+
+// ----------------------------------------------------------------- plain finish (P)
+
+// No filter: the draw is over the whole row.  The leader picks the chunk
+// from the CTAs' masses, re-reads it and finds the token.
+template <bool BF16, int NV, bool VEC>
+__device__ __noinline__ void leader_finish_plain(const SampleParams& P, SampleSmem& sm,
+                                                 const Ctx& c, uint4* stage, int row, float u,
+                                                 float m, float c2, int st, float* q_row) {
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  const int C = static_cast<int>(c.csize);
+  const int V = P.V;
+  float zrow = 0.0f;
+  for (int r = 0; r < C; ++r) {
+    const Summary& s = sm.gather[r];
+    if (s.f0 > -INFINITY) zrow += s.f1 * ex2((s.f0 - m) * c2);
+  }
+  float target = u * zrow;
+  if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
+  int cstar = -1, clast = -1;
+  float tau = 0.0f, cum = 0.0f;
+  for (int r = 0; r < C; ++r) {
+    const Summary& s = sm.gather[r];
+    const float mr = s.f0 > -INFINITY ? s.f1 * ex2((s.f0 - m) * c2) : 0.0f;
+    if (cstar < 0 && mr > 0.0f && target < cum + mr) {
+      cstar = r;
+      tau = target - cum;
+    }
+    if (mr > 0.0f) clast = r;
+    cum += mr;
+  }
+  if (cstar < 0) {
+    cstar = clast;
+    tau = INFINITY;
+  }
+  int tok = -1;
+  if (cstar >= 0) {
+    stage_chunk<BF16, NV, VEC>(P, row, cstar, stage, warp, lane);
+    tok = staged_search<BF16, NV, float>(
+        stage, cstar, [&](float x, int e) { return e < V ? weight(x, m, c2) : 0.0f; }, tau, sm,
+        tid, lane, warp);
+  }
+  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
+  if (q_row != nullptr) {
+    const float inv = 1.0f / zrow;
+    for (int r = 0; r < C; ++r) {
+      for_chunk<BF16, NV, VEC>(P, row, r, warp, lane, [&](float x, int e) {
+        if (e < V) q_row[e] = weight(x, m, c2) * inv;
+      });
+    }
+  }
+}
+
+// ----------------------------------------------------------------- the kernel
+
+// One cluster of C CTAs per row (grid C x B); rank 0 is the leader.
 template <bool BF16, int NV, bool VEC, bool ALL_GREEDY>
-__global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams P) {
+__global__ void __launch_bounds__(kThreads, 3)
+    sample_kernel(const __grid_constant__ SampleParams P) {
   using L = Layout<BF16>;
   constexpr int CHUNK = kThreads * NV * L::VW;  // elements per CTA
-  constexpr int NLEV = BF16 ? 2 : 4;            // 8-bit radix levels (fallback)
   constexpr int kWarpSpan = 32 * NV * L::VW;    // elements per warp
   __shared__ SampleSmem sm;
-  extern __shared__ __align__(128) unsigned char dyn[];
-  uint4* s_vec = reinterpret_cast<uint4*>(dyn);
-  float* l_val = reinterpret_cast<float*>(dyn + CHUNK * L::ELT);
-  int32_t* l_idx = reinterpret_cast<int32_t*>(l_val + P.list_cap);
-
-  // Every CTA of the cluster must have started before anyone stores into its
-  // shared memory: arrive now, wait just before the first remote store.
-  cluster_arrive();
+  extern __shared__ __align__(16) unsigned char dyn[];
+  float* l_val = reinterpret_cast<float*>(dyn);
+  int32_t* l_idx = reinterpret_cast<int32_t*>(dyn + kListCap * 4);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(dyn);
+  uint4* stage = reinterpret_cast<uint4*>(dyn);  // the leader's staged chunk (P, H finishes)
 
   Ctx c;
   c.tid = threadIdx.x;
@@ -747,19 +1405,27 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
   c.warp = c.tid >> 5;
   c.crank = cluster_rank();
   c.csize = cluster_size();
-  c.row = blockIdx.y;
-  c.V = P.V;
-  c.sv = s_vec;
   const int V = P.V;
-  const int row = c.row;
+  const int row = blockIdx.y;
   const int tid = c.tid, lane = c.lane, warp = c.warp;
-  const int cta_begin = static_cast<int>(c.crank) * CHUNK;
-  c.lane_base = cta_begin + ((warp * NV) * 32 + lane) * L::VW;
-  const bool has_pad = cta_begin + CHUNK > V;  // this slice reaches past the row end
-  constexpr uint32_t leader = 0;
-  const int R = P.list_cap / static_cast<int>(c.csize);  // list entries per CTA region
+  const int chunk = static_cast<int>(c.crank);
+  const int cta_begin = chunk * CHUNK;
+  const bool has_pad = cta_begin + CHUNK > V;
+  const bool is_leader = c.crank == 0;
+  const bool clustered = c.csize > 1;
 
-  // Row parameters (Sampler.prepare's normalisation).
+  // The leader's mbarrier collects one arrival from every other CTA.  The
+  // start barrier (relaxed arrive now; the pushing CTAs wait on it before
+  // their first remote store) orders its initialisation before any arrival.
+  if (clustered) {
+    if (is_leader && tid == 0) {
+      mbar_init(reinterpret_cast<uint64_t*>(&sm.bar), c.csize - 1);
+      fence_mbar_init();
+    }
+    cluster_arrive_relaxed();
+  }
+
+  // ---- row parameters (Sampler.prepare's normalisation).
   const bool greedy = ALL_GREEDY || !(P.temperature[row] > 0.0f);
   float T = 1.0f, p = 1.0f, u = 0.0f;
   int k = V;
@@ -776,94 +1442,309 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
     }
   }
   const float c2 = 1.4426950408889634f / T;  // log2(e) / T
+  const bool use_p = p < 1.0f;
+  const int R = (kListCap / static_cast<int>(c.csize)) & ~3;  // list entries per CTA region
+  int kind = kKindG;
+  if (!greedy) {
+    // K needs theta_c from the chunk's full warps: kw = ceil(k / full warps)
+    // <= 32 in every chunk; the last chunk has the fewest full warps.
+    const int nfull_min =
+        max(0, min(kWarps, (V - static_cast<int>(c.csize - 1) * CHUNK) / kWarpSpan));
+    if (k < V && k <= 256 && k <= R && nfull_min >= 1 && (k + nfull_min - 1) / nfull_min <= 32) {
+      kind = kKindK;
+    } else if (k == V && !use_p) {
+      kind = kKindP;
+    } else {
+      kind = BF16 ? kKindH : kKindF;
+    }
+  }
   float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
 
-  // ---- load the slice and take thread maxima (NaN-propagating).
+  // ---- load the slice; thread maximum (NaN-propagating).
   uint32_t d[NV][4];
-  load_slice<BF16, NV, VEC>(P, row, c.lane_base, d);
-  float tmax = -INFINITY;
-  int tidx = INT_MAX;
-  bool nan = false;
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const uint4 v = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
-    const float vm = vector_max<BF16>(v);
-    if (vm != vm) {
-      nan = true;
-    } else if (vm > tmax || tidx == INT_MAX) {
-      tmax = vm;
-      if (greedy) {
-        int first = INT_MAX;
-        for_vector<BF16>(v, c.lane_base + j * 32 * L::VW, [&](float x, int e) {
-          if (x == vm && e < first) first = e;
-        });
-        tidx = first;
-      } else {
-        tidx = 0;
-      }
-    }
-  }
+  load_chunk<BF16, NV, VEC>(P, row, chunk, warp, lane, d);
+  const float tmax = regs_max<BF16, NV>(d);
   if (q_row != nullptr) {
+    for_regs<BF16, NV>(d, chunk, warp, lane, [&](float, int e) {
+      if (e < V) q_row[e] = 0.0f;
+    });
+  }
+
+  Summary mine = {};
+  if (kind == kKindG) {
+    // ---- greedy: CTA maximum and its first index.
+    const float wmax = warp_max_nan(tmax);
+    if (lane == 0) sm.wf[warp] = wmax;
+    __syncthreads();
+    float cmax = sm.wf[0];
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const uint4 v = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
-      for_vector<BF16>(v, c.lane_base + j * 32 * L::VW, [&](float, int e) {
-        if (e < V) q_row[e] = 0.0f;
+    for (int w = 1; w < kWarps; ++w) cmax = fmax_nan(cmax, sm.wf[w]);
+    int idx = INT_MAX;
+    if (tmax == cmax) {
+      for_regs<BF16, NV>(d, chunk, warp, lane, [&](float x, int e) {
+        if (x == cmax && idx == INT_MAX) idx = e;
       });
+    }
+    idx = block_min_int(idx, sm.wi, lane, warp);
+    mine.f0 = cmax;
+    mine.i0 = idx;
+    mine.u0 = cmax != cmax ? 1u : 0u;
+  }
+
+  if constexpr (!ALL_GREEDY) {
+    if (kind == kKindK) {
+      // ---- top-k: candidates >= theta_c, the chunk-local bound.
+      const int nfull_cta = max(0, min(kWarps, (V - cta_begin) / kWarpSpan));
+      const int kw = (k + nfull_cta - 1) / nfull_cta;
+      const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
+      const float sorted = warp_sort_desc(tmax, lane);
+      const float tw = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
+      const float wmax = warp_max_nan(tmax);
+      if (lane == 0) {
+        sm.wt[warp] = tw;
+        sm.wf[warp] = wmax;
+      }
+      __syncthreads();
+      float theta = INFINITY, cmax = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        theta = fminf(theta, sm.wt[w]);
+        cmax = fmax_nan(cmax, sm.wf[w]);
+      }
+      const bool cnan = cmax != cmax;
+      // Candidate bitmask: bit b is element b of the thread (vector b / VW).
+      constexpr int kElems = NV * L::VW;
+      constexpr int kMaskWords = (kElems + 31) / 32;
+      uint32_t mask[kMaskWords];
+#pragma unroll
+      for (int w = 0; w < kMaskWords; ++w) mask[w] = 0u;
+      if (tmax >= theta) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int h = 0; h < L::EPW; ++h) {
+              const int b = (j * 4 + q) * L::EPW + h;
+              if (elem<BF16>(d[j][q], h) >= theta) mask[b >> 5] |= 1u << (b & 31);
+            }
+          }
+        }
+        if (has_pad && theta == -INFINITY) {
+          // Padding reads as -inf: it is a candidate only when theta is -inf.
+#pragma unroll
+          for (int j = 0; j < NV; ++j) {
+            const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+#pragma unroll
+            for (int b = 0; b < L::VW; ++b) {
+              const int bb = j * L::VW + b;
+              if (e0 + b >= V) mask[bb >> 5] &= ~(1u << (bb & 31));
+            }
+          }
+        }
+      }
+      auto totals = [&](uint32_t* wbase, uint32_t* total) -> uint32_t {
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int w = 0; w < kMaskWords; ++w) cnt += __popc(mask[w]);
+        const uint32_t wc = __reduce_add_sync(kFull, cnt);
+        if (lane == 0) sm.wu[warp] = wc;
+        __syncthreads();
+        uint32_t b = 0, t = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          if (w < warp) b += sm.wu[w];
+          t += sm.wu[w];
+        }
+        __syncthreads();
+        *wbase = b;
+        *total = t;
+        return wc;
+      };
+      uint32_t wbase, total;
+      uint32_t wc = totals(&wbase, &total);
+      if (static_cast<int>(total) > R && !cnan) {
+        // Ties push the count past the region: keep exactly the chunk's top-k.
+        int cloc = INT_MAX;
+        const float tloc = cta_select_topk<BF16, NV, VEC>(
+            P, sm, c, row, theta, static_cast<unsigned long long>(k), &cloc);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int h = 0; h < L::EPW; ++h) {
+              const int b = (j * 4 + q) * L::EPW + h;
+              const int e = e0 + q * L::EPW + h;
+              const float x = elem<BF16>(d[j][q], h);
+              if (!(x > tloc || (x == tloc && e < cloc))) mask[b >> 5] &= ~(1u << (b & 31));
+            }
+          }
+        }
+        wc = totals(&wbase, &total);
+      }
+      // Compact the candidates, in index order (vector by vector), into this
+      // CTA's region of its own list; the leader's region is its final place.
+      const uint32_t region = c.crank * static_cast<uint32_t>(R);
+      if (wc != 0) {
+        uint32_t acc = wbase;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+          const int b0 = j * L::VW;
+          const uint32_t vb = (mask[b0 >> 5] >> (b0 & 31)) & ((1u << L::VW) - 1u);
+          const uint32_t cj = __popc(vb);
+          if (__ballot_sync(kFull, cj != 0) == 0) continue;
+          const uint32_t incl = warp_inclusive_scan(cj, lane);
+          uint32_t pos = acc + incl - cj;
+          const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+          uint32_t bits = vb;
+          while (bits != 0u) {
+            const int b = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            const int q = b / L::EPW;
+            const uint32_t word = q == 0 ? d[j][0] : (q == 1 ? d[j][1] : (q == 2 ? d[j][2] : d[j][3]));
+            if (pos < static_cast<uint32_t>(R)) {
+              l_val[region + pos] = elem<BF16>(word, b % L::EPW);
+              l_idx[region + pos] = e0 + b;
+            }
+            ++pos;
+          }
+          acc += __shfl_sync(kFull, incl, 31);
+        }
+      }
+      const uint32_t nkeep = min(total, static_cast<uint32_t>(R));
+      __syncthreads();
+      if (clustered && !is_leader) {
+        // Copy the region into the leader's list: 16-byte stores (R % 4 == 0).
+        cluster_wait();
+        const uint32_t nv4 = (nkeep + 3u) / 4u;
+        const uint32_t dv = dsmem(l_val + region, 0);
+        const uint32_t di = dsmem(l_idx + region, 0);
+        const uint4* sv = reinterpret_cast<const uint4*>(l_val + region);
+        const uint4* si = reinterpret_cast<const uint4*>(l_idx + region);
+        for (uint32_t i = tid; i < nv4; i += kThreads) {
+          const uint4 a = sv[i];
+          const uint4 b = si[i];
+          st_dsmem_v4(dv + 16u * i, a.x, a.y, a.z, a.w);
+          st_dsmem_v4(di + 16u * i, b.x, b.y, b.z, b.w);
+        }
+      }
+      mine.f0 = cmax;
+      mine.i0 = static_cast<int32_t>(nkeep);
+      mine.u0 = cnan ? 1u : 0u;
+    } else if (kind == kKindP || (kind == kKindH && k == V)) {
+      // ---- chunk max and mass (online: relative to each thread's maximum).
+      float zt = 0.0f;
+      if (tmax > -INFINITY) {
+        // (x - tmax) * c2, not an fma with tmax * c2: for large c2 (T -> 0)
+        // the rounding of tmax * c2 would move the exponent by whole units.
+        for_regs<BF16, NV>(d, chunk, warp, lane, [&](float x, int) { zt += weight(x, tmax, c2); });
+      }
+      const float wmax = warp_max_nan(tmax);
+      const float zw = warp_sum(tmax > -INFINITY ? zt * ex2((tmax - wmax) * c2) : 0.0f);
+      if (lane == 0) {
+        sm.wf[warp] = wmax;
+        sm.wz[warp] = zw;
+      }
+      __syncthreads();
+      float cm = -INFINITY, cz = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w]);
+      if (cm > -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          if (sm.wf[w] > -INFINITY) cz += sm.wz[w] * ex2((sm.wf[w] - cm) * c2);
+        }
+      }
+      mine.f0 = cm;
+      mine.f1 = cz;
+      mine.u0 = cm != cm ? 1u : 0u;
+    } else {
+      // ---- H with top-k (no mass needed) and F: chunk max only.
+      const float wmax = warp_max_nan(tmax);
+      if (lane == 0) sm.wf[warp] = wmax;
+      __syncthreads();
+      float cm = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w]);
+      mine.f0 = cm;
+      mine.u0 = cm != cm ? 1u : 0u;
+    }
+    if constexpr (BF16) {
+      if (kind == kKindH) {
+        // ---- counts per 16-bit key over the window [a - kHistKeys + 1, a].
+        const float cm = mine.f0;
+        const bool finite = cm == cm && cm != INFINITY && cm != -INFINITY;
+        const uint32_t a = finite ? key16(cm) : 0u;
+        hist[tid] = 0u;
+        hist[tid + kThreads] = 0u;
+        __syncthreads();
+        if (finite) {
+          for_regs<true, NV>(d, chunk, warp, lane, [&](float x, int e) {
+            const uint32_t idx = a - key16(x);
+            if (idx < static_cast<uint32_t>(kHistKeys) && (!has_pad || e < V)) {
+              atomicAdd(&hist[idx >> 1], 1u << ((idx & 1u) * 16u));
+            }
+          });
+        }
+        __syncthreads();
+        mine.i0 = static_cast<int32_t>(a);
+        if (clustered && !is_leader) {
+          cluster_wait();
+          const uint32_t dst = dsmem(hist + c.crank * kHistWords, 0) + 8u * tid;
+          asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};"
+                       :: "r"(dst), "r"(hist[2 * tid]), "r"(hist[2 * tid + 1]) : "memory");
+        }
+      }
     }
   }
 
-  if (greedy) {
-    // ---- greedy rows: (max, first index) to the leader, which alone waits.
-    const int nan_any = __any_sync(kFull, nan);
-    float v = tmax;
-    int i = tidx;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(kFull, v, o);
-      const int oi = __shfl_xor_sync(kFull, i, o);
-      if (ov > v || (ov == v && oi < i)) {
-        v = ov;
-        i = oi;
-      }
-    }
-    if (lane == 0) {
-      sm.wf[warp] = v;
-      sm.wi[warp] = i;
-      sm.wu[warp] = static_cast<uint32_t>(nan_any);
-    }
-    __syncthreads();
-    cluster_wait();
+  // ---- publish: non-leaders push the summary and signal the leader.
+  if (!is_leader) {
+    if (kind != kKindK && kind != kKindH) cluster_wait();  // K and H waited before their stores
     if (tid == 0) {
-      float bv = sm.wf[0];
-      int bi = sm.wi[0];
-      uint32_t bn = sm.wu[0];
-      for (int w = 1; w < kWarps; ++w) {
-        if (sm.wf[w] > bv || (sm.wf[w] == bv && sm.wi[w] < bi)) {
-          bv = sm.wf[w];
-          bi = sm.wi[w];
-        }
-        bn |= sm.wu[w];
-      }
-      const uint32_t a = dsmem(&sm.gather[c.crank], leader);
-      st_dsmem_v4(a, __float_as_uint(bv), 0u, static_cast<uint32_t>(bi), bn);
+      const uint32_t a = dsmem(&sm.gather[c.crank], 0);
+      st_dsmem_v4(a, __float_as_uint(mine.f0), __float_as_uint(mine.f1),
+                  static_cast<uint32_t>(mine.i0), mine.u0);
     }
     __syncthreads();
-    cluster_arrive();
-    if (c.crank != leader) return;
-    cluster_wait();
+    if (tid == 0) mbar_remote_arrive(dsmem(&sm.bar, 0));
+    return;
+  }
+  if (tid == 0) sm.gather[0] = mine;
+  if (clustered) {
+    if (tid == 0) {
+      const long long t0 = globaltimer_ns();
+      bool ok = false;
+      while (!(ok = mbar_try_wait_cluster(reinterpret_cast<uint64_t*>(&sm.bar), 0u))) {
+        if (globaltimer_ns() - t0 > kWaitNs) break;
+      }
+      sm.bi[7] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (sm.bi[7] == 0) {
+      if (tid == 0) emit_token(P, row, -1, st | kStTimeout);
+      return;
+    }
+  } else {
+    __syncthreads();
+  }
+
+  // ---- the leader finishes the row.
+  const int C = static_cast<int>(c.csize);
+  if (kind == kKindG) {
     if (tid == 0) {
       float bv = -INFINITY;
       int bi = INT_MAX;
       uint32_t bn = 0;
-      for (uint32_t r = 0; r < c.csize; ++r) {
-        const float gv = sm.gather[r].f0;
-        const int gi = sm.gather[r].i0;
-        if (gv > bv || (gv == bv && gi < bi)) {
-          bv = gv;
-          bi = gi;
+      for (int r = 0; r < C; ++r) {
+        const Summary& s = sm.gather[r];
+        if (s.f0 > bv || (s.f0 == bv && s.i0 < bi)) {
+          bv = s.f0;
+          bi = s.i0;
         }
-        bn |= sm.gather[r].u0;
+        bn |= s.u0;
       }
       const int tok = bn ? -1 : bi;
       emit_token(P, row, tok, (bn ? kStNonFinite : 0) | st);
@@ -871,658 +1752,44 @@ __global__ void __launch_bounds__(kThreads, 3) sample_kernel(const SampleParams 
     }
     return;
   }
-
   if constexpr (!ALL_GREEDY) {
-    // ---- sampled rows: later passes read the slice from shared memory.
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      s_vec[(warp * NV + j) * 32 + lane] = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
+    float m = -INFINITY;
+    uint32_t rn = 0;
+    for (int r = 0; r < C; ++r) {
+      m = fmax_nan(m, sm.gather[r].f0);
+      rn |= sm.gather[r].u0;
     }
-    const bool use_p = p < 1.0f;
-    const int nan_any = __any_sync(kFull, nan);
-
-    // Chunk-local top-k: if this chunk has >= k elements >= theta_c, every
-    // element of the row's top-k that lies in this chunk is >= theta_c (k
-    // elements > the row's k-th value cannot exist), so each CTA can pick its
-    // candidates with no information from the others.  theta_c is the min over
-    // the chunk's full warps of their kw-th largest thread maximum,
-    // kw = ceil(k / full warps).  Uniform eligibility: k <= 256, k <= R, and
-    // the last CTA (fewest full warps) still has kw <= 32.
-    const int nfull_cta = max(0, min(kWarps, (V - cta_begin) / kWarpSpan));
-    const int nfull_min =
-        max(0, min(kWarps, (V - static_cast<int>(c.csize - 1) * CHUNK) / kWarpSpan));
-    const bool local_topk = k < V && k <= 256 && k <= R && nfull_min >= 1 &&
-                            (k + nfull_min - 1) / nfull_min <= 32;
-    if (local_topk) {
-      const int kw = (k + nfull_cta - 1) / nfull_cta;
-      const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
-      const float sorted = warp_sort_desc(tmax, lane);
-      const float tw = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
-      float wmax = tmax;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wmax = fmax_nan(wmax, __shfl_xor_sync(kFull, wmax, o));
-      if (lane == 0) {
-        sm.wt[warp] = tw;
-        sm.wf[warp] = wmax;
-        sm.wu[warp] = static_cast<uint32_t>(nan_any);
-      }
-      __syncthreads();
-      float theta = INFINITY, cmax = -INFINITY;
-      uint32_t cnan = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        theta = fminf(theta, sm.wt[w]);
-        cmax = fmax_nan(cmax, sm.wf[w]);
-        cnan |= sm.wu[w];
-      }
-      __syncthreads();
-      auto cand = [&](float x, int e) { return x >= theta && (!has_pad || e < V); };
-      uint32_t cnt = 0;
-      for_each<BF16, NV>(c, [&](float x, int e) { cnt += cand(x, e) ? 1u : 0u; });
-      const uint32_t wc = __reduce_add_sync(kFull, cnt);
-      if (lane == 0) sm.wu[warp] = wc;
-      __syncthreads();
-      uint32_t ncta = 0;
-      for (int w = 0; w < kWarps; ++w) ncta += sm.wu[w];
-      __syncthreads();
-      // Ties can push the count past the region: keep exactly the chunk's top-k.
-      float tloc = -INFINITY;
-      int cloc = INT_MAX;
-      if (static_cast<int>(ncta) > R) {
-        tloc = cta_select_topk<BF16, NV>(c, sm, cand, static_cast<unsigned long long>(k), &cloc);
-      }
-      const float tlv = tloc;
-      const int clv = cloc;
-      auto keep = [&](float x, int e) {
-        return cand(x, e) && (x > tlv || (x == tlv && e < clv));
-      };
-      cnt = 0;
-      for_each<BF16, NV>(c, [&](float x, int e) { cnt += keep(x, e) ? 1u : 0u; });
-      const uint32_t wk = __reduce_add_sync(kFull, cnt);
-      if (lane == 0) sm.wu[warp] = wk;
-      __syncthreads();
-      uint32_t woff = 0, nkeep = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        if (w < warp) woff += sm.wu[w];
-        nkeep += sm.wu[w];
-      }
-      cluster_wait();
-      {
-        const uint32_t base = static_cast<uint32_t>(c.crank) * R + woff;
-        const uint32_t a_val = dsmem(l_val, leader);
-        const uint32_t a_idx = dsmem(l_idx, leader);
-        uint32_t acc = 0;
-        for (int j = 0; j < NV; ++j) {
-          const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
-          const int e0 = c.lane_base + j * 32 * L::VW;
-          uint32_t cj = 0;
-          for_vector<BF16>(v, e0, [&](float x, int e) { cj += keep(x, e) ? 1u : 0u; });
-          if (__ballot_sync(kFull, cj != 0) == 0) continue;
-          const uint32_t incl = warp_inclusive_scan(cj, lane);
-          uint32_t pos = base + acc + incl - cj;
-          for_vector<BF16>(v, e0, [&](float x, int e) {
-            if (keep(x, e)) {
-              st_dsmem_f32(a_val + 4u * pos, x);
-              st_dsmem_u32(a_idx + 4u * pos, static_cast<uint32_t>(e));
-              ++pos;
-            }
-          });
-          acc += __shfl_sync(kFull, incl, 31);
-        }
-      }
-      if (tid == 0) {
-        const uint32_t a = dsmem(&sm.gather[c.crank], leader);
-        st_dsmem_v4(a, __float_as_uint(cmax), 0u, 0u, cnan);
-        st_dsmem_u32(dsmem(&sm.cnt[c.crank], leader), nkeep);
-      }
-      __syncthreads();
-      cluster_arrive();
-      if (c.crank != leader) return;
-      cluster_wait();
-      float m = -INFINITY;
-      uint32_t rn = 0;
-      for (uint32_t r = 0; r < c.csize; ++r) {
-        m = fmax_nan(m, sm.gather[r].f0);
-        rn |= sm.gather[r].u0;
-      }
-      if (rn != 0 || m != m || m == INFINITY || m == -INFINITY) {
-        const int est = (m == -INFINITY && rn == 0) ? kStAllNegInf : kStNonFinite;
-        if (tid == 0) emit_token(P, row, -1, est | st);
-        return;
-      }
-      leader_finish(P, sm, c, l_val, l_idx, R, row, true, k, use_p, p, 0ull, m, c2, u, st,
-                    q_row);
+    if (rn != 0 || m != m || m == INFINITY || m == -INFINITY) {
+      const int est = (m == -INFINITY && rn == 0) ? kStAllNegInf : kStNonFinite;
+      if (tid == 0) emit_token(P, row, -1, est | st);
       return;
     }
-
-    // ---- other sampled rows: one all-to-all exchange of the chunk maximum,
-    // the chunk mass (relative to the chunk maximum) and a bound theta_c.
-    const bool topk_row = k < V;
-    const bool need_z = !topk_row;
-    float zt = 0.0f;
-    if (need_z && tmax > -INFINITY) {
-      for_each<BF16, NV>(c, [&](float x, int) { zt += ex2((x - tmax) * c2); });
-    }
-    float wmax = tmax;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wmax = fmax_nan(wmax, __shfl_xor_sync(kFull, wmax, o));
-    const float zw = warp_sum(tmax > -INFINITY ? zt * ex2((tmax - wmax) * c2) : 0.0f);
-    float tw = -INFINITY;
-    if (topk_row) {
-      // kw-th largest thread maximum of every warp fully inside the row.
-      const int w_full = V / kWarpSpan;
-      const int kw = w_full > 0 ? (k + w_full - 1) / w_full : INT_MAX;
-      const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
-      if (kw <= 32) {
-        const float sorted = warp_sort_desc(tmax, lane);
-        tw = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
-      }
-    } else if (use_p) {
-      // Largest theta_w whose thread maxima above it carry >= p' of the
-      // warp's mass (p' = p raised by 1e-3, so that rounding rarely forces
-      // the fallback; the decision below is exact).  A warp without mass
-      // does not constrain theta.
-      const float sorted = warp_sort_desc(tmax, lane);
-      const float ws = sorted > -INFINITY ? ex2((sorted - wmax) * c2) : 0.0f;
-      const float cum = warp_inclusive_scan(ws, lane);
-      const float need = fminf(1.0f, p * 1.001f) * zw;
-      const unsigned hit = __ballot_sync(kFull, cum >= need);
-      tw = zw > 0.0f ? (hit ? __shfl_sync(kFull, sorted, __ffs(hit) - 1) : -INFINITY) : INFINITY;
-    }
-    if (lane == 0) {
-      sm.wt[warp] = tw;
-      sm.wf[warp] = wmax;
-      sm.wz[warp] = zw;
-      sm.wu[warp] = static_cast<uint32_t>(nan_any);
-    }
-    __syncthreads();
-    Slot mine = {};
-    {
-      float cm = -INFINITY, th = INFINITY, cz = 0.0f;
-      uint32_t cn = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        cm = fmax_nan(cm, sm.wf[w]);
-        th = fminf(th, sm.wt[w]);
-        cn |= sm.wu[w];
-      }
-      if (cm > -INFINITY) {
-        for (int w = 0; w < kWarps; ++w) {
-          if (sm.wf[w] > -INFINITY) cz += sm.wz[w] * ex2((sm.wf[w] - cm) * c2);
-        }
-      }
-      mine.f0 = cm;
-      mine.f1 = th;
-      mine.u0 = cn;
-      mine.pad0 = __float_as_uint(cz);
-    }
-    __syncthreads();
-    cluster_wait();
-    int ph = 0;
-    float m, theta, zrow, before_cta;
-    bool nan_row;
-    {
-      const Slot* s = push_exchange(sm, ph, c, mine);
-      float mm = -INFINITY, th = INFINITY;
-      uint32_t nn = 0;
-      for (uint32_t r = 0; r < c.csize; ++r) {
-        mm = fmax_nan(mm, s[r].f0);
-        th = fminf(th, s[r].f1);
-        nn |= s[r].u0;
-      }
-      float zz = 0.0f;
-      if (mm > -INFINITY && mm == mm) {
-        for (uint32_t r = 0; r < c.csize; ++r) {
-          if (s[r].f0 > -INFINITY) zz += __uint_as_float(s[r].pad0) * ex2((s[r].f0 - mm) * c2);
-        }
-      }
-      m = mm;
-      theta = th;
-      zrow = zz;
-      nan_row = nn != 0;
-      // CTA prefix of the masses, for the plain rows' draw (same summation
-      // order as zrow, so the CTA intervals tile [0, zrow) exactly).
-      float before = 0.0f;
-      for (uint32_t r = 0; r < c.crank; ++r) {
-        if (s[r].f0 > -INFINITY) before += __uint_as_float(s[r].pad0) * ex2((s[r].f0 - mm) * c2);
-      }
-      before_cta = before;
-    }
-    if (nan_row || m != m || m == INFINITY || m == -INFINITY) {
-      const int est = (m == -INFINITY && !nan_row) ? kStAllNegInf : kStNonFinite;
-      if (c.crank == leader && tid == 0) emit_token(P, row, -1, est | st);
+    if (kind == kKindK) {
+      if (tid < C) sm.cnt[tid] = static_cast<uint32_t>(sm.gather[tid].i0);
+      __syncthreads();
+      leader_finish_list(P, sm, c, l_val, l_idx, R, row, k, use_p, p, m, c2, u, st, q_row);
       return;
     }
-
-    if (!topk_row && !use_p) {
-      // ---- plain rows: draw over the whole row; the CTA holding the
-      // crossing finds the token.
-      // Keep the target strictly below zrow so that it falls in the interval
-      // of a CTA that holds mass.
-      float target = u * zrow;
-      if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
-      const float before = before_cta;
-      const float mine_z =
-          mine.f0 > -INFINITY ? __uint_as_float(mine.pad0) * ex2((mine.f0 - m) * c2) : 0.0f;
-      if (target >= before && target < before + mine_z) {
-        // Warp holding the crossing (sequential over warps).
-        const float tloc = target - before;
-        int wstar = -1;
-        float tw2 = INFINITY, cw = 0.0f;
-        int wlast = -1;
-        for (int w = 0; w < kWarps; ++w) {
-          const float ww = sm.wf[w] > -INFINITY ? sm.wz[w] * ex2((sm.wf[w] - m) * c2) : 0.0f;
-          if (wstar < 0 && tloc < cw + ww) {
-            wstar = w;
-            tw2 = tloc - cw;
-          }
-          if (ww > 0.0f) wlast = w;
-          cw += ww;
-        }
-        if (wstar < 0) {
-          wstar = wlast < 0 ? 0 : wlast;
-          tw2 = INFINITY;
-        }
-        if (warp == wstar) {
-          float acc = 0.0f;
-          int found = -1, lastpos = -1;
-          for (int j = 0; j < NV; ++j) {
-            const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
-            const int e0 = c.lane_base + j * 32 * L::VW;
-            float lj = 0.0f;
-            int llast = -1;
-            for_vector<BF16>(v, e0, [&](float x, int e) {
-              const float w = ex2((x - m) * c2);
-              lj += w;
-              if (w > 0.0f) llast = e;
-            });
-            const unsigned has = __ballot_sync(kFull, llast >= 0);
-            if (has != 0) lastpos = __shfl_sync(kFull, llast, 31 - __clz(has));
-            const float incl = warp_inclusive_scan(lj, lane);
-            const float stot = __shfl_sync(kFull, incl, 31);
-            if (tw2 < acc + stot) {
-              const unsigned bal = __ballot_sync(kFull, tw2 < acc + incl);
-              const int lx = bal ? __ffs(bal) - 1 : 31;
-              int sel = -1;
-              if (lane == lx) {
-                float run = acc + (incl - lj);
-                for_vector<BF16>(v, e0, [&](float x, int e) {
-                  run += ex2((x - m) * c2);
-                  if (sel < 0 && tw2 < run) sel = e;
-                });
-                if (sel < 0) sel = llast;
-              }
-              found = __shfl_sync(kFull, sel, lx);
-              if (found < 0) found = lastpos;
-              break;
-            }
-            acc += stot;
-          }
-          if (found < 0) found = lastpos;
-          if (lane == 0 && found >= 0) emit_token(P, row, found, st);
-        }
-      }
-      if (q_row != nullptr) {
-        const float inv = 1.0f / zrow;
-        for_each<BF16, NV>(c, [&](float x, int e) {
-          if (e < V) q_row[e] = ex2((x - m) * c2) * inv;
-        });
-      }
+    if (kind == kKindP) {
+      leader_finish_plain<BF16, NV, VEC>(P, sm, c, stage, row, u, m, c2, st, q_row);
       return;
     }
-
-    // ---- global theta: candidates >= theta into the leader's list.
-    const bool fast = theta > -INFINITY;
-    if (fast) {
-      auto cand = [&](float x, int e) { return x >= theta && (!has_pad || e < V); };
-      uint32_t cnt = 0;
-      unsigned long long mfx = 0;
-      for_each<BF16, NV>(c, [&](float x, int e) {
-        if (cand(x, e)) {
-          ++cnt;
-          if (!topk_row) mfx += mass_fx(ex2((x - m) * c2));
-        }
-      });
-      const uint32_t wc = __reduce_add_sync(kFull, cnt);
-      mfx = warp_sum(mfx);
-      if (lane == 0) {
-        sm.wu[warp] = wc;
-        sm.wl[warp] = mfx;
-      }
-      __syncthreads();
-      uint32_t woff = 0, ncta = 0;
-      unsigned long long mcta = 0;
-      for (int w = 0; w < kWarps; ++w) {
-        if (w < warp) woff += sm.wu[w];
-        ncta += sm.wu[w];
-        mcta += sm.wl[w];
-      }
-      if (static_cast<int>(ncta) <= R) {
-        const uint32_t base = static_cast<uint32_t>(c.crank) * R + woff;
-        const uint32_t a_val = dsmem(l_val, leader);
-        const uint32_t a_idx = dsmem(l_idx, leader);
-        uint32_t acc = 0;
-        for (int j = 0; j < NV; ++j) {
-          const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
-          const int e0 = c.lane_base + j * 32 * L::VW;
-          uint32_t cj = 0;
-          for_vector<BF16>(v, e0, [&](float x, int e) { cj += cand(x, e) ? 1u : 0u; });
-          if (__ballot_sync(kFull, cj != 0) == 0) continue;
-          const uint32_t incl = warp_inclusive_scan(cj, lane);
-          uint32_t pos = base + acc + incl - cj;
-          for_vector<BF16>(v, e0, [&](float x, int e) {
-            if (cand(x, e)) {
-              st_dsmem_f32(a_val + 4u * pos, x);
-              st_dsmem_u32(a_idx + 4u * pos, static_cast<uint32_t>(e));
-              ++pos;
-            }
-          });
-          acc += __shfl_sync(kFull, incl, 31);
-        }
-      }
-      Slot cs = {};
-      cs.u0 = ncta;
-      cs.l0 = mcta;
-      __syncthreads();
-      const Slot* s = push_exchange(sm, ph, c, cs);
-      // Uniform decision: every region fits, and (top-p rows) the list holds
-      // enough mass that no element below theta can be kept.
-      uint32_t over = 0;
-      unsigned long long lmass = 0;
-      for (uint32_t r = 0; r < c.csize; ++r) {
-        if (static_cast<int>(s[r].u0) > R) over = 1;
-        lmass += s[r].l0;
-      }
-      unsigned long long target_fx = 0;
-      if (!topk_row) {
-        const double t = static_cast<double>(p) * static_cast<double>(zrow) * 1099511627776.0;
-        target_fx = static_cast<unsigned long long>(ceil(t));
-        if (target_fx < 1) target_fx = 1;
-        if (lmass < target_fx) over = 1;
-      }
-      if (over == 0) {
-        if (c.crank != leader) return;
-        if (tid < static_cast<int>(c.csize)) sm.cnt[tid] = s[tid].u0;
-        __syncthreads();
-        leader_finish(P, sm, c, l_val, l_idx, R, row, topk_row, k, use_p, p, target_fx, m, c2, u,
-                      st, q_row);
-        return;
-      }
-      // Over capacity: every CTA falls through to the on-chip fallback.
-    }
-
-    // ---- fallback / plain rows: whole-row passes over the on-chip slices.
-    float tk = -INFINITY;
-    int ck = INT_MAX;
-    bool pulled = false;  // other CTAs read this CTA's histograms: final barrier due
-    auto tie_cutoff = [&](auto member, unsigned long long r) -> int {
-      // First r members (index order) across the cluster; returns this
-      // CTA's index cutoff.
-      uint32_t cnt = 0;
-      for_each<BF16, NV>(c, [&](float x, int e) { cnt += member(x, e) ? 1u : 0u; });
-      const uint32_t wc = __reduce_add_sync(kFull, cnt);
-      if (lane == 0) sm.wu[warp] = wc;
-      __syncthreads();
-      Slot cs = {};
-      for (int w = 0; w < kWarps; ++w) cs.u0 += sm.wu[w];
-      const Slot* s = push_exchange(sm, ph, c, cs);
-      unsigned long long before = 0;
-      for (uint32_t r2 = 0; r2 < c.crank; ++r2) before += s[r2].u0;
-      const uint32_t mine_cnt = s[c.crank].u0;
-      unsigned long long rl = r > before ? r - before : 0ull;
-      if (rl > mine_cnt) rl = mine_cnt;
-      int cut;
-      if (rl == 0) {
-        cut = INT_MIN;
-      } else if (rl >= mine_cnt) {
-        cut = INT_MAX;
-      } else {
-        uint32_t cum = 0, rw = 0;
-        int wstar = kWarps - 1;
-        for (int w = 0; w < kWarps; ++w) {
-          if (cum + sm.wu[w] >= rl) {
-            wstar = w;
-            rw = static_cast<uint32_t>(rl) - cum;
-            break;
+    if constexpr (BF16) {
+      if (kind == kKindH) {
+        float zrow = 0.0f;
+        if (k == V) {
+          for (int r = 0; r < C; ++r) {
+            const Summary& s = sm.gather[r];
+            if (s.f0 > -INFINITY) zrow += s.f1 * ex2((s.f0 - m) * c2);
           }
-          cum += sm.wu[w];
         }
-        if (warp == wstar) {
-          uint32_t acc = 0;
-          int found = INT_MAX;
-          for (int j = 0; j < NV; ++j) {
-            const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
-            const int e0 = c.lane_base + j * 32 * L::VW;
-            uint32_t cj = 0;
-            for_vector<BF16>(v, e0, [&](float x, int e) { cj += member(x, e) ? 1u : 0u; });
-            const uint32_t incl = warp_inclusive_scan(cj, lane);
-            const uint32_t stot = __shfl_sync(kFull, incl, 31);
-            if (acc + stot >= rw) {
-              const unsigned bal = __ballot_sync(kFull, acc + incl >= rw);
-              const int lx = __ffs(bal) - 1;
-              int sel = INT_MAX;
-              if (lane == lx) {
-                uint32_t need = rw - (acc + incl - cj);
-                for_vector<BF16>(v, e0, [&](float x, int e) {
-                  if (member(x, e)) {
-                    if (need == 1 && sel == INT_MAX) sel = e;
-                    --need;
-                  }
-                });
-              }
-              found = __shfl_sync(kFull, sel, lx);
-              break;
-            }
-            acc += stot;
-          }
-          if (lane == 0) sm.bi[1] = found == INT_MAX ? INT_MAX : found + 1;
+        if (leader_finish_hist<NV, VEC>(P, sm, c, hist, stage, row, k, use_p, p, u, m, zrow, c2,
+                                        st, q_row)) {
+          return;
         }
-        __syncthreads();
-        cut = sm.bi[1];
-      }
-      __syncthreads();
-      return cut;
-    };
-
-    if (topk_row) {
-      // Count radix select of the k-th key over the whole row.
-      uint32_t prefix = 0, pmask = 0;
-      unsigned long long rem = static_cast<unsigned long long>(k);
-      for (int lvl = 0; lvl < NLEV; ++lvl) {
-        const int shift = 24 - 8 * lvl;
-        PullBuf& pb = sm.pull[ph & 1];
-        pb.lo[tid] = 0u;
-        __syncthreads();
-        for_each<BF16, NV>(c, [&](float x, int) {
-          const uint32_t key = float_key(x);
-          if ((key & pmask) == prefix) atomicAdd(&pb.lo[(key >> shift) & 0xffu], 1u);
-        });
-        cluster_sync();
-        ++ph;
-        pulled = true;
-        unsigned long long tot = 0;
-        for (uint32_t r = 0; r < c.csize; ++r) tot += ld_dsmem_u32(dsmem(&pb.lo[tid], r));
-        unsigned long long above;
-        const int b = select_bucket(tot, rem, sm, &above, tid, lane, warp);
-        rem -= above;
-        prefix |= static_cast<uint32_t>(b) << shift;
-        pmask |= 0xffu << shift;
-      }
-      if (BF16 && !(prefix & 0x80000000u)) prefix |= 0xffffu;  // bf16 negatives: low bits ones
-      tk = key_float(prefix);
-      const float tkv = tk;
-      ck = tie_cutoff([&](float x, int) { return x == tkv; }, rem);
-    }
-    const float tkf = tk;
-    const int ckf = ck;
-    auto in_k = [&](float x, int e) { return x > tkf || (x == tkf && e < ckf); };
-
-    float tp = tk;
-    int cp = ck;
-    if (use_p) {
-      uint32_t prefix = 0, pmask = 0;
-      unsigned long long rem = 0;
-      for (int lvl = 0; lvl < NLEV; ++lvl) {
-        const int shift = 24 - 8 * lvl;
-        PullBuf& pb = sm.pull[ph & 1];
-        pb.lo[tid] = 0u;
-        pb.hi[tid] = 0u;
-        __syncthreads();
-        for_each<BF16, NV>(c, [&](float x, int e) {
-          const uint32_t key = float_key(x);
-          if ((key & pmask) == prefix && in_k(x, e)) {
-            const uint32_t d = (key >> shift) & 0xffu;
-            atomic_add_u64_split(&pb.lo[d], &pb.hi[d], mass_fx(ex2((x - m) * c2)));
-          }
-        });
-        cluster_sync();
-        ++ph;
-        pulled = true;
-        unsigned long long tot = 0;
-        for (uint32_t r = 0; r < c.csize; ++r) {
-          tot += (static_cast<unsigned long long>(ld_dsmem_u32(dsmem(&pb.hi[tid], r))) << 32) +
-                 ld_dsmem_u32(dsmem(&pb.lo[tid], r));
-        }
-        if (lvl == 0) {
-          // Target: keep while (mass before) < p * Z_k, Z_k the exact total.
-          const unsigned long long z_fx =
-              block_suffix_scan<unsigned long long>(tot, sm.wl, lane, warp);
-          if (tid == 0) sm.bl[0] = z_fx;
-          __syncthreads();
-          const unsigned long long zt = sm.bl[0];
-          rem = static_cast<unsigned long long>(
-              ceil(static_cast<double>(zt) * static_cast<double>(p)));
-          if (rem < 1) rem = 1;
-          if (rem > zt) rem = zt;
-          __syncthreads();
-        }
-        unsigned long long above;
-        const int b = select_bucket(tot, rem, sm, &above, tid, lane, warp);
-        rem -= above;
-        prefix |= static_cast<uint32_t>(b) << shift;
-        pmask |= 0xffu << shift;
-      }
-      if (BF16 && !(prefix & 0x80000000u)) prefix |= 0xffffu;
-      tp = key_float(prefix);
-      const unsigned long long wt = mass_fx(ex2((tp - m) * c2));
-      const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
-      const float tpv = tp;
-      cp = tie_cutoff([&](float x, int e) { return x == tpv && in_k(x, e); }, rp);
-      if (tp == tk && ck < cp) cp = ck;  // the cut counted only K members
-    }
-    const float tpf = tp;
-    const int cpf = cp;
-    auto in_s = [&](float x, int e) {
-      return in_k(x, e) && (x > tpf || (x == tpf && e < cpf));
-    };
-
-    // ---- inverse CDF over S in vocab order.
-    float ts = 0.0f;
-    for_each<BF16, NV>(c, [&](float x, int e) {
-      if (in_s(x, e)) ts += ex2((x - m) * c2);
-    });
-    const float wsum = warp_sum(ts);
-    if (lane == 0) sm.wf[warp] = wsum;
-    __syncthreads();
-    Slot cs = {};
-    for (int w = 0; w < kWarps; ++w) cs.f0 += sm.wf[w];
-    const Slot* s = push_exchange(sm, ph, c, cs);
-    if (warp == 0) {
-      const float t = lane < static_cast<int>(c.csize) ? s[lane].f0 : 0.0f;
-      const float cum = warp_inclusive_scan(t, lane);
-      const float Z = __shfl_sync(kFull, cum, 31);
-      const float target = u * Z;
-      const unsigned hit = __ballot_sync(kFull, lane < static_cast<int>(c.csize) && target < cum);
-      int rstar;
-      float tloc;
-      if (hit != 0) {
-        rstar = __ffs(hit) - 1;
-        tloc = target - __shfl_sync(kFull, cum - t, rstar);
-      } else {
-        const unsigned pos = __ballot_sync(kFull, lane < static_cast<int>(c.csize) && t > 0.0f);
-        rstar = pos ? 31 - __clz(pos) : 0;
-        tloc = INFINITY;  // take the last kept token with mass
-      }
-      if (lane == 0) {
-        sm.bi[0] = rstar;
-        sm.bf[0] = tloc;
-        sm.bf[1] = Z;
       }
     }
-    __syncthreads();
-    const int rstar = sm.bi[0];
-    const float tloc = sm.bf[0];
-    const float zs_all = sm.bf[1];
-    if (c.crank == static_cast<uint32_t>(rstar)) {
-      int wstar = -1;
-      float tw = INFINITY;
-      float cw = 0.0f;
-      int wlast = -1;
-      for (int w = 0; w < kWarps; ++w) {
-        const float nc = cw + sm.wf[w];
-        if (wstar < 0 && tloc < nc) {
-          wstar = w;
-          tw = tloc - cw;
-        }
-        if (sm.wf[w] > 0.0f) wlast = w;
-        cw = nc;
-      }
-      if (wstar < 0) {
-        wstar = wlast < 0 ? 0 : wlast;
-        tw = INFINITY;
-      }
-      if (warp == wstar) {
-        float acc = 0.0f;
-        int found = -1;
-        int lastpos = -1;
-        for (int j = 0; j < NV; ++j) {
-          const uint4 v = s_vec[(warp * NV + j) * 32 + lane];
-          const int e0 = c.lane_base + j * 32 * L::VW;
-          float lj = 0.0f;
-          int llast = -1;
-          for_vector<BF16>(v, e0, [&](float x, int e) {
-            if (in_s(x, e)) {
-              const float w = ex2((x - m) * c2);
-              lj += w;
-              if (w > 0.0f) llast = e;
-            }
-          });
-          const unsigned has = __ballot_sync(kFull, llast >= 0);
-          if (has != 0) lastpos = __shfl_sync(kFull, llast, 31 - __clz(has));
-          const float incl = warp_inclusive_scan(lj, lane);
-          const float stot = __shfl_sync(kFull, incl, 31);
-          if (tw < acc + stot) {
-            const unsigned bal = __ballot_sync(kFull, tw < acc + incl);
-            const int lx = bal ? __ffs(bal) - 1 : 31;
-            int sel = -1;
-            if (lane == lx) {
-              float run = acc + (incl - lj);
-              for_vector<BF16>(v, e0, [&](float x, int e) {
-                if (in_s(x, e)) {
-                  run += ex2((x - m) * c2);
-                  if (sel < 0 && tw < run) sel = e;
-                }
-              });
-              if (sel < 0) sel = llast;
-            }
-            found = __shfl_sync(kFull, sel, lx);
-            if (found < 0) found = lastpos;
-            break;
-          }
-          acc += stot;
-        }
-        if (found < 0) found = lastpos;
-        if (lane == 0) emit_token(P, row, found, found < 0 ? (st | kStNonFinite) : st);
-      }
-    }
-    if (q_row != nullptr) {
-      const float inv = 1.0f / zs_all;
-      for_each<BF16, NV>(c, [&](float x, int e) {
-        if (e < V) q_row[e] = in_s(x, e) ? ex2((x - m) * c2) * inv : 0.0f;
-      });
-    }
-    // Other CTAs read this CTA's histograms after the barriers above; stay
-    // until every CTA is past them.
-    if (pulled) cluster_sync();
-
+    leader_fallback<BF16>(P, sm, c, row, k, use_p, p, u, m, c2, st, q_row);
   }
 }
 

@@ -10,31 +10,11 @@
 
 namespace pkv {
 
-// Candidate-list capacity: as large as fits next to the slice while keeping
-// three CTAs per SM (else two, else one), at most 4096 entries.
-inline int list_capacity(size_t slice_bytes) {
-  constexpr size_t kSmemPerSm = 228 * 1024;
-  constexpr size_t kPerCtaReserved = 1024;
-  constexpr size_t kStatic = sizeof(SampleSmem) + 256;
-  for (int per_sm = 3; per_sm >= 1; --per_sm) {
-    const size_t budget = kSmemPerSm / per_sm;
-    const size_t used = kPerCtaReserved + kStatic + slice_bytes;
-    if (budget <= used) continue;
-    size_t cap = (budget - used) / 8;
-    if (cap > 4096) cap = 4096;
-    cap = cap / 256 * 256;
-    if (cap >= 1024) return static_cast<int>(cap);
-  }
-  return 1024;
-}
-
 template <bool BF16, int NV, bool VEC, bool AG>
 cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
   auto kern = sample_kernel<BF16, NV, VEC, AG>;
-  constexpr size_t kSliceBytes = static_cast<size_t>(kThreads) * NV * 16;
-  static const int cap = list_capacity(kSliceBytes);
-  // An all-greedy batch uses neither the slice copy nor the list.
-  const size_t dyn = AG ? 0 : kSliceBytes + static_cast<size_t>(cap) * 8;
+  // An all-greedy batch uses neither the candidate list nor the histograms.
+  const size_t dyn = AG ? 0 : static_cast<size_t>(sample_dyn_bytes<NV>());
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaSuccess;
@@ -48,7 +28,7 @@ cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  P.list_cap = cap;
+  P.list_cap = kListCap;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(C), static_cast<unsigned>(P.B), 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -67,7 +47,10 @@ cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
 template <bool BF16, bool AG>
 cudaError_t launch_sample_dtype(const SampleParams& P, const SampleConfig& c,
                                 cudaStream_t stream) {
-  if (!c.vec) return launch_one<BF16, kNvScalar, false, AG>(P, c.cluster, stream);
+  if (!c.vec) {
+    if (c.nv == 10) return launch_one<BF16, 10, false, AG>(P, c.cluster, stream);
+    return launch_one<BF16, kNvScalar, false, AG>(P, c.cluster, stream);
+  }
   switch (c.nv) {
     case 4: return launch_one<BF16, 4, true, AG>(P, c.cluster, stream);
     case 8: return launch_one<BF16, 8, true, AG>(P, c.cluster, stream);
