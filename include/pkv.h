@@ -71,9 +71,12 @@ const char* pkv_last_error(void);
 int pkv_version(void);
 
 /*
- * Scratch bytes pkv_sample_batch needs for (B, V, dtype).  The kernels keep
- * all intermediate state on chip, so this is 0; the argument pair stays in the
- * ABI so that callers already pass a workspace.
+ * Device bytes of the workspace pkv_sample_batch needs for (B, V, dtype), or
+ * 0 for invalid arguments.  The sampler runs as two kernels: the first splits
+ * every row into chunks and leaves one record per (row, chunk) in the
+ * workspace (about 2 KB each); the second settles each row from its records.
+ * The caller owns the workspace; it needs no initialisation and may be reused
+ * by later calls on the same stream.
  */
 size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt);
 
@@ -111,10 +114,13 @@ size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt);
  *   probs_out   [B, V] fp32 or NULL: debug output of the kept-set
  *               probabilities (one-hot for greedy rows); leave NULL when timing.
  *   status      device int32 status word or NULL.
- *   workspace   may be NULL (see pkv_sample_workspace_bytes).
+ *   workspace   device memory of at least pkv_sample_workspace_bytes(B, V, dt)
+ *               bytes (workspace_bytes), 16-byte aligned; not to be shared by
+ *               calls that may run concurrently.
  * Errors: PKV_EINVAL (NULL required pointer, B < 1, B > 65535, V < 1,
- * row_stride < V, bad dtype, pool sizes < 1), PKV_EUNSUPPORTED (V above
- * PKV_MAX_VOCAB_*), PKV_ECUDA (launch failure).
+ * row_stride < V, bad dtype, pool sizes < 1, workspace missing, too small or
+ * unaligned), PKV_EUNSUPPORTED (V above PKV_MAX_VOCAB_*), PKV_ECUDA (launch
+ * failure).
  */
 int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
                      const float* temperature, const int32_t* top_k, const float* top_p,

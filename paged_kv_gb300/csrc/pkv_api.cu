@@ -10,15 +10,17 @@
 #include <cstdio>
 #include <cstring>
 
+#include <algorithm>
+
 #include "../../include/pkv.h"
 #include "launch_config.h"
 #include "page_kernels.h"
 #include "sample_params.h"
 
 namespace pkv {
-cudaError_t launch_sample_bf16(const SampleParams& P, const SampleConfig& c, bool all_greedy,
+cudaError_t launch_sample_bf16(const SampleParams& P, const SampleConfig& c, int num_sms,
                                cudaStream_t stream);
-cudaError_t launch_sample_fp32(const SampleParams& P, const SampleConfig& c, bool all_greedy,
+cudaError_t launch_sample_fp32(const SampleParams& P, const SampleConfig& c, int num_sms,
                                cudaStream_t stream);
 }  // namespace pkv
 
@@ -65,13 +67,19 @@ extern "C" {
 
 const char* pkv_last_error(void) { return g_err; }
 
-int pkv_version(void) { return 100; }
+int pkv_version(void) { return 200; }
 
 size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt) {
-  (void)B;
-  (void)V;
-  (void)dt;
-  return 0;
+  if (B < 1 || V < 1 || (dt != PKV_FP32 && dt != PKV_BF16)) return 0;
+  // The larger of the aligned and the element-load launch shapes.
+  size_t chunks = 0;
+  for (bool vec : {true, false}) {
+    pkv::SampleConfig cfg;
+    if (pkv::choose_sample_config(B, V, dt == PKV_BF16, vec, num_sms(), &cfg)) {
+      chunks = std::max(chunks, static_cast<size_t>(cfg.chunks));
+    }
+  }
+  return static_cast<size_t>(B) * chunks * pkv::kChunkSlotBytes;
 }
 
 int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
@@ -80,8 +88,6 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
                      int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
                      const int64_t* wb_cols, float* probs_out, int32_t* status,
                      void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   if (logits == nullptr) return fail(PKV_EINVAL, "logits is NULL");
   if (out_tokens == nullptr) return fail(PKV_EINVAL, "out_tokens is NULL");
   if (dt != PKV_FP32 && dt != PKV_BF16) return fail(PKV_EINVAL, "dtype %d is not fp32 or bf16", dt);
@@ -101,12 +107,19 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
   const int max_v = bf16 ? PKV_MAX_VOCAB_BF16 : PKV_MAX_VOCAB_FP32;
   if (V > max_v) return fail(PKV_EUNSUPPORTED, "V=%d above the maximum %d", V, max_v);
   const size_t elt = bf16 ? 2 : 4;
-  // The TMA bulk-copy path needs 16-byte-aligned row starts and row lengths.
+  // The bulk-copy path needs 16-byte-aligned row starts and row lengths.
   const bool vec = aligned16(logits) && ((static_cast<uint64_t>(row_stride) * elt) % 16 == 0) &&
                    ((static_cast<uint64_t>(V) * elt) % 16 == 0);
   pkv::SampleConfig cfg;
   if (!pkv::choose_sample_config(B, V, bf16, vec, num_sms(), &cfg))
     return fail(PKV_EUNSUPPORTED, "no launch shape covers V=%d", V);
+  if (static_cast<int64_t>(cfg.chunks - 1) * cfg.chunk >= V)
+    return fail(PKV_EUNSUPPORTED, "launch shape with an empty chunk (V=%d)", V);
+  const size_t need = static_cast<size_t>(B) * cfg.chunks * pkv::kChunkSlotBytes;
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(PKV_EINVAL, "workspace of %zu bytes needed (pkv_sample_workspace_bytes), got %zu",
+                need, workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+  if (!aligned16(workspace)) return fail(PKV_EINVAL, "workspace is not 16-byte aligned");
 
   pkv::SampleParams P;
   P.logits = logits;
@@ -126,11 +139,11 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
   P.probs_out = probs_out;
   P.status = status;
   P.cta_chunk = cfg.chunk;
-  P.list_cap = 0;  // set by the launcher for the chosen kernel
-  const bool all_greedy = temperature == nullptr;
+  P.chunks = cfg.chunks;
+  P.workspace = workspace;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = bf16 ? pkv::launch_sample_bf16(P, cfg, all_greedy, s)
-                             : pkv::launch_sample_fp32(P, cfg, all_greedy, s);
+  const cudaError_t e = bf16 ? pkv::launch_sample_bf16(P, cfg, num_sms(), s)
+                             : pkv::launch_sample_fp32(P, cfg, num_sms(), s);
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
   return ok();
 }

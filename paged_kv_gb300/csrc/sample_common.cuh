@@ -1,4 +1,8 @@
-// Batched per-request sampler for sm_103a.
+// Shared pieces of the batched sampler for sm_103a: constants, the
+// per-chunk workspace slot, element access on 16-byte vectors, block helpers
+// (one 256-thread group = 8 warps synchronises on its own named barrier),
+// the candidate-list selects, the CTA-local top-k, chunk searches and the
+// exact fallback over global memory.
 //
 // Operation ("mini-sglang from Scratch", page "The engine and the sampler",
 // section "The sampler": Sampler.sample / sample_torch): greedy rows return
@@ -8,37 +12,29 @@
 // drawn by inverse CDF in ascending vocab index against the supplied uniform.
 // Order between equal logits is by ascending index everywhere.
 //
-// GB300 design:
-//   * One thread-block cluster of C CTAs per row (grid C x B).  CTA r owns
-//     the contiguous slice [r*chunk, (r+1)*chunk) of the row and keeps it in
-//     registers (16-byte loads, every logit read from HBM once).  Warp w of
-//     a CTA owns a contiguous sub-slice; its vector j covers 32 consecutive
-//     16-byte groups, one per lane.
-//   * No all-to-all exchange.  Every CTA reduces its slice to a small
-//     summary (plus candidates or a histogram), pushes it into the leader
-//     CTA's shared memory, signals the leader's mbarrier with one
-//     release-arrive and exits.  Only the leader waits.  The one cluster
-//     barrier, at the start (relaxed arrive; waited on only by the CTAs that
-//     push), guarantees that the leader runs before anyone writes into it.
-//   * Row kinds, each finished by the leader:
-//       G  greedy: (max, first index) per CTA.
-//       K  top-k with k <= 256: a chunk-local lower bound theta_c on the
-//          row's k-th value (a chunk holding k elements >= theta_c cannot
-//          miss any of the row's top-k) selects candidates with no global
-//          information; the leader selects exactly on the candidate list.
-//       P  plain (no filter): chunk max and mass; the leader picks the
-//          chunk of the draw and re-reads that chunk (an L2 hit) to find the
-//          token.
-//       H  top-p, or top-k with k > 256, on bf16 rows: all elements with one
-//          bf16 value share one weight, so exact counts per value give exact
-//          masses.  Each CTA counts its elements per value over a window of
-//          1024 values below its maximum; the leader merges the counts,
-//          settles the top-k and top-p cuts exactly (2^-40 fixed-point
-//          masses), picks the chunk of the draw and re-reads it.
-//       F  whatever the above cannot settle (a cut below the window; fp32
-//          rows with top-p or k > 256): the leader selects exactly by radix
-//          passes over the row in global memory.
-//   * No tensor cores (nothing here is a contraction); exp is MUFU.EX2.
+// Two kernels (sample_stream.cuh, sample_finish.cuh):
+//   * stream: persistent CTAs, two groups of 8 warps each; every group works
+//     through its (row, chunk) items, fed by a ring of 1-D bulk copies
+//     (cp.async.bulk + mbarrier) from global into shared memory, so the next
+//     chunk is in flight while the current one is reduced.  Each item leaves
+//     a small record in the workspace: a summary, per-warp masses (plain
+//     rows), a candidate list (top-k rows) or a count histogram (top-p rows).
+//   * finish: one CTA per row (programmatic dependent launch) reads the
+//     records of its row and settles the token exactly.
+// Row kinds:
+//   G  greedy: (max, first index) per chunk.
+//   K  top-k with k <= 256: a chunk-local lower bound theta_c on the row's
+//      k-th value (a chunk holding k elements >= theta_c cannot miss any of
+//      the row's top-k) selects candidates with no global information.
+//   P  plain (no filter): chunk and per-warp (max, mass); the finisher picks
+//      the warp of the draw and re-reads that warp's slice.
+//   H  top-p, or top-k with k > 256, on bf16 rows: all elements with one bf16
+//      value share one weight, so exact counts per value give exact masses;
+//      each chunk counts its elements per value over the 1024 values below
+//      its maximum.
+//   F  whatever the above cannot settle (a cut below the window; fp32 rows
+//      with top-p or k > 256): radix passes over the row in global memory.
+// No tensor cores (nothing here is a contraction); exp is MUFU.EX2.
 #pragma once
 
 #include <climits>
@@ -50,27 +46,35 @@
 
 namespace pkv {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;                  // threads of one group (and of a finish CTA)
 constexpr int kWarps = kThreads / 32;
+constexpr int kGroups = 2;                     // groups per stream CTA
 constexpr int kBuckets = 256;
-constexpr int kMaxClusterCtas = 16;
-constexpr int kHistKeys = 1024;                // values counted below a CTA's maximum (H rows)
+constexpr int kMaxChunks = 16;                 // chunks per row
+constexpr int kHistKeys = 1024;                // values counted below a chunk's maximum (H rows)
 constexpr int kHistWords = kHistKeys / 2;      // two 16-bit counts per word
-constexpr int kListCap = 4096;                 // candidate entries in the leader (K rows)
-constexpr int kSampleDynBytes = kListCap * 8;  // the list, or C histograms
-
-// Dynamic shared memory of a sampled launch: the list or the histograms,
-// later (leader only) one staged chunk of kThreads * NV 16-byte vectors.
-template <int NV>
-constexpr int sample_dyn_bytes() {
-  return kThreads * NV * 16 > kSampleDynBytes ? kThreads * NV * 16 : kSampleDynBytes;
-}
-static_assert(kMaxClusterCtas * kHistWords * 4 == kSampleDynBytes, "dynamic shared memory");
-static_assert(kHistKeys == 4 * kThreads, "four merged histogram keys per leader thread");
+constexpr int kListRegion = 256;               // candidate entries per chunk (K rows), >= k
+constexpr int kListCap = kMaxChunks * kListRegion;
+constexpr int kListBytes = kListCap * 8;       // the finisher's list, or its C histograms
+static_assert(kMaxChunks * kHistWords * 4 == kListBytes, "list and histograms share the space");
+static_assert(kHistKeys == 4 * kThreads, "four merged histogram keys per finisher thread");
 static_assert(kHistWords == 2 * kThreads, "two histogram words per thread");
+static_assert(kListRegion * 2 == kHistWords, "a chunk's list and histogram fill one payload");
+
+// Dynamic shared memory of the finish kernel.  From offset 0: the candidate
+// list or the histograms, later (H rows) one staged chunk of kThreads * NV
+// 16-byte vectors; then the fixed-point mass per merged key.
+template <int NV>
+constexpr int finish_table_offset() {
+  return kThreads * NV * 16 > kListBytes ? kThreads * NV * 16 : kListBytes;
+}
+template <int NV>
+constexpr int finish_dyn_bytes() {
+  return finish_table_offset<NV>() + kHistKeys * 8;
+}
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
 constexpr double kMassScaleD = 1099511627776.0;
-constexpr long long kWaitNs = 2000000000ll;     // the leader's wait for the other CTAs (2 s)
+constexpr long long kWaitNs = 2000000000ll;     // bound of every wait on a bulk copy (2 s)
 
 constexpr int kStNonFinite = 1;
 constexpr int kStAllNegInf = 2;
@@ -81,21 +85,30 @@ constexpr int kStTimeout = 64;
 
 enum RowKind { kKindG = 0, kKindK = 1, kKindP = 2, kKindH = 3, kKindF = 4 };
 
-// One CTA's summary, pushed into the leader's gather[rank] with one 16-byte
-// store (hence the alignment).
+// One chunk's summary.
 struct __align__(16) Summary {
-  float f0;     // G: CTA max; others: chunk max (NaN if the chunk has a NaN)
+  float f0;     // G: chunk max; others: chunk max (NaN if the chunk has a NaN)
   float f1;     // P, and H without top-k: chunk mass relative to f0
   int32_t i0;   // G: first index of the max; K: candidate count; H: 16-bit key of f0
-  uint32_t u0;  // NaN seen
+  uint32_t u0;  // bit 0: NaN seen; bit 1: a bulk copy timed out
+};
+
+// The workspace record of one (row, chunk): written by the stream kernel,
+// read by the finish kernel.
+struct __align__(16) ChunkSlot {
+  Summary s;
+  float wm[kWarps];               // P rows: per-warp maximum
+  float wz[kWarps];               // P rows: per-warp mass relative to wm
+  uint32_t payload[kHistWords];   // K: values [0, 256) then indices; H: packed counts
 };
 
 struct SampleSmem {
-  unsigned long long bar;  // the leader's gather mbarrier
-  Summary gather[kMaxClusterCtas];
-  uint32_t cnt[kMaxClusterCtas];
-  uint32_t ties[kMaxClusterCtas];
-  unsigned long long cmass[kMaxClusterCtas][kWarps];
+  Summary gather[kMaxChunks];
+  __align__(16) float gwm[kMaxChunks][kWarps];  // P rows: per-warp max of each chunk
+  __align__(16) float gwz[kMaxChunks][kWarps];  // P rows: per-warp mass relative to gwm
+  uint32_t cnt[kMaxChunks];
+  uint32_t ties[kMaxChunks];
+  unsigned long long cmass[kMaxChunks][kWarps];
   unsigned long long scan[kBuckets];
   uint32_t hlo[kBuckets];  // histograms of the list and fallback selects
   uint32_t hhi[kBuckets];
@@ -106,11 +119,19 @@ struct SampleSmem {
   float wt[kWarps];
   float wz[kWarps];
   int32_t bi[8];
+  float bf4[4];
   unsigned long long bl[8];
 };
 
-static_assert(sizeof(Summary) == 16, "one 16-byte store per summary");
-static_assert(offsetof(SampleSmem, gather) % 16 == 0, "16-byte stores into gather");
+static_assert(sizeof(Summary) == 16, "one 16-byte record");
+static_assert(sizeof(ChunkSlot) == kChunkSlotBytes, "workspace record size");
+
+// Barrier of the calling thread's group of kThreads threads (named barrier
+// 1 + group); a finish CTA is one group.
+__device__ __forceinline__ void group_sync() {
+  asm volatile("bar.sync %0, %1;" :: "r"(1 + (threadIdx.x / kThreads)), "n"(kThreads)
+               : "memory");
+}
 
 // ----------------------------------------------------------------- element access
 
@@ -142,8 +163,9 @@ __device__ __forceinline__ void for_vec(const uint32_t (&w)[4], int e0, F&& f) {
 }
 
 struct Ctx {
-  int tid, lane, warp;
-  uint32_t crank, csize;
+  int tid, lane, warp;  // within the group
+  uint32_t crank;       // chunk of the row
+  uint32_t csize;       // chunks per row
 };
 
 // Row index of the first element of vector j of (warp, lane) in chunk `chunk`.
@@ -201,26 +223,38 @@ __device__ __forceinline__ void load_chunk(const SampleParams& P, int row, int c
 // NaN-propagating maximum of the thread's registers.
 template <bool BF16, int NV>
 __device__ __forceinline__ float regs_max(const uint32_t (&d)[NV][4]) {
+  // Four independent chains (one per word of a vector) keep the dependency
+  // chain short.
   if constexpr (BF16) {
-    uint32_t m2 = d[0][0];
+    uint32_t m2[4] = {d[0][0], d[0][1], d[0][2], d[0][3]};
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
+    for (int j = 1; j < NV; ++j) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (j != 0 || q != 0) m2 = bf16x2_max_nan(m2, d[j][q]);
-      }
+      for (int q = 0; q < 4; ++q) m2[q] = bf16x2_max_nan(m2[q], d[j][q]);
     }
+    const uint32_t r = bf16x2_max_nan(bf16x2_max_nan(m2[0], m2[1]), bf16x2_max_nan(m2[2], m2[3]));
+    return fmax_nan(elem<true>(r, 0), elem<true>(r, 1));
+  } else {
+    float m[4] = {__uint_as_float(d[0][0]), __uint_as_float(d[0][1]), __uint_as_float(d[0][2]),
+                  __uint_as_float(d[0][3])};
+#pragma unroll
+    for (int j = 1; j < NV; ++j) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m[q] = fmax_nan(m[q], __uint_as_float(d[j][q]));
+    }
+    return fmax_nan(fmax_nan(m[0], m[1]), fmax_nan(m[2], m[3]));
+  }
+}
+
+// Maximum of one 16-bit-element vector (NaN-propagating).
+template <bool BF16>
+__device__ __forceinline__ float vec_max(const uint32_t (&w)[4]) {
+  if constexpr (BF16) {
+    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(w[0], w[1]), bf16x2_max_nan(w[2], w[3]));
     return fmax_nan(elem<true>(m2, 0), elem<true>(m2, 1));
   } else {
-    float m = __uint_as_float(d[0][0]);
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (j != 0 || q != 0) m = fmax_nan(m, __uint_as_float(d[j][q]));
-      }
-    }
-    return m;
+    return fmax_nan(fmax_nan(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                    fmax_nan(__uint_as_float(w[2]), __uint_as_float(w[3])));
   }
 }
 
@@ -249,10 +283,10 @@ template <typename T>
 __device__ __forceinline__ T block_suffix_scan(T v, T* s_w, int lane, int warp) {
   v = warp_suffix_scan(v, lane);
   if (lane == 0) s_w[warp] = v;
-  __syncthreads();
+  group_sync();
   T add = 0;
   for (int w = warp + 1; w < kWarps; ++w) add += s_w[w];
-  __syncthreads();
+  group_sync();
   return v + add;
 }
 
@@ -261,13 +295,13 @@ template <typename T>
 __device__ __forceinline__ T block_exclusive_scan(T v, T* s_w, int lane, int warp, T* total) {
   const T incl = warp_inclusive_scan(v, lane);
   if (lane == 31) s_w[warp] = incl;
-  __syncthreads();
+  group_sync();
   T before = 0, all = 0;
   for (int w = 0; w < kWarps; ++w) {
     if (w < warp) before += s_w[w];
     all += s_w[w];
   }
-  __syncthreads();
+  group_sync();
   *total = all;
   return before + incl - v;
 }
@@ -276,32 +310,32 @@ template <typename T>
 __device__ __forceinline__ T block_sum(T v, T* s_w, int lane, int warp) {
   v = warp_sum(v);
   if (lane == 0) s_w[warp] = v;
-  __syncthreads();
+  group_sync();
   T r = 0;
   for (int w = 0; w < kWarps; ++w) r += s_w[w];
-  __syncthreads();
+  group_sync();
   return r;
 }
 
 __device__ __forceinline__ int block_max_int(int v, int32_t* s_w, int lane, int warp) {
   v = __reduce_max_sync(kFull, v);
   if (lane == 0) s_w[warp] = v;
-  __syncthreads();
+  group_sync();
   int r = s_w[0];
 #pragma unroll
   for (int w = 1; w < kWarps; ++w) r = max(r, s_w[w]);
-  __syncthreads();
+  group_sync();
   return r;
 }
 
 __device__ __forceinline__ int block_min_int(int v, int32_t* s_w, int lane, int warp) {
   v = __reduce_min_sync(kFull, v);
   if (lane == 0) s_w[warp] = v;
-  __syncthreads();
+  group_sync();
   int r = s_w[0];
 #pragma unroll
   for (int w = 1; w < kWarps; ++w) r = min(r, s_w[w]);
-  __syncthreads();
+  group_sync();
   return r;
 }
 
@@ -322,7 +356,7 @@ __device__ __forceinline__ int select_bucket(unsigned long long tot, unsigned lo
   int b = block_max_int(S >= rem ? tid : -1, sm.wi, lane, warp);
   if (b < 0) b = 0;  // unreachable: callers keep rem <= S(0)
   *above = (b + 1 < kBuckets) ? sm.scan[b + 1] : 0ull;
-  __syncthreads();
+  group_sync();
   return b;
 }
 
@@ -358,18 +392,17 @@ __device__ __forceinline__ void emit_token(const SampleParams& P, int row, int t
 
 // ----------------------------------------------------------------- warp helpers
 
-// 32 floats sorted descending across the warp (bitonic network).
-__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const float o = __shfl_xor_sync(kFull, v, j);
-      const bool keep_max = ((lane & j) == 0) == ((lane & k) == 0);
-      v = keep_max ? fmaxf(v, o) : fminf(v, o);
-    }
+// The kw-th largest (1 <= kw <= 32) of the lanes' keys, by a bit-serial
+// search with ballots: keep a candidate bit when at least kw lanes have a key
+// >= the prefix with that bit set.
+__device__ __forceinline__ uint32_t warp_kth_largest_key(uint32_t key, int kw, int top_bit,
+                                                         int low_bit) {
+  uint32_t prefix = 0u;
+  for (int bit = top_bit; bit >= low_bit; --bit) {
+    const uint32_t cand = prefix | (1u << bit);
+    if (__popc(__ballot_sync(kFull, key >= cand)) >= kw) prefix = cand;
   }
-  return v;
+  return prefix;
 }
 
 // ----------------------------------------------------------------- chunk search
@@ -449,7 +482,7 @@ __device__ __forceinline__ int chunk_search(const SampleParams& P, int row, int 
     }
     sm.wi[warp] = wl;
   }
-  __syncthreads();
+  group_sync();
   int wstar = -1, lastpos = -1;
   T tw = 0, acc = 0;
   for (int w = 0; w < kWarps; ++w) {
@@ -501,13 +534,13 @@ __device__ __forceinline__ int chunk_search(const SampleParams& P, int row, int 
     }
     if (lane == 0) sm.bi[6] = found;
   }
-  __syncthreads();
+  group_sync();
   int res = lastpos;
   if (wstar >= 0) {
     res = sm.bi[6];
     if (res < 0 || res == INT_MAX) res = sm.wi[wstar];
   }
-  __syncthreads();
+  group_sync();
   return res;
 }
 
@@ -558,7 +591,7 @@ __device__ __forceinline__ int staged_search(const uint4* sv, int chunk, F&& f, 
     }
     sm.wi[warp] = wl;
   }
-  __syncthreads();
+  group_sync();
   int wstar = -1, lastpos = -1;
   T tw = 0, acc = 0;
   for (int w = 0; w < kWarps; ++w) {
@@ -610,13 +643,13 @@ __device__ __forceinline__ int staged_search(const uint4* sv, int chunk, F&& f, 
     }
     if (lane == 0) sm.bi[6] = found;
   }
-  __syncthreads();
+  group_sync();
   int res = lastpos;
   if (wstar >= 0) {
     res = sm.bi[6];
     if (res < 0 || res == INT_MAX) res = sm.wi[wstar];
   }
-  __syncthreads();
+  group_sync();
   return res;
 }
 
@@ -648,7 +681,7 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
     sm.wu[c.warp] = kand;
     sm.wi[c.warp] = static_cast<int32_t>(kor);
   }
-  __syncthreads();
+  group_sync();
   uint32_t a = 0xffffffffu, o = 0u;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
@@ -658,7 +691,7 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
   unsigned long long rem = target;
   const uint32_t diff = a ^ o;  // bits on which the kept keys differ
   if (diff == 0u) {
-    __syncthreads();
+    group_sync();
     *rem_out = rem;
     return key_float(a);
   }
@@ -673,7 +706,7 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
     const uint32_t amask = hi == 31 ? 0u : (0xffffffffu << (hi + 1));  // bits above the digit
     sm.hlo[c.tid] = 0u;
     if constexpr (MASS) sm.hhi[c.tid] = 0u;
-    __syncthreads();
+    group_sync();
     for (int i = c.tid; i < n; i += kThreads) {
       if (!keep(i)) continue;
       const uint32_t key = float_key(val[i]);
@@ -685,26 +718,26 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
         atomicAdd(&sm.hlo[dg], 1u);
       }
     }
-    __syncthreads();
+    group_sync();
     const unsigned long long tot =
         MASS ? ((static_cast<unsigned long long>(sm.hhi[c.tid]) << 32) | sm.hlo[c.tid])
              : static_cast<unsigned long long>(sm.hlo[c.tid]);
     // Suffix sums S(t) over buckets; the bucket b with S(b + 1) < rem <= S(b).
     const unsigned long long sw = warp_suffix_scan(tot, c.lane);
     if (c.lane == 0) sm.wl[c.warp] = sw;
-    __syncthreads();
+    group_sync();
     unsigned long long S = sw;
     for (int w = c.warp + 1; w < kWarps; ++w) S += sm.wl[w];
     if (S >= rem && S - tot < rem) {
       sm.bi[4] = c.tid;
       sm.bl[6] = S - tot;
     }
-    __syncthreads();
+    group_sync();
     const int b = sm.bi[4];
     rem -= sm.bl[6];
     prefix |= static_cast<uint32_t>(b) << lo;
   }
-  __syncthreads();
+  group_sync();
   *rem_out = rem;
   return key_float(prefix);
 }
@@ -723,7 +756,7 @@ __device__ __forceinline__ int list_tie_cut(int n, M&& member, unsigned long lon
   uint32_t total;
   const uint32_t before = block_exclusive_scan<uint32_t>(cnt, sm.wu, c.lane, c.warp, &total);
   if (c.tid == 0) sm.bi[3] = n;
-  __syncthreads();
+  group_sync();
   if (r <= total && before < r && r <= before + cnt) {
     uint32_t need = static_cast<uint32_t>(r - before);
     for (int i = i0; i < i1; ++i) {
@@ -733,9 +766,9 @@ __device__ __forceinline__ int list_tie_cut(int n, M&& member, unsigned long lon
       }
     }
   }
-  __syncthreads();
+  group_sync();
   const int cut = sm.bi[3];
-  __syncthreads();
+  group_sync();
   return cut;
 }
 
@@ -764,7 +797,7 @@ __device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&
                                  c.lane, c.warp);
   const int lastpos = block_max_int(last, sm.wi, c.lane, c.warp);
   if (c.tid == 0) sm.bi[2] = lastpos;
-  __syncthreads();
+  group_sync();
   if (cand != INT_MAX && c.tid == cand) {
     float run = before;
     int sel = -1;
@@ -779,10 +812,10 @@ __device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&
     }
     sm.bi[2] = sel >= 0 ? sel : last;
   }
-  __syncthreads();
+  group_sync();
   const int pos = sm.bi[2];
   *zs = total;
-  __syncthreads();
+  group_sync();
   return pos >= 0 ? idx[pos] : -1;
 }
 
@@ -792,7 +825,7 @@ __device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&
 // select, ties by index), top-p inside K (mass select on 2^-40 fixed-point
 // weights), renormalisation and the inverse-CDF draw.  Emits the token and,
 // if asked, the probabilities of the kept tokens.
-static __device__ __noinline__ void leader_finish_list(const SampleParams& P, SampleSmem& sm,
+static __device__ __forceinline__ void leader_finish_list(const SampleParams& P, SampleSmem& sm,
                                                 const Ctx& c, float* l_val, int32_t* l_idx, int R,
                                                 int row, int k, bool use_p, float p, float m,
                                                 float c2, float u, int st, float* q_row) {
@@ -819,7 +852,7 @@ static __device__ __noinline__ void leader_finish_list(const SampleParams& P, Sa
           mi[q] = l_idx[r * R + off];
         }
       }
-      __syncthreads();
+      group_sync();
 #pragma unroll
       for (int q = 0; q < kMovePer; ++q) {
         const int i = b0 + q * kThreads + tid;
@@ -828,7 +861,7 @@ static __device__ __noinline__ void leader_finish_list(const SampleParams& P, Sa
           l_idx[i] = mi[q];
         }
       }
-      __syncthreads();
+      group_sync();
     }
   }
   unsigned long long rk;
@@ -902,13 +935,13 @@ __device__ __noinline__ float cta_select_topk(const SampleParams& P, SampleSmem&
     sm.wu[c.warp] = lo;
     sm.wi[c.warp] = static_cast<int32_t>(hi);
   }
-  __syncthreads();
+  group_sync();
   uint32_t kmin = 0xffffffffu, kmax = 0u;
   for (int w = 0; w < kWarps; ++w) {
     kmin = min(kmin, sm.wu[w]);
     kmax = max(kmax, static_cast<uint32_t>(sm.wi[w]));
   }
-  __syncthreads();
+  group_sync();
   unsigned long long rem = k;
   uint32_t prefix = kmin;
   if (kmin != kmax) {
@@ -919,13 +952,13 @@ __device__ __noinline__ float cta_select_topk(const SampleParams& P, SampleSmem&
       const uint32_t dmask = (1u << (hb - lb + 1)) - 1u;
       const uint32_t amask = static_cast<uint32_t>(~((2ull << hb) - 1ull));
       sm.hlo[c.tid] = 0u;
-      __syncthreads();
+      group_sync();
       for_chunk<BF16, NV, VEC>(P, row, chunk, c.warp, c.lane, [&](float x, int e) {
         if (!keep(x, e)) return;
         const uint32_t key = float_key(x);
         if ((key & amask) == (prefix & amask)) atomicAdd(&sm.hlo[(key >> lb) & dmask], 1u);
       });
-      __syncthreads();
+      group_sync();
       unsigned long long above;
       const int b = select_bucket(sm.hlo[c.tid], rem, sm, &above, c.tid, c.lane, c.warp);
       rem -= above;
@@ -974,7 +1007,7 @@ __device__ __forceinline__ int row_tie_cut(const SampleParams& P, int row, M&& m
   const unsigned long long before =
       block_exclusive_scan<unsigned long long>(cnt, sm.wl, c.lane, c.warp, &total);
   if (c.tid == 0) sm.bi[3] = INT_MAX;
-  __syncthreads();
+  group_sync();
   if (r <= total && before < r && r <= before + cnt) {
     unsigned long long need = r - before;
     for (int e = i0; e < i1; ++e) {
@@ -984,9 +1017,9 @@ __device__ __forceinline__ int row_tie_cut(const SampleParams& P, int row, M&& m
       }
     }
   }
-  __syncthreads();
+  group_sync();
   const int cut = sm.bi[3];
-  __syncthreads();
+  group_sync();
   return cut;
 }
 
@@ -1004,7 +1037,7 @@ __device__ __forceinline__ float row_select(const SampleParams& P, int row, K&& 
     const int shift = 24 - 8 * lvl;
     sm.hlo[c.tid] = 0u;
     sm.hhi[c.tid] = 0u;
-    __syncthreads();
+    group_sync();
     for (int e = c.tid; e < V; e += kThreads) {
       const float x = load_elem<BF16>(P, row, e);
       if (!keep(x, e)) continue;
@@ -1017,7 +1050,7 @@ __device__ __forceinline__ float row_select(const SampleParams& P, int row, K&& 
         atomicAdd(&sm.hlo[dg], 1u);
       }
     }
-    __syncthreads();
+    group_sync();
     const unsigned long long tot =
         MASS ? ((static_cast<unsigned long long>(sm.hhi[c.tid]) << 32) | sm.hlo[c.tid])
              : static_cast<unsigned long long>(sm.hlo[c.tid]);
@@ -1099,7 +1132,7 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
       static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(zs));
   const int lastpos = block_max_int(last, sm.wi, lane, warp);
   if (tid == 0) sm.bi[2] = lastpos;
-  __syncthreads();
+  group_sync();
   if (seg > 0 && tdraw >= before && tdraw < before + seg) {
     unsigned long long run = before;
     int sel = last;
@@ -1115,7 +1148,7 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
     }
     sm.bi[2] = sel;
   }
-  __syncthreads();
+  group_sync();
   const int tok = sm.bi[2];
   if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
   if (q_row != nullptr) {
@@ -1127,670 +1160,58 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
   }
 }
 
-// ----------------------------------------------------------------- histogram finish (H)
+// ----------------------------------------------------------------- row parameters
 
-// The leader merges the C count histograms (CTA r counted its elements per
-// 16-bit key over the kHistKeys keys below a_r = gather[r].i0, the key of its
-// maximum), settles top-k and top-p exactly, picks the chunk holding the draw,
-// re-reads it and finds the token.  Returns false, having emitted nothing,
-// when a cut lies below the merged window; the caller then runs the exact
-// fallback.
-template <int NV, bool VEC>
-__device__ __noinline__ bool leader_finish_hist(const SampleParams& P, SampleSmem& sm,
-                                                const Ctx& c, const uint32_t* hist, uint4* stage,
-                                                int row,
-                                                int k, bool use_p, float p, float u, float m,
-                                                float zrow, float c2, int st, float* q_row) {
-  const int tid = c.tid, lane = c.lane, warp = c.warp;
-  const int C = static_cast<int>(c.csize);
-  const int V = P.V;
-  const bool topk = k < V;
-  const uint32_t A = key16(m);
-  // Count of CTA r at merged key i (key A - i); 0 above the CTA's maximum.
-  auto count_at = [&](int r, uint32_t i) -> uint32_t {
-    const uint32_t delta = A - static_cast<uint32_t>(sm.gather[r].i0);
-    if (i > A || i < delta) return 0u;
-    const uint32_t idx = i - delta;
-    return (hist[r * kHistWords + (idx >> 1)] >> ((idx & 1u) * 16u)) & 0xffffu;
-  };
-  // Merged key i (0 = the row maximum); thread t holds keys 4t .. 4t + 3.
-  uint32_t cnt[4];
-  unsigned long long wfx[4];
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const uint32_t i = static_cast<uint32_t>(4 * tid + jj);
-    uint32_t n = 0;
-    for (int r = 0; r < C; ++r) n += count_at(r, i);
-    cnt[jj] = n;
-    wfx[jj] = n ? mass_fx(weight(key16_float(A - i), m, c2)) : 0ull;
-  }
-  // ---- top-k by count: keys i < ik are wholly in K, key ik keeps rk members.
-  int ik = kHistKeys;
-  unsigned long long rk = 0;
-  if (topk) {
-    const uint32_t local = cnt[0] + cnt[1] + cnt[2] + cnt[3];
-    uint32_t total;
-    const uint32_t before = block_exclusive_scan<uint32_t>(local, sm.wu, lane, warp, &total);
-    if (total < static_cast<uint32_t>(k)) return false;  // k-th value below the window
-    int cand = INT_MAX;
-    uint32_t run = before;
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      if (run < static_cast<uint32_t>(k) && run + cnt[jj] >= static_cast<uint32_t>(k)) {
-        cand = 4 * tid + jj;
-        sm.bl[0] = static_cast<unsigned long long>(k) - run;  // one owner
-      }
-      run += cnt[jj];
-    }
-    ik = block_min_int(cand, sm.wi, lane, warp);
-    rk = sm.bl[0];
-    __syncthreads();
-  }
-  unsigned long long mk[4];  // mass of K at each key
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int i = 4 * tid + jj;
-    mk[jj] = i < ik ? cnt[jj] * wfx[jj] : (i == ik ? rk * wfx[jj] : 0ull);
-  }
-  // ---- top-p inside K by mass: keys i < is wholly in S, key is keeps rs.
-  int is = ik;
-  unsigned long long rs = rk;
-  if (use_p) {
-    const unsigned long long local = mk[0] + mk[1] + mk[2] + mk[3];
-    unsigned long long zk;
-    const unsigned long long before =
-        block_exclusive_scan<unsigned long long>(local, sm.wl, lane, warp, &zk);
-    unsigned long long target;
-    if (topk) {
-      target =
-          static_cast<unsigned long long>(ceil(static_cast<double>(zk) * static_cast<double>(p)));
-      if (target > zk) target = zk;
-    } else {
-      target = static_cast<unsigned long long>(
-          ceil(static_cast<double>(zrow) * kMassScaleD * static_cast<double>(p)));
-      if (zk < target) return false;  // the top-p cut lies below the window
-    }
-    if (target < 1) target = 1;
-    int cand = INT_MAX;
-    unsigned long long run = before;
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      if (run < target && run + mk[jj] >= target) {
-        cand = 4 * tid + jj;
-        // Members j of the cut key are kept iff run + j * w < target.
-        const unsigned long long rem = target - run;
-        unsigned long long rp = wfx[jj] == 0 ? ~0ull : (rem + wfx[jj] - 1) / wfx[jj];
-        if (cand == ik && rp > rk) rp = rk;
-        sm.bl[1] = rp;  // one owner
-      }
-      run += mk[jj];
-    }
-    is = block_min_int(cand, sm.wi, lane, warp);
-    rs = sm.bl[1];
-    __syncthreads();
-  }
-  if (is >= kHistKeys) return false;  // unreachable when the masses add up
-  // ---- per-chunk masses of S: keys above the cut wholly, then the cut key's
-  // members in chunk order (chunks are in index order).
-  for (int r = 0; r < C; ++r) {
-    unsigned long long part = 0;
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int i = 4 * tid + jj;
-      if (i < is) part += count_at(r, static_cast<uint32_t>(i)) * wfx[jj];
-    }
-    part = warp_sum(part);
-    if (lane == 0) sm.cmass[r][warp] = part;
-  }
-  if ((is >> 2) == tid) sm.bl[2] = pick4(wfx, is & 3);
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned long long wcut = sm.bl[2];
-    unsigned long long zs = 0, ties_before = 0;
-    for (int r = 0; r < C; ++r) {
-      unsigned long long mr = 0;
-      for (int w = 0; w < kWarps; ++w) mr += sm.cmass[r][w];
-      const uint32_t ties = count_at(r, static_cast<uint32_t>(is));
-      unsigned long long kept = 0;
-      if (ties_before < rs) kept = min(static_cast<unsigned long long>(ties), rs - ties_before);
-      ties_before += ties;
-      sm.cnt[r] = static_cast<uint32_t>(kept);
-      sm.ties[r] = ties;
-      mr += kept * wcut;
-      sm.cmass[r][0] = mr;
-      zs += mr;
-    }
-    const unsigned long long tdraw =
-        static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(zs));
-    unsigned long long cum = 0, tau = 0;
-    int cstar = -1, clast = -1;
-    for (int r = 0; r < C; ++r) {
-      const unsigned long long mr = sm.cmass[r][0];
-      if (cstar < 0 && mr > 0 && tdraw < cum + mr) {
-        cstar = r;
-        tau = tdraw - cum;
-      }
-      if (mr > 0) clast = r;
-      cum += mr;
-    }
-    if (cstar < 0) {
-      cstar = clast;
-      tau = ~0ull;  // the chunk's last token with mass
-    }
-    sm.bi[0] = cstar;
-    sm.bl[3] = tau;
-    sm.bl[5] = zs;
-  }
-  __syncthreads();
-  const int cstar = sm.bi[0];
-  const unsigned long long tau = sm.bl[3];
-  const unsigned long long zs = sm.bl[5];
-  const uint32_t ks = A - static_cast<uint32_t>(is);  // the cut key
-  __syncthreads();
-  // The histograms are consumed: the staging area may overwrite them.
-  // Members of the cut key kept in chunk r (staged): all, none, or those
-  // with index below the returned cut (the first sm.cnt[r]).
-  auto chunk_cut = [&](int r) -> int {
-    const uint32_t kept = sm.cnt[r];
-    if (kept >= sm.ties[r]) return INT_MAX;
-    if (kept == 0) return INT_MIN;
-    return staged_search<true, NV, unsigned long long>(
-               stage, r,
-               [&](float x, int e) { return (e < V && key16(x) == ks) ? 1ull : 0ull; },
-               static_cast<unsigned long long>(kept) - 1ull, sm, tid, lane, warp) + 1;
-  };
-  int tok = -1;
-  if (cstar >= 0) {
-    stage_chunk<true, NV, VEC>(P, row, cstar, stage, warp, lane);
-    const int ecut = chunk_cut(cstar);
-    tok = staged_search<true, NV, unsigned long long>(
-        stage, cstar,
-        [&](float x, int e) {
-          const uint32_t kx = key16(x);
-          const bool in = e < V && (kx > ks || (kx == ks && e < ecut));
-          return in ? mass_fx(weight(x, m, c2)) : 0ull;
-        },
-        tau, sm, tid, lane, warp);
-  }
-  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
-  if (q_row != nullptr) {
-    const float inv = 1.0f / (static_cast<float>(zs) / kMassScale);
-    for (int r = 0; r < C; ++r) {
-      __syncthreads();
-      stage_chunk<true, NV, VEC>(P, row, r, stage, warp, lane);
-      const int ecut = chunk_cut(r);
-      for_staged<true, NV>(stage, r, warp, lane, [&](float x, int e) {
-        if (e < V) {
-          const uint32_t kx = key16(x);
-          const bool in = kx > ks || (kx == ks && e < ecut);
-          q_row[e] = in ? weight(x, m, c2) * inv : 0.0f;
-        }
-      });
-    }
-  }
-  return true;
-}
+// Sampler.prepare's normalisation of one row, and the row's kind (the same
+// decision in both kernels).
+struct RowParams {
+  float T, p, u, c2;
+  int k;     // V when top-k is off
+  int st;    // status bits found so far (a bad uniform)
+  int kind;
+  bool use_p;
+};
 
-// ----------------------------------------------------------------- plain finish (P)
-
-// No filter: the draw is over the whole row.  The leader picks the chunk
-// from the CTAs' masses, re-reads it and finds the token.
-template <bool BF16, int NV, bool VEC>
-__device__ __noinline__ void leader_finish_plain(const SampleParams& P, SampleSmem& sm,
-                                                 const Ctx& c, uint4* stage, int row, float u,
-                                                 float m, float c2, int st, float* q_row) {
-  const int tid = c.tid, lane = c.lane, warp = c.warp;
-  const int C = static_cast<int>(c.csize);
-  const int V = P.V;
-  float zrow = 0.0f;
-  for (int r = 0; r < C; ++r) {
-    const Summary& s = sm.gather[r];
-    if (s.f0 > -INFINITY) zrow += s.f1 * ex2((s.f0 - m) * c2);
-  }
-  float target = u * zrow;
-  if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
-  int cstar = -1, clast = -1;
-  float tau = 0.0f, cum = 0.0f;
-  for (int r = 0; r < C; ++r) {
-    const Summary& s = sm.gather[r];
-    const float mr = s.f0 > -INFINITY ? s.f1 * ex2((s.f0 - m) * c2) : 0.0f;
-    if (cstar < 0 && mr > 0.0f && target < cum + mr) {
-      cstar = r;
-      tau = target - cum;
-    }
-    if (mr > 0.0f) clast = r;
-    cum += mr;
-  }
-  if (cstar < 0) {
-    cstar = clast;
-    tau = INFINITY;
-  }
-  int tok = -1;
-  if (cstar >= 0) {
-    stage_chunk<BF16, NV, VEC>(P, row, cstar, stage, warp, lane);
-    tok = staged_search<BF16, NV, float>(
-        stage, cstar, [&](float x, int e) { return e < V ? weight(x, m, c2) : 0.0f; }, tau, sm,
-        tid, lane, warp);
-  }
-  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
-  if (q_row != nullptr) {
-    const float inv = 1.0f / zrow;
-    for (int r = 0; r < C; ++r) {
-      for_chunk<BF16, NV, VEC>(P, row, r, warp, lane, [&](float x, int e) {
-        if (e < V) q_row[e] = weight(x, m, c2) * inv;
-      });
-    }
-  }
-}
-
-// ----------------------------------------------------------------- the kernel
-
-// One cluster of C CTAs per row (grid C x B); rank 0 is the leader.
-template <bool BF16, int NV, bool VEC, bool ALL_GREEDY>
-__global__ void __launch_bounds__(kThreads, 3)
-    sample_kernel(const __grid_constant__ SampleParams P) {
+template <bool BF16, int NV>
+__device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, int C) {
   using L = Layout<BF16>;
-  constexpr int CHUNK = kThreads * NV * L::VW;  // elements per CTA
-  constexpr int kWarpSpan = 32 * NV * L::VW;    // elements per warp
-  __shared__ SampleSmem sm;
-  extern __shared__ __align__(16) unsigned char dyn[];
-  float* l_val = reinterpret_cast<float*>(dyn);
-  int32_t* l_idx = reinterpret_cast<int32_t*>(dyn + kListCap * 4);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(dyn);
-  uint4* stage = reinterpret_cast<uint4*>(dyn);  // the leader's staged chunk (P, H finishes)
-
-  Ctx c;
-  c.tid = threadIdx.x;
-  c.lane = c.tid & 31;
-  c.warp = c.tid >> 5;
-  c.crank = cluster_rank();
-  c.csize = cluster_size();
+  constexpr int CHUNK = kThreads * NV * L::VW;
+  constexpr int kWarpSpan = 32 * NV * L::VW;
   const int V = P.V;
-  const int row = blockIdx.y;
-  const int tid = c.tid, lane = c.lane, warp = c.warp;
-  const int chunk = static_cast<int>(c.crank);
-  const int cta_begin = chunk * CHUNK;
-  const bool has_pad = cta_begin + CHUNK > V;
-  const bool is_leader = c.crank == 0;
-  const bool clustered = c.csize > 1;
-
-  // The leader's mbarrier collects one arrival from every other CTA.  The
-  // start barrier (relaxed arrive now; the pushing CTAs wait on it before
-  // their first remote store) orders its initialisation before any arrival.
-  if (clustered) {
-    if (is_leader && tid == 0) {
-      mbar_init(reinterpret_cast<uint64_t*>(&sm.bar), c.csize - 1);
-      fence_mbar_init();
-    }
-    cluster_arrive_relaxed();
-  }
-
-  // ---- row parameters (Sampler.prepare's normalisation).
-  const bool greedy = ALL_GREEDY || !(P.temperature[row] > 0.0f);
-  float T = 1.0f, p = 1.0f, u = 0.0f;
-  int k = V;
-  int st = 0;
+  RowParams r;
+  r.T = 1.0f;
+  r.p = 1.0f;
+  r.u = 0.0f;
+  r.k = V;
+  r.st = 0;
+  r.kind = kKindG;
+  const bool greedy = P.temperature == nullptr || !(P.temperature[row] > 0.0f);
   if (!greedy) {
-    T = fmaxf(P.temperature[row], 1e-6f);
-    k = P.top_k != nullptr ? P.top_k[row] : -1;
+    r.T = fmaxf(P.temperature[row], 1e-6f);
+    int k = P.top_k != nullptr ? P.top_k[row] : -1;
     if (k < 1 || k >= V) k = V;
-    p = P.top_p != nullptr ? fminf(fmaxf(P.top_p[row], 1e-6f), 1.0f) : 1.0f;
-    u = P.uniform[row];
+    r.k = k;
+    r.p = P.top_p != nullptr ? fminf(fmaxf(P.top_p[row], 1e-6f), 1.0f) : 1.0f;
+    float u = P.uniform[row];
     if (!(u >= 0.0f && u < 1.0f)) {
-      st |= kStBadUniform;
+      r.st |= kStBadUniform;
       u = (u != u) ? 0.0f : fminf(fmaxf(u, 0.0f), 0x1.fffffep-1f);
     }
-  }
-  const float c2 = 1.4426950408889634f / T;  // log2(e) / T
-  const bool use_p = p < 1.0f;
-  const int R = (kListCap / static_cast<int>(c.csize)) & ~3;  // list entries per CTA region
-  int kind = kKindG;
-  if (!greedy) {
-    // K needs theta_c from the chunk's full warps: kw = ceil(k / full warps)
-    // <= 32 in every chunk; the last chunk has the fewest full warps.
-    const int nfull_min =
-        max(0, min(kWarps, (V - static_cast<int>(c.csize - 1) * CHUNK) / kWarpSpan));
-    if (k < V && k <= 256 && k <= R && nfull_min >= 1 && (k + nfull_min - 1) / nfull_min <= 32) {
-      kind = kKindK;
-    } else if (k == V && !use_p) {
-      kind = kKindP;
+    r.u = u;
+    // K needs theta_c from every chunk's full warps: kw = ceil(k / full
+    // warps) <= 32; the last chunk has the fewest full warps.
+    const int nfull_min = max(0, min(kWarps, (V - (C - 1) * CHUNK) / kWarpSpan));
+    if (k < V && k <= kListRegion && nfull_min >= 1 && (k + nfull_min - 1) / nfull_min <= 32) {
+      r.kind = kKindK;
+    } else if (k == V && !(r.p < 1.0f)) {
+      r.kind = kKindP;
     } else {
-      kind = BF16 ? kKindH : kKindF;
+      r.kind = BF16 ? kKindH : kKindF;
     }
   }
-  float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
-
-  // ---- load the slice; thread maximum (NaN-propagating).
-  uint32_t d[NV][4];
-  load_chunk<BF16, NV, VEC>(P, row, chunk, warp, lane, d);
-  const float tmax = regs_max<BF16, NV>(d);
-  if (q_row != nullptr) {
-    for_regs<BF16, NV>(d, chunk, warp, lane, [&](float, int e) {
-      if (e < V) q_row[e] = 0.0f;
-    });
-  }
-
-  Summary mine = {};
-  if (kind == kKindG) {
-    // ---- greedy: CTA maximum and its first index.
-    const float wmax = warp_max_nan(tmax);
-    if (lane == 0) sm.wf[warp] = wmax;
-    __syncthreads();
-    float cmax = sm.wf[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) cmax = fmax_nan(cmax, sm.wf[w]);
-    int idx = INT_MAX;
-    if (tmax == cmax) {
-      for_regs<BF16, NV>(d, chunk, warp, lane, [&](float x, int e) {
-        if (x == cmax && idx == INT_MAX) idx = e;
-      });
-    }
-    idx = block_min_int(idx, sm.wi, lane, warp);
-    mine.f0 = cmax;
-    mine.i0 = idx;
-    mine.u0 = cmax != cmax ? 1u : 0u;
-  }
-
-  if constexpr (!ALL_GREEDY) {
-    if (kind == kKindK) {
-      // ---- top-k: candidates >= theta_c, the chunk-local bound.
-      const int nfull_cta = max(0, min(kWarps, (V - cta_begin) / kWarpSpan));
-      const int kw = (k + nfull_cta - 1) / nfull_cta;
-      const bool full = cta_begin + (warp + 1) * kWarpSpan <= V;
-      const float sorted = warp_sort_desc(tmax, lane);
-      const float tw = full ? __shfl_sync(kFull, sorted, kw - 1) : INFINITY;
-      const float wmax = warp_max_nan(tmax);
-      if (lane == 0) {
-        sm.wt[warp] = tw;
-        sm.wf[warp] = wmax;
-      }
-      __syncthreads();
-      float theta = INFINITY, cmax = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        theta = fminf(theta, sm.wt[w]);
-        cmax = fmax_nan(cmax, sm.wf[w]);
-      }
-      const bool cnan = cmax != cmax;
-      // Candidate bitmask: bit b is element b of the thread (vector b / VW).
-      constexpr int kElems = NV * L::VW;
-      constexpr int kMaskWords = (kElems + 31) / 32;
-      uint32_t mask[kMaskWords];
-#pragma unroll
-      for (int w = 0; w < kMaskWords; ++w) mask[w] = 0u;
-      if (tmax >= theta) {
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int h = 0; h < L::EPW; ++h) {
-              const int b = (j * 4 + q) * L::EPW + h;
-              if (elem<BF16>(d[j][q], h) >= theta) mask[b >> 5] |= 1u << (b & 31);
-            }
-          }
-        }
-        if (has_pad && theta == -INFINITY) {
-          // Padding reads as -inf: it is a candidate only when theta is -inf.
-#pragma unroll
-          for (int j = 0; j < NV; ++j) {
-            const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
-#pragma unroll
-            for (int b = 0; b < L::VW; ++b) {
-              const int bb = j * L::VW + b;
-              if (e0 + b >= V) mask[bb >> 5] &= ~(1u << (bb & 31));
-            }
-          }
-        }
-      }
-      auto totals = [&](uint32_t* wbase, uint32_t* total) -> uint32_t {
-        uint32_t cnt = 0;
-#pragma unroll
-        for (int w = 0; w < kMaskWords; ++w) cnt += __popc(mask[w]);
-        const uint32_t wc = __reduce_add_sync(kFull, cnt);
-        if (lane == 0) sm.wu[warp] = wc;
-        __syncthreads();
-        uint32_t b = 0, t = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          if (w < warp) b += sm.wu[w];
-          t += sm.wu[w];
-        }
-        __syncthreads();
-        *wbase = b;
-        *total = t;
-        return wc;
-      };
-      uint32_t wbase, total;
-      uint32_t wc = totals(&wbase, &total);
-      if (static_cast<int>(total) > R && !cnan) {
-        // Ties push the count past the region: keep exactly the chunk's top-k.
-        int cloc = INT_MAX;
-        const float tloc = cta_select_topk<BF16, NV, VEC>(
-            P, sm, c, row, theta, static_cast<unsigned long long>(k), &cloc);
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-#pragma unroll
-            for (int h = 0; h < L::EPW; ++h) {
-              const int b = (j * 4 + q) * L::EPW + h;
-              const int e = e0 + q * L::EPW + h;
-              const float x = elem<BF16>(d[j][q], h);
-              if (!(x > tloc || (x == tloc && e < cloc))) mask[b >> 5] &= ~(1u << (b & 31));
-            }
-          }
-        }
-        wc = totals(&wbase, &total);
-      }
-      // Compact the candidates, in index order (vector by vector), into this
-      // CTA's region of its own list; the leader's region is its final place.
-      const uint32_t region = c.crank * static_cast<uint32_t>(R);
-      if (wc != 0) {
-        uint32_t acc = wbase;
-#pragma unroll
-        for (int j = 0; j < NV; ++j) {
-          const int b0 = j * L::VW;
-          const uint32_t vb = (mask[b0 >> 5] >> (b0 & 31)) & ((1u << L::VW) - 1u);
-          const uint32_t cj = __popc(vb);
-          if (__ballot_sync(kFull, cj != 0) == 0) continue;
-          const uint32_t incl = warp_inclusive_scan(cj, lane);
-          uint32_t pos = acc + incl - cj;
-          const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
-          uint32_t bits = vb;
-          while (bits != 0u) {
-            const int b = __ffs(bits) - 1;
-            bits &= bits - 1u;
-            const int q = b / L::EPW;
-            const uint32_t word = q == 0 ? d[j][0] : (q == 1 ? d[j][1] : (q == 2 ? d[j][2] : d[j][3]));
-            if (pos < static_cast<uint32_t>(R)) {
-              l_val[region + pos] = elem<BF16>(word, b % L::EPW);
-              l_idx[region + pos] = e0 + b;
-            }
-            ++pos;
-          }
-          acc += __shfl_sync(kFull, incl, 31);
-        }
-      }
-      const uint32_t nkeep = min(total, static_cast<uint32_t>(R));
-      __syncthreads();
-      if (clustered && !is_leader) {
-        // Copy the region into the leader's list: 16-byte stores (R % 4 == 0).
-        cluster_wait();
-        const uint32_t nv4 = (nkeep + 3u) / 4u;
-        const uint32_t dv = dsmem(l_val + region, 0);
-        const uint32_t di = dsmem(l_idx + region, 0);
-        const uint4* sv = reinterpret_cast<const uint4*>(l_val + region);
-        const uint4* si = reinterpret_cast<const uint4*>(l_idx + region);
-        for (uint32_t i = tid; i < nv4; i += kThreads) {
-          const uint4 a = sv[i];
-          const uint4 b = si[i];
-          st_dsmem_v4(dv + 16u * i, a.x, a.y, a.z, a.w);
-          st_dsmem_v4(di + 16u * i, b.x, b.y, b.z, b.w);
-        }
-      }
-      mine.f0 = cmax;
-      mine.i0 = static_cast<int32_t>(nkeep);
-      mine.u0 = cnan ? 1u : 0u;
-    } else if (kind == kKindP || (kind == kKindH && k == V)) {
-      // ---- chunk max and mass (online: relative to each thread's maximum).
-      float zt = 0.0f;
-      if (tmax > -INFINITY) {
-        // (x - tmax) * c2, not an fma with tmax * c2: for large c2 (T -> 0)
-        // the rounding of tmax * c2 would move the exponent by whole units.
-        for_regs<BF16, NV>(d, chunk, warp, lane, [&](float x, int) { zt += weight(x, tmax, c2); });
-      }
-      const float wmax = warp_max_nan(tmax);
-      const float zw = warp_sum(tmax > -INFINITY ? zt * ex2((tmax - wmax) * c2) : 0.0f);
-      if (lane == 0) {
-        sm.wf[warp] = wmax;
-        sm.wz[warp] = zw;
-      }
-      __syncthreads();
-      float cm = -INFINITY, cz = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w]);
-      if (cm > -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          if (sm.wf[w] > -INFINITY) cz += sm.wz[w] * ex2((sm.wf[w] - cm) * c2);
-        }
-      }
-      mine.f0 = cm;
-      mine.f1 = cz;
-      mine.u0 = cm != cm ? 1u : 0u;
-    } else {
-      // ---- H with top-k (no mass needed) and F: chunk max only.
-      const float wmax = warp_max_nan(tmax);
-      if (lane == 0) sm.wf[warp] = wmax;
-      __syncthreads();
-      float cm = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w]);
-      mine.f0 = cm;
-      mine.u0 = cm != cm ? 1u : 0u;
-    }
-    if constexpr (BF16) {
-      if (kind == kKindH) {
-        // ---- counts per 16-bit key over the window [a - kHistKeys + 1, a].
-        const float cm = mine.f0;
-        const bool finite = cm == cm && cm != INFINITY && cm != -INFINITY;
-        const uint32_t a = finite ? key16(cm) : 0u;
-        hist[tid] = 0u;
-        hist[tid + kThreads] = 0u;
-        __syncthreads();
-        if (finite) {
-          for_regs<true, NV>(d, chunk, warp, lane, [&](float x, int e) {
-            const uint32_t idx = a - key16(x);
-            if (idx < static_cast<uint32_t>(kHistKeys) && (!has_pad || e < V)) {
-              atomicAdd(&hist[idx >> 1], 1u << ((idx & 1u) * 16u));
-            }
-          });
-        }
-        __syncthreads();
-        mine.i0 = static_cast<int32_t>(a);
-        if (clustered && !is_leader) {
-          cluster_wait();
-          const uint32_t dst = dsmem(hist + c.crank * kHistWords, 0) + 8u * tid;
-          asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};"
-                       :: "r"(dst), "r"(hist[2 * tid]), "r"(hist[2 * tid + 1]) : "memory");
-        }
-      }
-    }
-  }
-
-  // ---- publish: non-leaders push the summary and signal the leader.
-  if (!is_leader) {
-    if (kind != kKindK && kind != kKindH) cluster_wait();  // K and H waited before their stores
-    if (tid == 0) {
-      const uint32_t a = dsmem(&sm.gather[c.crank], 0);
-      st_dsmem_v4(a, __float_as_uint(mine.f0), __float_as_uint(mine.f1),
-                  static_cast<uint32_t>(mine.i0), mine.u0);
-    }
-    __syncthreads();
-    if (tid == 0) mbar_remote_arrive(dsmem(&sm.bar, 0));
-    return;
-  }
-  if (tid == 0) sm.gather[0] = mine;
-  if (clustered) {
-    if (tid == 0) {
-      const long long t0 = globaltimer_ns();
-      bool ok = false;
-      while (!(ok = mbar_try_wait_cluster(reinterpret_cast<uint64_t*>(&sm.bar), 0u))) {
-        if (globaltimer_ns() - t0 > kWaitNs) break;
-      }
-      sm.bi[7] = ok ? 1 : 0;
-    }
-    __syncthreads();
-    if (sm.bi[7] == 0) {
-      if (tid == 0) emit_token(P, row, -1, st | kStTimeout);
-      return;
-    }
-  } else {
-    __syncthreads();
-  }
-
-  // ---- the leader finishes the row.
-  const int C = static_cast<int>(c.csize);
-  if (kind == kKindG) {
-    if (tid == 0) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-      uint32_t bn = 0;
-      for (int r = 0; r < C; ++r) {
-        const Summary& s = sm.gather[r];
-        if (s.f0 > bv || (s.f0 == bv && s.i0 < bi)) {
-          bv = s.f0;
-          bi = s.i0;
-        }
-        bn |= s.u0;
-      }
-      const int tok = bn ? -1 : bi;
-      emit_token(P, row, tok, (bn ? kStNonFinite : 0) | st);
-      if (q_row != nullptr && tok >= 0) q_row[tok] = 1.0f;
-    }
-    return;
-  }
-  if constexpr (!ALL_GREEDY) {
-    float m = -INFINITY;
-    uint32_t rn = 0;
-    for (int r = 0; r < C; ++r) {
-      m = fmax_nan(m, sm.gather[r].f0);
-      rn |= sm.gather[r].u0;
-    }
-    if (rn != 0 || m != m || m == INFINITY || m == -INFINITY) {
-      const int est = (m == -INFINITY && rn == 0) ? kStAllNegInf : kStNonFinite;
-      if (tid == 0) emit_token(P, row, -1, est | st);
-      return;
-    }
-    if (kind == kKindK) {
-      if (tid < C) sm.cnt[tid] = static_cast<uint32_t>(sm.gather[tid].i0);
-      __syncthreads();
-      leader_finish_list(P, sm, c, l_val, l_idx, R, row, k, use_p, p, m, c2, u, st, q_row);
-      return;
-    }
-    if (kind == kKindP) {
-      leader_finish_plain<BF16, NV, VEC>(P, sm, c, stage, row, u, m, c2, st, q_row);
-      return;
-    }
-    if constexpr (BF16) {
-      if (kind == kKindH) {
-        float zrow = 0.0f;
-        if (k == V) {
-          for (int r = 0; r < C; ++r) {
-            const Summary& s = sm.gather[r];
-            if (s.f0 > -INFINITY) zrow += s.f1 * ex2((s.f0 - m) * c2);
-          }
-        }
-        if (leader_finish_hist<NV, VEC>(P, sm, c, hist, stage, row, k, use_p, p, u, m, zrow, c2,
-                                        st, q_row)) {
-          return;
-        }
-      }
-    }
-    leader_fallback<BF16>(P, sm, c, row, k, use_p, p, u, m, c2, st, q_row);
-  }
+  r.use_p = r.p < 1.0f;
+  r.c2 = 1.4426950408889634f / r.T;  // log2(e) / T
+  return r;
 }
 
 }  // namespace pkv

@@ -1,61 +1,68 @@
-// Cluster launch of the sampler kernel for one logits dtype.  Included by
-// exactly one translation unit per dtype so that the instantiations compile in
-// parallel.
+// Launch of the two sampler kernels for one logits dtype: the persistent
+// stream kernel, then the finish kernel as its programmatic dependent.
+// Included by exactly one translation unit per dtype so that the
+// instantiations compile in parallel.
 #pragma once
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "launch_config.h"
-#include "sample_kernel.cuh"
+#include "sample_finish.cuh"
+#include "sample_stream.cuh"
 
 namespace pkv {
 
-template <bool BF16, int NV, bool VEC, bool AG>
-cudaError_t launch_one(SampleParams P, int C, cudaStream_t stream) {
-  auto kern = sample_kernel<BF16, NV, VEC, AG>;
-  // An all-greedy batch uses neither the candidate list nor the histograms.
-  const size_t dyn = AG ? 0 : static_cast<size_t>(sample_dyn_bytes<NV>());
+template <bool BF16, int NV, bool VEC>
+cudaError_t launch_pair(const SampleParams& P, int num_sms, cudaStream_t stream) {
+  auto skern = stream_kernel<BF16, NV, VEC>;
+  auto fkern = finish_kernel<BF16, NV, VEC>;
+  constexpr int kStreamDyn = stream_dyn_bytes<NV>();
+  constexpr int kFinishDyn = finish_dyn_bytes<NV>();
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaSuccess;
-    if (dyn > 0) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(dyn));
-      if (e != cudaSuccess) return e;
-    }
-    // Clusters of 9..16 CTAs are a non-portable size; opt in once per kernel.
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kStreamDyn);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fkern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishDyn);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  P.list_cap = kListCap;
+  const int items = P.B * P.chunks;
+  const int ctas = std::min(num_sms, (items + kGroups - 1) / kGroups);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(C), static_cast<unsigned>(P.B), 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = dyn;
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads * kGroups, 1, 1);
+  cfg.dynamicSmemBytes = kStreamDyn;
   cfg.stream = stream;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, skern, P);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t fcfg = {};
+  fcfg.gridDim = dim3(static_cast<unsigned>(P.B), 1, 1);
+  fcfg.blockDim = dim3(kThreads, 1, 1);
+  fcfg.dynamicSmemBytes = kFinishDyn;
+  fcfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, P);
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  fcfg.attrs = attr;
+  fcfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&fcfg, fkern, P);
 }
 
-template <bool BF16, bool AG>
-cudaError_t launch_sample_dtype(const SampleParams& P, const SampleConfig& c,
+template <bool BF16>
+cudaError_t launch_sample_dtype(const SampleParams& P, const SampleConfig& c, int num_sms,
                                 cudaStream_t stream) {
   if (!c.vec) {
-    if (c.nv == 10) return launch_one<BF16, 10, false, AG>(P, c.cluster, stream);
-    return launch_one<BF16, kNvScalar, false, AG>(P, c.cluster, stream);
+    if (c.nv == 10) return launch_pair<BF16, 10, false>(P, num_sms, stream);
+    return launch_pair<BF16, kNvScalar, false>(P, num_sms, stream);
   }
   switch (c.nv) {
-    case 4: return launch_one<BF16, 4, true, AG>(P, c.cluster, stream);
-    case 8: return launch_one<BF16, 8, true, AG>(P, c.cluster, stream);
-    case 10: return launch_one<BF16, 10, true, AG>(P, c.cluster, stream);
-    case 16: return launch_one<BF16, 16, true, AG>(P, c.cluster, stream);
+    case 4: return launch_pair<BF16, 4, true>(P, num_sms, stream);
+    case 8: return launch_pair<BF16, 8, true>(P, num_sms, stream);
+    case 10: return launch_pair<BF16, 10, true>(P, num_sms, stream);
+    case 16: return launch_pair<BF16, 16, true>(P, num_sms, stream);
     default: return cudaErrorInvalidValue;
   }
 }

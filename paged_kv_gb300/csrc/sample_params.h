@@ -1,9 +1,14 @@
 // Launch parameters of the sampler kernel (host and device side).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 
 namespace pkv {
+
+// Bytes of one workspace record (ChunkSlot in sample_common.cuh): a 16-byte
+// summary, 2 x 8 per-warp floats and a 2 KB payload.
+constexpr size_t kChunkSlotBytes = 16 + 64 + 2048;
 
 struct SampleParams {
   const void* logits;        // [B, row_stride] fp32 or bf16
@@ -22,8 +27,9 @@ struct SampleParams {
   const int64_t* wb_cols;    // [B]
   float* probs_out;          // [B, V] or nullptr
   int32_t* status;           // device status word or nullptr
-  int cta_chunk;             // elements owned by one CTA of a row's cluster
-  int list_cap;              // candidate-list entries in the leader's shared memory
+  int cta_chunk;             // elements of one chunk (one item of the stream kernel)
+  int chunks;                // chunks per row
+  void* workspace;           // [B * chunks] ChunkSlot records (stream -> finish)
 };
 
 }  // namespace pkv

@@ -103,6 +103,28 @@ def sample_workspace_bytes(B: int, V: int, dtype: torch.dtype) -> int:
     return int(load().pkv_sample_workspace_bytes(B, V, PKV_BF16 if dtype == torch.bfloat16 else PKV_FP32))
 
 
+_workspaces = {}
+
+
+def sample_workspace_bytes(B: int, V: int, dtype: torch.dtype) -> int:
+    """pkv_sample_workspace_bytes for a [B, V] batch of ``dtype`` logits."""
+    code = PKV_BF16 if dtype == torch.bfloat16 else PKV_FP32
+    return int(load().pkv_sample_workspace_bytes(int(B), int(V), code))
+
+
+def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A cached uint8 device buffer of at least ``nbytes`` (grown as needed).
+
+    Calls on different streams of one device must pass their own workspace.
+    """
+    key = (device.type, device.index)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
 def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = None,
                  top_k: Optional[torch.Tensor] = None, top_p: Optional[torch.Tensor] = None,
                  uniform: Optional[torch.Tensor] = None,
@@ -110,11 +132,13 @@ def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = Non
                  token_pool: Optional[torch.Tensor] = None,
                  wb_rows: Optional[torch.Tensor] = None, wb_cols: Optional[torch.Tensor] = None,
                  probs_out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                 stream=None) -> torch.Tensor:
+                 workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """pkv_sample_batch: one int32 token per row of ``logits`` [B, V].
 
     ``logits`` is fp32 or bf16 with unit column stride (any row stride).
-    Returns ``out_tokens`` (allocated here if not given).  See include/pkv.h.
+    ``workspace`` (a uint8 CUDA tensor) defaults to a buffer cached per
+    device.  Returns ``out_tokens`` (allocated here if not given).  See
+    include/pkv.h.
     """
     lib = load()
     if logits.dim() != 2 or not logits.is_cuda:
@@ -135,6 +159,11 @@ def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = Non
         if token_pool.dim() != 2:
             raise ValueError("token_pool must be 2-D")
         pool_rows, pool_cols = token_pool.shape
+    need = int(lib.pkv_sample_workspace_bytes(B, V, dcode))
+    if workspace is None:
+        workspace = _workspace(logits.device, need)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous uint8 CUDA tensor")
     rc = lib.pkv_sample_batch(
         logits.data_ptr(), dcode, B, V, logits.stride(0),
         _dev(temperature, torch.float32, "temperature", B),
@@ -143,7 +172,7 @@ def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = Non
         _dev(token_pool, torch.int32, "token_pool"), pool_rows, pool_cols,
         _dev(wb_rows, torch.int32, "wb_rows", B), _dev(wb_cols, torch.int64, "wb_cols", B),
         _dev(probs_out, torch.float32, "probs_out", B * V), _dev(status, torch.int32, "status", 1),
-        None, 0, _stream(stream, logits.device))
+        workspace.data_ptr(), workspace.numel(), _stream(stream, logits.device))
     _check(rc)
     return out_tokens
 

@@ -31,8 +31,29 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_version_and_workspace():
-    assert pkv.version() == 100
-    assert pkv.load().pkv_sample_workspace_bytes(256, 151936, 1) == 0
+    lib = pkv.load()
+    assert pkv.version() == 200
+    # One 2128-byte record per (row, chunk); the mixed batch's rows are 8
+    # chunks of 20480 bf16 logits.
+    assert lib.pkv_sample_workspace_bytes(256, 151936, 1) == 256 * 8 * 2128
+    assert lib.pkv_sample_workspace_bytes(1024, 256000, 1) == 1024 * 16 * 2128
+    assert lib.pkv_sample_workspace_bytes(0, 100, 1) == 0
+    assert lib.pkv_sample_workspace_bytes(4, 0, 1) == 0
+    assert lib.pkv_sample_workspace_bytes(4, 100, 7) == 0
+
+
+def test_sample_batch_requires_a_workspace():
+    lib = pkv.load()
+    p = ctypes.c_void_p(256)
+    need = lib.pkv_sample_workspace_bytes(256, 151936, 1)
+    common = (p, 1, 256, 151936, 151936, None, None, None, None, p, None, 0, 0,
+              None, None, None, None)
+    rc = lib.pkv_sample_batch(*common, None, 0, None)
+    assert rc == pkv.PKV_EINVAL and "workspace" in pkv.last_error()
+    rc = lib.pkv_sample_batch(*common, p, need - 1, None)
+    assert rc == pkv.PKV_EINVAL and "workspace" in pkv.last_error()
+    rc = lib.pkv_sample_batch(*common, ctypes.c_void_p(264), need, None)
+    assert rc == pkv.PKV_EINVAL and "aligned" in pkv.last_error()
 
 
 def test_host_validation_launches_nothing():
