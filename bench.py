@@ -34,8 +34,10 @@ if ROOT not in sys.path:
 METRIC = "sampled tokens/s and logits GB/s vs GB300 HBM peak at B=256, V=151936 bf16"
 UNIT = "tokens/s"
 WORKLOAD = "mixed"
-KERNEL_SOURCES = ("paged_kv_gb300/csrc/sample_kernel.cuh", "paged_kv_gb300/csrc/device_common.cuh",
-                  "paged_kv_gb300/csrc/launch_config.h", "paged_kv_gb300/csrc/sample_launch.cuh")
+KERNEL_SOURCES = ("paged_kv_gb300/csrc/sample_common.cuh", "paged_kv_gb300/csrc/sample_stream.cuh",
+                  "paged_kv_gb300/csrc/sample_finish.cuh", "paged_kv_gb300/csrc/sample_launch.cuh",
+                  "paged_kv_gb300/csrc/device_common.cuh", "paged_kv_gb300/csrc/launch_config.h")
+GRAPH_LEN = 20  # steps per captured CUDA graph
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sampler_mixed_traffic.json")
 
 
@@ -126,6 +128,56 @@ def timed_steps(step, steps: int, warmup: int, dist_mod=None, device=None) -> fl
         for i in range(steps):
             step(i)
         ms = (time.perf_counter() - t0) * 1e3
+    barrier(dist_mod, device)
+    return max_over_ranks(ms, dist_mod, device)
+
+
+def make_graph(fn, n: int, device):
+    """Captures n calls fn(0..n-1) into one CUDA graph (after two warm calls
+    on the capture stream, so that lazy allocations happen outside it)."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for i in range(2):
+            fn(i)
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    with torch.cuda.graph(g, stream=s):
+        for i in range(n):
+            fn(i)
+    torch.cuda.synchronize(device)
+    return g
+
+
+def timed_graph_steps(fn, steps: int, warmup: int, dist_mod, device) -> float:
+    """Times exactly `steps` calls of fn, replayed from CUDA graphs of
+    GRAPH_LEN calls (plus one graph for the remainder) so that host launch
+    cost does not enter; at least `warmup` untimed calls first.  Barriers,
+    synchronisation and the max over ranks as in timed_steps."""
+    import torch
+
+    glen = max(1, min(GRAPH_LEN, steps))
+    full = make_graph(fn, glen, device)
+    rem = steps % glen
+    tail = make_graph(fn, rem, device) if rem else None
+    for _ in range(max(1, -(-warmup // glen))):
+        full.replay()
+    torch.cuda.synchronize(device)
+    barrier(dist_mod, device)
+    torch.cuda.synchronize(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps // glen):
+        full.replay()
+    if tail is not None:
+        tail.replay()
+    end.record()
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(end)
     barrier(dist_mod, device)
     return max_over_ranks(ms, dist_mod, device)
 
@@ -283,27 +335,28 @@ def run_ours(args):
         pkv.fill_page_table(cached, dev_len, tidx, w.page_size, free, pt, total, status)
 
     with ClockSampler(physical_gpu_index(local_rank)) as clocks:
-        ms = timed_steps(step, args.steps, args.warmup, dist_mod, device)
+        ms = timed_graph_steps(step, args.steps, args.warmup, dist_mod, device)
     torch.cuda.synchronize(device)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status word {int(status.item())} after the timed run")
     ms_per_step = ms / args.steps
     value = world * w.B / (ms_per_step * 1e-3)
 
-    # Dominant kernel (the sampler) alone, timed with events on the stream it
-    # is launched on (torch's current stream).
+    # The dominant operation (one pkv_sample_batch: stream + finish kernel)
+    # alone, replayed from graphs and timed with events on the replay stream.
     n_k = max(200, min(args.steps, 5000))
-    ms_k = timed_steps(lambda i: pkv.sample_batch(bufs[i % nbuf], t, k, p, u, out_tokens=out,
-                                                  token_pool=pool, wb_rows=rows, wb_cols=cols,
-                                                  status=status),
-                       n_k, args.warmup, dist_mod, device)
+    ms_k = timed_graph_steps(lambda i: pkv.sample_batch(bufs[i % nbuf], t, k, p, u,
+                                                        out_tokens=out, token_pool=pool,
+                                                        wb_rows=rows, wb_cols=cols,
+                                                        status=status),
+                             n_k, args.warmup, dist_mod, device)
     us_k = ms_k / n_k * 1e3
     alg = algorithmic_bytes(w)
     achieved = alg / (us_k * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
-    ms_f = timed_steps(lambda i: pkv.fill_page_table(cached, dev_len, tidx, w.page_size, free,
-                                                     pt, total, status),
-                       n_k, args.warmup, dist_mod, device)
+    ms_f = timed_graph_steps(lambda i: pkv.fill_page_table(cached, dev_len, tidx, w.page_size,
+                                                           free, pt, total, status),
+                             n_k, args.warmup, dist_mod, device)
 
     # End to end through the public API from pinned host buffers: H2D of the
     # step's inputs, the two calls, D2H of the tokens and the page total.
@@ -353,13 +406,16 @@ def run_ours(args):
                        "l2": f"logits rotate over {nbuf} buffers ({nbuf * logit_bytes >> 20} MiB > 2x L2)"},
             "logits_gbs": round(world * logit_bytes / (ms_per_step * 1e-3) / 1e9, 1),
             "page_fill_us": round(ms_f / n_k * 1e3, 3),
-            "roofline": {"bound": "hbm", "kernel": "sample_kernel", "achieved": round(achieved, 1),
+            "roofline": {"bound": "hbm", "kernel": "pkv_sample_batch (stream_kernel + finish_kernel)",
+                         "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
                          "algorithmic_bytes": alg, "us_per_launch": round(us_k, 3)},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 3 * args.steps,
+            "timing": f"device value and roofline: CUDA graphs of {GRAPH_LEN} steps replayed; "
+                      "e2e: host-launched calls",
             "clocks": clocks.summary(),
             "cpu_baseline": cpu,
         }

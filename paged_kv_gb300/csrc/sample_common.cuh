@@ -53,24 +53,31 @@ constexpr int kBuckets = 256;
 constexpr int kMaxChunks = 16;                 // chunks per row
 constexpr int kHistKeys = 1024;                // values counted below a chunk's maximum (H rows)
 constexpr int kHistWords = kHistKeys / 2;      // two 16-bit counts per word
-constexpr int kListRegion = 256;               // candidate entries per chunk (K rows), >= k
-constexpr int kListCap = kMaxChunks * kListRegion;
+constexpr int kMaxK = 256;                     // largest k of a K row
+constexpr int kListCap = kMaxChunks * kMaxK;   // candidates the finisher keeps (K rows)
 constexpr int kListBytes = kListCap * 8;       // the finisher's list, or its C histograms
 static_assert(kMaxChunks * kHistWords * 4 == kListBytes, "list and histograms share the space");
 static_assert(kHistKeys == 4 * kThreads, "four merged histogram keys per finisher thread");
 static_assert(kHistWords == 2 * kThreads, "two histogram words per thread");
-static_assert(kListRegion * 2 == kHistWords, "a chunk's list and histogram fill one payload");
 
-// Dynamic shared memory of the finish kernel.  From offset 0: the candidate
-// list or the histograms, later (H rows) one staged chunk of kThreads * NV
-// 16-byte vectors; then the fixed-point mass per merged key.
+
+// Dynamic shared memory of the finish kernel.  [0, kListBytes): the
+// candidate list (K rows) or the histograms (H rows), later overwritten (H)
+// by one staged chunk of kThreads * NV 16-byte vectors; K rows keep the
+// thread maxima at kFinOffTm and the per-vector counts at kFinOffCnt; H rows
+// keep the fixed-point mass per merged key at finish_table_offset.
+constexpr int kMaxCandVecs = 4096;  // candidate vectors a K row's finisher handles
+constexpr int kFinOffTm = kListBytes;
+constexpr int kFinOffCnt = kFinOffTm + kMaxChunks * kThreads * 4;
+constexpr int kFinKEnd = kFinOffCnt + kMaxCandVecs * 4;
 template <int NV>
 constexpr int finish_table_offset() {
-  return kThreads * NV * 16 > kListBytes ? kThreads * NV * 16 : kListBytes;
+  return kThreads * NV * 16 > kFinOffCnt ? kThreads * NV * 16 : kFinOffCnt;
 }
 template <int NV>
 constexpr int finish_dyn_bytes() {
-  return finish_table_offset<NV>() + kHistKeys * 8;
+  return finish_table_offset<NV>() + kHistKeys * 8 > kFinKEnd ? finish_table_offset<NV>() + kHistKeys * 8
+                                                              : kFinKEnd;
 }
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
 constexpr double kMassScaleD = 1099511627776.0;
@@ -87,19 +94,23 @@ enum RowKind { kKindG = 0, kKindK = 1, kKindP = 2, kKindH = 3, kKindF = 4 };
 
 // One chunk's summary.
 struct __align__(16) Summary {
-  float f0;     // G: chunk max; others: chunk max (NaN if the chunk has a NaN)
-  float f1;     // P, and H without top-k: chunk mass relative to f0
-  int32_t i0;   // G: first index of the max; K: candidate count; H: 16-bit key of f0
-  uint32_t u0;  // bit 0: NaN seen; bit 1: a bulk copy timed out
+  float f0;     // unused
+  float f1;     // unused
+  int32_t i0;   // H: 16-bit key of the chunk maximum (the histogram's anchor)
+  uint32_t u0;  // bit 1: a bulk copy timed out
 };
 
 // The workspace record of one (row, chunk): written by the stream kernel,
-// read by the finish kernel.
+// read by the finish kernel.  Warp w of the chunk owns wm[w] (its maximum,
+// NaN if it saw a NaN) and wz[w] (P rows and H rows without top-k: its mass
+// relative to wm[w]); thread t owns tmax[t] (K rows: its maximum); H rows
+// keep their count histogram in hist.
 struct __align__(16) ChunkSlot {
   Summary s;
-  float wm[kWarps];               // P rows: per-warp maximum
-  float wz[kWarps];               // P rows: per-warp mass relative to wm
-  uint32_t payload[kHistWords];   // K: values [0, 256) then indices; H: packed counts
+  float wm[kWarps];
+  float wz[kWarps];
+  float tmax[kThreads];
+  uint32_t hist[kHistWords];
 };
 
 struct SampleSmem {
@@ -258,6 +269,18 @@ __device__ __forceinline__ float vec_max(const uint32_t (&w)[4]) {
   }
 }
 
+// x.lo >= t and x.hi >= t for the two bf16 values of a word (t2 holds t in
+// both halves; NaN compares false, -0 equals +0): bit 0 and bit 1.
+__device__ __forceinline__ uint32_t bf16x2_ge(uint32_t x, uint32_t t2) {
+  uint32_t r;
+  asm("{\n\t.reg .pred p, q;\n\t"
+      "setp.ge.bf16x2 p|q, %1, %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@q or.b32 %0, %0, 2;\n\t}"
+      : "=r"(r) : "r"(x), "r"(t2));
+  return r;
+}
+
 // 16-bit order-preserving key of a bf16 value held as a float (-0 folded).
 __device__ __forceinline__ uint32_t key16(float x) { return float_key(x) >> 16; }
 
@@ -391,19 +414,6 @@ __device__ __forceinline__ void emit_token(const SampleParams& P, int row, int t
 }
 
 // ----------------------------------------------------------------- warp helpers
-
-// The kw-th largest (1 <= kw <= 32) of the lanes' keys, by a bit-serial
-// search with ballots: keep a candidate bit when at least kw lanes have a key
-// >= the prefix with that bit set.
-__device__ __forceinline__ uint32_t warp_kth_largest_key(uint32_t key, int kw, int top_bit,
-                                                         int low_bit) {
-  uint32_t prefix = 0u;
-  for (int bit = top_bit; bit >= low_bit; --bit) {
-    const uint32_t cand = prefix | (1u << bit);
-    if (__popc(__ballot_sync(kFull, key >= cand)) >= kw) prefix = cand;
-  }
-  return prefix;
-}
 
 // ----------------------------------------------------------------- chunk search
 //
@@ -819,51 +829,17 @@ __device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&
   return pos >= 0 ? idx[pos] : -1;
 }
 
-// K rows.  The leader holds every candidate of the row in its list, region r
-// (entries r*R .. r*R + cnt[r]) coming from CTA r, each region in index
-// order.  Packs the regions, then finishes exactly on the list: top-k (count
-// select, ties by index), top-p inside K (mass select on 2^-40 fixed-point
-// weights), renormalisation and the inverse-CDF draw.  Emits the token and,
-// if asked, the probabilities of the kept tokens.
+// K rows.  The finisher holds every candidate of the row in its list,
+// entries 0 .. n-1 in index order.  Finishes exactly on the list: top-k
+// (count select, ties by index), top-p inside K (mass select on 2^-40
+// fixed-point weights), renormalisation and the inverse-CDF draw.  Emits the
+// token and, if asked, the probabilities of the kept tokens.
 static __device__ __forceinline__ void leader_finish_list(const SampleParams& P, SampleSmem& sm,
-                                                const Ctx& c, float* l_val, int32_t* l_idx, int R,
-                                                int row, int k, bool use_p, float p, float m,
-                                                float c2, float u, int st, float* q_row) {
+                                                          const Ctx& c, float* l_val,
+                                                          int32_t* l_idx, int n, int row, int k,
+                                                          bool use_p, float p, float m, float c2,
+                                                          float u, int st, float* q_row) {
   const int tid = c.tid, lane = c.lane, warp = c.warp;
-  int n = 0;
-  for (uint32_t r = 0; r < c.csize; ++r) n += static_cast<int>(sm.cnt[r]);
-  {
-    // Packed index i comes from region r at offset i - (earlier counts),
-    // never from a position below i: read, barrier, write.
-    constexpr int kMovePer = 16;
-    float mv[kMovePer];
-    int mi[kMovePer];
-    for (int b0 = 0; b0 < n; b0 += kThreads * kMovePer) {
-#pragma unroll
-      for (int q = 0; q < kMovePer; ++q) {
-        const int i = b0 + q * kThreads + tid;
-        if (i < n) {
-          int r = 0, off = i;
-          while (off >= static_cast<int>(sm.cnt[r])) {
-            off -= static_cast<int>(sm.cnt[r]);
-            ++r;
-          }
-          mv[q] = l_val[r * R + off];
-          mi[q] = l_idx[r * R + off];
-        }
-      }
-      group_sync();
-#pragma unroll
-      for (int q = 0; q < kMovePer; ++q) {
-        const int i = b0 + q * kThreads + tid;
-        if (i < n) {
-          l_val[i] = mv[q];
-          l_idx[i] = mi[q];
-        }
-      }
-      group_sync();
-    }
-  }
   unsigned long long rk;
   const float tk = list_select<false>(l_val, n, [](int) { return true; },
                                       [](int) { return 1ull; },
@@ -905,73 +881,6 @@ static __device__ __forceinline__ void leader_finish_list(const SampleParams& P,
       if (in_s(i)) q_row[l_idx[i]] = w_of(i) * inv;
     }
   }
-}
-
-// ----------------------------------------------------------------- CTA-local top-k
-
-// Exact top-k of this CTA's elements x >= theta (e < V), by (value desc,
-// index asc): returns t and *cut such that they are {x > t} and {x == t,
-// e < cut}.  Radix select over keys with 32-bit shared atomics, re-reading
-// the chunk from global memory; used only when ties overflow a K row's list
-// region.
-template <bool BF16, int NV, bool VEC>
-__device__ __noinline__ float cta_select_topk(const SampleParams& P, SampleSmem& sm, const Ctx& c,
-                                              int row, float theta, unsigned long long k,
-                                              int* cut) {
-  const int chunk = static_cast<int>(c.crank);
-  const int V = P.V;
-  auto keep = [&](float x, int e) { return x >= theta && e < V; };
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  for_chunk<BF16, NV, VEC>(P, row, chunk, c.warp, c.lane, [&](float x, int e) {
-    if (keep(x, e)) {
-      const uint32_t key = float_key(x);
-      lo = min(lo, key);
-      hi = max(hi, key);
-    }
-  });
-  lo = __reduce_min_sync(kFull, lo);
-  hi = __reduce_max_sync(kFull, hi);
-  if (c.lane == 0) {
-    sm.wu[c.warp] = lo;
-    sm.wi[c.warp] = static_cast<int32_t>(hi);
-  }
-  group_sync();
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int w = 0; w < kWarps; ++w) {
-    kmin = min(kmin, sm.wu[w]);
-    kmax = max(kmax, static_cast<uint32_t>(sm.wi[w]));
-  }
-  group_sync();
-  unsigned long long rem = k;
-  uint32_t prefix = kmin;
-  if (kmin != kmax) {
-    const int top = 31 - __clz(kmin ^ kmax);
-    prefix = static_cast<uint32_t>(static_cast<unsigned long long>(kmin) & ~((2ull << top) - 1ull));
-    for (int hb = top; hb >= 0; hb -= 8) {
-      const int lb = hb >= 7 ? hb - 7 : 0;
-      const uint32_t dmask = (1u << (hb - lb + 1)) - 1u;
-      const uint32_t amask = static_cast<uint32_t>(~((2ull << hb) - 1ull));
-      sm.hlo[c.tid] = 0u;
-      group_sync();
-      for_chunk<BF16, NV, VEC>(P, row, chunk, c.warp, c.lane, [&](float x, int e) {
-        if (!keep(x, e)) return;
-        const uint32_t key = float_key(x);
-        if ((key & amask) == (prefix & amask)) atomicAdd(&sm.hlo[(key >> lb) & dmask], 1u);
-      });
-      group_sync();
-      unsigned long long above;
-      const int b = select_bucket(sm.hlo[c.tid], rem, sm, &above, c.tid, c.lane, c.warp);
-      rem -= above;
-      prefix |= static_cast<uint32_t>(b) << lb;
-    }
-  }
-  const float t = key_float(prefix);
-  // Cut after the rem-th member equal to t (index order).
-  const int pos = chunk_search<BF16, NV, VEC, unsigned long long>(
-      P, row, chunk, [&](float x, int e) { return (keep(x, e) && x == t) ? 1ull : 0ull; },
-      rem - 1ull, sm, c.tid, c.lane, c.warp);
-  *cut = pos >= 0 ? pos + 1 : INT_MAX;
-  return t;
 }
 
 // ----------------------------------------------------------------- exact fallback (F)
@@ -1175,8 +1084,6 @@ struct RowParams {
 template <bool BF16, int NV>
 __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, int C) {
   using L = Layout<BF16>;
-  constexpr int CHUNK = kThreads * NV * L::VW;
-  constexpr int kWarpSpan = 32 * NV * L::VW;
   const int V = P.V;
   RowParams r;
   r.T = 1.0f;
@@ -1198,10 +1105,11 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
       u = (u != u) ? 0.0f : fminf(fmaxf(u, 0.0f), 0x1.fffffep-1f);
     }
     r.u = u;
-    // K needs theta_c from every chunk's full warps: kw = ceil(k / full
-    // warps) <= 32; the last chunk has the fewest full warps.
-    const int nfull_min = max(0, min(kWarps, (V - (C - 1) * CHUNK) / kWarpSpan));
-    if (k < V && k <= kListRegion && nfull_min >= 1 && (k + nfull_min - 1) / nfull_min <= 32) {
+    // K bounds the k-th value by the k-th largest thread maximum: it needs
+    // at least k threads whose elements all lie inside the row.
+    const int full_threads = V / (NV * L::VW);
+    (void)C;
+    if (k < V && k <= kMaxK && full_threads >= k) {
       r.kind = kKindK;
     } else if (k == V && !(r.p < 1.0f)) {
       r.kind = kKindP;

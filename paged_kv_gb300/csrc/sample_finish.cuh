@@ -346,73 +346,201 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant_
   const ChunkSlot* slots = static_cast<const ChunkSlot*>(P.workspace) + static_cast<size_t>(row) * C;
   const RowParams rp = row_params<BF16, NV>(P, row, C);
   float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
+  // Per-warp maxima of every chunk (NaN-propagating), summaries, flags.
+  for (int i = tid; i < C * kWarps; i += kThreads) {
+    sm.gwm[i / kWarps][i % kWarps] = slots[i / kWarps].wm[i % kWarps];
+    sm.gwz[i / kWarps][i % kWarps] = slots[i / kWarps].wz[i % kWarps];
+  }
   if (tid < C) sm.gather[tid] = slots[tid].s;
   group_sync();
   uint32_t flags = 0;
-  for (int r = 0; r < C; ++r) flags |= sm.gather[r].u0;
+  float m = -INFINITY;
+  for (int r = 0; r < C; ++r) {
+    flags |= sm.gather[r].u0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) m = fmax_nan(m, sm.gwm[r][w]);
+  }
   if (flags & 2u) {
     if (tid == 0) emit_token(P, row, -1, rp.st | kStTimeout);
     return;
   }
   if (rp.kind == kKindG) {
-    if (tid == 0) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
-      for (int r = 0; r < C; ++r) {
-        const Summary& s = sm.gather[r];
-        if (s.f0 > bv || (s.f0 == bv && s.i0 < bi)) {
-          bv = s.f0;
-          bi = s.i0;
-        }
+    // ---- greedy: the first (chunk, warp) in index order holding the row
+    // maximum; its warp slice is re-read to find the first index.
+    if (m != m) {
+      if (tid == 0) emit_token(P, row, -1, kStNonFinite | rp.st);
+      return;
+    }
+    int first = INT_MAX;
+    for (int i = tid; i < C * kWarps; i += kThreads) {
+      if (sm.gwm[i / kWarps][i % kWarps] == m) first = min(first, i);
+    }
+    first = block_min_int(first, sm.wi, c.lane, c.warp);
+    if (c.warp == 0) {
+      // One batch of loads for the warp's whole slice, then the first match
+      // in index order (vector j, then lane, then element).
+      const int r = first / kWarps, w = first % kWarps;
+      uint32_t d[NV][4];
+      load_chunk<BF16, NV, VEC>(P, row, r, w, c.lane, d);
+      int idx = INT_MAX;
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        int mine = INT_MAX;
+        for_vec<BF16>(d[j], vec_base<BF16, NV>(r, w, c.lane, j), [&](float x, int e) {
+          if (x == m && e < V && mine == INT_MAX) mine = e;
+        });
+        const int jm = __reduce_min_sync(kFull, mine);
+        if (idx == INT_MAX) idx = jm;
       }
-      const int tok = flags ? -1 : bi;
-      emit_token(P, row, tok, (flags ? kStNonFinite : 0) | rp.st);
-      if (q_row != nullptr && tok >= 0) q_row[tok] = 1.0f;
+      if (c.lane == 0) {
+        emit_token(P, row, idx, rp.st);
+        if (q_row != nullptr) q_row[idx] = 1.0f;
+      }
     }
     return;
   }
-  float m = -INFINITY;
-  for (int r = 0; r < C; ++r) m = fmax_nan(m, sm.gather[r].f0);
-  if (flags != 0 || m != m || m == INFINITY || m == -INFINITY) {
-    const int est = (m == -INFINITY && flags == 0) ? kStAllNegInf : kStNonFinite;
+  if (m != m || m == INFINITY || m == -INFINITY) {
+    const int est = (m == -INFINITY) ? kStAllNegInf : kStNonFinite;
     if (tid == 0) emit_token(P, row, -1, est | rp.st);
     return;
   }
   if (rp.kind == kKindK) {
-    if (tid < C) sm.cnt[tid] = static_cast<uint32_t>(sm.gather[tid].i0);
+    // ---- top-k.  theta = the k-th largest thread maximum of the row: at
+    // least k elements are >= theta, so every element of the top-k is >=
+    // theta and lies in a thread whose maximum is >= theta.  Those threads'
+    // vectors are re-read (an L2 hit); their elements >= theta form the
+    // candidate list, in index order.
+    using L = Layout<BF16>;
+    float* tm = reinterpret_cast<float*>(dyn + kFinOffTm);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(dyn + kFinOffCnt);
+    const int nT = C * kThreads;
+    for (int i = tid; i < nT; i += kThreads) tm[i] = slots[i / kThreads].tmax[i % kThreads];
     group_sync();
-    for (int r = 0; r < C; ++r) {
-      const uint32_t n = sm.cnt[r];
-      for (uint32_t i = tid; i < n; i += kThreads) {
-        l_val[r * kListRegion + i] = __uint_as_float(slots[r].payload[i]);
-        l_idx[r * kListRegion + i] = static_cast<int32_t>(slots[r].payload[kListRegion + i]);
+    unsigned long long rk;
+    const float theta = list_select<false>(tm, nT, [](int) { return true; },
+                                           [](int) { return 1ull; },
+                                           static_cast<unsigned long long>(rp.k), sm, c, &rk);
+    // Candidate lanes of each (chunk, warp) pair q = chunk * kWarps + warp;
+    // vector (q, j, lane) of a candidate lane has rank
+    //   vbase[q] + j * popc(M_q) + popc(M_q below lane)
+    // among the candidate vectors, which is index order.
+    uint32_t* Mq = reinterpret_cast<uint32_t*>(sm.scan);     // kMaxChunks * kWarps <= 128
+    uint32_t* vbase = Mq + kMaxChunks * kWarps;              // ... and their bases
+    for (int q = c.warp; q < C * kWarps; q += kWarps) {
+      const unsigned mq = __ballot_sync(kFull, tm[q * 32 + c.lane] >= theta);
+      if (c.lane == 0) Mq[q] = mq;
+    }
+    group_sync();
+    if (tid == 0) {
+      uint32_t acc = 0;
+      for (int q = 0; q < C * kWarps; ++q) {
+        vbase[q] = acc;
+        acc += static_cast<uint32_t>(__popc(Mq[q])) * NV;
+      }
+      sm.bi[0] = static_cast<int32_t>(acc);
+    }
+    group_sync();
+    const int nvec = sm.bi[0];
+    if (nvec <= kMaxCandVecs && theta > -INFINITY) {
+      // Each thread takes candidate vectors v = tid + r * kThreads (at most
+      // kKeep kept in registers; more are re-read).
+      constexpr int kKeep = 4;
+      uint32_t keepv[kKeep][4];
+      auto decode = [&](int v, uint32_t (&w4)[4]) -> int {
+        int q = 0;
+        while (q + 1 < C * kWarps && vbase[q + 1] <= static_cast<uint32_t>(v)) ++q;
+        const uint32_t mq = Mq[q];
+        const int pc = __popc(mq);
+        const int off = v - static_cast<int>(vbase[q]);
+        const int j = off / pc;
+        int nth = off % pc;
+        uint32_t bits = mq;
+        while (nth-- > 0) bits &= bits - 1u;
+        const int lane_q = __ffs(bits) - 1;
+        const int e0 = vec_base<BF16, NV>(q / kWarps, q % kWarps, lane_q, j);
+        load_vec<BF16, NV, VEC>(P, row, e0, w4);
+        return e0;
+      };
+      int keep_e0[kKeep];
+      auto count_vec = [&](int v, uint32_t (&w4)[4], int* e0_out) {
+        const int e0 = decode(v, w4);
+        uint32_t nc = 0;
+        for_vec<BF16>(w4, e0, [&](float x, int e) { nc += (e < V && x >= theta) ? 1u : 0u; });
+        cnt[v] = nc;
+        *e0_out = e0;
+      };
+#pragma unroll
+      for (int r = 0; r < kKeep; ++r) {
+        const int v = tid + r * kThreads;
+        if (v < nvec) count_vec(v, keepv[r], &keep_e0[r]);
+      }
+      for (int v = tid + kKeep * kThreads; v < nvec; v += kThreads) {
+        uint32_t w4[4];
+        int e0;
+        count_vec(v, w4, &e0);
+      }
+      group_sync();
+      // Exclusive prefix of the counts in vector order: contiguous segments.
+      const int per = (nvec + kThreads - 1) / kThreads;
+      const int i0 = min(nvec, tid * per), i1 = min(nvec, i0 + per);
+      uint32_t seg = 0;
+      for (int i = i0; i < i1; ++i) seg += cnt[i];
+      uint32_t total;
+      uint32_t run = block_exclusive_scan<uint32_t>(seg, sm.wu, c.lane, c.warp, &total);
+      for (int i = i0; i < i1; ++i) {
+        const uint32_t t = cnt[i];
+        cnt[i] = run;
+        run += t;
+      }
+      group_sync();
+      if (total <= static_cast<uint32_t>(kListCap)) {
+        auto place = [&](int v, const uint32_t (&w4)[4], int e0) {
+          uint32_t pos = cnt[v];
+          for_vec<BF16>(w4, e0, [&](float x, int e) {
+            if (e < V && x >= theta) {
+              l_val[pos] = x;
+              l_idx[pos] = e;
+              ++pos;
+            }
+          });
+        };
+#pragma unroll
+        for (int r = 0; r < kKeep; ++r) {
+          const int v = tid + r * kThreads;
+          if (v < nvec) place(v, keepv[r], keep_e0[r]);
+        }
+        for (int v = tid + kKeep * kThreads; v < nvec; v += kThreads) {
+          uint32_t w4[4];
+          const int e0 = decode(v, w4);
+          place(v, w4, e0);
+        }
+        group_sync();
+        leader_finish_list(P, sm, c, l_val, l_idx, static_cast<int>(total), row, rp.k, rp.use_p,
+                           rp.p, m, rp.c2, rp.u, rp.st, q_row);
+        return;
       }
     }
-    group_sync();
-    leader_finish_list(P, sm, c, l_val, l_idx, kListRegion, row, rp.k, rp.use_p, rp.p, m, rp.c2,
-                       rp.u, rp.st, q_row);
-    return;
+    // Pathological ties or -inf rows: more candidates than the list holds.
   }
   if (rp.kind == kKindP) {
-    for (int i = tid; i < C * kWarps; i += kThreads) {
-      sm.gwm[i / kWarps][i % kWarps] = slots[i / kWarps].wm[i % kWarps];
-      sm.gwz[i / kWarps][i % kWarps] = slots[i / kWarps].wz[i % kWarps];
-    }
-    group_sync();
     leader_finish_plain<BF16, NV, VEC>(P, sm, c, row, rp.u, m, rp.c2, rp.st, q_row);
     return;
   }
   if constexpr (BF16) {
     if (rp.kind == kKindH) {
       for (int r = 0; r < C; ++r) {
-        hist[r * kHistWords + tid] = slots[r].payload[tid];
-        hist[r * kHistWords + tid + kThreads] = slots[r].payload[tid + kThreads];
+        const uint32_t* h = slots[r].hist;
+        hist[r * kHistWords + tid] = h[tid];
+        hist[r * kHistWords + tid + kThreads] = h[tid + kThreads];
       }
       float zrow = 0.0f;
       if (rp.k == V) {
         for (int r = 0; r < C; ++r) {
-          const Summary& s = sm.gather[r];
-          if (s.f0 > -INFINITY) zrow += s.f1 * ex2((s.f0 - m) * rp.c2);
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            const float mw = sm.gwm[r][w];
+            if (mw > -INFINITY) zrow += sm.gwz[r][w] * ex2((mw - m) * rp.c2);
+          }
         }
       }
       group_sync();

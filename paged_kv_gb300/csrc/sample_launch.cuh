@@ -33,7 +33,7 @@ cudaError_t launch_pair(const SampleParams& P, int num_sms, cudaStream_t stream)
   const int ctas = std::min(num_sms, (items + kGroups - 1) / kGroups);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
-  cfg.blockDim = dim3(kThreads * kGroups, 1, 1);
+  cfg.blockDim = dim3(kStreamThreads, 1, 1);
   cfg.dynamicSmemBytes = kStreamDyn;
   cfg.stream = stream;
   cudaError_t e = cudaLaunchKernelEx(&cfg, skern, P);

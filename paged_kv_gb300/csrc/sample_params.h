@@ -7,8 +7,8 @@
 namespace pkv {
 
 // Bytes of one workspace record (ChunkSlot in sample_common.cuh): a 16-byte
-// summary, 2 x 8 per-warp floats and a 2 KB payload.
-constexpr size_t kChunkSlotBytes = 16 + 64 + 2048;
+// summary, 2 floats per warp, a float per thread and a 2 KB histogram.
+constexpr size_t kChunkSlotBytes = 16 + 64 + 256 * 4 + 2048;
 
 struct SampleParams {
   const void* logits;        // [B, row_stride] fp32 or bf16

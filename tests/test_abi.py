@@ -33,10 +33,10 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_workspace():
     lib = pkv.load()
     assert pkv.version() == 200
-    # One 2128-byte record per (row, chunk); the mixed batch's rows are 8
+    # One 3152-byte record per (row, chunk); the mixed batch's rows are 8
     # chunks of 20480 bf16 logits.
-    assert lib.pkv_sample_workspace_bytes(256, 151936, 1) == 256 * 8 * 2128
-    assert lib.pkv_sample_workspace_bytes(1024, 256000, 1) == 1024 * 16 * 2128
+    assert lib.pkv_sample_workspace_bytes(256, 151936, 1) == 256 * 8 * 3152
+    assert lib.pkv_sample_workspace_bytes(1024, 256000, 1) == 1024 * 16 * 3152
     assert lib.pkv_sample_workspace_bytes(0, 100, 1) == 0
     assert lib.pkv_sample_workspace_bytes(4, 0, 1) == 0
     assert lib.pkv_sample_workspace_bytes(4, 100, 7) == 0
