@@ -16,7 +16,7 @@ namespace pkv {
 // when a cut lies below the merged window; the caller then runs the exact
 // fallback.
 template <int NV, bool VEC>
-__device__ __noinline__ bool leader_finish_hist(const SampleParams& P, SampleSmem& sm,
+__device__ __forceinline__ bool leader_finish_hist(const SampleParams& P, SampleSmem& sm,
                                                   const Ctx& c, const uint32_t* hist, uint4* stage,
                                                   unsigned long long* table, int row,
                                                 int k, bool use_p, float p, float u, float m,
@@ -416,10 +416,48 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant_
     const int nT = C * kThreads;
     for (int i = tid; i < nT; i += kThreads) tm[i] = slots[i / kThreads].tmax[i % kThreads];
     group_sync();
-    unsigned long long rk;
-    const float theta = list_select<false>(tm, nT, [](int) { return true; },
-                                           [](int) { return 1ull; },
-                                           static_cast<unsigned long long>(rp.k), sm, c, &rk);
+    // theta: count the thread maxima per 16-bit key below the row maximum
+    // (bucket i = key(m) - key; keys beyond 255 share the last bucket) and
+    // take the key where the count from the top reaches k.  For bf16 rows
+    // this is the exact k-th largest thread maximum when it lies within 256
+    // values of the maximum; otherwise (and for fp32 rows) a lower bound on
+    // it, which is still valid: at least k thread maxima are >= theta.
+    const uint32_t km = key16(m);
+    sm.hlo[tid] = 0u;
+    group_sync();
+    for (int i = tid; i < nT; i += kThreads) {
+      const float t = tm[i];
+      if (t == t) {
+        const uint32_t kt = key16(t);
+        atomicAdd(&sm.hlo[kt >= km ? 0u : min(km - kt, 255u)], 1u);
+      }
+    }
+    group_sync();
+    {
+      // Inclusive prefix from the top: bucket tid counts keys km - tid.
+      const uint32_t h = sm.hlo[tid];
+      uint32_t tot;
+      const uint32_t before = block_exclusive_scan<uint32_t>(h, sm.wu, c.lane, c.warp, &tot);
+      if (before < static_cast<uint32_t>(rp.k) && before + h >= static_cast<uint32_t>(rp.k)) {
+        sm.bi[1] = tid;
+      }
+      if (tid == 0 && tot < static_cast<uint32_t>(rp.k)) sm.bi[1] = -1;
+    }
+    group_sync();
+    const int bk = sm.bi[1];
+    group_sync();
+    // Bucket bk < 255 holds only 16-bit key km - bk: the smallest value with
+    // that key (low 16 bits of the 32-bit key cleared) is the exact k-th
+    // largest for bf16 and a lower bound for fp32.  Past the last bucket the
+    // exact select runs on all thread maxima.
+    float theta = -INFINITY;
+    if (bk >= 0 && bk < 255) {
+      theta = key16_float(km - static_cast<uint32_t>(bk));
+    } else if (bk == 255) {
+      unsigned long long rk;
+      theta = list_select<false>(tm, nT, [](int) { return true; }, [](int) { return 1ull; },
+                                 static_cast<unsigned long long>(rp.k), sm, c, &rk);
+    }
     // Candidate lanes of each (chunk, warp) pair q = chunk * kWarps + warp;
     // vector (q, j, lane) of a candidate lane has rank
     //   vbase[q] + j * popc(M_q) + popc(M_q below lane)
@@ -447,16 +485,20 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant_
       constexpr int kKeep = 4;
       uint32_t keepv[kKeep][4];
       auto decode = [&](int v, uint32_t (&w4)[4]) -> int {
-        int q = 0;
-        while (q + 1 < C * kWarps && vbase[q + 1] <= static_cast<uint32_t>(v)) ++q;
+        // The pair q with vbase[q] <= v < vbase[q + 1] (binary search), then
+        // the vector j and the candidate lane within it.
+        int lo = 0, hi = C * kWarps - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (vbase[mid] <= static_cast<uint32_t>(v)) lo = mid;
+          else hi = mid - 1;
+        }
+        const int q = lo;
         const uint32_t mq = Mq[q];
         const int pc = __popc(mq);
         const int off = v - static_cast<int>(vbase[q]);
         const int j = off / pc;
-        int nth = off % pc;
-        uint32_t bits = mq;
-        while (nth-- > 0) bits &= bits - 1u;
-        const int lane_q = __ffs(bits) - 1;
+        const int lane_q = static_cast<int>(__fns(mq, 0u, off % pc + 1));
         const int e0 = vec_base<BF16, NV>(q / kWarps, q % kWarps, lane_q, j);
         load_vec<BF16, NV, VEC>(P, row, e0, w4);
         return e0;
