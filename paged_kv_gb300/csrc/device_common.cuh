@@ -223,6 +223,19 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float(u);
 }
 
+// ----------------------------------------------------------------- cp.async
+
+// 16-byte asynchronous copy global -> shared (L2 only, no L1 allocation).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_addr(dst)), "l"(src)
+               : "memory");
+}
+
+// Waits until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- warp
 
 template <typename T>
@@ -230,6 +243,17 @@ __device__ __forceinline__ T warp_sum(T v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
+}
+
+// Warp sum of 64-bit unsigned values in three 32-bit reductions (fields of
+// 24, 24 and 16 bits, whose lane sums cannot overflow).  Exact whenever the
+// total fits in 64 bits.
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+  const uint32_t lo = __reduce_add_sync(kFull, static_cast<uint32_t>(v & 0xffffffull));
+  const uint32_t mid = __reduce_add_sync(kFull, static_cast<uint32_t>((v >> 24) & 0xffffffull));
+  const uint32_t hi = __reduce_add_sync(kFull, static_cast<uint32_t>(v >> 48));
+  return (static_cast<unsigned long long>(hi) << 48) + (static_cast<unsigned long long>(mid) << 24) +
+         lo;
 }
 
 // Inclusive prefix over lanes: lane l gets v_0 + ... + v_l.

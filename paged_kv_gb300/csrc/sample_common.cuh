@@ -55,30 +55,24 @@ constexpr int kHistKeys = 1024;                // values counted below a chunk's
 constexpr int kHistWords = kHistKeys / 2;      // two 16-bit counts per word
 constexpr int kMaxK = 256;                     // largest k of a K row
 constexpr int kListCap = kMaxChunks * kMaxK;   // candidates the finisher keeps (K rows)
-constexpr int kListBytes = kListCap * 8;       // the finisher's list, or its C histograms
-static_assert(kMaxChunks * kHistWords * 4 == kListBytes, "list and histograms share the space");
+constexpr int kListBytes = kListCap * 8;       // the finisher's candidate list
 static_assert(kHistKeys == 4 * kThreads, "four merged histogram keys per finisher thread");
 static_assert(kHistWords == 2 * kThreads, "two histogram words per thread");
 
 
-// Dynamic shared memory of the finish kernel.  [0, kListBytes): the
-// candidate list (K rows) or the histograms (H rows), later overwritten (H)
-// by one staged chunk of kThreads * NV 16-byte vectors; K rows keep the
-// thread maxima at kFinOffTm and the per-vector counts at kFinOffCnt; H rows
-// keep the fixed-point mass per merged key at finish_table_offset.
+// Dynamic shared memory of the finish kernel (all offsets 16-byte aligned):
+// the row's thread maxima (K rows) and count histograms (H rows), copied from
+// the workspace records; then the candidate list and per-vector counts (K
+// rows).  H rows keep the fixed-point mass per merged key at kFinOffTable and,
+// once the histograms are consumed, stage one chunk from offset 0.
 constexpr int kMaxCandVecs = 4096;  // candidate vectors a K row's finisher handles
-constexpr int kFinOffTm = kListBytes;
-constexpr int kFinOffCnt = kFinOffTm + kMaxChunks * kThreads * 4;
-constexpr int kFinKEnd = kFinOffCnt + kMaxCandVecs * 4;
-template <int NV>
-constexpr int finish_table_offset() {
-  return kThreads * NV * 16 > kFinOffCnt ? kThreads * NV * 16 : kFinOffCnt;
-}
-template <int NV>
-constexpr int finish_dyn_bytes() {
-  return finish_table_offset<NV>() + kHistKeys * 8 > kFinKEnd ? finish_table_offset<NV>() + kHistKeys * 8
-                                                              : kFinKEnd;
-}
+constexpr int kFinOffTm = 0;
+constexpr int kFinOffHist = kFinOffTm + kMaxChunks * kThreads * 4;
+constexpr int kFinOffList = kFinOffHist + kMaxChunks * kHistWords * 4;
+constexpr int kFinOffCnt = kFinOffList + kListBytes;
+constexpr int kFinishDynBytes = kFinOffCnt + kMaxCandVecs * 4;
+constexpr int kFinOffTable = kFinishDynBytes - kHistKeys * 8;
+static_assert(kThreads * 16 * 16 <= kFinOffTable, "a staged chunk (NV <= 16) below the mass table");
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
 constexpr double kMassScaleD = 1099511627776.0;
 constexpr long long kWaitNs = 2000000000ll;     // bound of every wait on a bulk copy (2 s)
@@ -136,6 +130,13 @@ struct SampleSmem {
 
 static_assert(sizeof(Summary) == 16, "one 16-byte record");
 static_assert(sizeof(ChunkSlot) == kChunkSlotBytes, "workspace record size");
+// Byte offsets of the record's parts (the finisher copies them in 16-byte pieces).
+constexpr int kSlotOffWm = 16, kSlotOffWz = 48, kSlotOffTmax = 80, kSlotOffHist = 1104;
+constexpr int kSlotPieces = kChunkSlotBytes / 16;
+static_assert(offsetof(ChunkSlot, wm) == kSlotOffWm && offsetof(ChunkSlot, wz) == kSlotOffWz &&
+                  offsetof(ChunkSlot, tmax) == kSlotOffTmax &&
+                  offsetof(ChunkSlot, hist) == kSlotOffHist && kChunkSlotBytes % 16 == 0,
+              "record layout");
 
 // Barrier of the calling thread's group of kThreads threads (named barrier
 // 1 + group); a finish CTA is one group.
@@ -170,6 +171,19 @@ __device__ __forceinline__ void for_vec(const uint32_t (&w)[4], int e0, F&& f) {
   for (int q = 0; q < 4; ++q) {
 #pragma unroll
     for (int h = 0; h < L::EPW; ++h) f(elem<BF16>(w[q], h), e0 + q * L::EPW + h);
+  }
+}
+
+// for_vec as a loop that is not unrolled (one copy of f's code), for code
+// that runs once per row: there instruction fetch, not issue, sets the pace.
+template <bool BF16, typename F>
+__device__ __forceinline__ void for_vec_c(const uint4 v, int e0, F&& f) {
+  using L = Layout<BF16>;
+#pragma unroll 1
+  for (int t = 0; t < L::VW; ++t) {
+    const int q = t / L::EPW;
+    const uint32_t w = q < 2 ? (q == 0 ? v.x : v.y) : (q == 2 ? v.z : v.w);
+    f(elem<BF16>(w, t % L::EPW), e0 + t);
   }
 }
 
@@ -450,6 +464,35 @@ __device__ __forceinline__ void load_vec(const SampleParams& P, int row, int e0,
   }
 }
 
+// Stages this thread's NV vectors of chunk `chunk` of `row` in shared memory,
+// in the register layout of load_chunk: vector j of (warp, lane) at
+// sv[(warp * NV + j) * 32 + lane].  Vectors inside an aligned row move by
+// 16-byte asynchronous copies, the rest by element loads (-inf past V).  On
+// return the thread's own vectors are in place (no barrier: each thread
+// reads back only what it staged).  A loop, not unrolled: the finisher runs
+// it once per row, so its code size matters more than its issue rate.
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ void stage_own(const SampleParams& P, int row, int chunk, uint4* sv,
+                                          int warp, int lane) {
+  using L = Layout<BF16>;
+  const char* rp = static_cast<const char*>(P.logits) +
+                   static_cast<size_t>(row) * static_cast<size_t>(P.row_stride) * L::ELT;
+  const int V = P.V;
+#pragma unroll 1
+  for (int j = 0; j < NV; ++j) {
+    const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
+    uint4* dst = sv + (warp * NV + j) * 32 + lane;
+    if (VEC && e0 + L::VW <= V) {
+      cp_async16(dst, rp + static_cast<size_t>(e0) * L::ELT);
+    } else {
+      uint32_t w[4];
+      load_vec<BF16, NV, false>(P, row, e0, w);
+      *dst = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  cp_async_wait_all();
+}
+
 // f(x, e) for every element the thread owns in chunk `chunk`, index order
 // within the thread.
 template <bool BF16, int NV, bool VEC, typename F>
@@ -462,205 +505,6 @@ __device__ __forceinline__ void for_chunk(const SampleParams& P, int row, int ch
     load_vec<BF16, NV, VEC>(P, row, e0, w);
     for_vec<BF16>(w, e0, f);
   }
-}
-
-// The first element, in index order, of chunk `chunk` of `row` at which the
-// running sum of f(x, e) exceeds tau.  Returns its row index; when rounding
-// leaves tau at or above the running sum where it was expected to cross, the
-// last element with f > 0 before that point; -1 if the chunk has no element
-// with f > 0.  T is unsigned long long (exact: counts or fixed-point masses)
-// or float.  Index order is (warp, vector j, lane, element): the search
-// narrows warp -> vector -> lane -> element.
-template <bool BF16, int NV, bool VEC, typename T, typename F>
-__device__ __forceinline__ int chunk_search(const SampleParams& P, int row, int chunk, F&& f,
-                                            T tau, SampleSmem& sm, int tid, int lane, int warp) {
-  T tt = 0;
-  int last = -1;
-  for_chunk<BF16, NV, VEC>(P, row, chunk, warp, lane, [&](float x, int e) {
-    const T w = f(x, e);
-    tt += w;
-    if (w > T(0)) last = e;
-  });
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(kFull, tt, o);
-  const int wl = __reduce_max_sync(kFull, last);
-  if (lane == 0) {
-    if constexpr (sizeof(T) == 8) {
-      sm.wl[warp] = static_cast<unsigned long long>(tt);
-    } else {
-      sm.wf[warp] = static_cast<float>(tt);
-    }
-    sm.wi[warp] = wl;
-  }
-  group_sync();
-  int wstar = -1, lastpos = -1;
-  T tw = 0, acc = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    T ww;
-    if constexpr (sizeof(T) == 8) {
-      ww = static_cast<T>(sm.wl[w]);
-    } else {
-      ww = static_cast<T>(sm.wf[w]);
-    }
-    if (wstar < 0 && ww > T(0) && tau < acc + ww) {
-      wstar = w;
-      tw = tau - acc;
-    }
-    lastpos = max(lastpos, sm.wi[w]);
-    acc += ww;
-  }
-  if (warp == wstar) {
-    int found = -1;
-    T a = 0;
-#pragma unroll 1
-    for (int j = 0; j < NV && found < 0; ++j) {
-      const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
-      uint32_t v[4];
-      load_vec<BF16, NV, VEC>(P, row, e0, v);
-      T sj = 0;
-      for_vec<BF16>(v, e0, [&](float x, int e) { sj += f(x, e); });
-      const T incl = warp_inclusive_scan(sj, lane);
-      const T tot = __shfl_sync(kFull, incl, 31);
-      if (tw < a + tot) {
-        const unsigned bal = __ballot_sync(kFull, tw < a + incl);
-        const int lx = bal ? __ffs(bal) - 1 : 31;
-        int sel = -1, lpos = -1;
-        if (lane == lx) {
-          T run = a + incl - sj;
-          for_vec<BF16>(v, e0, [&](float x, int e) {
-            const T w = f(x, e);
-            run += w;
-            if (w > T(0)) {
-              lpos = e;
-              if (sel < 0 && tw < run) sel = e;
-            }
-          });
-          if (sel < 0) sel = lpos;
-        }
-        found = __shfl_sync(kFull, sel, lx);
-        if (found < 0) found = INT_MAX;  // nothing found where expected: rounding
-      }
-      a += tot;
-    }
-    if (lane == 0) sm.bi[6] = found;
-  }
-  group_sync();
-  int res = lastpos;
-  if (wstar >= 0) {
-    res = sm.bi[6];
-    if (res < 0 || res == INT_MAX) res = sm.wi[wstar];
-  }
-  group_sync();
-  return res;
-}
-
-// The leader's copy of one chunk in shared memory, same layout as the
-// registers: vector j of (warp, lane) at sv[(warp * NV + j) * 32 + lane].
-// All NV loads of a thread are issued together (one L2 round trip); each
-// thread reads back only its own vectors, so no barrier is needed.
-template <bool BF16, int NV, bool VEC>
-__device__ __forceinline__ void stage_chunk(const SampleParams& P, int row, int chunk, uint4* sv,
-                                            int warp, int lane) {
-  uint32_t d[NV][4];
-  load_chunk<BF16, NV, VEC>(P, row, chunk, warp, lane, d);
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    sv[(warp * NV + j) * 32 + lane] = make_uint4(d[j][0], d[j][1], d[j][2], d[j][3]);
-  }
-}
-
-template <bool BF16, int NV, typename F>
-__device__ __forceinline__ void for_staged(const uint4* sv, int chunk, int warp, int lane, F&& f) {
-#pragma unroll 2
-  for (int j = 0; j < NV; ++j) {
-    const uint4 v = sv[(warp * NV + j) * 32 + lane];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    for_vec<BF16>(w, vec_base<BF16, NV>(chunk, warp, lane, j), f);
-  }
-}
-
-// chunk_search over a staged chunk (same contract as chunk_search).
-template <bool BF16, int NV, typename T, typename F>
-__device__ __forceinline__ int staged_search(const uint4* sv, int chunk, F&& f, T tau,
-                                             SampleSmem& sm, int tid, int lane, int warp) {
-  T tt = 0;
-  int last = -1;
-  for_staged<BF16, NV>(sv, chunk, warp, lane, [&](float x, int e) {
-    const T w = f(x, e);
-    tt += w;
-    if (w > T(0)) last = e;
-  });
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tt += __shfl_xor_sync(kFull, tt, o);
-  const int wl = __reduce_max_sync(kFull, last);
-  if (lane == 0) {
-    if constexpr (sizeof(T) == 8) {
-      sm.wl[warp] = static_cast<unsigned long long>(tt);
-    } else {
-      sm.wf[warp] = static_cast<float>(tt);
-    }
-    sm.wi[warp] = wl;
-  }
-  group_sync();
-  int wstar = -1, lastpos = -1;
-  T tw = 0, acc = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    T ww;
-    if constexpr (sizeof(T) == 8) {
-      ww = static_cast<T>(sm.wl[w]);
-    } else {
-      ww = static_cast<T>(sm.wf[w]);
-    }
-    if (wstar < 0 && ww > T(0) && tau < acc + ww) {
-      wstar = w;
-      tw = tau - acc;
-    }
-    lastpos = max(lastpos, sm.wi[w]);
-    acc += ww;
-  }
-  if (warp == wstar) {
-    int found = -1;
-    T a = 0;
-#pragma unroll 1
-    for (int j = 0; j < NV && found < 0; ++j) {
-      const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
-      const uint4 v4 = sv[(warp * NV + j) * 32 + lane];
-      const uint32_t v[4] = {v4.x, v4.y, v4.z, v4.w};
-      T sj = 0;
-      for_vec<BF16>(v, e0, [&](float x, int e) { sj += f(x, e); });
-      const T incl = warp_inclusive_scan(sj, lane);
-      const T tot = __shfl_sync(kFull, incl, 31);
-      if (tw < a + tot) {
-        const unsigned bal = __ballot_sync(kFull, tw < a + incl);
-        const int lx = bal ? __ffs(bal) - 1 : 31;
-        int sel = -1, lpos = -1;
-        if (lane == lx) {
-          T run = a + incl - sj;
-          for_vec<BF16>(v, e0, [&](float x, int e) {
-            const T w = f(x, e);
-            run += w;
-            if (w > T(0)) {
-              lpos = e;
-              if (sel < 0 && tw < run) sel = e;
-            }
-          });
-          if (sel < 0) sel = lpos;
-        }
-        found = __shfl_sync(kFull, sel, lx);
-        if (found < 0) found = INT_MAX;  // nothing found where expected: rounding
-      }
-      a += tot;
-    }
-    if (lane == 0) sm.bi[6] = found;
-  }
-  group_sync();
-  int res = lastpos;
-  if (wstar >= 0) {
-    res = sm.bi[6];
-    if (res < 0 || res == INT_MAX) res = sm.wi[wstar];
-  }
-  group_sync();
-  return res;
 }
 
 // ----------------------------------------------------------------- list selects

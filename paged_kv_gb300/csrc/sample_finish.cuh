@@ -9,40 +9,48 @@ namespace pkv {
 
 // ----------------------------------------------------------------- histogram finish (H)
 
-// The leader merges the C count histograms (CTA r counted its elements per
-// 16-bit key over the kHistKeys keys below a_r = gather[r].i0, the key of its
-// maximum), settles top-k and top-p exactly, picks the chunk holding the draw,
-// re-reads it and finds the token.  Returns false, having emitted nothing,
-// when a cut lies below the merged window; the caller then runs the exact
-// fallback.
+// Chunk r counted its elements per 16-bit key over the kHistKeys keys below
+// a_r = gather[r].i0, the key of its maximum: h16[r * kHistKeys + d] is the
+// count of key a_r - d.  Merged key i (0 = the row maximum, key A - i) has
+// count sum_r h_r[i - (A - a_r)]; every element within kHistKeys keys of the
+// row maximum is counted in its chunk (a_r <= A).
+//
+// The finisher settles top-k (by count) and top-p (by fixed-point mass)
+// exactly on the merged keys: keys i < is are wholly in the kept set S, the
+// first rs members (in index order) of key is are in it too.  It then picks
+// the chunk holding the draw from per-chunk masses of S, re-reads that chunk
+// into registers and finds the token with one pass of per-vector sums.
+// Returns false, having emitted nothing, when a cut lies below the merged
+// window; the caller then runs the exact fallback.
 template <int NV, bool VEC>
-__device__ __forceinline__ bool leader_finish_hist(const SampleParams& P, SampleSmem& sm,
-                                                  const Ctx& c, const uint32_t* hist, uint4* stage,
-                                                  unsigned long long* table, int row,
-                                                int k, bool use_p, float p, float u, float m,
-                                                float zrow, float c2, int st, float* q_row) {
+__device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& sm, const Ctx& c,
+                                            const uint32_t* hist, unsigned long long* table,
+                                            uint4* stage, int row, const RowParams& rp, float m,
+                                            float zrow, float* q_row) {
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   const int C = static_cast<int>(c.csize);
   const int V = P.V;
+  const int k = rp.k;
   const bool topk = k < V;
+  const uint16_t* h16 = reinterpret_cast<const uint16_t*>(hist);
   const uint32_t A = key16(m);
-  // Count of CTA r at merged key i (key A - i); 0 above the CTA's maximum.
-  auto count_at = [&](int r, uint32_t i) -> uint32_t {
+
+  // ---- merged counts and fixed-point weights; thread t holds keys 4t .. 4t + 3.
+  uint32_t cnt[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 1
+  for (int r = 0; r < C; ++r) {
     const uint32_t delta = A - static_cast<uint32_t>(sm.gather[r].i0);
-    if (i > A || i < delta) return 0u;
-    const uint32_t idx = i - delta;
-    return (hist[r * kHistWords + (idx >> 1)] >> ((idx & 1u) * 16u)) & 0xffffu;
-  };
-  // Merged key i (0 = the row maximum); thread t holds keys 4t .. 4t + 3.
-  uint32_t cnt[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t i = static_cast<uint32_t>(4 * tid + jj);
+      if (i >= delta) cnt[jj] += h16[r * kHistKeys + (i - delta)];
+    }
+  }
   unsigned long long wfx[4];
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const uint32_t i = static_cast<uint32_t>(4 * tid + jj);
-    uint32_t n = 0;
-    for (int r = 0; r < C; ++r) n += count_at(r, i);
-    cnt[jj] = n;
-    wfx[jj] = n ? mass_fx(weight(key16_float(A - i), m, c2)) : 0ull;
+    wfx[jj] = cnt[jj] ? mass_fx(weight(key16_float(A - i), m, rp.c2)) : 0ull;
     table[i] = wfx[jj];
   }
   // ---- top-k by count: keys i < ik are wholly in K, key ik keeps rk members.
@@ -52,7 +60,7 @@ __device__ __forceinline__ bool leader_finish_hist(const SampleParams& P, Sample
     const uint32_t local = cnt[0] + cnt[1] + cnt[2] + cnt[3];
     uint32_t total;
     const uint32_t before = block_exclusive_scan<uint32_t>(local, sm.wu, lane, warp, &total);
-    if (total < static_cast<uint32_t>(k)) return false;  // k-th value below the window
+    if (total < static_cast<uint32_t>(k)) return false;  // the k-th value lies below the window
     int cand = INT_MAX;
     uint32_t run = before;
 #pragma unroll
@@ -65,145 +73,252 @@ __device__ __forceinline__ bool leader_finish_hist(const SampleParams& P, Sample
     }
     ik = block_min_int(cand, sm.wi, lane, warp);
     rk = sm.bl[0];
-    group_sync();
-  }
-  unsigned long long mk[4];  // mass of K at each key
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int i = 4 * tid + jj;
-    mk[jj] = i < ik ? cnt[jj] * wfx[jj] : (i == ik ? rk * wfx[jj] : 0ull);
   }
   // ---- top-p inside K by mass: keys i < is wholly in S, key is keeps rs.
   int is = ik;
   unsigned long long rs = rk;
-  if (use_p) {
+  if (rp.use_p) {
+    unsigned long long mk[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int i = 4 * tid + jj;
+      mk[jj] = i < ik ? cnt[jj] * wfx[jj] : (i == ik ? rk * wfx[jj] : 0ull);
+    }
     const unsigned long long local = mk[0] + mk[1] + mk[2] + mk[3];
     unsigned long long zk;
     const unsigned long long before =
         block_exclusive_scan<unsigned long long>(local, sm.wl, lane, warp, &zk);
     unsigned long long target;
     if (topk) {
-      target =
-          static_cast<unsigned long long>(ceil(static_cast<double>(zk) * static_cast<double>(p)));
+      target = static_cast<unsigned long long>(
+          ceil(static_cast<double>(zk) * static_cast<double>(rp.p)));
       if (target > zk) target = zk;
     } else {
       target = static_cast<unsigned long long>(
-          ceil(static_cast<double>(zrow) * kMassScaleD * static_cast<double>(p)));
+          ceil(static_cast<double>(zrow) * kMassScaleD * static_cast<double>(rp.p)));
       if (zk < target) return false;  // the top-p cut lies below the window
     }
     if (target < 1) target = 1;
     int cand = INT_MAX;
-    unsigned long long run = before;
+    unsigned long long run = before, rem = 0, wc = 0;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       if (run < target && run + mk[jj] >= target) {
         cand = 4 * tid + jj;
-        // Members j of the cut key are kept iff run + j * w < target.
-        const unsigned long long rem = target - run;
-        unsigned long long rp = wfx[jj] == 0 ? ~0ull : (rem + wfx[jj] - 1) / wfx[jj];
-        if (cand == ik && rp > rk) rp = rk;
-        sm.bl[1] = rp;  // one owner
+        rem = target - run;
+        wc = wfx[jj];
       }
       run += mk[jj];
     }
+    if (cand != INT_MAX) {
+      // Members j of the cut key are kept iff run + j * w < target (one owner).
+      unsigned long long need = wc == 0 ? ~0ull : (rem + wc - 1) / wc;
+      if (cand == ik && need > rk) need = rk;
+      sm.bl[1] = need;
+    }
     is = block_min_int(cand, sm.wi, lane, warp);
     rs = sm.bl[1];
-    group_sync();
   }
   if (is >= kHistKeys) return false;  // unreachable when the masses add up
-  // ---- per-chunk masses of S: keys above the cut wholly (warp w sums chunks
-  // w, w + 8), then the cut key's members in chunk order (chunks are in index
-  // order).
+  const unsigned long long wcut = table[is];
+  // ---- per-chunk mass of S above the cut key and the cut key's members.
   for (int r = warp; r < C; r += kWarps) {
+    const uint32_t delta = A - static_cast<uint32_t>(sm.gather[r].i0);
     unsigned long long part = 0;
     for (int i = lane; i < is; i += 32) {
-      part += count_at(r, static_cast<uint32_t>(i)) * table[i];
+      if (static_cast<uint32_t>(i) >= delta) part += h16[r * kHistKeys + (i - delta)] * table[i];
     }
-    part = warp_sum(part);
-    if (lane == 0) sm.cmass[r][0] = part;
+    part = warp_sum_u64(part);
+    if (lane == 0) {
+      sm.cmass[r][0] = part;
+      sm.ties[r] = static_cast<uint32_t>(is) >= delta ? h16[r * kHistKeys + (is - delta)] : 0u;
+    }
   }
   group_sync();
-  if (tid == 0) {
-    const unsigned long long wcut = table[is];
-    unsigned long long zs = 0, ties_before = 0;
-    for (int r = 0; r < C; ++r) {
-      unsigned long long mr = sm.cmass[r][0];
-      const uint32_t ties = count_at(r, static_cast<uint32_t>(is));
-      unsigned long long kept = 0;
-      if (ties_before < rs) kept = min(static_cast<unsigned long long>(ties), rs - ties_before);
-      ties_before += ties;
-      sm.cnt[r] = static_cast<uint32_t>(kept);
-      sm.ties[r] = ties;
-      mr += kept * wcut;
-      sm.cmass[r][0] = mr;
-      zs += mr;
+  // ---- the chunk holding the draw (warp 0, lane r = chunk r; C <= 32):
+  // chunk r keeps the first kept_r = clamp(rs - ties before r, 0, ties_r)
+  // members of the cut key, since they follow one another in index order.
+  if (warp == 0) {
+    const bool v = lane < C;
+    const uint32_t ties = v ? sm.ties[lane] : 0u;
+    const uint32_t tb = warp_inclusive_scan(ties, lane) - ties;
+    const unsigned long long kept =
+        v ? min(static_cast<unsigned long long>(ties), rs > tb ? rs - tb : 0ull) : 0ull;
+    const unsigned long long mr = v ? sm.cmass[lane][0] + kept * wcut : 0ull;
+    const unsigned long long incl = warp_inclusive_scan(mr, lane);
+    const unsigned long long zs = __shfl_sync(kFull, incl, 31);
+    unsigned long long tdraw =
+        static_cast<unsigned long long>(static_cast<double>(rp.u) * static_cast<double>(zs));
+    if (tdraw >= zs) tdraw = zs - 1;  // zs >= the row maximum's own weight > 0
+    const unsigned bal = __ballot_sync(kFull, v && tdraw < incl);
+    const int cstar = bal ? __ffs(bal) - 1 : C - 1;
+    if (v) sm.cnt[lane] = static_cast<uint32_t>(kept);
+    if (lane == cstar) {
+      sm.bi[0] = cstar;
+      sm.bl[3] = tdraw - (incl - mr);
+      sm.bl[5] = zs;
     }
-    const unsigned long long tdraw =
-        static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(zs));
-    unsigned long long cum = 0, tau = 0;
-    int cstar = -1, clast = -1;
-    for (int r = 0; r < C; ++r) {
-      const unsigned long long mr = sm.cmass[r][0];
-      if (cstar < 0 && mr > 0 && tdraw < cum + mr) {
-        cstar = r;
-        tau = tdraw - cum;
-      }
-      if (mr > 0) clast = r;
-      cum += mr;
-    }
-    if (cstar < 0) {
-      cstar = clast;
-      tau = ~0ull;  // the chunk's last token with mass
-    }
-    sm.bi[0] = cstar;
-    sm.bl[3] = tau;
-    sm.bl[5] = zs;
   }
   group_sync();
   const int cstar = sm.bi[0];
   const unsigned long long tau = sm.bl[3];
   const unsigned long long zs = sm.bl[5];
-  const uint32_t ks = A - static_cast<uint32_t>(is);  // the cut key
-  group_sync();
-  // The histograms are consumed: the staging area may overwrite them.
-  // Members of the cut key kept in chunk r (staged): all, none, or those
-  // with index below the returned cut (the first sm.cnt[r]).
-  auto chunk_cut = [&](int r) -> int {
-    const uint32_t kept = sm.cnt[r];
-    if (kept >= sm.ties[r]) return INT_MAX;
-    if (kept == 0) return INT_MIN;
-    return staged_search<true, NV, unsigned long long>(
-               stage, r,
-               [&](float x, int e) { return (e < V && key16(x) == ks) ? 1ull : 0ull; },
-               static_cast<unsigned long long>(kept) - 1ull, sm, tid, lane, warp) + 1;
+  const uint32_t kept_c = sm.cnt[cstar];
+  // In a chunk, the mass of S before a position is the mass above the cut
+  // key plus wcut * min(cut-key members so far, kept): the first kept
+  // members count, later ones do not.  The histograms are consumed: the
+  // chunk is staged over them.
+  auto above_and_ties = [&](const uint4 v4, int e0, unsigned long long* a, uint32_t* t) {
+    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+    unsigned long long s = 0;
+    uint32_t n = 0;
+    for_vec<true>(w4, e0, [&](float x, int e) {
+      if (e < V) {
+        const uint32_t i = A - key16(x);
+        if (i < static_cast<uint32_t>(is)) s += table[i];
+        n += i == static_cast<uint32_t>(is) ? 1u : 0u;
+      }
+    });
+    *a = s;
+    *t = n;
   };
-  int tok = -1;
-  if (cstar >= 0) {
-    stage_chunk<true, NV, VEC>(P, row, cstar, stage, warp, lane);
-    const int ecut = chunk_cut(cstar);
-    tok = staged_search<true, NV, unsigned long long>(
-        stage, cstar,
-        [&](float x, int e) {
-          const uint32_t i = A - key16(x);  // merged key index; >= is for keys below the cut
-          const bool in = e < V && (static_cast<int>(i) < is || (static_cast<int>(i) == is && e < ecut));
-          return in ? table[i] : 0ull;
-        },
-        tau, sm, tid, lane, warp);
+  stage_own<true, NV, VEC>(P, row, cstar, stage, warp, lane);
+  // Per (warp, vector) sums; entry q = warp * NV + j is in index order.
+#pragma unroll 1
+  for (int j = 0; j < NV; ++j) {
+    unsigned long long a;
+    uint32_t t;
+    above_and_ties(stage[(warp * NV + j) * 32 + lane], vec_base<true, NV>(cstar, warp, lane, j),
+                   &a, &t);
+    a = warp_sum_u64(a);
+    t = __reduce_add_sync(kFull, t);
+    if (lane == 0) {
+      sm.scan[warp * NV + j] = a;
+      sm.hlo[warp * NV + j] = t;
+    }
   }
-  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
+  group_sync();
+  if (warp == 0) {
+    constexpr int nq = kWarps * NV;
+    unsigned long long carry_a = 0;
+    uint32_t carry_t = 0;
+    int qstar = -1;
+    unsigned long long a_before = 0;
+    uint32_t t_before = 0;
+#pragma unroll 1
+    for (int base = 0; base < nq; base += 32) {
+      const int q = base + lane;
+      const unsigned long long a = q < nq ? sm.scan[q] : 0ull;
+      const uint32_t t = q < nq ? sm.hlo[q] : 0u;
+      const unsigned long long ai = warp_inclusive_scan(a, lane) + carry_a;
+      const uint32_t ti = warp_inclusive_scan(t, lane) + carry_t;
+      const unsigned long long pi = ai + wcut * min(static_cast<unsigned long long>(ti),
+                                                    static_cast<unsigned long long>(kept_c));
+      const unsigned bal = __ballot_sync(kFull, q < nq && tau < pi);
+      if (qstar < 0 && bal) {
+        const int ls = __ffs(bal) - 1;
+        qstar = base + ls;
+        a_before = __shfl_sync(kFull, ai - a, ls);
+        t_before = __shfl_sync(kFull, ti - t, ls);
+      }
+      carry_a = __shfl_sync(kFull, ai, 31);
+      carry_t = __shfl_sync(kFull, ti, 31);
+    }
+    if (lane == 0) {
+      sm.bi[2] = qstar;
+      sm.bl[6] = a_before;
+      sm.bi[3] = static_cast<int32_t>(t_before);
+    }
+  }
+  group_sync();
+  const int qstar = sm.bi[2];
+  if (qstar >= 0 && warp == qstar / NV) {
+    const int jstar = qstar % NV;
+    const uint4 v4 = stage[(warp * NV + jstar) * 32 + lane];
+    const int e0 = vec_base<true, NV>(cstar, warp, lane, jstar);
+    unsigned long long a;
+    uint32_t t;
+    above_and_ties(v4, e0, &a, &t);
+    const unsigned long long ai = warp_inclusive_scan(a, lane) + sm.bl[6];
+    const uint32_t ti = warp_inclusive_scan(t, lane) + static_cast<uint32_t>(sm.bi[3]);
+    const unsigned long long pi =
+        ai + wcut * min(static_cast<unsigned long long>(ti), static_cast<unsigned long long>(kept_c));
+    const unsigned bal = __ballot_sync(kFull, tau < pi);
+    const int ls = bal ? __ffs(bal) - 1 : 31;
+    int sel = -1;
+    if (lane == ls) {
+      // Walk the lane's elements with the mass of S before each.
+      unsigned long long above = ai - a;
+      uint32_t tc = ti - t;
+      int last = -1;
+      for_vec_c<true>(v4, e0, [&](float x, int e) {
+        if (e < V) {
+          const uint32_t i = A - key16(x);
+          const unsigned long long pb =
+              above + wcut * min(static_cast<unsigned long long>(tc),
+                                 static_cast<unsigned long long>(kept_c));
+          unsigned long long w = 0;
+          if (i < static_cast<uint32_t>(is)) {
+            w = table[i];
+            above += w;
+          } else if (i == static_cast<uint32_t>(is)) {
+            w = tc < kept_c ? wcut : 0ull;
+            ++tc;
+          }
+          if (w > 0) {
+            last = e;
+            if (sel < 0 && tau < pb + w) sel = e;
+          }
+        }
+      });
+      if (sel < 0) sel = last;
+    }
+    const int tok = __shfl_sync(kFull, sel, ls);
+    if (lane == 0) emit_token(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st);
+  }
+  if (qstar < 0 && tid == 0) emit_token(P, row, -1, rp.st | kStNonFinite);
   if (q_row != nullptr) {
+    // Debug output: q over every chunk; a cut-key member is kept when its
+    // rank among the chunk's members is below kept_r.
     const float inv = 1.0f / (static_cast<float>(zs) / kMassScale);
     for (int r = 0; r < C; ++r) {
       group_sync();
-      stage_chunk<true, NV, VEC>(P, row, r, stage, warp, lane);
-      const int ecut = chunk_cut(r);
-      for_staged<true, NV>(stage, r, warp, lane, [&](float x, int e) {
-        if (e < V) {
-          const uint32_t kx = key16(x);
-          const bool in = kx > ks || (kx == ks && e < ecut);
-          q_row[e] = in ? weight(x, m, c2) * inv : 0.0f;
+      stage_own<true, NV, VEC>(P, row, r, stage, warp, lane);
+      for (int j = 0; j < NV; ++j) {
+        unsigned long long a;
+        uint32_t t;
+        above_and_ties(stage[(warp * NV + j) * 32 + lane], vec_base<true, NV>(r, warp, lane, j),
+                       &a, &t);
+        t = __reduce_add_sync(kFull, t);
+        if (lane == 0) sm.hlo[warp * NV + j] = t;
+      }
+      group_sync();
+      if (tid == 0) {
+        uint32_t acc = 0;
+        for (int q = 0; q < kWarps * NV; ++q) {
+          const uint32_t t = sm.hlo[q];
+          sm.hlo[q] = acc;
+          acc += t;
         }
-      });
+      }
+      group_sync();
+      const uint32_t kept_r = sm.cnt[r];
+      for (int j = 0; j < NV; ++j) {
+        const int e0 = vec_base<true, NV>(r, warp, lane, j);
+        const uint4 v4 = stage[(warp * NV + j) * 32 + lane];
+        unsigned long long a;
+        uint32_t t;
+        above_and_ties(v4, e0, &a, &t);
+        uint32_t rank = sm.hlo[warp * NV + j] + warp_inclusive_scan(t, lane) - t;
+        for_vec_c<true>(v4, e0, [&](float x, int e) {
+          if (e < V) {
+            const uint32_t i = A - key16(x);
+            bool in = i < static_cast<uint32_t>(is);
+            if (i == static_cast<uint32_t>(is)) in = rank++ < kept_r;
+            q_row[e] = in ? weight(x, m, rp.c2) * inv : 0.0f;
+          }
+        });
+      }
     }
   }
   return true;
@@ -322,16 +437,16 @@ __device__ __forceinline__ void leader_finish_plain(const SampleParams& P, Sampl
 // of the stream kernel: griddepcontrol.wait returns once that grid has
 // completed and its writes are visible.
 template <bool BF16, int NV, bool VEC>
-__global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant__ SampleParams P) {
+__global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_constant__ SampleParams P) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ SampleSmem sm;
   extern __shared__ __align__(128) unsigned char dyn[];
-  float* l_val = reinterpret_cast<float*>(dyn);
-  int32_t* l_idx = reinterpret_cast<int32_t*>(dyn + kListCap * 4);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(dyn);
-  uint4* stage = reinterpret_cast<uint4*>(dyn);
-  unsigned long long* table =
-      reinterpret_cast<unsigned long long*>(dyn + finish_table_offset<NV>());
+  float* tm = reinterpret_cast<float*>(dyn + kFinOffTm);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(dyn + kFinOffHist);
+  float* l_val = reinterpret_cast<float*>(dyn + kFinOffList);
+  int32_t* l_idx = reinterpret_cast<int32_t*>(dyn + kFinOffList + kListCap * 4);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(dyn + kFinOffCnt);
+  unsigned long long* table = reinterpret_cast<unsigned long long*>(dyn + kFinOffTable);
 
   const int row = blockIdx.x;
   const int C = P.chunks;
@@ -344,14 +459,32 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant_
   c.csize = static_cast<uint32_t>(C);
   const int tid = c.tid;
   const ChunkSlot* slots = static_cast<const ChunkSlot*>(P.workspace) + static_cast<size_t>(row) * C;
+  // The row's records in one batch of 16-byte asynchronous copies:
+  // summaries and per-warp values into sm, thread maxima into tm, count
+  // histograms into hist.  The row parameters load meanwhile.
+  {
+    const char* src = reinterpret_cast<const char*>(slots);
+    for (int pc = tid; pc < C * kSlotPieces; pc += kThreads) {
+      const int r = pc / kSlotPieces;
+      const int off = (pc - r * kSlotPieces) * 16;
+      char* dst;
+      if (off < kSlotOffWm) {
+        dst = reinterpret_cast<char*>(&sm.gather[r]);
+      } else if (off < kSlotOffWz) {
+        dst = reinterpret_cast<char*>(&sm.gwm[r][0]) + (off - kSlotOffWm);
+      } else if (off < kSlotOffTmax) {
+        dst = reinterpret_cast<char*>(&sm.gwz[r][0]) + (off - kSlotOffWz);
+      } else if (off < kSlotOffHist) {
+        dst = reinterpret_cast<char*>(tm + r * kThreads) + (off - kSlotOffTmax);
+      } else {
+        dst = reinterpret_cast<char*>(hist + r * kHistWords) + (off - kSlotOffHist);
+      }
+      cp_async16(dst, src + static_cast<size_t>(pc) * 16);
+    }
+  }
   const RowParams rp = row_params<BF16, NV>(P, row, C);
   float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
-  // Per-warp maxima of every chunk (NaN-propagating), summaries, flags.
-  for (int i = tid; i < C * kWarps; i += kThreads) {
-    sm.gwm[i / kWarps][i % kWarps] = slots[i / kWarps].wm[i % kWarps];
-    sm.gwz[i / kWarps][i % kWarps] = slots[i / kWarps].wz[i % kWarps];
-  }
-  if (tid < C) sm.gather[tid] = slots[tid].s;
+  cp_async_wait_all();
   group_sync();
   uint32_t flags = 0;
   float m = -INFINITY;
@@ -410,12 +543,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant_
     // theta and lies in a thread whose maximum is >= theta.  Those threads'
     // vectors are re-read (an L2 hit); their elements >= theta form the
     // candidate list, in index order.
-    using L = Layout<BF16>;
-    float* tm = reinterpret_cast<float*>(dyn + kFinOffTm);
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(dyn + kFinOffCnt);
     const int nT = C * kThreads;
-    for (int i = tid; i < nT; i += kThreads) tm[i] = slots[i / kThreads].tmax[i % kThreads];
-    group_sync();
     // theta: count the thread maxima per 16-bit key below the row maximum
     // (bucket i = key(m) - key; keys beyond 255 share the last bucket) and
     // take the key where the count from the top reaches k.  For bf16 rows
@@ -570,11 +698,6 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant_
   }
   if constexpr (BF16) {
     if (rp.kind == kKindH) {
-      for (int r = 0; r < C; ++r) {
-        const uint32_t* h = slots[r].hist;
-        hist[r * kHistWords + tid] = h[tid];
-        hist[r * kHistWords + tid + kThreads] = h[tid + kThreads];
-      }
       float zrow = 0.0f;
       if (rp.k == V) {
         for (int r = 0; r < C; ++r) {
@@ -585,9 +708,8 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const __grid_constant_
           }
         }
       }
-      group_sync();
-      if (leader_finish_hist<NV, VEC>(P, sm, c, hist, stage, table, row, rp.k, rp.use_p, rp.p,
-                                      rp.u, m, zrow, rp.c2, rp.st, q_row)) {
+      if (finish_hist<NV, VEC>(P, sm, c, hist, table, reinterpret_cast<uint4*>(dyn), row, rp, m,
+                               zrow, q_row)) {
         return;
       }
     }

@@ -19,7 +19,7 @@ cudaError_t launch_pair(const SampleParams& P, int num_sms, cudaStream_t stream)
   auto skern = stream_kernel<BF16, NV, VEC>;
   auto fkern = finish_kernel<BF16, NV, VEC>;
   constexpr int kStreamDyn = stream_dyn_bytes<NV>();
-  constexpr int kFinishDyn = finish_dyn_bytes<NV>();
+  constexpr int kFinishDyn = kFinishDynBytes;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -1,7 +1,9 @@
 // Stream kernel of the batched sampler: persistent CTAs of kGroups groups of
-// kThreads threads.  Group g of CTA b works through the items (row, chunk)
-// it = b * kGroups + g + n * (gridDim.x * kGroups), n = 0, 1, ...; a chunk is
-// kThreads * NV 16-byte vectors of one row.  Aligned rows arrive through a
+// kThreads threads.  The items (row, chunk) are ranked with the rows in
+// falling cost order (build_order) and dealt out in rounds, one rank per
+// group and round (item_rank); each group takes its rounds in an order
+// rotated by its index (group_round).  A chunk is kThreads * NV 16-byte
+// vectors of one row.  Aligned rows arrive through a
 // per-group ring of kStages shared-memory stages filled by 1-D bulk copies
 // (cp.async.bulk, completion counted on an mbarrier), issued kStages items
 // ahead, so the next chunk is in flight while the current one is reduced.
@@ -111,6 +113,102 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
 // producer warp per group.
 constexpr int kStreamThreads = kGroups * (kThreads + 32);
 
+// Largest batch whose rows the stream kernel orders by cost (one 16-bit
+// entry per row in shared memory); larger batches go in row order.
+constexpr int kOrderRows = 4096;
+constexpr int kOrderPerThread = (kOrderRows + kStreamThreads - 1) / kStreamThreads;
+
+// Cost class of a row's items in the stream kernel: 0 for the count
+// histogram (top-p rows without a small top-k), 1 for plain rows (one exp
+// per element), 2 for the rest (a maximum and a few stores).
+template <bool BF16, int NV>
+__device__ __forceinline__ int row_cost_class(const SampleParams& P, int row) {
+  const int kind = row_params<BF16, NV>(P, row, 0).kind;
+  return kind == kKindH ? 0 : (kind == kKindP ? 1 : 2);
+}
+
+// order[0 .. B) = the rows sorted by cost class, stable in row index.  All
+// threads of the CTA call it; it ends with a CTA barrier.  Thread t ranks
+// rows [t * kOrderPerThread, (t + 1) * kOrderPerThread): three 16-bit class
+// counts packed in a 64-bit word, one CTA-wide exclusive scan.
+template <bool BF16, int NV>
+__device__ __forceinline__ void build_order(const SampleParams& P, uint16_t* order,
+                                            unsigned long long* wsum) {
+  constexpr int kWarpsAll = kStreamThreads / 32;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const int r0 = t * kOrderPerThread;
+  uint32_t cls = 0;
+  unsigned long long cnt = 0;
+#pragma unroll
+  for (int j = 0; j < kOrderPerThread; ++j) {
+    const int r = r0 + j;
+    if (r < P.B) {
+      const int c = row_cost_class<BF16, NV>(P, r);
+      cls |= static_cast<uint32_t>(c) << (2 * j);
+      cnt += 1ull << (16 * c);
+    }
+  }
+  unsigned long long incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const unsigned long long v = lane < kWarpsAll ? wsum[lane] : 0ull;
+    unsigned long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane < kWarpsAll) wsum[lane] = x - v;
+    if (lane == 31) wsum[kWarpsAll] = x;
+  }
+  __syncthreads();
+  const unsigned long long before = wsum[w] + (incl - cnt);
+  const unsigned long long total = wsum[kWarpsAll];
+  uint32_t pos[3];
+  pos[0] = static_cast<uint32_t>(before & 0xffffu);
+  pos[1] = static_cast<uint32_t>(total & 0xffffu) + static_cast<uint32_t>((before >> 16) & 0xffffu);
+  pos[2] = static_cast<uint32_t>(total & 0xffffu) + static_cast<uint32_t>((total >> 16) & 0xffffu) +
+           static_cast<uint32_t>((before >> 32) & 0xffffu);
+#pragma unroll
+  for (int j = 0; j < kOrderPerThread; ++j) {
+    const int r = r0 + j;
+    if (r < P.B) {
+      const uint32_t c = (cls >> (2 * j)) & 3u;
+      const uint32_t at = c == 0 ? pos[0]++ : (c == 1 ? pos[1]++ : pos[2]++);
+      order[at] = static_cast<uint16_t>(r);
+    }
+  }
+  __syncthreads();
+}
+
+// Rank of a group's item in round n: rounds of G ranks dealt to the groups
+// in alternating direction, so that the expensive ranks at the front of the
+// order spread evenly over the groups.  Monotone in n for every group.
+__device__ __forceinline__ int item_rank(int n, int G, int gid) {
+  return n * G + ((n & 1) ? (G - 1 - gid) : gid);
+}
+
+// Rounds in which group gid has an item (ranks below `items`).
+__device__ __forceinline__ int group_rounds(int items, int G, int gid) {
+  const int full = items / G, rem = items % G;
+  const int at = (full & 1) ? (G - 1 - gid) : gid;
+  return full + (at < rem ? 1 : 0);
+}
+
+// Round of the group's i-th item: its rounds rotated by gid, so that the
+// groups meet the expensive front rounds at different times and their
+// compute overlaps the other groups' streaming.
+__device__ __forceinline__ int group_round(int i, int R, int gid) {
+  const int n = i + gid % R;
+  return n >= R ? n - R : n;
+}
+
 template <bool BF16, int NV, bool VEC>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     stream_kernel(const __grid_constant__ SampleParams P) {
@@ -121,6 +219,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   __shared__ SampleSmem smg[kGroups];
   __shared__ __align__(8) unsigned long long full[kGroups][kStages];
   __shared__ __align__(8) unsigned long long empty[kGroups][kStages];
+  __shared__ uint16_t order[kOrderRows];
+  __shared__ unsigned long long order_sum[kStreamThreads / 32 + 1];
   extern __shared__ __align__(128) unsigned char dyn[];
 
   // The finish kernel may be scheduled as soon as our CTAs retire.
@@ -149,6 +249,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       }
       fence_mbar_init();
     }
+  }
+  const bool ordered = P.B <= kOrderRows;
+  if (ordered) {
+    build_order<BF16, NV>(P, order, order_sum);  // ends with a CTA barrier
+  } else {
     __syncthreads();
   }
 
@@ -159,9 +264,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       if ((threadIdx.x & 31) == 0) {
         const char* logits = static_cast<const char*>(P.logits);
         int issued = 0;
-        for (int n = 0;; ++n) {
-          const int it = gid + n * G;
-          if (it >= items) break;
+        const int R = group_rounds(items, G, gid);
+        for (int n = 0; n < R; ++n) {
+          const int q = item_rank(group_round(n, R, gid), G, gid);
           const int s = n % kStages;
           if (n >= kStages) {
             const uint32_t parity = static_cast<uint32_t>(n / kStages - 1) & 1u;
@@ -172,7 +277,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             }
             if (!ok) break;  // the consumers stopped: issue nothing more
           }
-          const int r = it / C, ch = it % C;
+          const int r = ordered ? static_cast<int>(order[q / C]) : q / C, ch = q % C;
           const int e0 = ch * CHUNK;
           // Every chunk starts inside the row (the launch never makes an empty one).
           const uint32_t bytes = static_cast<uint32_t>(max(0, min(CHUNK, V - e0))) * L::ELT;
@@ -211,12 +316,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       reinterpret_cast<uint32_t*>(dyn + kGroups * kStages * kStageBytes) + group * kHistWords;
   ChunkSlot* ws = static_cast<ChunkSlot*>(P.workspace);
   bool timed_out = false;
-  for (int n = 0;; ++n) {
-    const int it = gid + n * G;
-    if (it >= items) break;
-    const int row = it / C, chunk = it % C;
+  const int R = group_rounds(items, G, gid);
+  for (int n = 0; n < R; ++n) {
+    const int q = item_rank(group_round(n, R, gid), G, gid);
+    const int row = ordered ? static_cast<int>(order[q / C]) : q / C, chunk = q % C;
     c.crank = static_cast<uint32_t>(chunk);
-    ChunkSlot* slot = ws + it;
+    ChunkSlot* slot = ws + (static_cast<size_t>(row) * C + chunk);
     const RowParams rp = row_params<BF16, NV>(P, row, C);  // loads overlap the wait
     uint32_t d[NV][4];
     if constexpr (VEC) {
