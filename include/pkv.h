@@ -55,8 +55,9 @@ typedef enum { PKV_FP32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_ST_COL_OOB 8       /* write-back / page-table column out of range  */
 #define PKV_ST_BAD_UNIFORM 16  /* uniform outside [0,1): clamped, still drawn  */
 #define PKV_ST_NOSPC 32        /* page fill: more pages needed than are free   */
-#define PKV_ST_TIMEOUT 64      /* a row's CTAs did not report in time (internal
-                                  error; the row's token is -1)                */
+#define PKV_ST_TIMEOUT 64      /* a row's records are missing or untrusted (a
+                                  copy did not land in time, or the workspace
+                                  was not initialised); the token is -1       */
 
 /* Largest vocabulary the sampler handles for each dtype. */
 #define PKV_MAX_VOCAB_BF16 524288
@@ -73,12 +74,23 @@ int pkv_version(void);
 /*
  * Device bytes of the workspace pkv_sample_batch needs for (B, V, dtype), or
  * 0 for invalid arguments.  The sampler runs as two kernels: the first splits
- * every row into chunks and leaves one record per (row, chunk) in the
- * workspace (about 2 KB each); the second settles each row from its records.
- * The caller owns the workspace; it needs no initialisation and may be reused
- * by later calls on the same stream.
+ * every row into chunks, hands the chunks out to its CTAs from a counter in
+ * the workspace header and leaves one record per (row, chunk) in the
+ * workspace (about 3 KB each); the second settles each row from its
+ * records.  The caller owns the workspace.  Before its first use it must be
+ * initialised once, by pkv_sample_workspace_init or by zeroing it; every
+ * call then leaves it ready for the next call on the same stream.  A
+ * workspace must not be used by two calls that may run concurrently.
  */
 size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt);
+
+/*
+ * pkv_sample_workspace_init -- enqueues on `stream` the zeroing of the
+ * workspace header (the first 256 bytes).  workspace: device pointer, 16-byte
+ * aligned, workspace_bytes >= 256.  Errors: PKV_EINVAL (NULL, too small,
+ * unaligned), PKV_ECUDA.
+ */
+int pkv_sample_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /*
  * pkv_sample_batch -- one token per row of a [B, V] logits matrix.
@@ -115,8 +127,9 @@ size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt);
  *               probabilities (one-hot for greedy rows); leave NULL when timing.
  *   status      device int32 status word or NULL.
  *   workspace   device memory of at least pkv_sample_workspace_bytes(B, V, dt)
- *               bytes (workspace_bytes), 16-byte aligned; not to be shared by
- *               calls that may run concurrently.
+ *               bytes (workspace_bytes), 16-byte aligned, initialised once
+ *               before its first use (pkv_sample_workspace_init); not to be
+ *               shared by calls that may run concurrently.
  * Errors: PKV_EINVAL (NULL required pointer, B < 1, B > 65535, V < 1,
  * row_stride < V, bad dtype, pool sizes < 1, workspace missing, too small or
  * unaligned), PKV_EUNSUPPORTED (V above PKV_MAX_VOCAB_*), PKV_ECUDA (launch

@@ -67,7 +67,7 @@ extern "C" {
 
 const char* pkv_last_error(void) { return g_err; }
 
-int pkv_version(void) { return 200; }
+int pkv_version(void) { return 300; }
 
 size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt) {
   if (B < 1 || V < 1 || (dt != PKV_FP32 && dt != PKV_BF16)) return 0;
@@ -79,7 +79,19 @@ size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt) {
       chunks = std::max(chunks, static_cast<size_t>(cfg.chunks));
     }
   }
-  return static_cast<size_t>(B) * chunks * pkv::kChunkSlotBytes;
+  return pkv::kWorkspaceHeaderBytes + static_cast<size_t>(B) * chunks * pkv::kChunkSlotBytes;
+}
+
+int pkv_sample_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (workspace == nullptr) return fail(PKV_EINVAL, "workspace is NULL");
+  if (workspace_bytes < pkv::kWorkspaceHeaderBytes)
+    return fail(PKV_EINVAL, "workspace of %zu bytes is smaller than its %zu-byte header",
+                workspace_bytes, pkv::kWorkspaceHeaderBytes);
+  if (!aligned16(workspace)) return fail(PKV_EINVAL, "workspace is not 16-byte aligned");
+  const cudaError_t e = cudaMemsetAsync(workspace, 0, pkv::kWorkspaceHeaderBytes,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace initialisation");
+  return ok();
 }
 
 int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
@@ -115,7 +127,8 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
     return fail(PKV_EUNSUPPORTED, "no launch shape covers V=%d", V);
   if (static_cast<int64_t>(cfg.chunks - 1) * cfg.chunk >= V)
     return fail(PKV_EUNSUPPORTED, "launch shape with an empty chunk (V=%d)", V);
-  const size_t need = static_cast<size_t>(B) * cfg.chunks * pkv::kChunkSlotBytes;
+  const size_t need =
+      pkv::kWorkspaceHeaderBytes + static_cast<size_t>(B) * cfg.chunks * pkv::kChunkSlotBytes;
   if (workspace == nullptr || workspace_bytes < need)
     return fail(PKV_EINVAL, "workspace of %zu bytes needed (pkv_sample_workspace_bytes), got %zu",
                 need, workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);

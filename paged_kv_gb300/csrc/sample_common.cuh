@@ -54,28 +54,24 @@ constexpr int kMaxChunks = 16;                 // chunks per row
 constexpr int kHistKeys = 1024;                // values counted below a chunk's maximum (H rows)
 constexpr int kHistWords = kHistKeys / 2;      // two 16-bit counts per word
 constexpr int kMaxK = 256;                     // largest k of a K row
-constexpr int kListCap = kMaxChunks * kMaxK;   // candidates the finisher keeps (K rows)
-constexpr int kListBytes = kListCap * 8;       // the finisher's candidate list
 static_assert(kHistKeys == 4 * kThreads, "four merged histogram keys per finisher thread");
 static_assert(kHistWords == 2 * kThreads, "two histogram words per thread");
 
 
-// Dynamic shared memory of the finish kernel (all offsets 16-byte aligned):
-// the row's thread maxima (K rows) and count histograms (H rows), copied from
-// the workspace records; then the candidate list and per-vector counts (K
-// rows).  H rows keep the fixed-point mass per merged key at kFinOffTable and,
-// once the histograms are consumed, stage one chunk from offset 0.
-constexpr int kMaxCandVecs = 4096;  // candidate vectors a K row's finisher handles
-constexpr int kFinOffTm = 0;
-constexpr int kFinOffHist = kFinOffTm + kMaxChunks * kThreads * 4;
-constexpr int kFinOffList = kFinOffHist + kMaxChunks * kHistWords * 4;
-constexpr int kFinOffCnt = kFinOffList + kListBytes;
-constexpr int kFinishDynBytes = kFinOffCnt + kMaxCandVecs * 4;
-constexpr int kFinOffTable = kFinishDynBytes - kHistKeys * 8;
+// Dynamic shared memory of the finish kernel (offsets 16-byte aligned): the
+// row's records (one bulk copy), the K rows' candidate list (values, then
+// indices) and the H rows' fixed-point mass per merged key.  An H row stages
+// its draw chunk from offset 0 once the records are consumed.
+constexpr int kFinListCap = 2048;
+constexpr int kFinRecBytes = kMaxChunks * static_cast<int>(kChunkSlotBytes);
+constexpr int kFinOffList = kFinRecBytes;
+constexpr int kFinOffTable = kFinOffList + kFinListCap * 8;
+constexpr int kFinishDynBytes = kFinOffTable + kHistKeys * 8;
+static_assert(kFinRecBytes % 16 == 0, "aligned regions");
 static_assert(kThreads * 16 * 16 <= kFinOffTable, "a staged chunk (NV <= 16) below the mass table");
+static_assert(kFinListCap * 2 >= kMaxChunks * kThreads, "the thread maxima fit the list region");
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
-constexpr double kMassScaleD = 1099511627776.0;
-constexpr long long kWaitNs = 2000000000ll;     // bound of every wait on a bulk copy (2 s)
+constexpr long long kWaitNs = 500000000ll;      // bound of every wait on a bulk copy (0.5 s)
 
 constexpr int kStNonFinite = 1;
 constexpr int kStAllNegInf = 2;
@@ -91,7 +87,7 @@ struct __align__(16) Summary {
   float f0;     // unused
   float f1;     // unused
   int32_t i0;   // H: 16-bit key of the chunk maximum (the histogram's anchor)
-  uint32_t u0;  // bit 1: a bulk copy timed out
+  uint32_t u0;  // unused
 };
 
 // The workspace record of one (row, chunk): written by the stream kernel,
@@ -103,14 +99,14 @@ struct __align__(16) ChunkSlot {
   Summary s;
   float wm[kWarps];
   float wz[kWarps];
+  uint32_t wseq[kWarps];  // per warp: the call's record number, 0 when its data is not trusted
+  uint32_t pad[kWarps];
   float tmax[kThreads];
   uint32_t hist[kHistWords];
 };
 
 struct SampleSmem {
   Summary gather[kMaxChunks];
-  __align__(16) float gwm[kMaxChunks][kWarps];  // P rows: per-warp max of each chunk
-  __align__(16) float gwz[kMaxChunks][kWarps];  // P rows: per-warp mass relative to gwm
   uint32_t cnt[kMaxChunks];
   uint32_t ties[kMaxChunks];
   unsigned long long cmass[kMaxChunks][kWarps];
@@ -131,12 +127,16 @@ struct SampleSmem {
 static_assert(sizeof(Summary) == 16, "one 16-byte record");
 static_assert(sizeof(ChunkSlot) == kChunkSlotBytes, "workspace record size");
 // Byte offsets of the record's parts (the finisher copies them in 16-byte pieces).
-constexpr int kSlotOffWm = 16, kSlotOffWz = 48, kSlotOffTmax = 80, kSlotOffHist = 1104;
-constexpr int kSlotPieces = kChunkSlotBytes / 16;
-static_assert(offsetof(ChunkSlot, wm) == kSlotOffWm && offsetof(ChunkSlot, wz) == kSlotOffWz &&
-                  offsetof(ChunkSlot, tmax) == kSlotOffTmax &&
-                  offsetof(ChunkSlot, hist) == kSlotOffHist && kChunkSlotBytes % 16 == 0,
-              "record layout");
+static_assert(offsetof(ChunkSlot, tmax) % 16 == 0 && offsetof(ChunkSlot, hist) % 16 == 0 &&
+                  kChunkSlotBytes % 16 == 0,
+              "records move by 16-byte bulk copies");
+
+__device__ __forceinline__ WorkspaceHeader* ws_header(const SampleParams& P) {
+  return static_cast<WorkspaceHeader*>(P.workspace);
+}
+__device__ __forceinline__ ChunkSlot* ws_records(const SampleParams& P) {
+  return reinterpret_cast<ChunkSlot*>(static_cast<char*>(P.workspace) + kWorkspaceHeaderBytes);
+}
 
 // Barrier of the calling thread's group of kThreads threads (named barrier
 // 1 + group); a finish CTA is one group.
@@ -306,8 +306,57 @@ __device__ __forceinline__ float weight(float x, float m, float c2) {
   return ex2(__fmul_rn(__fsub_rn(x, m), c2));
 }
 
-__device__ __forceinline__ unsigned long long mass_fx(float w) {
-  return static_cast<unsigned long long>(__float2ull_rz(w * kMassScale));
+// Fixed-point arithmetic without FP64 or 64-bit float<->integer conversion
+// instructions (on this GPU both run at a few hundred cycles each).
+
+// floor(x * 2^40) for a finite x in [0, 2^23), by shifting its significand.
+__device__ __forceinline__ unsigned long long fx40(float x) {
+  const uint32_t b = __float_as_uint(x);
+  const int e = static_cast<int>((b >> 23) & 0xffu);
+  if (e == 0 || (b >> 31)) return 0ull;  // zero, subnormal (below 2^-126) or negative
+  if (e >= 127 + 23) return ~0ull;        // outside the domain (not reached for weights)
+  const unsigned long long mnt = static_cast<unsigned long long>((b & 0x7fffffu) | 0x800000u);
+  const int sh = e - 127 - 23 + 40;      // x * 2^40 = mnt * 2^sh
+  if (sh >= 0) return mnt << sh;
+  return sh > -32 ? (mnt >> -sh) : 0ull;
+}
+
+// The fixed-point mass of a weight w in [0, 1]: floor(w * 2^40).
+__device__ __forceinline__ unsigned long long mass_fx(float w) { return fx40(w); }
+
+// ceil(z * f) (up = true) or floor(z * f) for z < 2^60 and a finite f in
+// [0, 1], exactly: f = mnt * 2^-s with a 24-bit mnt, the product in 128 bits.
+__device__ __forceinline__ unsigned long long mul_fx(unsigned long long z, float f, bool up) {
+  const uint32_t b = __float_as_uint(f);
+  const int e = static_cast<int>((b >> 23) & 0xffu);
+  if (e == 0 || (b >> 31) || z == 0) return 0ull;
+  const unsigned long long mnt = static_cast<unsigned long long>((b & 0x7fffffu) | 0x800000u);
+  const int s = 127 + 23 - e;  // f = mnt * 2^-s, s >= 23 for f <= 1
+  const unsigned long long lo = z * mnt;
+  const unsigned long long hi = __umul64hi(z, mnt);
+  if (s >= 64) {
+    // z * f < 2^60 * 2^-40: the quotient is hi >> (s - 64) (s < 128 here).
+    const int t = s - 64;
+    const unsigned long long q = t < 64 ? (hi >> t) : 0ull;
+    const bool frac = lo != 0 || (t < 64 ? (hi & ((1ull << t) - 1ull)) != 0 : hi != 0);
+    return q + ((up && frac) ? 1ull : 0ull);
+  }
+  const unsigned long long q = (hi << (64 - s)) | (lo >> s);
+  const bool frac = (lo & ((1ull << s) - 1ull)) != 0;
+  return q + ((up && frac) ? 1ull : 0ull);
+}
+
+// ceil(rem / w) for w > 0 and a quotient below 2^21, by bisection on
+// j * w >= rem (integer multiplies only).
+__device__ __forceinline__ unsigned long long ceil_div_small(unsigned long long rem,
+                                                             unsigned long long w) {
+  unsigned long long lo = 0, hi = 1ull << 21;
+  while (lo < hi) {
+    const unsigned long long mid = (lo + hi) >> 1;
+    if (mid * w >= rem) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
 }
 
 __device__ __forceinline__ unsigned long long pick4(const unsigned long long (&a)[4], int j) {
@@ -596,137 +645,6 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
   return key_float(prefix);
 }
 
-// Position cut for ties in the list: among entries with member(i), the first
-// r (list order = index order) are kept.  Returns the position after the r-th
-// member (n if there are fewer than r).
-template <typename M>
-__device__ __forceinline__ int list_tie_cut(int n, M&& member, unsigned long long r,
-                                            SampleSmem& sm, const Ctx& c) {
-  const int per = (n + kThreads - 1) / kThreads;
-  const int i0 = min(n, c.tid * per);
-  const int i1 = min(n, i0 + per);
-  uint32_t cnt = 0;
-  for (int i = i0; i < i1; ++i) cnt += member(i) ? 1u : 0u;
-  uint32_t total;
-  const uint32_t before = block_exclusive_scan<uint32_t>(cnt, sm.wu, c.lane, c.warp, &total);
-  if (c.tid == 0) sm.bi[3] = n;
-  group_sync();
-  if (r <= total && before < r && r <= before + cnt) {
-    uint32_t need = static_cast<uint32_t>(r - before);
-    for (int i = i0; i < i1; ++i) {
-      if (member(i) && --need == 0) {
-        sm.bi[3] = i + 1;
-        break;
-      }
-    }
-  }
-  group_sync();
-  const int cut = sm.bi[3];
-  group_sync();
-  return cut;
-}
-
-// Inverse CDF over the list entries with in_s(i): the first entry (list
-// order) whose cumulative weight exceeds u * Z_S; else the last with weight.
-// Writes Z_S to *zs.  Returns the row index of the token (-1 if none).
-template <typename S, typename W>
-__device__ __forceinline__ int list_draw(const int32_t* idx, int n, S&& in_s, W&& w_of, float u,
-                                         SampleSmem& sm, const Ctx& c, float* zs) {
-  const int per = (n + kThreads - 1) / kThreads;
-  const int i0 = min(n, c.tid * per);
-  const int i1 = min(n, i0 + per);
-  float seg = 0.0f;
-  int last = -1;
-  for (int i = i0; i < i1; ++i) {
-    if (in_s(i)) {
-      const float w = w_of(i);
-      seg += w;
-      if (w > 0.0f) last = i;
-    }
-  }
-  float total;
-  const float before = block_exclusive_scan<float>(seg, sm.wt, c.lane, c.warp, &total);
-  const float target = u * total;
-  const int cand = block_min_int((target < before + seg && seg > 0.0f) ? c.tid : INT_MAX, sm.wi,
-                                 c.lane, c.warp);
-  const int lastpos = block_max_int(last, sm.wi, c.lane, c.warp);
-  if (c.tid == 0) sm.bi[2] = lastpos;
-  group_sync();
-  if (cand != INT_MAX && c.tid == cand) {
-    float run = before;
-    int sel = -1;
-    for (int i = i0; i < i1; ++i) {
-      if (in_s(i)) {
-        run += w_of(i);
-        if (target < run) {
-          sel = i;
-          break;
-        }
-      }
-    }
-    sm.bi[2] = sel >= 0 ? sel : last;
-  }
-  group_sync();
-  const int pos = sm.bi[2];
-  *zs = total;
-  group_sync();
-  return pos >= 0 ? idx[pos] : -1;
-}
-
-// K rows.  The finisher holds every candidate of the row in its list,
-// entries 0 .. n-1 in index order.  Finishes exactly on the list: top-k
-// (count select, ties by index), top-p inside K (mass select on 2^-40
-// fixed-point weights), renormalisation and the inverse-CDF draw.  Emits the
-// token and, if asked, the probabilities of the kept tokens.
-static __device__ __forceinline__ void leader_finish_list(const SampleParams& P, SampleSmem& sm,
-                                                          const Ctx& c, float* l_val,
-                                                          int32_t* l_idx, int n, int row, int k,
-                                                          bool use_p, float p, float m, float c2,
-                                                          float u, int st, float* q_row) {
-  const int tid = c.tid, lane = c.lane, warp = c.warp;
-  unsigned long long rk;
-  const float tk = list_select<false>(l_val, n, [](int) { return true; },
-                                      [](int) { return 1ull; },
-                                      static_cast<unsigned long long>(k), sm, c, &rk);
-  const int cut_k = list_tie_cut(n, [&](int i) { return l_val[i] == tk; }, rk, sm, c);
-  auto in_k = [&](int i) { return l_val[i] > tk || (l_val[i] == tk && i < cut_k); };
-  auto w_of = [&](int i) { return weight(l_val[i], m, c2); };
-  float tp = tk;
-  int cut_p = cut_k;
-  if (use_p) {
-    unsigned long long zfx = 0;
-    for (int i = tid; i < n; i += kThreads) {
-      if (in_k(i)) zfx += mass_fx(w_of(i));
-    }
-    const unsigned long long z = block_sum<unsigned long long>(zfx, sm.wl, lane, warp);
-    unsigned long long target_fx =
-        static_cast<unsigned long long>(ceil(static_cast<double>(z) * static_cast<double>(p)));
-    if (target_fx < 1) target_fx = 1;
-    if (target_fx > z) target_fx = z;
-    unsigned long long rem;
-    tp = list_select<true>(l_val, n, in_k, [&](int i) { return mass_fx(w_of(i)); }, target_fx, sm,
-                           c, &rem);
-    // Members of the threshold group share one weight wt: member j (index
-    // order) is kept iff above + j * wt < target, i.e. j < ceil(rem / wt).
-    const unsigned long long wt = mass_fx(weight(tp, m, c2));
-    const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
-    const float tpv = tp;
-    cut_p = list_tie_cut(n, [&](int i) { return l_val[i] == tpv && in_k(i); }, rp, sm, c);
-  }
-  const float tpv = tp;
-  const int cpv = cut_p;
-  auto in_s = [&](int i) { return in_k(i) && (l_val[i] > tpv || (l_val[i] == tpv && i < cpv)); };
-  float zs;
-  const int tok = list_draw(l_idx, n, in_s, w_of, u, sm, c, &zs);
-  if (tid == 0) emit_token(P, row, tok, tok < 0 ? (st | kStNonFinite) : st);
-  if (q_row != nullptr) {
-    const float inv = 1.0f / zs;
-    for (int i = tid; i < n; i += kThreads) {
-      if (in_s(i)) q_row[l_idx[i]] = w_of(i) * inv;
-    }
-  }
-}
-
 // ----------------------------------------------------------------- exact fallback (F)
 //
 // The leader alone settles the row by radix passes over the row in global
@@ -848,14 +766,13 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
       if (in_k(x, e)) z += wfx(x, e);
     }
     z = block_sum<unsigned long long>(z, sm.wl, lane, warp);
-    unsigned long long target =
-        static_cast<unsigned long long>(ceil(static_cast<double>(z) * static_cast<double>(p)));
+    unsigned long long target = mul_fx(z, p, true);
     if (target < 1) target = 1;
     if (target > z) target = z;
     unsigned long long rem;
     tp = row_select<BF16, true>(P, row, in_k, wfx, target, sm, c, &rem);
     const unsigned long long wt = mass_fx(weight(tp, m, c2));
-    const unsigned long long rp = wt == 0 ? ~0ull : (rem + wt - 1) / wt;
+    const unsigned long long rp = wt == 0 ? ~0ull : ceil_div_small(rem, wt);
     const float tpv = tp;
     cp = row_tie_cut<BF16>(P, row, [&](float x, int e) { return x == tpv && in_k(x, e); }, rp, sm,
                            c);
@@ -881,8 +798,7 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
   unsigned long long zs;
   const unsigned long long before =
       block_exclusive_scan<unsigned long long>(seg, sm.wl, lane, warp, &zs);
-  const unsigned long long tdraw =
-      static_cast<unsigned long long>(static_cast<double>(u) * static_cast<double>(zs));
+  const unsigned long long tdraw = mul_fx(zs, u, false);
   const int lastpos = block_max_int(last, sm.wi, lane, warp);
   if (tid == 0) sm.bi[2] = lastpos;
   group_sync();

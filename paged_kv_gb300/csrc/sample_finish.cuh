@@ -1,49 +1,417 @@
 // Finish kernel of the batched sampler: one CTA per row reads the stream
 // kernel's records of the row from the workspace and settles the token (see
 // sample_common.cuh for the row kinds).
+//
+// Every phase here runs once per row, so the kernel is built for latency:
+// the records arrive in one bulk copy, per-record work is spread over the
+// threads and combined by warp reductions (no thread walks the C * 8 warp
+// records alone), and the write-back coordinates are loaded at the start.
 #pragma once
 
 #include "sample_common.cuh"
 
 namespace pkv {
 
+// The row's head: its maximum m over the warp maxima (NaN if any is NaN),
+// the first record entry (chunk * kWarps + warp, index order) holding m, and
+// whether any warp record is stale (not from this call).
+struct RowHead {
+  float m;
+  int first;
+  bool nan;
+  bool stale;
+};
+
+__device__ __forceinline__ RowHead row_head(const ChunkSlot* recs, int C, uint32_t seq,
+                                            SampleSmem& sm, const Ctx& c) {
+  const int i = c.tid;
+  const bool in = i < C * kWarps;
+  const float x = in ? recs[i / kWarps].wm[i % kWarps] : -INFINITY;
+  const bool nan = x != x;
+  const bool stale = in && recs[i / kWarps].wseq[i % kWarps] != seq;
+  const uint32_t key = nan ? 0u : float_key(x);
+  const uint32_t wk = __reduce_max_sync(kFull, key);
+  const int wfirst = static_cast<int>(
+      __reduce_min_sync(kFull, (in && !nan && key == wk) ? static_cast<uint32_t>(i) : 0x7fffffffu));
+  const unsigned flags = (__any_sync(kFull, nan) ? 1u : 0u) | (__any_sync(kFull, stale) ? 2u : 0u);
+  if (c.lane == 0) {
+    sm.wu[c.warp] = wk;
+    sm.wi[c.warp] = wfirst;
+    sm.bi[c.warp] = static_cast<int32_t>(flags);
+  }
+  group_sync();
+  uint32_t k = 0;
+  unsigned f = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    k = max(k, sm.wu[w]);
+    f |= static_cast<unsigned>(sm.bi[w]);
+  }
+  int first = INT_MAX;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    if (sm.wu[w] == k) first = min(first, sm.wi[w]);
+  }
+  group_sync();
+  RowHead h;
+  h.m = (f & 1u) ? __uint_as_float(0x7fc00000u) : key_float(k);
+  h.first = first;
+  h.nan = (f & 1u) != 0;
+  h.stale = (f & 2u) != 0;
+  return h;
+}
+
+// The write-back coordinates of a row, loaded early so that emitting the
+// token costs no dependent global loads.
+struct WriteBack {
+  int64_t col;
+  int64_t prow;
+};
+
+__device__ __forceinline__ WriteBack load_write_back(const SampleParams& P, int row) {
+  WriteBack wb;
+  wb.col = -1;
+  wb.prow = 0;
+  if (P.token_pool != nullptr) {
+    wb.col = P.wb_cols[row];
+    wb.prow = P.wb_rows[row];
+  }
+  return wb;
+}
+
+// out_tokens[row] = tok and the fused write-back (column < 0: no write; a
+// token of -1 is not written); status bits are OR-ed in.
+__device__ __forceinline__ void emit(const SampleParams& P, int row, int tok, int st,
+                                     const WriteBack& wb) {
+  P.out_tokens[row] = tok;
+  if (P.token_pool != nullptr && tok >= 0 && wb.col >= 0) {
+    if (wb.prow < 0 || wb.prow >= P.pool_rows) {
+      st |= kStRowOOB;
+    } else if (wb.col >= P.pool_cols) {
+      st |= kStColOOB;
+    } else {
+      P.token_pool[wb.prow * P.pool_cols + wb.col] = tok;
+    }
+  }
+  if (st != 0 && P.status != nullptr) atomicOr(P.status, st);
+}
+
+// ----------------------------------------------------------------- plain finish (P)
+
+// No filter: the draw is over the whole row.  The record masses (warp w of
+// chunk r: wz relative to its maximum wm) are scanned in index order to find
+// the (chunk, warp) holding u * Z; that warp re-reads its slice and finds the
+// token with per-vector sums.
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ void finish_plain(const SampleParams& P, SampleSmem& sm, const Ctx& c,
+                                             const ChunkSlot* recs, int row, const RowParams& rp,
+                                             float m, const WriteBack& wb, float* q_row) {
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  const int C = static_cast<int>(c.csize);
+  const int V = P.V;
+  const int nrec = C * kWarps;
+  float mw = 0.0f;
+  if (tid < nrec) {
+    const float wmax = recs[tid / kWarps].wm[tid % kWarps];
+    if (wmax > -INFINITY) mw = recs[tid / kWarps].wz[tid % kWarps] * ex2((wmax - m) * rp.c2);
+  }
+  float zrow;
+  const float before = block_exclusive_scan<float>(mw, sm.wt, lane, warp, &zrow);
+  float target = rp.u * zrow;
+  if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
+  // The entry whose interval holds target; rounding can leave none: then
+  // the last entry with mass.
+  const int hit = block_min_int(
+      (mw > 0.0f && target >= before && target < before + mw) ? tid : INT_MAX, sm.wi, lane, warp);
+  const int lastm = block_max_int(mw > 0.0f ? tid : -1, sm.wi, lane, warp);
+  const int estar = hit != INT_MAX ? hit : lastm;
+  if (tid == estar) sm.bf4[0] = hit != INT_MAX ? target - before : INFINITY;
+  group_sync();
+  const float tau = sm.bf4[0];
+  if (estar >= 0 && warp == estar % kWarps) {
+    const int r = estar / kWarps;
+    uint32_t d[NV][4];
+    load_chunk<BF16, NV, VEC>(P, row, r, warp, lane, d);
+    // Per-vector lane sums, then the vector holding tau, the lane, the element.
+    float s[NV];
+    int lastl = -1;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      float sj = 0.0f;
+      for_vec<BF16>(d[j], vec_base<BF16, NV>(r, warp, lane, j), [&](float x, int e) {
+        const float w = e < V ? weight(x, m, rp.c2) : 0.0f;
+        sj += w;
+        if (w > 0.0f) lastl = e;
+      });
+      s[j] = sj;
+    }
+    float tot[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) tot[j] = warp_sum(s[j]);
+    int jstar = -1;
+    float a = 0.0f, abefore = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+      if (jstar < 0 && tot[j] > 0.0f && tau < a + tot[j]) {
+        jstar = j;
+        abefore = a;
+      }
+      a += tot[j];
+    }
+    const int lastw = __reduce_max_sync(kFull, lastl);  // the slice's last element with mass
+    int tok = lastw;
+    if (jstar >= 0) {
+      float sj = 0.0f;
+      uint32_t v4[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int j = 0; j < NV; ++j) {
+        if (j == jstar) {
+          sj = s[j];
+          v4[0] = d[j][0];
+          v4[1] = d[j][1];
+          v4[2] = d[j][2];
+          v4[3] = d[j][3];
+        }
+      }
+      const float incl = warp_inclusive_scan(sj, lane) + abefore;
+      const unsigned bal = __ballot_sync(kFull, tau < incl);
+      const int ls = bal ? __ffs(bal) - 1 : 31;
+      int sel = -1;
+      if (lane == ls) {
+        float run = incl - sj;
+        int lastv = -1;
+        for_vec<BF16>(v4, vec_base<BF16, NV>(r, warp, lane, jstar), [&](float x, int e) {
+          const float w = e < V ? weight(x, m, rp.c2) : 0.0f;
+          run += w;
+          if (w > 0.0f) {
+            lastv = e;
+            if (sel < 0 && tau < run) sel = e;
+          }
+        });
+        if (sel < 0) sel = lastv;
+      }
+      const int found = __shfl_sync(kFull, sel, ls);
+      if (found >= 0) tok = found;
+    }
+    if (lane == 0) emit(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
+  }
+  if (estar < 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
+  if (q_row != nullptr) {
+    const float inv = 1.0f / zrow;
+    for (int r = 0; r < C; ++r) {
+      uint32_t d[NV][4];
+      load_chunk<BF16, NV, VEC>(P, row, r, warp, lane, d);
+      for_regs<BF16, NV>(d, r, warp, lane, [&](float x, int e) {
+        if (e < V) q_row[e] = weight(x, m, rp.c2) * inv;
+      });
+    }
+  }
+}
+
+// ----------------------------------------------------------------- top-k finish (K)
+
+// theta = the k-th largest thread maximum of the row (or a lower bound on
+// it): at least k elements are >= theta, so the top-k lies in the threads
+// whose maximum is >= theta.  Their vectors are re-read (an L2 hit) and the
+// elements >= theta appended to a list (any order).  The list is ranked by
+// (value desc, index asc) with all-pairs comparisons (it holds about k
+// entries), which gives the top-k in order; top-p is a prefix scan over it,
+// and the draw a scan over the kept entries in index order.  Returns false,
+// having emitted nothing, when the list overflows (pathological ties); the
+// caller then runs the exact fallback.
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ bool finish_topk(const SampleParams& P, SampleSmem& sm, const Ctx& c,
+                                            const ChunkSlot* recs, float* l_val, int32_t* l_idx,
+                                            int row, const RowParams& rp, float m,
+                                            const WriteBack& wb, float* q_row) {
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  const int C = static_cast<int>(c.csize);
+  const int V = P.V;
+  const int k = rp.k;
+  const int nT = C * kThreads;
+  auto tmax_at = [&](int i) { return recs[i / kThreads].tmax[i % kThreads]; };
+  // ---- theta: thread maxima counted per 16-bit key below the row maximum
+  // (bucket i = key(m) - key; keys beyond 255 share the last bucket); the
+  // key where the count from the top reaches k.  For bf16 rows it is the
+  // exact k-th largest thread maximum when within 256 values of m;
+  // otherwise a lower bound, or (last bucket) the exact select.
+  const uint32_t km = key16(m);
+  sm.hlo[tid] = 0u;
+  group_sync();
+  for (int i = tid; i < nT; i += kThreads) {
+    const float t = tmax_at(i);
+    if (t == t) {
+      const uint32_t kt = key16(t);
+      atomicAdd(&sm.hlo[kt >= km ? 0u : min(km - kt, 255u)], 1u);
+    }
+  }
+  group_sync();
+  {
+    const uint32_t h = sm.hlo[tid];
+    uint32_t tot;
+    const uint32_t before = block_exclusive_scan<uint32_t>(h, sm.wu, lane, warp, &tot);
+    if (before < static_cast<uint32_t>(k) && before + h >= static_cast<uint32_t>(k)) sm.bi[1] = tid;
+    if (tid == 0 && tot < static_cast<uint32_t>(k)) sm.bi[1] = -1;
+  }
+  group_sync();
+  const int bk = sm.bi[1];
+  group_sync();
+  if (bk < 0) return false;
+  float theta;
+  if (bk < 255) {
+    theta = key16_float(km - static_cast<uint32_t>(bk));
+  } else {
+    for (int i = tid; i < nT; i += kThreads) l_val[i] = tmax_at(i);
+    group_sync();
+    unsigned long long rk;
+    theta = list_select<false>(l_val, nT, [](int) { return true; }, [](int) { return 1ull; },
+                               static_cast<unsigned long long>(k), sm, c, &rk);
+  }
+  if (!(theta > -INFINITY)) return false;
+  // ---- candidate threads, then their vectors: elements >= theta appended.
+  uint16_t* cand = reinterpret_cast<uint16_t*>(sm.scan);  // up to 4 * kBuckets thread ids
+  constexpr int kCandCap = 4 * kBuckets;
+  if (tid == 0) {
+    sm.bi[4] = 0;
+    sm.bi[5] = 0;
+  }
+  group_sync();
+  for (int i = tid; i < nT; i += kThreads) {
+    if (tmax_at(i) >= theta) {
+      const int at = atomicAdd(&sm.bi[4], 1);
+      if (at < kCandCap) cand[at] = static_cast<uint16_t>(i);
+    }
+  }
+  group_sync();
+  const int ncand = sm.bi[4];
+  if (ncand > kCandCap) return false;
+  for (int v = tid; v < ncand * NV; v += kThreads) {
+    const int i = cand[v / NV], j = v % NV;
+    const int ct = i % kThreads;
+    const int e0 = vec_base<BF16, NV>(i / kThreads, ct / 32, ct % 32, j);
+    uint32_t w4[4];
+    load_vec<BF16, NV, VEC>(P, row, e0, w4);
+    for_vec<BF16>(w4, e0, [&](float x, int e) {
+      if (e < V && x >= theta) {
+        const int at = atomicAdd(&sm.bi[5], 1);
+        if (at < kFinListCap) {
+          l_val[at] = x;
+          l_idx[at] = e;
+        }
+      }
+    });
+  }
+  group_sync();
+  const int n = sm.bi[5];
+  if (n > kFinListCap || n < k) return false;
+  // ---- ranks in (value desc, index asc); sorted[rank] for rank < k.
+  uint32_t* sorted = sm.hlo;
+  for (int i = tid; i < n; i += kThreads) {
+    const float vi = l_val[i];
+    const int ii = l_idx[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) {
+      const float vj = l_val[j];
+      rank += (vj > vi || (vj == vi && l_idx[j] < ii)) ? 1 : 0;
+    }
+    if (rank < k) sorted[rank] = static_cast<uint32_t>(i);
+  }
+  group_sync();
+  // ---- top-p inside K: thread t < k holds the t-th of the order.
+  const bool in_k = tid < k;
+  const int me = in_k ? static_cast<int>(sorted[tid]) : 0;
+  const float xv = in_k ? l_val[me] : -INFINITY;
+  const int xi = in_k ? l_idx[me] : INT_MAX;
+  const float wf = in_k ? weight(xv, m, rp.c2) : 0.0f;
+  const unsigned long long w = in_k ? mass_fx(wf) : 0ull;
+  unsigned long long zk;
+  const unsigned long long before =
+      block_exclusive_scan<unsigned long long>(w, sm.wl, lane, warp, &zk);
+  unsigned long long target = zk + 1ull;  // p == 1: keep all of K
+  if (rp.use_p) {
+    target = mul_fx(zk, rp.p, true);
+    if (target < 1ull) target = 1ull;
+    if (target > zk) target = zk;
+  }
+  const bool kept = in_k && before < target;
+  const int s = block_max_int(kept ? tid + 1 : 0, sm.wi, lane, warp);  // S = the first s of the order
+  // ---- draw in index order over S: entry t goes to position pos_t.
+  unsigned long long* wpos = sm.scan;  // the candidate ids are consumed
+  int32_t* ipos = reinterpret_cast<int32_t*>(sm.hhi);
+  group_sync();
+  if (kept) {
+    int pos = 0;
+    for (int u = 0; u < s; ++u) pos += l_idx[sorted[u]] < xi ? 1 : 0;
+    wpos[pos] = w;
+    ipos[pos] = xi;
+  }
+  group_sync();
+  const unsigned long long wp = tid < s ? wpos[tid] : 0ull;
+  unsigned long long zs;
+  const unsigned long long bp =
+      block_exclusive_scan<unsigned long long>(wp, sm.wl, lane, warp, &zs);
+  const unsigned long long tdraw = mul_fx(zs, rp.u, false);
+  const int hit = block_min_int(
+      (tid < s && wp > 0 && tdraw >= bp && tdraw < bp + wp) ? tid : INT_MAX, sm.wi, lane, warp);
+  const int lastw = block_max_int((tid < s && wp > 0) ? tid : -1, sm.wi, lane, warp);
+  const int pstar = hit != INT_MAX ? hit : lastw;
+  if (tid == 0) {
+    const int tok = pstar >= 0 ? ipos[pstar] : -1;
+    emit(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
+  }
+  if (q_row != nullptr) {
+    const float zf = block_sum<float>(kept ? wf : 0.0f, sm.wt, lane, warp);
+    if (kept) q_row[xi] = wf / zf;
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------- histogram finish (H)
 
 // Chunk r counted its elements per 16-bit key over the kHistKeys keys below
-// a_r = gather[r].i0, the key of its maximum: h16[r * kHistKeys + d] is the
-// count of key a_r - d.  Merged key i (0 = the row maximum, key A - i) has
-// count sum_r h_r[i - (A - a_r)]; every element within kHistKeys keys of the
-// row maximum is counted in its chunk (a_r <= A).
+// a_r = its summary's i0, the key of its maximum: 16-bit count d of its
+// histogram is the count of key a_r - d.  Merged key i (0 = the row maximum,
+// key A - i) has count sum_r h_r[i - (A - a_r)]; every element within
+// kHistKeys keys of the row maximum is counted in its chunk (a_r <= A).
 //
 // The finisher settles top-k (by count) and top-p (by fixed-point mass)
 // exactly on the merged keys: keys i < is are wholly in the kept set S, the
 // first rs members (in index order) of key is are in it too.  It then picks
-// the chunk holding the draw from per-chunk masses of S, re-reads that chunk
-// into registers and finds the token with one pass of per-vector sums.
-// Returns false, having emitted nothing, when a cut lies below the merged
-// window; the caller then runs the exact fallback.
+// the chunk holding the draw from per-chunk masses of S, stages that chunk
+// and finds the token with one pass of per-vector sums.  Returns false,
+// having emitted nothing, when a cut lies below the merged window; the
+// caller then runs the exact fallback.
 template <int NV, bool VEC>
 __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& sm, const Ctx& c,
-                                            const uint32_t* hist, unsigned long long* table,
+                                            const ChunkSlot* recs, unsigned long long* table,
                                             uint4* stage, int row, const RowParams& rp, float m,
-                                            float zrow, float* q_row) {
+                                            const WriteBack& wb, float* q_row) {
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   const int C = static_cast<int>(c.csize);
   const int V = P.V;
   const int k = rp.k;
   const bool topk = k < V;
-  const uint16_t* h16 = reinterpret_cast<const uint16_t*>(hist);
   const uint32_t A = key16(m);
-
+  // The row's total mass (for top-p without top-k), from the warp records.
+  float zrow = 0.0f;
+  if (!topk) {
+    float mw = 0.0f;
+    if (tid < C * kWarps) {
+      const float wmax = recs[tid / kWarps].wm[tid % kWarps];
+      if (wmax > -INFINITY) mw = recs[tid / kWarps].wz[tid % kWarps] * ex2((wmax - m) * rp.c2);
+    }
+    zrow = block_sum<float>(mw, sm.wt, lane, warp);
+  }
   // ---- merged counts and fixed-point weights; thread t holds keys 4t .. 4t + 3.
   uint32_t cnt[4] = {0u, 0u, 0u, 0u};
 #pragma unroll 1
   for (int r = 0; r < C; ++r) {
-    const uint32_t delta = A - static_cast<uint32_t>(sm.gather[r].i0);
+    const uint32_t delta = A - static_cast<uint32_t>(recs[r].s.i0);
+    const uint16_t* h16 = reinterpret_cast<const uint16_t*>(recs[r].hist);
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const uint32_t i = static_cast<uint32_t>(4 * tid + jj);
-      if (i >= delta) cnt[jj] += h16[r * kHistKeys + (i - delta)];
+      if (i >= delta) cnt[jj] += h16[i - delta];
     }
   }
   unsigned long long wfx[4];
@@ -90,12 +458,10 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
         block_exclusive_scan<unsigned long long>(local, sm.wl, lane, warp, &zk);
     unsigned long long target;
     if (topk) {
-      target = static_cast<unsigned long long>(
-          ceil(static_cast<double>(zk) * static_cast<double>(rp.p)));
+      target = mul_fx(zk, rp.p, true);
       if (target > zk) target = zk;
     } else {
-      target = static_cast<unsigned long long>(
-          ceil(static_cast<double>(zrow) * kMassScaleD * static_cast<double>(rp.p)));
+      target = mul_fx(fx40(zrow), rp.p, true);
       if (zk < target) return false;  // the top-p cut lies below the window
     }
     if (target < 1) target = 1;
@@ -112,7 +478,7 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     }
     if (cand != INT_MAX) {
       // Members j of the cut key are kept iff run + j * w < target (one owner).
-      unsigned long long need = wc == 0 ? ~0ull : (rem + wc - 1) / wc;
+      unsigned long long need = wc == 0 ? ~0ull : ceil_div_small(rem, wc);
       if (cand == ik && need > rk) need = rk;
       sm.bl[1] = need;
     }
@@ -123,15 +489,16 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   const unsigned long long wcut = table[is];
   // ---- per-chunk mass of S above the cut key and the cut key's members.
   for (int r = warp; r < C; r += kWarps) {
-    const uint32_t delta = A - static_cast<uint32_t>(sm.gather[r].i0);
+    const uint32_t delta = A - static_cast<uint32_t>(recs[r].s.i0);
+    const uint16_t* h16 = reinterpret_cast<const uint16_t*>(recs[r].hist);
     unsigned long long part = 0;
     for (int i = lane; i < is; i += 32) {
-      if (static_cast<uint32_t>(i) >= delta) part += h16[r * kHistKeys + (i - delta)] * table[i];
+      if (static_cast<uint32_t>(i) >= delta) part += h16[i - delta] * table[i];
     }
     part = warp_sum_u64(part);
     if (lane == 0) {
       sm.cmass[r][0] = part;
-      sm.ties[r] = static_cast<uint32_t>(is) >= delta ? h16[r * kHistKeys + (is - delta)] : 0u;
+      sm.ties[r] = static_cast<uint32_t>(is) >= delta ? h16[is - delta] : 0u;
     }
   }
   group_sync();
@@ -147,8 +514,7 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     const unsigned long long mr = v ? sm.cmass[lane][0] + kept * wcut : 0ull;
     const unsigned long long incl = warp_inclusive_scan(mr, lane);
     const unsigned long long zs = __shfl_sync(kFull, incl, 31);
-    unsigned long long tdraw =
-        static_cast<unsigned long long>(static_cast<double>(rp.u) * static_cast<double>(zs));
+    unsigned long long tdraw = mul_fx(zs, rp.u, false);
     if (tdraw >= zs) tdraw = zs - 1;  // zs >= the row maximum's own weight > 0
     const unsigned bal = __ballot_sync(kFull, v && tdraw < incl);
     const int cstar = bal ? __ffs(bal) - 1 : C - 1;
@@ -166,8 +532,8 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   const uint32_t kept_c = sm.cnt[cstar];
   // In a chunk, the mass of S before a position is the mass above the cut
   // key plus wcut * min(cut-key members so far, kept): the first kept
-  // members count, later ones do not.  The histograms are consumed: the
-  // chunk is staged over them.
+  // members count, later ones do not.  The records are consumed: the chunk
+  // is staged over them.
   auto above_and_ties = [&](const uint4 v4, int e0, unsigned long long* a, uint32_t* t) {
     const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
     unsigned long long s = 0;
@@ -274,9 +640,9 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
       if (sel < 0) sel = last;
     }
     const int tok = __shfl_sync(kFull, sel, ls);
-    if (lane == 0) emit_token(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st);
+    if (lane == 0) emit(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
   }
-  if (qstar < 0 && tid == 0) emit_token(P, row, -1, rp.st | kStNonFinite);
+  if (qstar < 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
   if (q_row != nullptr) {
     // Debug output: q over every chunk; a cut-key member is kept when its
     // rank among the chunk's members is below kept_r.
@@ -324,113 +690,6 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   return true;
 }
 
-// ----------------------------------------------------------------- plain finish (P)
-
-// No filter: the draw is over the whole row.  The leader picks the chunk and
-// the warp from the CTAs' per-warp masses; that warp re-reads its slice of
-// the chunk (one batch of loads) and finds the token.
-template <bool BF16, int NV, bool VEC>
-__device__ __forceinline__ void leader_finish_plain(const SampleParams& P, SampleSmem& sm,
-                                                    const Ctx& c, int row, float u, float m,
-                                                    float c2, int st, float* q_row) {
-  using L = Layout<BF16>;
-  const int tid = c.tid, lane = c.lane, warp = c.warp;
-  const int C = static_cast<int>(c.csize);
-  const int V = P.V;
-  if (tid == 0) {
-    auto wmass = [&](int r, int w) {
-      const float mw = sm.gwm[r][w];
-      return mw > -INFINITY ? sm.gwz[r][w] * ex2((mw - m) * c2) : 0.0f;
-    };
-    float zrow = 0.0f;
-    for (int r = 0; r < C; ++r) {
-      for (int w = 0; w < kWarps; ++w) zrow += wmass(r, w);
-    }
-    float target = u * zrow;
-    if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
-    int rstar = -1, wstar = -1, rlast = -1, wlast = -1;
-    float tau = 0.0f, cum = 0.0f;
-    for (int r = 0; r < C; ++r) {
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = wmass(r, w);
-        if (rstar < 0 && mw > 0.0f && target < cum + mw) {
-          rstar = r;
-          wstar = w;
-          tau = target - cum;
-        }
-        if (mw > 0.0f) {
-          rlast = r;
-          wlast = w;
-        }
-        cum += mw;
-      }
-    }
-    if (rstar < 0) {
-      rstar = rlast;
-      wstar = wlast;
-      tau = INFINITY;
-    }
-    sm.bi[0] = rstar;
-    sm.bi[1] = wstar;
-    sm.bf4[0] = tau;
-    sm.bf4[1] = zrow;
-  }
-  group_sync();
-  const int rstar = sm.bi[0];
-  const int wstar = sm.bi[1];
-  const float tau = sm.bf4[0];
-  const float zrow = sm.bf4[1];
-  if (warp == wstar && rstar >= 0) {
-    uint32_t d[NV][4];
-    load_chunk<BF16, NV, VEC>(P, row, rstar, warp, lane, d);
-    int found = -1, lastpos = -1;
-    float a = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      const int e0 = vec_base<BF16, NV>(rstar, warp, lane, j);
-      float sj = 0.0f;
-      int lj = -1;
-      for_vec<BF16>(d[j], e0, [&](float x, int e) {
-        const float w = e < V ? weight(x, m, c2) : 0.0f;
-        sj += w;
-        if (w > 0.0f) lj = e;
-      });
-      const unsigned has = __ballot_sync(kFull, lj >= 0);
-      if (has != 0u) lastpos = __shfl_sync(kFull, lj, 31 - __clz(has));
-      const float incl = warp_inclusive_scan(sj, lane);
-      const float tot = __shfl_sync(kFull, incl, 31);
-      if (found < 0 && tau < a + tot) {
-        const unsigned bal = __ballot_sync(kFull, tau < a + incl);
-        const int lx = bal ? __ffs(bal) - 1 : 31;
-        int sel = -1;
-        if (lane == lx) {
-          float run = a + incl - sj;
-          for_vec<BF16>(d[j], e0, [&](float x, int e) {
-            const float w = e < V ? weight(x, m, c2) : 0.0f;
-            run += w;
-            if (sel < 0 && w > 0.0f && tau < run) sel = e;
-          });
-          if (sel < 0) sel = lj;
-        }
-        found = __shfl_sync(kFull, sel, lx);
-        if (found < 0) found = lastpos;
-      }
-      a += tot;
-    }
-    if (found < 0) found = lastpos;  // rounding: the warp's last token with mass
-    if (lane == 0) emit_token(P, row, found, found < 0 ? (st | kStNonFinite) : st);
-  }
-  if (rstar < 0 && tid == 0) emit_token(P, row, -1, st | kStNonFinite);
-  if (q_row != nullptr) {
-    const float inv = 1.0f / zrow;
-    for (int r = 0; r < C; ++r) {
-      for_chunk<BF16, NV, VEC>(P, row, r, warp, lane, [&](float x, int e) {
-        if (e < V) q_row[e] = weight(x, m, c2) * inv;
-      });
-    }
-  }
-}
-
 // ----------------------------------------------------------------- the finish kernel
 
 // One CTA of kThreads threads per row.  Launched as a programmatic dependent
@@ -438,14 +697,12 @@ __device__ __forceinline__ void leader_finish_plain(const SampleParams& P, Sampl
 // completed and its writes are visible.
 template <bool BF16, int NV, bool VEC>
 __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_constant__ SampleParams P) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ SampleSmem sm;
+  __shared__ __align__(8) unsigned long long rec_bar;
   extern __shared__ __align__(128) unsigned char dyn[];
-  float* tm = reinterpret_cast<float*>(dyn + kFinOffTm);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(dyn + kFinOffHist);
+  ChunkSlot* recs = reinterpret_cast<ChunkSlot*>(dyn);
   float* l_val = reinterpret_cast<float*>(dyn + kFinOffList);
-  int32_t* l_idx = reinterpret_cast<int32_t*>(dyn + kFinOffList + kListCap * 4);
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(dyn + kFinOffCnt);
+  int32_t* l_idx = reinterpret_cast<int32_t*>(dyn + kFinOffList + kFinListCap * 4);
   unsigned long long* table = reinterpret_cast<unsigned long long*>(dyn + kFinOffTable);
 
   const int row = blockIdx.x;
@@ -458,260 +715,101 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
   c.crank = 0;
   c.csize = static_cast<uint32_t>(C);
   const int tid = c.tid;
-  const ChunkSlot* slots = static_cast<const ChunkSlot*>(P.workspace) + static_cast<size_t>(row) * C;
-  // The row's records in one batch of 16-byte asynchronous copies:
-  // summaries and per-warp values into sm, thread maxima into tm, count
-  // histograms into hist.  The row parameters load meanwhile.
-  {
-    const char* src = reinterpret_cast<const char*>(slots);
-    for (int pc = tid; pc < C * kSlotPieces; pc += kThreads) {
-      const int r = pc / kSlotPieces;
-      const int off = (pc - r * kSlotPieces) * 16;
-      char* dst;
-      if (off < kSlotOffWm) {
-        dst = reinterpret_cast<char*>(&sm.gather[r]);
-      } else if (off < kSlotOffWz) {
-        dst = reinterpret_cast<char*>(&sm.gwm[r][0]) + (off - kSlotOffWm);
-      } else if (off < kSlotOffTmax) {
-        dst = reinterpret_cast<char*>(&sm.gwz[r][0]) + (off - kSlotOffWz);
-      } else if (off < kSlotOffHist) {
-        dst = reinterpret_cast<char*>(tm + r * kThreads) + (off - kSlotOffTmax);
-      } else {
-        dst = reinterpret_cast<char*>(hist + r * kHistWords) + (off - kSlotOffHist);
-      }
-      cp_async16(dst, src + static_cast<size_t>(pc) * 16);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(&rec_bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The row's records in one bulk copy (they are contiguous), completing on
+  // rec_bar; the row parameters and write-back coordinates load meanwhile.
+  const uint32_t rec_bytes = static_cast<uint32_t>(C) * static_cast<uint32_t>(kChunkSlotBytes);
+  if (tid == 0) {
+    const char* src = reinterpret_cast<const char*>(ws_records(P) + static_cast<size_t>(row) * C);
+    mbar_arrive_expect_tx(bar, rec_bytes);
+    for (uint32_t off = 0; off < rec_bytes; off += 16384u) {
+      bulk_copy_g2s(dyn + off, src + off, min(16384u, rec_bytes - off), bar);
     }
   }
   const RowParams rp = row_params<BF16, NV>(P, row, C);
+  const WriteBack wb = load_write_back(P, row);
+  const uint32_t seq = __ldcg(&ws_header(P)->calls);  // the stream kernel's call number
   float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
-  cp_async_wait_all();
-  group_sync();
-  uint32_t flags = 0;
-  float m = -INFINITY;
-  for (int r = 0; r < C; ++r) {
-    flags |= sm.gather[r].u0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) m = fmax_nan(m, sm.gwm[r][w]);
+  group_sync();  // the barrier's initialisation is visible to every waiter
+  bool landed = mbar_try_wait(bar, 0u);
+  if (!landed) {
+    const long long t0 = globaltimer_ns();
+    while (!(landed = mbar_try_wait(bar, 0u))) {
+      if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
   }
-  if (flags & 2u) {
-    if (tid == 0) emit_token(P, row, -1, rp.st | kStTimeout);
+  if (!__syncthreads_and(landed ? 1 : 0)) {
+    // The copy did not land: nothing here is trusted, and the shared memory
+    // must outlive the copy, so wait for it (bounded) before leaving.
+    if (tid == 0) {
+      emit(P, row, -1, rp.st | kStTimeout, wb);
+      const long long t0 = globaltimer_ns();
+      while (!mbar_try_wait(bar, 0u)) {
+        if (globaltimer_ns() - t0 > kWaitNs) break;
+      }
+    }
     return;
   }
+  const RowHead head = row_head(recs, C, seq, sm, c);
+  if (head.stale) {
+    if (tid == 0) emit(P, row, -1, rp.st | kStTimeout, wb);
+    return;
+  }
+  const float m = head.m;
   if (rp.kind == kKindG) {
-    // ---- greedy: the first (chunk, warp) in index order holding the row
-    // maximum; its warp slice is re-read to find the first index.
-    if (m != m) {
-      if (tid == 0) emit_token(P, row, -1, kStNonFinite | rp.st);
+    // ---- greedy: in the first (chunk, warp) holding the row maximum, the
+    // lanes whose thread maximum is m re-read their vectors (one batch of
+    // loads) and the first index holding m wins.
+    if (head.nan) {
+      if (tid == 0) emit(P, row, -1, kStNonFinite | rp.st, wb);
       return;
     }
-    int first = INT_MAX;
-    for (int i = tid; i < C * kWarps; i += kThreads) {
-      if (sm.gwm[i / kWarps][i % kWarps] == m) first = min(first, i);
+    const int r = head.first / kWarps, w = head.first % kWarps;
+    const unsigned lanes = __ballot_sync(kFull, recs[r].tmax[w * 32 + c.lane] == m);
+    const int nl = __popc(lanes);
+    int idx = INT_MAX;
+    for (int t = tid; t < nl * NV; t += kThreads) {
+      const int l = static_cast<int>(__fns(lanes, 0u, t / NV + 1));
+      const int e0 = vec_base<BF16, NV>(r, w, l, t % NV);
+      uint32_t w4[4];
+      load_vec<BF16, NV, VEC>(P, row, e0, w4);
+      for_vec<BF16>(w4, e0, [&](float x, int e) {
+        if (x == m && e < V) idx = min(idx, e);
+      });
     }
-    first = block_min_int(first, sm.wi, c.lane, c.warp);
-    if (c.warp == 0) {
-      // One batch of loads for the warp's whole slice, then the first match
-      // in index order (vector j, then lane, then element).
-      const int r = first / kWarps, w = first % kWarps;
-      uint32_t d[NV][4];
-      load_chunk<BF16, NV, VEC>(P, row, r, w, c.lane, d);
-      int idx = INT_MAX;
-#pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        int mine = INT_MAX;
-        for_vec<BF16>(d[j], vec_base<BF16, NV>(r, w, c.lane, j), [&](float x, int e) {
-          if (x == m && e < V && mine == INT_MAX) mine = e;
-        });
-        const int jm = __reduce_min_sync(kFull, mine);
-        if (idx == INT_MAX) idx = jm;
-      }
-      if (c.lane == 0) {
-        emit_token(P, row, idx, rp.st);
-        if (q_row != nullptr) q_row[idx] = 1.0f;
-      }
+    idx = block_min_int(idx, sm.wi, c.lane, c.warp);
+    if (tid == 0) {
+      const int tok = idx == INT_MAX ? -1 : idx;
+      emit(P, row, tok, tok < 0 ? (kStNonFinite | rp.st) : rp.st, wb);
+      if (q_row != nullptr && tok >= 0) q_row[tok] = 1.0f;
     }
     return;
   }
-  if (m != m || m == INFINITY || m == -INFINITY) {
+  if (head.nan || m == INFINITY || m == -INFINITY) {
     const int est = (m == -INFINITY) ? kStAllNegInf : kStNonFinite;
-    if (tid == 0) emit_token(P, row, -1, est | rp.st);
+    if (tid == 0) emit(P, row, -1, est | rp.st, wb);
+    return;
+  }
+  if (rp.kind == kKindP) {
+    finish_plain<BF16, NV, VEC>(P, sm, c, recs, row, rp, m, wb, q_row);
     return;
   }
   if (rp.kind == kKindK) {
-    // ---- top-k.  theta = the k-th largest thread maximum of the row: at
-    // least k elements are >= theta, so every element of the top-k is >=
-    // theta and lies in a thread whose maximum is >= theta.  Those threads'
-    // vectors are re-read (an L2 hit); their elements >= theta form the
-    // candidate list, in index order.
-    const int nT = C * kThreads;
-    // theta: count the thread maxima per 16-bit key below the row maximum
-    // (bucket i = key(m) - key; keys beyond 255 share the last bucket) and
-    // take the key where the count from the top reaches k.  For bf16 rows
-    // this is the exact k-th largest thread maximum when it lies within 256
-    // values of the maximum; otherwise (and for fp32 rows) a lower bound on
-    // it, which is still valid: at least k thread maxima are >= theta.
-    const uint32_t km = key16(m);
-    sm.hlo[tid] = 0u;
+    if (finish_topk<BF16, NV, VEC>(P, sm, c, recs, l_val, l_idx, row, rp, m, wb, q_row)) return;
     group_sync();
-    for (int i = tid; i < nT; i += kThreads) {
-      const float t = tm[i];
-      if (t == t) {
-        const uint32_t kt = key16(t);
-        atomicAdd(&sm.hlo[kt >= km ? 0u : min(km - kt, 255u)], 1u);
-      }
-    }
-    group_sync();
-    {
-      // Inclusive prefix from the top: bucket tid counts keys km - tid.
-      const uint32_t h = sm.hlo[tid];
-      uint32_t tot;
-      const uint32_t before = block_exclusive_scan<uint32_t>(h, sm.wu, c.lane, c.warp, &tot);
-      if (before < static_cast<uint32_t>(rp.k) && before + h >= static_cast<uint32_t>(rp.k)) {
-        sm.bi[1] = tid;
-      }
-      if (tid == 0 && tot < static_cast<uint32_t>(rp.k)) sm.bi[1] = -1;
-    }
-    group_sync();
-    const int bk = sm.bi[1];
-    group_sync();
-    // Bucket bk < 255 holds only 16-bit key km - bk: the smallest value with
-    // that key (low 16 bits of the 32-bit key cleared) is the exact k-th
-    // largest for bf16 and a lower bound for fp32.  Past the last bucket the
-    // exact select runs on all thread maxima.
-    float theta = -INFINITY;
-    if (bk >= 0 && bk < 255) {
-      theta = key16_float(km - static_cast<uint32_t>(bk));
-    } else if (bk == 255) {
-      unsigned long long rk;
-      theta = list_select<false>(tm, nT, [](int) { return true; }, [](int) { return 1ull; },
-                                 static_cast<unsigned long long>(rp.k), sm, c, &rk);
-    }
-    // Candidate lanes of each (chunk, warp) pair q = chunk * kWarps + warp;
-    // vector (q, j, lane) of a candidate lane has rank
-    //   vbase[q] + j * popc(M_q) + popc(M_q below lane)
-    // among the candidate vectors, which is index order.
-    uint32_t* Mq = reinterpret_cast<uint32_t*>(sm.scan);     // kMaxChunks * kWarps <= 128
-    uint32_t* vbase = Mq + kMaxChunks * kWarps;              // ... and their bases
-    for (int q = c.warp; q < C * kWarps; q += kWarps) {
-      const unsigned mq = __ballot_sync(kFull, tm[q * 32 + c.lane] >= theta);
-      if (c.lane == 0) Mq[q] = mq;
-    }
-    group_sync();
-    if (tid == 0) {
-      uint32_t acc = 0;
-      for (int q = 0; q < C * kWarps; ++q) {
-        vbase[q] = acc;
-        acc += static_cast<uint32_t>(__popc(Mq[q])) * NV;
-      }
-      sm.bi[0] = static_cast<int32_t>(acc);
-    }
-    group_sync();
-    const int nvec = sm.bi[0];
-    if (nvec <= kMaxCandVecs && theta > -INFINITY) {
-      // Each thread takes candidate vectors v = tid + r * kThreads (at most
-      // kKeep kept in registers; more are re-read).
-      constexpr int kKeep = 4;
-      uint32_t keepv[kKeep][4];
-      auto decode = [&](int v, uint32_t (&w4)[4]) -> int {
-        // The pair q with vbase[q] <= v < vbase[q + 1] (binary search), then
-        // the vector j and the candidate lane within it.
-        int lo = 0, hi = C * kWarps - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (vbase[mid] <= static_cast<uint32_t>(v)) lo = mid;
-          else hi = mid - 1;
-        }
-        const int q = lo;
-        const uint32_t mq = Mq[q];
-        const int pc = __popc(mq);
-        const int off = v - static_cast<int>(vbase[q]);
-        const int j = off / pc;
-        const int lane_q = static_cast<int>(__fns(mq, 0u, off % pc + 1));
-        const int e0 = vec_base<BF16, NV>(q / kWarps, q % kWarps, lane_q, j);
-        load_vec<BF16, NV, VEC>(P, row, e0, w4);
-        return e0;
-      };
-      int keep_e0[kKeep];
-      auto count_vec = [&](int v, uint32_t (&w4)[4], int* e0_out) {
-        const int e0 = decode(v, w4);
-        uint32_t nc = 0;
-        for_vec<BF16>(w4, e0, [&](float x, int e) { nc += (e < V && x >= theta) ? 1u : 0u; });
-        cnt[v] = nc;
-        *e0_out = e0;
-      };
-#pragma unroll
-      for (int r = 0; r < kKeep; ++r) {
-        const int v = tid + r * kThreads;
-        if (v < nvec) count_vec(v, keepv[r], &keep_e0[r]);
-      }
-      for (int v = tid + kKeep * kThreads; v < nvec; v += kThreads) {
-        uint32_t w4[4];
-        int e0;
-        count_vec(v, w4, &e0);
-      }
-      group_sync();
-      // Exclusive prefix of the counts in vector order: contiguous segments.
-      const int per = (nvec + kThreads - 1) / kThreads;
-      const int i0 = min(nvec, tid * per), i1 = min(nvec, i0 + per);
-      uint32_t seg = 0;
-      for (int i = i0; i < i1; ++i) seg += cnt[i];
-      uint32_t total;
-      uint32_t run = block_exclusive_scan<uint32_t>(seg, sm.wu, c.lane, c.warp, &total);
-      for (int i = i0; i < i1; ++i) {
-        const uint32_t t = cnt[i];
-        cnt[i] = run;
-        run += t;
-      }
-      group_sync();
-      if (total <= static_cast<uint32_t>(kListCap)) {
-        auto place = [&](int v, const uint32_t (&w4)[4], int e0) {
-          uint32_t pos = cnt[v];
-          for_vec<BF16>(w4, e0, [&](float x, int e) {
-            if (e < V && x >= theta) {
-              l_val[pos] = x;
-              l_idx[pos] = e;
-              ++pos;
-            }
-          });
-        };
-#pragma unroll
-        for (int r = 0; r < kKeep; ++r) {
-          const int v = tid + r * kThreads;
-          if (v < nvec) place(v, keepv[r], keep_e0[r]);
-        }
-        for (int v = tid + kKeep * kThreads; v < nvec; v += kThreads) {
-          uint32_t w4[4];
-          const int e0 = decode(v, w4);
-          place(v, w4, e0);
-        }
-        group_sync();
-        leader_finish_list(P, sm, c, l_val, l_idx, static_cast<int>(total), row, rp.k, rp.use_p,
-                           rp.p, m, rp.c2, rp.u, rp.st, q_row);
-        return;
-      }
-    }
-    // Pathological ties or -inf rows: more candidates than the list holds.
-  }
-  if (rp.kind == kKindP) {
-    leader_finish_plain<BF16, NV, VEC>(P, sm, c, row, rp.u, m, rp.c2, rp.st, q_row);
-    return;
   }
   if constexpr (BF16) {
     if (rp.kind == kKindH) {
-      float zrow = 0.0f;
-      if (rp.k == V) {
-        for (int r = 0; r < C; ++r) {
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            const float mw = sm.gwm[r][w];
-            if (mw > -INFINITY) zrow += sm.gwz[r][w] * ex2((mw - m) * rp.c2);
-          }
-        }
-      }
-      if (finish_hist<NV, VEC>(P, sm, c, hist, table, reinterpret_cast<uint4*>(dyn), row, rp, m,
-                               zrow, q_row)) {
+      if (finish_hist<NV, VEC>(P, sm, c, recs, table, reinterpret_cast<uint4*>(dyn), row, rp, m,
+                               wb, q_row)) {
         return;
       }
+      group_sync();
     }
   }
   leader_fallback<BF16>(P, sm, c, row, rp.k, rp.use_p, rp.p, rp.u, m, rp.c2, rp.st, q_row);

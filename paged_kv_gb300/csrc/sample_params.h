@@ -7,8 +7,19 @@
 namespace pkv {
 
 // Bytes of one workspace record (ChunkSlot in sample_common.cuh): a 16-byte
-// summary, 2 floats per warp, a float per thread and a 2 KB histogram.
-constexpr size_t kChunkSlotBytes = 16 + 64 + 256 * 4 + 2048;
+// summary, 4 words per warp, a float per thread and a 2 KB histogram.
+constexpr size_t kChunkSlotBytes = 16 + 128 + 256 * 4 + 2048;
+
+// The workspace starts with this header; the records follow it.  It must be
+// zero before the first call; every call leaves it ready for the next one.
+struct WorkspaceHeader {
+  uint32_t ticket;  // next item rank to hand out (stream kernel)
+  uint32_t done;    // stream CTAs finished in this call
+  uint32_t calls;   // calls completed; records of call n carry n + 1
+  uint32_t pad[61];
+};
+constexpr size_t kWorkspaceHeaderBytes = 256;
+static_assert(sizeof(WorkspaceHeader) == kWorkspaceHeaderBytes, "header size");
 
 struct SampleParams {
   const void* logits;        // [B, row_stride] fp32 or bf16
@@ -29,7 +40,7 @@ struct SampleParams {
   int32_t* status;           // device status word or nullptr
   int cta_chunk;             // elements of one chunk (one item of the stream kernel)
   int chunks;                // chunks per row
-  void* workspace;           // [B * chunks] ChunkSlot records (stream -> finish)
+  void* workspace;           // WorkspaceHeader, then [B * chunks] ChunkSlot records
 };
 
 }  // namespace pkv

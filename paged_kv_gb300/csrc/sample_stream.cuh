@@ -33,9 +33,8 @@ constexpr int stream_dyn_bytes() {
 
 // Reduces one chunk (registers d, the kernel's layout) to its workspace
 // record.  All threads of the group call it.  Every warp records its maximum;
-// greedy rows need nothing else (the finisher finds the first index), plain
-// rows add the warp's mass, top-k rows the warp's candidates, top-p rows a
-// count histogram of the chunk.
+// plain rows add the warp's mass, greedy and top-k rows the thread maxima,
+// top-p rows a count histogram of the chunk.
 template <bool BF16, int NV, bool VEC>
 __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& sm, const Ctx& c,
                                              uint32_t* hist, ChunkSlot* slot, int row, int chunk,
@@ -72,9 +71,10 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
     }
     const float zw = warp_sum(tmax > -INFINITY ? zt * ex2((tmax - wmax) * c2) : 0.0f);
     if (lane == 0) slot->wz[warp] = zw;
-  } else if (rp.kind == kKindK) {
+  } else if (rp.kind == kKindK || rp.kind == kKindG) {
     // ---- top-k: the thread maxima; the finisher bounds the row's k-th
     // value by the k-th largest of them and re-reads the few threads above.
+    // Greedy: the finisher re-reads the threads holding the row maximum.
     slot->tmax[tid] = tmax;
   }
   if constexpr (BF16) {
@@ -187,28 +187,21 @@ __device__ __forceinline__ void build_order(const SampleParams& P, uint16_t* ord
   __syncthreads();
 }
 
-// Rank of a group's item in round n: rounds of G ranks dealt to the groups
-// in alternating direction, so that the expensive ranks at the front of the
-// order spread evenly over the groups.  Monotone in n for every group.
-__device__ __forceinline__ int item_rank(int n, int G, int gid) {
-  return n * G + ((n & 1) ? (G - 1 - gid) : gid);
+// Row and chunk of item rank q (rows in cost order when `ordered`).
+__device__ __forceinline__ void item_of(int q, int C, bool ordered, const uint16_t* order, int* row,
+                                        int* chunk) {
+  const int r = q / C;
+  *row = ordered ? static_cast<int>(order[r]) : r;
+  *chunk = q - r * C;
 }
 
-// Rounds in which group gid has an item (ranks below `items`).
-__device__ __forceinline__ int group_rounds(int items, int G, int gid) {
-  const int full = items / G, rem = items % G;
-  const int at = (full & 1) ? (G - 1 - gid) : gid;
-  return full + (at < rem ? 1 : 0);
-}
-
-// Round of the group's i-th item: its rounds rotated by gid, so that the
-// groups meet the expensive front rounds at different times and their
-// compute overlaps the other groups' streaming.
-__device__ __forceinline__ int group_round(int i, int R, int gid) {
-  const int n = i + gid % R;
-  return n >= R ? n - R : n;
-}
-
+// Items are handed out one at a time from the workspace header's ticket
+// counter, so a group that meets an expensive item takes fewer of the
+// cheap ones.  The last CTA to finish resets the counters and advances the
+// call number, which every record of this call carries (wseq): the finish
+// kernel trusts a record only with the current number, so a record a group
+// could not fill (a copy that timed out) or left from an earlier call is
+// never read as valid.
 template <bool BF16, int NV, bool VEC>
 __global__ void __launch_bounds__(kStreamThreads, 1)
     stream_kernel(const __grid_constant__ SampleParams P) {
@@ -219,6 +212,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   __shared__ SampleSmem smg[kGroups];
   __shared__ __align__(8) unsigned long long full[kGroups][kStages];
   __shared__ __align__(8) unsigned long long empty[kGroups][kStages];
+  __shared__ int stage_item[kGroups][kStages];  // rank copied into the stage, -1: no more
+  __shared__ int group_item[kGroups];           // rank of the group's item (element-load path)
   __shared__ uint16_t order[kOrderRows];
   __shared__ unsigned long long order_sum[kStreamThreads / 32 + 1];
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -231,14 +226,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   const int C = P.chunks;
   const int V = P.V;
   const int items = P.B * C;
-  const int G = gridDim.x * kGroups;
-  const int gid = blockIdx.x * kGroups + group;
+  WorkspaceHeader* hdr = ws_header(P);
+  uint32_t seq = __ldcg(&hdr->calls) + 1u;  // never 0: 0 marks an untrusted record
+  if (seq == 0u) seq = 1u;
   unsigned char* ring = dyn + group * kStages * kStageBytes;
   uint64_t* fullb = reinterpret_cast<uint64_t*>(full[group]);
   uint64_t* emptyb = reinterpret_cast<uint64_t*>(empty[group]);
 
   if constexpr (VEC) {
-    // full[s]: the producer's expect-tx arrival plus the copy's bytes;
+    // full[s]: the producer's arrival (with the copy's bytes) completes it;
     // empty[s]: one arrival per consumer warp once its vectors are loaded.
     if (threadIdx.x == 0) {
       for (int g = 0; g < kGroups; ++g) {
@@ -258,15 +254,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   }
 
   if (producer) {
-    // ---- producer warp of the group (lane 0): bulk copies kStages items
-    // ahead, each into a stage its consumers have emptied.
+    // ---- producer warp of the group (lane 0): takes a ticket whenever a
+    // stage is free, publishes its rank in stage_item and bulk-copies the
+    // chunk; past the last item it publishes -1 with a plain arrival.
     if constexpr (VEC) {
       if ((threadIdx.x & 31) == 0) {
         const char* logits = static_cast<const char*>(P.logits);
-        int issued = 0;
-        const int R = group_rounds(items, G, gid);
-        for (int n = 0; n < R; ++n) {
-          const int q = item_rank(group_round(n, R, gid), G, gid);
+        int sent = -1, last_copy[kStages];
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) last_copy[s] = -1;
+        for (int n = 0;; ++n) {
           const int s = n % kStages;
           if (n >= kStages) {
             const uint32_t parity = static_cast<uint32_t>(n / kStages - 1) & 1u;
@@ -277,24 +274,37 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             }
             if (!ok) break;  // the consumers stopped: issue nothing more
           }
-          const int r = ordered ? static_cast<int>(order[q / C]) : q / C, ch = q % C;
+          const int q = static_cast<int>(atomicAdd(&hdr->ticket, 1u));
+          if (q >= items) {
+            stage_item[group][s] = -1;
+            mbar_arrive(&fullb[s]);
+            sent = n;
+            break;
+          }
+          int r, ch;
+          item_of(q, C, ordered, order, &r, &ch);
           const int e0 = ch * CHUNK;
           // Every chunk starts inside the row (the launch never makes an empty one).
           const uint32_t bytes = static_cast<uint32_t>(max(0, min(CHUNK, V - e0))) * L::ELT;
           const char* src = logits + (static_cast<size_t>(r) * static_cast<size_t>(P.row_stride) +
                                       static_cast<size_t>(e0)) * L::ELT;
+          stage_item[group][s] = q;
           mbar_arrive_expect_tx(&fullb[s], bytes);
           for (uint32_t off = 0; off < bytes; off += 16384u) {
             bulk_copy_g2s(ring + s * kStageBytes + off, src + off, min(16384u, bytes - off),
                           &fullb[s]);
           }
-          issued = n + 1;
+          last_copy[s] = n;
         }
         // Before the CTA's shared memory can go away, every issued copy must
-        // have landed: wait (bounded) for each stage's last phase.
-        for (int s = 0; s < kStages && s < issued; ++s) {
-          const int last = s + ((issued - 1 - s) / kStages) * kStages;  // last item in stage s
-          const uint32_t parity = static_cast<uint32_t>(last / kStages) & 1u;
+        // have landed: wait (bounded) for the last copy of each stage.  The
+        // stage that took the final -1 is skipped: its last copy was consumed
+        // before that phase began (and a completed later phase would alias
+        // the parity).
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) {
+          if (last_copy[s] < 0 || (sent >= 0 && s == sent % kStages)) continue;
+          const uint32_t parity = static_cast<uint32_t>(last_copy[s] / kStages) & 1u;
           const long long t0 = globaltimer_ns();
           while (!mbar_try_wait(&fullb[s], parity)) {
             if (globaltimer_ns() - t0 > kWaitNs) break;
@@ -302,73 +312,85 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         }
       }
     }
-    return;
-  }
-
-  // ---- consumers.
-  Ctx c;
-  c.tid = threadIdx.x % kThreads;
-  c.lane = c.tid & 31;
-  c.warp = c.tid >> 5;
-  c.csize = static_cast<uint32_t>(C);
-  SampleSmem& sm = smg[group];
-  uint32_t* hist =
-      reinterpret_cast<uint32_t*>(dyn + kGroups * kStages * kStageBytes) + group * kHistWords;
-  ChunkSlot* ws = static_cast<ChunkSlot*>(P.workspace);
-  bool timed_out = false;
-  const int R = group_rounds(items, G, gid);
-  for (int n = 0; n < R; ++n) {
-    const int q = item_rank(group_round(n, R, gid), G, gid);
-    const int row = ordered ? static_cast<int>(order[q / C]) : q / C, chunk = q % C;
-    c.crank = static_cast<uint32_t>(chunk);
-    ChunkSlot* slot = ws + (static_cast<size_t>(row) * C + chunk);
-    const RowParams rp = row_params<BF16, NV>(P, row, C);  // loads overlap the wait
-    uint32_t d[NV][4];
-    if constexpr (VEC) {
-      // Each warp waits for the stage on its own, loads its vectors and
-      // signals the producer; no group-wide barrier on the data path.
-      const int s = n % kStages;
-      const uint32_t parity = static_cast<uint32_t>(n / kStages) & 1u;
-      bool ok = false;
-      if (!timed_out) {
-        ok = mbar_try_wait(&fullb[s], parity);
+  } else {
+    // ---- consumers.
+    Ctx c;
+    c.tid = threadIdx.x % kThreads;
+    c.lane = c.tid & 31;
+    c.warp = c.tid >> 5;
+    c.csize = static_cast<uint32_t>(C);
+    SampleSmem& sm = smg[group];
+    uint32_t* hist =
+        reinterpret_cast<uint32_t*>(dyn + kGroups * kStages * kStageBytes) + group * kHistWords;
+    ChunkSlot* ws = ws_records(P);
+    bool trusted = true;  // this warp has seen every copy land
+    for (int n = 0;; ++n) {
+      uint32_t d[NV][4];
+      int q;
+      if constexpr (VEC) {
+        // Each warp waits for the stage on its own (bounded), reads the rank,
+        // loads its vectors and signals the producer; no group-wide barrier
+        // on the data path.  After a timeout the warp still reads the rank
+        // (written long before) and goes on, so that the group's barriers
+        // stay matched, but its records are marked untrusted.
+        const int s = n % kStages;
+        const uint32_t parity = static_cast<uint32_t>(n / kStages) & 1u;
+        bool ok = mbar_try_wait(&fullb[s], parity);
         if (!ok) {
           const long long t0 = globaltimer_ns();
           while (!(ok = mbar_try_wait(&fullb[s], parity))) {
             if (globaltimer_ns() - t0 > kWaitNs) break;
           }
         }
-      }
-      const uint4* sv = reinterpret_cast<const uint4*>(ring + s * kStageBytes);
+        if (!ok) trusted = false;
+        q = *static_cast<volatile int*>(&stage_item[group][s]);
+        if (q < 0) break;
+        int row, chunk;
+        item_of(q, C, ordered, order, &row, &chunk);
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + s * kStageBytes);
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        const int e0 = vec_base<BF16, NV>(chunk, c.warp, c.lane, j);
-        if (e0 < V) {
-          const uint4 v = sv[(c.warp * NV + j) * 32 + c.lane];
-          d[j][0] = v.x;
-          d[j][1] = v.y;
-          d[j][2] = v.z;
-          d[j][3] = v.w;
-        } else {
-          const uint32_t ninf = BF16 ? 0xff80ff80u : 0xff800000u;
-          d[j][0] = d[j][1] = d[j][2] = d[j][3] = ninf;
+        for (int j = 0; j < NV; ++j) {
+          const int e0 = vec_base<BF16, NV>(chunk, c.warp, c.lane, j);
+          if (e0 < V) {
+            const uint4 v = sv[(c.warp * NV + j) * 32 + c.lane];
+            d[j][0] = v.x;
+            d[j][1] = v.y;
+            d[j][2] = v.z;
+            d[j][3] = v.w;
+          } else {
+            const uint32_t ninf = BF16 ? 0xff80ff80u : 0xff800000u;
+            d[j][0] = d[j][1] = d[j][2] = d[j][3] = ninf;
+          }
         }
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(&emptyb[s]);
+      } else {
+        // Element loads: thread 0 of the group takes the ticket.
+        if (c.tid == 0) group_item[group] = static_cast<int>(atomicAdd(&hdr->ticket, 1u));
+        group_sync();
+        q = group_item[group];
+        group_sync();
+        if (q >= items) break;
+        int row, chunk;
+        item_of(q, C, ordered, order, &row, &chunk);
+        load_chunk<BF16, NV, false>(P, row, chunk, c.warp, c.lane, d);
       }
-      __syncwarp();
-      if (c.lane == 0) mbar_arrive(&emptyb[s]);
-      if (!ok) timed_out = true;
-    } else {
-      load_chunk<BF16, NV, false>(P, row, chunk, c.warp, c.lane, d);
+      int row, chunk;
+      item_of(q, C, ordered, order, &row, &chunk);
+      c.crank = static_cast<uint32_t>(chunk);
+      ChunkSlot* slot = ws + (static_cast<size_t>(row) * C + chunk);
+      const RowParams rp = row_params<BF16, NV>(P, row, C);
+      reduce_chunk<BF16, NV, VEC>(P, sm, c, hist, slot, row, chunk, rp, d);
+      if (c.lane == 0) slot->wseq[c.warp] = trusted ? seq : 0u;
     }
-    reduce_chunk<BF16, NV, VEC>(P, sm, c, hist, slot, row, chunk, rp, d);
-    if (timed_out && c.lane == 0) {
-      // A copy did not arrive: this and every later record of the warp is
-      // flagged (its data is not trusted).  The warp keeps going without
-      // waiting, so that the group's barriers stay matched.
-      Summary bad = {};
-      bad.u0 = 2u;
-      slot->s = bad;
-    }
+  }
+  // ---- the last CTA out resets the counters for the next call (the next
+  // kernel on the stream sees them once this grid has completed).
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(&hdr->done, 1u) == gridDim.x - 1) {
+    hdr->ticket = 0u;
+    hdr->done = 0u;
+    hdr->calls = seq;
   }
 }
 

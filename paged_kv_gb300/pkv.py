@@ -51,6 +51,8 @@ def load() -> ctypes.CDLL:
             lib.pkv_version.argtypes = []
             lib.pkv_sample_workspace_bytes.restype = sz
             lib.pkv_sample_workspace_bytes.argtypes = [i32, i32, i32]
+            lib.pkv_sample_workspace_init.restype = i32
+            lib.pkv_sample_workspace_init.argtypes = [vp, sz, vp]
             lib.pkv_sample_batch.restype = i32
             lib.pkv_sample_batch.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp,
                                              i64, i64, vp, vp, vp, vp, vp, sz, vp]
@@ -99,10 +101,6 @@ def _stream(stream, device) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def sample_workspace_bytes(B: int, V: int, dtype: torch.dtype) -> int:
-    return int(load().pkv_sample_workspace_bytes(B, V, PKV_BF16 if dtype == torch.bfloat16 else PKV_FP32))
-
-
 _workspaces = {}
 
 
@@ -112,15 +110,24 @@ def sample_workspace_bytes(B: int, V: int, dtype: torch.dtype) -> int:
     return int(load().pkv_sample_workspace_bytes(int(B), int(V), code))
 
 
+def sample_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    """pkv_sample_workspace_init: readies a new workspace (zeroes its header)."""
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous uint8 CUDA tensor")
+    _check(load().pkv_sample_workspace_init(workspace.data_ptr(), workspace.numel(),
+                                            _stream(stream, workspace.device)))
+
+
 def _workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A cached uint8 device buffer of at least ``nbytes`` (grown as needed).
+    """A cached, zero-initialised uint8 device buffer of at least ``nbytes``
+    (replaced by a larger one as needed).
 
     Calls on different streams of one device must pass their own workspace.
     """
     key = (device.type, device.index)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 
@@ -136,9 +143,9 @@ def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = Non
     """pkv_sample_batch: one int32 token per row of ``logits`` [B, V].
 
     ``logits`` is fp32 or bf16 with unit column stride (any row stride).
-    ``workspace`` (a uint8 CUDA tensor) defaults to a buffer cached per
-    device.  Returns ``out_tokens`` (allocated here if not given).  See
-    include/pkv.h.
+    ``workspace`` (a uint8 CUDA tensor, initialised once with
+    sample_workspace_init or zeroed) defaults to a buffer cached per device.
+    Returns ``out_tokens`` (allocated here if not given).  See include/pkv.h.
     """
     lib = load()
     if logits.dim() != 2 or not logits.is_cuda:

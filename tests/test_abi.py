@@ -32,11 +32,11 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_workspace():
     lib = pkv.load()
-    assert pkv.version() == 200
-    # One 3152-byte record per (row, chunk); the mixed batch's rows are 8
-    # chunks of 20480 bf16 logits.
-    assert lib.pkv_sample_workspace_bytes(256, 151936, 1) == 256 * 8 * 3152
-    assert lib.pkv_sample_workspace_bytes(1024, 256000, 1) == 1024 * 16 * 3152
+    assert pkv.version() == 300
+    # A 256-byte header, then one 3216-byte record per (row, chunk); the
+    # mixed batch's rows are 8 chunks of 20480 bf16 logits.
+    assert lib.pkv_sample_workspace_bytes(256, 151936, 1) == 256 + 256 * 8 * 3216
+    assert lib.pkv_sample_workspace_bytes(1024, 256000, 1) == 256 + 1024 * 16 * 3216
     assert lib.pkv_sample_workspace_bytes(0, 100, 1) == 0
     assert lib.pkv_sample_workspace_bytes(4, 0, 1) == 0
     assert lib.pkv_sample_workspace_bytes(4, 100, 7) == 0
@@ -54,6 +54,16 @@ def test_sample_batch_requires_a_workspace():
     assert rc == pkv.PKV_EINVAL and "workspace" in pkv.last_error()
     rc = lib.pkv_sample_batch(*common, ctypes.c_void_p(264), need, None)
     assert rc == pkv.PKV_EINVAL and "aligned" in pkv.last_error()
+
+
+def test_workspace_init_validates_before_any_launch():
+    lib = pkv.load()
+    assert lib.pkv_sample_workspace_init(None, 4096, None) == pkv.PKV_EINVAL
+    assert "NULL" in pkv.last_error()
+    assert lib.pkv_sample_workspace_init(ctypes.c_void_p(256), 255, None) == pkv.PKV_EINVAL
+    assert "header" in pkv.last_error()
+    assert lib.pkv_sample_workspace_init(ctypes.c_void_p(264), 4096, None) == pkv.PKV_EINVAL
+    assert "aligned" in pkv.last_error()
 
 
 def test_host_validation_launches_nothing():
