@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             }
             if (!ok) break;  // the consumers stopped: issue nothing more
           }
-          const int q = static_cast<int>(atomicAdd(&hdr->ticket, 1u));
-          if (q >= items) {
+          const uint32_t t = atomicAdd(&hdr->ticket, 1u);
+          const int q = static_cast<int>(t);
+          if (t >= static_cast<uint32_t>(items)) {
             stage_item[group][s] = -1;
             mbar_arrive(&fullb[s]);
             sent = n;
@@ -366,7 +367,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         if (c.lane == 0) mbar_arrive(&emptyb[s]);
       } else {
         // Element loads: thread 0 of the group takes the ticket.
-        if (c.tid == 0) group_item[group] = static_cast<int>(atomicAdd(&hdr->ticket, 1u));
+        if (c.tid == 0) {
+          const uint32_t t = atomicAdd(&hdr->ticket, 1u);
+          group_item[group] = t >= static_cast<uint32_t>(items) ? items : static_cast<int>(t);
+        }
         group_sync();
         q = group_item[group];
         group_sync();

@@ -193,6 +193,52 @@ def test_deterministic_across_calls():
     np.testing.assert_array_equal(a, b)
 
 
+def test_workspace_header_is_checked_and_repaired():
+    # A workspace whose header was never initialised (here: a ticket counter
+    # past every item) hands out no chunks, so every row's records are stale:
+    # every token is -1 with status bit 64 and nothing is written back.  The
+    # call leaves the header reset, and the next call on it is exact.
+    w = workloads.mixed(B=24, V=32768)
+    B, V = w.logits.shape
+    ws = torch.zeros(pkv.sample_workspace_bytes(B, V, w.logits.dtype), dtype=torch.uint8,
+                     device=DEV)
+    hdr = ws[:16].view(torch.int32)
+    hdr[0] = 0x7FFFFF00  # ticket
+    hdr[2] = 7           # calls
+    L = w.logits.to(DEV)
+    args = (_d(w.temperature), _d(w.top_k), _d(w.top_p), _d(w.uniform))
+    pool = torch.zeros((B, 64), dtype=torch.int32, device=DEV)
+    rows = torch.arange(B, dtype=torch.int32)
+    cols = torch.zeros(B, dtype=torch.int64)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tok = pkv.sample_batch(L, *args, token_pool=pool, wb_rows=_d(rows), wb_cols=_d(cols),
+                           status=status, workspace=ws)
+    torch.cuda.synchronize()
+    assert (tok.cpu().numpy() == -1).all()
+    assert int(status.item()) & pkv.ST_TIMEOUT
+    assert int(pool.abs().sum().item()) == 0
+    assert hdr.cpu().tolist()[:3] == [0, 0, 8]
+    status.zero_()
+    tok = pkv.sample_batch(L, *args, status=status, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    check_sampler(w.logits, w.temperature, w.top_k, w.top_p, w.uniform, tok.cpu().numpy())
+
+
+def test_workspace_init_readies_a_dirty_buffer():
+    w = workloads.mixed(B=16, V=20000)
+    B, V = w.logits.shape
+    ws = torch.full((pkv.sample_workspace_bytes(B, V, w.logits.dtype),), 0xA5, dtype=torch.uint8,
+                    device=DEV)
+    pkv.sample_workspace_init(ws)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tok = pkv.sample_batch(w.logits.to(DEV), _d(w.temperature), _d(w.top_k), _d(w.top_p),
+                           _d(w.uniform), status=status, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    check_sampler(w.logits, w.temperature, w.top_k, w.top_p, w.uniform, tok.cpu().numpy())
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 
