@@ -143,6 +143,25 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
                      void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_sample_batch_noalloc -- pkv_sample_batch without a caller workspace.
+ *
+ * Same arguments, meaning and errors as pkv_sample_batch, minus the
+ * workspace: the sampler's scratch is a 16 MiB device array inside the
+ * library (one per device, zero at load time, left ready by every call), so
+ * the call allocates nothing anywhere.  Calls on one device share that array:
+ * they must not run concurrently (on different streams without ordering).
+ * Errors: those of pkv_sample_batch, plus PKV_EUNSUPPORTED when
+ * pkv_sample_workspace_bytes(B, V, dt) exceeds 16 MiB (e.g. B=1024,
+ * V=256000), and PKV_ECUDA when the array's address cannot be read.
+ */
+int pkv_sample_batch_noalloc(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                             const float* temperature, const int32_t* top_k, const float* top_p,
+                             const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                             int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                             const int64_t* wb_cols, float* probs_out, int32_t* status,
+                             pkv_stream_t stream);
+
+/*
  * pkv_writeback_tokens -- token_pool[rows[b], cols[b]] = tokens[b].
  *
  * The standalone form of the write-back in Scheduler._forward ("The scheduler

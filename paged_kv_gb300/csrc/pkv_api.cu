@@ -94,12 +94,15 @@ int pkv_sample_workspace_init(void* workspace, size_t workspace_bytes, pkv_strea
   return ok();
 }
 
-int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
-                     const float* temperature, const int32_t* top_k, const float* top_p,
-                     const float* uniform, int32_t* out_tokens, int32_t* token_pool,
-                     int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
-                     const int64_t* wb_cols, float* probs_out, int32_t* status,
-                     void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Host checks of pkv_sample_batch's arguments other than the workspace.
+int sample_args_error(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                      const float* temperature, const float* uniform, const int32_t* out_tokens,
+                      const int32_t* token_pool, int64_t pool_rows, int64_t pool_cols,
+                      const int32_t* wb_rows, const int64_t* wb_cols) {
   if (logits == nullptr) return fail(PKV_EINVAL, "logits is NULL");
   if (out_tokens == nullptr) return fail(PKV_EINVAL, "out_tokens is NULL");
   if (dt != PKV_FP32 && dt != PKV_BF16) return fail(PKV_EINVAL, "dtype %d is not fp32 or bf16", dt);
@@ -115,9 +118,49 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
       return fail(PKV_EINVAL, "token pool shape [%lld, %lld] is empty", (long long)pool_rows,
                   (long long)pool_cols);
   }
-  const bool bf16 = dt == PKV_BF16;
-  const int max_v = bf16 ? PKV_MAX_VOCAB_BF16 : PKV_MAX_VOCAB_FP32;
+  const int max_v = dt == PKV_BF16 ? PKV_MAX_VOCAB_BF16 : PKV_MAX_VOCAB_FP32;
   if (V > max_v) return fail(PKV_EUNSUPPORTED, "V=%d above the maximum %d", V, max_v);
+  return PKV_OK;
+}
+
+// Scratch of pkv_sample_batch_noalloc: a zero-initialised device array of
+// the library (one instance per device), used as the sampler workspace.
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(16) << 20;
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// The array's address on the current device, looked up once per device.
+cudaError_t static_scratch(void** out) {
+  static void* cache[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && cache[dev] != nullptr) {
+    *out = cache[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev] = p;
+  *out = p;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                     const float* temperature, const int32_t* top_k, const float* top_p,
+                     const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                     int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                     const int64_t* wb_cols, float* probs_out, int32_t* status,
+                     void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  const int bad = sample_args_error(logits, dt, B, V, row_stride, temperature, uniform,
+                                    out_tokens, token_pool, pool_rows, pool_cols, wb_rows,
+                                    wb_cols);
+  if (bad != PKV_OK) return bad;
+  const bool bf16 = dt == PKV_BF16;
   const size_t elt = bf16 ? 2 : 4;
   // The bulk-copy path needs 16-byte-aligned row starts and row lengths.
   const bool vec = aligned16(logits) && ((static_cast<uint64_t>(row_stride) * elt) % 16 == 0) &&
@@ -159,6 +202,30 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
                              : pkv::launch_sample_fp32(P, cfg, num_sms(), s);
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
   return ok();
+}
+
+int pkv_sample_batch_noalloc(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                             const float* temperature, const int32_t* top_k, const float* top_p,
+                             const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                             int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                             const int64_t* wb_cols, float* probs_out, int32_t* status,
+                             pkv_stream_t stream) {
+  const int bad = sample_args_error(logits, dt, B, V, row_stride, temperature, uniform,
+                                    out_tokens, token_pool, pool_rows, pool_cols, wb_rows,
+                                    wb_cols);
+  if (bad != PKV_OK) return bad;
+  const size_t need = pkv_sample_workspace_bytes(B, V, dt);
+  if (need > kStaticScratchBytes)
+    return fail(PKV_EUNSUPPORTED,
+                "B=%d, V=%d needs %zu bytes of scratch; the static scratch holds %zu "
+                "(pass a workspace to pkv_sample_batch)",
+                B, V, need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  const cudaError_t e = static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
+  return pkv_sample_batch(logits, dt, B, V, row_stride, temperature, top_k, top_p, uniform,
+                          out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols,
+                          probs_out, status, scratch, kStaticScratchBytes, stream);
 }
 
 int pkv_writeback_tokens(const int32_t* tokens, const int32_t* rows, const int64_t* cols, int B,

@@ -51,6 +51,9 @@ def load() -> ctypes.CDLL:
             lib.pkv_version.argtypes = []
             lib.pkv_sample_workspace_bytes.restype = sz
             lib.pkv_sample_workspace_bytes.argtypes = [i32, i32, i32]
+            lib.pkv_sample_batch_noalloc.restype = i32
+            lib.pkv_sample_batch_noalloc.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp,
+                                                     vp, i64, i64, vp, vp, vp, vp, vp]
             lib.pkv_sample_workspace_init.restype = i32
             lib.pkv_sample_workspace_init.argtypes = [vp, sz, vp]
             lib.pkv_sample_batch.restype = i32
@@ -180,6 +183,49 @@ def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = Non
         _dev(wb_rows, torch.int32, "wb_rows", B), _dev(wb_cols, torch.int64, "wb_cols", B),
         _dev(probs_out, torch.float32, "probs_out", B * V), _dev(status, torch.int32, "status", 1),
         workspace.data_ptr(), workspace.numel(), _stream(stream, logits.device))
+    _check(rc)
+    return out_tokens
+
+
+def sample_batch_noalloc(logits: torch.Tensor, temperature: Optional[torch.Tensor] = None,
+                         top_k: Optional[torch.Tensor] = None,
+                         top_p: Optional[torch.Tensor] = None,
+                         uniform: Optional[torch.Tensor] = None,
+                         out_tokens: torch.Tensor = None,
+                         token_pool: Optional[torch.Tensor] = None,
+                         wb_rows: Optional[torch.Tensor] = None,
+                         wb_cols: Optional[torch.Tensor] = None,
+                         probs_out: Optional[torch.Tensor] = None,
+                         status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pkv_sample_batch_noalloc: sample_batch with the library's own static
+    scratch; ``out_tokens`` (int32 [B], on the logits' device) is required, so
+    that nothing is allocated.  See include/pkv.h."""
+    lib = load()
+    if logits.dim() != 2 or not logits.is_cuda or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D CUDA tensor with unit column stride")
+    if logits.dtype == torch.bfloat16:
+        dcode = PKV_BF16
+    elif logits.dtype == torch.float32:
+        dcode = PKV_FP32
+    else:
+        raise TypeError(f"logits dtype {logits.dtype} is not fp32 or bf16")
+    if out_tokens is None:
+        raise ValueError("out_tokens is required")
+    B, V = logits.shape
+    pool_rows = pool_cols = 0
+    if token_pool is not None:
+        if token_pool.dim() != 2:
+            raise ValueError("token_pool must be 2-D")
+        pool_rows, pool_cols = token_pool.shape
+    rc = lib.pkv_sample_batch_noalloc(
+        logits.data_ptr(), dcode, B, V, logits.stride(0),
+        _dev(temperature, torch.float32, "temperature", B),
+        _dev(top_k, torch.int32, "top_k", B), _dev(top_p, torch.float32, "top_p", B),
+        _dev(uniform, torch.float32, "uniform", B), _dev(out_tokens, torch.int32, "out_tokens", B),
+        _dev(token_pool, torch.int32, "token_pool"), pool_rows, pool_cols,
+        _dev(wb_rows, torch.int32, "wb_rows", B), _dev(wb_cols, torch.int64, "wb_cols", B),
+        _dev(probs_out, torch.float32, "probs_out", B * V), _dev(status, torch.int32, "status", 1),
+        _stream(stream, logits.device))
     _check(rc)
     return out_tokens
 
