@@ -285,43 +285,50 @@ __device__ __forceinline__ bool finish_topk(const SampleParams& P, SampleSmem& s
   group_sync();
   const int ncand = sm.bi[4];
   if (ncand > kCandCap) return false;
-  for (int v = tid; v < ncand * NV; v += kThreads) {
-    const int i = cand[v / NV], j = v % NV;
-    const int ct = i % kThreads;
-    const int e0 = vec_base<BF16, NV>(i / kThreads, ct / 32, ct % 32, j);
-    uint32_t w4[4];
-    load_vec<BF16, NV, VEC>(P, row, e0, w4);
+  // Entries are packed sort keys: order key of the value above, the
+  // complement of the index below, so that a larger key comes first in
+  // (value desc, index asc).
+  unsigned long long* list = reinterpret_cast<unsigned long long*>(l_val);
+  auto append = [&](const uint32_t (&w4)[4], int e0) {
     for_vec<BF16>(w4, e0, [&](float x, int e) {
       if (e < V && x >= theta) {
         const int at = atomicAdd(&sm.bi[5], 1);
         if (at < kFinListCap) {
-          l_val[at] = x;
-          l_idx[at] = e;
+          list[at] = (static_cast<unsigned long long>(float_key(x)) << 32) |
+                     static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e));
         }
       }
     });
+  };
+  auto cand_vec = [&](int v) {
+    const int i = cand[v / NV];
+    const int ct = i % kThreads;
+    return vec_base<BF16, NV>(i / kThreads, ct / 32, ct % 32, v % NV);
+  };
+  for (int v = tid; v < ncand * NV; v += kThreads) {
+    const int e = cand_vec(v);
+    uint32_t w[4];
+    load_vec<BF16, NV, VEC>(P, row, e, w);
+    append(w, e);
   }
   group_sync();
   const int n = sm.bi[5];
   if (n > kFinListCap || n < k) return false;
-  // ---- ranks in (value desc, index asc); sorted[rank] for rank < k.
+  // ---- ranks: the number of entries with a larger key; sorted[rank] for rank < k.
   uint32_t* sorted = sm.hlo;
   for (int i = tid; i < n; i += kThreads) {
-    const float vi = l_val[i];
-    const int ii = l_idx[i];
+    const unsigned long long ki = list[i];
     int rank = 0;
-    for (int j = 0; j < n; ++j) {
-      const float vj = l_val[j];
-      rank += (vj > vi || (vj == vi && l_idx[j] < ii)) ? 1 : 0;
-    }
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) rank += list[j] > ki ? 1 : 0;
     if (rank < k) sorted[rank] = static_cast<uint32_t>(i);
   }
   group_sync();
   // ---- top-p inside K: thread t < k holds the t-th of the order.
   const bool in_k = tid < k;
-  const int me = in_k ? static_cast<int>(sorted[tid]) : 0;
-  const float xv = in_k ? l_val[me] : -INFINITY;
-  const int xi = in_k ? l_idx[me] : INT_MAX;
+  const unsigned long long kme = in_k ? list[sorted[tid]] : 0ull;
+  const float xv = in_k ? key_float(static_cast<uint32_t>(kme >> 32)) : -INFINITY;
+  const int xi = in_k ? static_cast<int>(0xffffffffu - static_cast<uint32_t>(kme)) : INT_MAX;
   const float wf = in_k ? weight(xv, m, rp.c2) : 0.0f;
   const unsigned long long w = in_k ? mass_fx(wf) : 0ull;
   unsigned long long zk;
@@ -338,10 +345,14 @@ __device__ __forceinline__ bool finish_topk(const SampleParams& P, SampleSmem& s
   // ---- draw in index order over S: entry t goes to position pos_t.
   unsigned long long* wpos = sm.scan;  // the candidate ids are consumed
   int32_t* ipos = reinterpret_cast<int32_t*>(sm.hhi);
+  int32_t* korder = reinterpret_cast<int32_t*>(sm.hlo);  // sorted[] is consumed
+  group_sync();
+  if (kept) korder[tid] = xi;
   group_sync();
   if (kept) {
     int pos = 0;
-    for (int u = 0; u < s; ++u) pos += l_idx[sorted[u]] < xi ? 1 : 0;
+#pragma unroll 4
+    for (int u = 0; u < s; ++u) pos += korder[u] < xi ? 1 : 0;
     wpos[pos] = w;
     ipos[pos] = xi;
   }
