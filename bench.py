@@ -1,9 +1,10 @@
 """Benchmark of the decode-step tail on GB300.
 
-One step = one pass of the whole hot path over one batch: pkv_sample_batch
-(temperature / top-k / top-p / inverse-CDF sampling with the fused token
-write-back) followed by pkv_fill_page_table (page allocation + page-table
-fill).  Workload: the mixed batch B=256, V=151936, bf16 logits N(0, 3^2),
+One step = one pass of the whole hot path over one batch: pkv_decode_tail,
+i.e. pkv_sample_batch (temperature / top-k / top-p / inverse-CDF sampling
+with the fused token write-back) and pkv_fill_page_table (page allocation +
+page-table fill) in one call, the fill running beside the sampler's second
+kernel.  Workload: the mixed batch B=256, V=151936, bf16 logits N(0, 3^2),
 every 3rd row greedy, pages of 16 tokens.  Logits rotate over enough
 buffers to exceed twice the L2 size, so every step reads them from HBM.
 
@@ -330,9 +331,8 @@ def run_ours(args):
     out = torch.empty(w.B, dtype=torch.int32, device=device)
 
     def step(i):
-        pkv.sample_batch(bufs[i % nbuf], t, k, p, u, out_tokens=out, token_pool=pool,
-                         wb_rows=rows, wb_cols=cols, status=status)
-        pkv.fill_page_table(cached, dev_len, tidx, w.page_size, free, pt, total, status)
+        pkv.decode_tail(bufs[i % nbuf], t, k, p, u, out, pool, rows, cols, cached, dev_len, tidx,
+                        w.page_size, free, pt, total, status)
 
     with ClockSampler(physical_gpu_index(local_rank)) as clocks:
         ms = timed_graph_steps(step, args.steps, args.warmup, dist_mod, device)
@@ -377,11 +377,10 @@ def run_ours(args):
         d_logits.copy_(h_logits, non_blocking=True)
         for n in d_in:
             d_in[n].copy_(h_in[n], non_blocking=True)
-        pkv.sample_batch(d_logits, d_in["temperature"], d_in["top_k"], d_in["top_p"],
-                         d_in["uniform"], out_tokens=out, token_pool=pool,
-                         wb_rows=d_in["wb_rows"], wb_cols=d_in["wb_cols"], status=status)
-        pkv.fill_page_table(d_in["cached_len"], d_in["device_len"], d_in["table_idx"],
-                            w.page_size, free, pt, total, status)
+        pkv.decode_tail(d_logits, d_in["temperature"], d_in["top_k"], d_in["top_p"],
+                        d_in["uniform"], out, pool, d_in["wb_rows"], d_in["wb_cols"],
+                        d_in["cached_len"], d_in["device_len"], d_in["table_idx"], w.page_size,
+                        free, pt, total, status)
         h_tok.copy_(out, non_blocking=True)
         h_total.copy_(total, non_blocking=True)
 
@@ -413,7 +412,7 @@ def run_ours(args):
                          "algorithmic_bytes": alg, "us_per_launch": round(us_k, 3)},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": 2 * args.steps,
             "timing": f"device value and roofline: CUDA graphs of {GRAPH_LEN} steps replayed; "
                       "e2e: host-launched calls",
             "clocks": clocks.summary(),

@@ -162,6 +162,29 @@ int pkv_sample_batch_noalloc(const void* logits, pkv_dtype dt, int B, int V, int
                              pkv_stream_t stream);
 
 /*
+ * pkv_decode_tail -- the whole decode-step tail in one call: pkv_sample_batch
+ * (with its fused write-back) and pkv_fill_page_table for the same step.
+ *
+ * The page fill has no dependence on the sampled tokens, so it runs in extra
+ * CTAs of the sampler's second kernel while the rows are being settled.  The
+ * arguments are those of the two calls (the sampler's B, V, logits ... and
+ * the fill's cached_len ... with its own batch size fill_B and the page
+ * table); `status` is shared; there is no probs_out.  Results, status bits
+ * and errors are exactly those of the two calls made one after the other.
+ * Host errors of either argument set return before anything is launched.
+ */
+int pkv_decode_tail(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                    const float* temperature, const int32_t* top_k, const float* top_p,
+                    const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                    int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                    const int64_t* wb_cols, int32_t* status, void* workspace,
+                    size_t workspace_bytes, const int32_t* cached_len, const int32_t* device_len,
+                    const int32_t* table_idx, int fill_B, int page_size,
+                    const int32_t* free_slots, int64_t free_count, int32_t* page_table,
+                    int64_t pt_rows, int64_t pt_cols, int64_t* total_out,
+                    pkv_stream_t stream);
+
+/*
  * pkv_writeback_tokens -- token_pool[rows[b], cols[b]] = tokens[b].
  *
  * The standalone form of the write-back in Scheduler._forward ("The scheduler

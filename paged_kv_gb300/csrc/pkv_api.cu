@@ -123,6 +123,41 @@ int sample_args_error(const void* logits, pkv_dtype dt, int B, int V, int64_t ro
   return PKV_OK;
 }
 
+// Host checks of the page-fill arguments; fills *F when they pass.
+int fill_args(const int32_t* cached_len, const int32_t* device_len, const int32_t* table_idx,
+              int B, int page_size, const int32_t* free_slots, int64_t free_count,
+              int32_t* page_table, int64_t pt_rows, int64_t pt_cols, int64_t* total_out,
+              int32_t* status, pkv::FillParams* F) {
+  if (B < 0 || B > PKV_MAX_FILL_BATCH)
+    return fail(PKV_EINVAL, "B=%d outside [0, %d]", B, PKV_MAX_FILL_BATCH);
+  if (page_size < 1) return fail(PKV_EINVAL, "page_size=%d < 1", page_size);
+  if (B > 0) {
+    if (cached_len == nullptr || device_len == nullptr || table_idx == nullptr ||
+        page_table == nullptr || (free_slots == nullptr && free_count > 0))
+      return fail(PKV_EINVAL, "NULL pointer argument");
+    if (free_count < 0 || free_count > INT32_MAX)
+      return fail(PKV_EINVAL, "free_count=%lld outside [0, 2^31)", (long long)free_count);
+    if (pt_rows < 1 || pt_cols < 1) return fail(PKV_EINVAL, "empty page table");
+  }
+  F->cached_len = cached_len;
+  F->device_len = device_len;
+  F->table_idx = table_idx;
+  F->B = B;
+  F->page_size = page_size;
+  F->free_slots = free_slots;
+  F->free_count = free_count;
+  F->page_table = page_table;
+  F->pt_rows = pt_rows;
+  F->pt_cols = pt_cols;
+  F->total_out = total_out;
+  F->status = status;
+  F->vec4 = (page_size % 4 == 0) && (pt_cols % 4 == 0) && aligned16(page_table);
+  return PKV_OK;
+}
+
+// Page-fill CTAs appended to the finish kernel by pkv_decode_tail.
+constexpr int kFusedFillCtas = 32;
+
 // Scratch of pkv_sample_batch_noalloc: a zero-initialised device array of
 // the library (one instance per device), used as the sampler workspace.
 constexpr size_t kStaticScratchBytes = static_cast<size_t>(16) << 20;
@@ -150,12 +185,17 @@ cudaError_t static_scratch(void** out) {
 
 extern "C" {
 
-int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
-                     const float* temperature, const int32_t* top_k, const float* top_p,
-                     const float* uniform, int32_t* out_tokens, int32_t* token_pool,
-                     int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
-                     const int64_t* wb_cols, float* probs_out, int32_t* status,
-                     void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// pkv_sample_batch, with an optional page fill run by extra finish CTAs.
+int sample_launch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                  const float* temperature, const int32_t* top_k, const float* top_p,
+                  const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                  int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                  const int64_t* wb_cols, float* probs_out, int32_t* status, void* workspace,
+                  size_t workspace_bytes, pkv_stream_t stream, const pkv::FillParams* fill) {
   const int bad = sample_args_error(logits, dt, B, V, row_stride, temperature, uniform,
                                     out_tokens, token_pool, pool_rows, pool_cols, wb_rows,
                                     wb_cols);
@@ -197,11 +237,28 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
   P.cta_chunk = cfg.chunk;
   P.chunks = cfg.chunks;
   P.workspace = workspace;
+  P.fill = fill != nullptr ? *fill : pkv::FillParams{};
+  P.fill_ctas = (fill != nullptr && fill->B > 0) ? kFusedFillCtas : 0;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = bf16 ? pkv::launch_sample_bf16(P, cfg, num_sms(), s)
                              : pkv::launch_sample_fp32(P, cfg, num_sms(), s);
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                     const float* temperature, const int32_t* top_k, const float* top_p,
+                     const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                     int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                     const int64_t* wb_cols, float* probs_out, int32_t* status,
+                     void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  return sample_launch(logits, dt, B, V, row_stride, temperature, top_k, top_p, uniform,
+                       out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols, probs_out,
+                       status, workspace, workspace_bytes, stream, nullptr);
 }
 
 int pkv_sample_batch_noalloc(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
@@ -278,9 +335,10 @@ int pkv_fill_page_table(const int32_t* cached_len, const int32_t* device_len,
                         const int32_t* free_slots, int64_t free_count, int32_t* page_table,
                         int64_t pt_rows, int64_t pt_cols, int64_t* total_out, int32_t* status,
                         pkv_stream_t stream) {
-  if (B < 0 || B > PKV_MAX_FILL_BATCH)
-    return fail(PKV_EINVAL, "B=%d outside [0, %d]", B, PKV_MAX_FILL_BATCH);
-  if (page_size < 1) return fail(PKV_EINVAL, "page_size=%d < 1", page_size);
+  pkv::FillParams F;
+  const int bad = fill_args(cached_len, device_len, table_idx, B, page_size, free_slots,
+                            free_count, page_table, pt_rows, pt_cols, total_out, status, &F);
+  if (bad != PKV_OK) return bad;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (B == 0) {
     if (total_out != nullptr) {
@@ -289,29 +347,33 @@ int pkv_fill_page_table(const int32_t* cached_len, const int32_t* device_len,
     }
     return ok();
   }
-  if (cached_len == nullptr || device_len == nullptr || table_idx == nullptr ||
-      page_table == nullptr || (free_slots == nullptr && free_count > 0))
-    return fail(PKV_EINVAL, "NULL pointer argument");
-  if (free_count < 0 || free_count > INT32_MAX)
-    return fail(PKV_EINVAL, "free_count=%lld outside [0, 2^31)", (long long)free_count);
-  if (pt_rows < 1 || pt_cols < 1) return fail(PKV_EINVAL, "empty page table");
-  pkv::FillParams F;
-  F.cached_len = cached_len;
-  F.device_len = device_len;
-  F.table_idx = table_idx;
-  F.B = B;
-  F.page_size = page_size;
-  F.free_slots = free_slots;
-  F.free_count = free_count;
-  F.page_table = page_table;
-  F.pt_rows = pt_rows;
-  F.pt_cols = pt_cols;
-  F.total_out = total_out;
-  F.status = status;
-  F.vec4 = (page_size % 4 == 0) && (pt_cols % 4 == 0) && aligned16(page_table);
   const cudaError_t e = pkv::launch_fill_page_table(F, num_sms(), s);
   if (e != cudaSuccess) return cuda_fail(e, "page-fill launch");
   return ok();
+}
+
+int pkv_decode_tail(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                    const float* temperature, const int32_t* top_k, const float* top_p,
+                    const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                    int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
+                    const int64_t* wb_cols, int32_t* status, void* workspace,
+                    size_t workspace_bytes, const int32_t* cached_len, const int32_t* device_len,
+                    const int32_t* table_idx, int fill_B, int page_size,
+                    const int32_t* free_slots, int64_t free_count, int32_t* page_table,
+                    int64_t pt_rows, int64_t pt_cols, int64_t* total_out,
+                    pkv_stream_t stream) {
+  pkv::FillParams F;
+  const int bad = fill_args(cached_len, device_len, table_idx, fill_B, page_size, free_slots,
+                            free_count, page_table, pt_rows, pt_cols, total_out, status, &F);
+  if (bad != PKV_OK) return bad;
+  if (fill_B == 0 && total_out != nullptr) {
+    const cudaError_t e =
+        cudaMemsetAsync(total_out, 0, sizeof(int64_t), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "total_out reset");
+  }
+  return sample_launch(logits, dt, B, V, row_stride, temperature, top_k, top_p, uniform,
+                       out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols, nullptr,
+                       status, workspace, workspace_bytes, stream, &F);
 }
 
 }  // extern "C"

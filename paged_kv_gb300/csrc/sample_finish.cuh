@@ -8,6 +8,7 @@
 // records alone), and the write-back coordinates are loaded at the start.
 #pragma once
 
+#include "page_fill.cuh"
 #include "sample_common.cuh"
 
 namespace pkv {
@@ -716,6 +717,13 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
   int32_t* l_idx = reinterpret_cast<int32_t*>(dyn + kFinOffList + kFinListCap * 4);
   unsigned long long* table = reinterpret_cast<unsigned long long*>(dyn + kFinOffTable);
 
+  if (static_cast<int>(blockIdx.x) >= P.B) {
+    // Fused page allocation and table fill: independent of the stream
+    // kernel's output, so these CTAs start at once (no griddepcontrol.wait).
+    fill::page_fill_cta<kThreads>(P.fill, reinterpret_cast<int32_t*>(dyn),
+                                  static_cast<int>(blockIdx.x) - P.B, P.fill_ctas);
+    return;
+  }
   const int row = blockIdx.x;
   const int C = P.chunks;
   const int V = P.V;

@@ -39,7 +39,7 @@ cudaError_t launch_pair(const SampleParams& P, int num_sms, cudaStream_t stream)
   cudaError_t e = cudaLaunchKernelEx(&cfg, skern, P);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t fcfg = {};
-  fcfg.gridDim = dim3(static_cast<unsigned>(P.B), 1, 1);
+  fcfg.gridDim = dim3(static_cast<unsigned>(P.B + P.fill_ctas), 1, 1);
   fcfg.blockDim = dim3(kThreads, 1, 1);
   fcfg.dynamicSmemBytes = kFinishDyn;
   fcfg.stream = stream;

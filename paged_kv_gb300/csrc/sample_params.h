@@ -4,6 +4,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "page_kernels.h"
+
 namespace pkv {
 
 // Bytes of one workspace record (ChunkSlot in sample_common.cuh): a 16-byte
@@ -41,6 +43,8 @@ struct SampleParams {
   int cta_chunk;             // elements of one chunk (one item of the stream kernel)
   int chunks;                // chunks per row
   void* workspace;           // WorkspaceHeader, then [B * chunks] ChunkSlot records
+  FillParams fill;           // page allocation + table fill run by extra finish CTAs
+  int fill_ctas;             // 0: no fused page fill
 };
 
 }  // namespace pkv

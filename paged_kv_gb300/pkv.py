@@ -54,6 +54,10 @@ def load() -> ctypes.CDLL:
             lib.pkv_sample_batch_noalloc.restype = i32
             lib.pkv_sample_batch_noalloc.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp,
                                                      vp, i64, i64, vp, vp, vp, vp, vp]
+            lib.pkv_decode_tail.restype = i32
+            lib.pkv_decode_tail.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp, i64,
+                                            i64, vp, vp, vp, vp, sz, vp, vp, vp, i32, i32, vp,
+                                            i64, vp, i64, i64, vp, vp]
             lib.pkv_sample_workspace_init.restype = i32
             lib.pkv_sample_workspace_init.argtypes = [vp, sz, vp]
             lib.pkv_sample_batch.restype = i32
@@ -226,6 +230,51 @@ def sample_batch_noalloc(logits: torch.Tensor, temperature: Optional[torch.Tenso
         _dev(wb_rows, torch.int32, "wb_rows", B), _dev(wb_cols, torch.int64, "wb_cols", B),
         _dev(probs_out, torch.float32, "probs_out", B * V), _dev(status, torch.int32, "status", 1),
         _stream(stream, logits.device))
+    _check(rc)
+    return out_tokens
+
+
+def decode_tail(logits: torch.Tensor, temperature, top_k, top_p, uniform,
+                out_tokens: torch.Tensor, token_pool, wb_rows, wb_cols,
+                cached_len: torch.Tensor, device_len: torch.Tensor, table_idx: torch.Tensor,
+                page_size: int, free_slots: torch.Tensor, page_table: torch.Tensor,
+                total_out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pkv_decode_tail: sample_batch (with its write-back) and fill_page_table
+    of one decode step in one call.  Returns ``out_tokens``."""
+    lib = load()
+    if logits.dim() != 2 or not logits.is_cuda or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D CUDA tensor with unit column stride")
+    if logits.dtype == torch.bfloat16:
+        dcode = PKV_BF16
+    elif logits.dtype == torch.float32:
+        dcode = PKV_FP32
+    else:
+        raise TypeError(f"logits dtype {logits.dtype} is not fp32 or bf16")
+    B, V = logits.shape
+    pool_rows = pool_cols = 0
+    if token_pool is not None:
+        pool_rows, pool_cols = token_pool.shape
+    if page_table.dim() != 2:
+        raise ValueError("page_table must be 2-D")
+    need = int(lib.pkv_sample_workspace_bytes(B, V, dcode))
+    if workspace is None:
+        workspace = _workspace(logits.device, need)
+    fb = cached_len.numel()
+    rc = lib.pkv_decode_tail(
+        logits.data_ptr(), dcode, B, V, logits.stride(0),
+        _dev(temperature, torch.float32, "temperature", B),
+        _dev(top_k, torch.int32, "top_k", B), _dev(top_p, torch.float32, "top_p", B),
+        _dev(uniform, torch.float32, "uniform", B), _dev(out_tokens, torch.int32, "out_tokens", B),
+        _dev(token_pool, torch.int32, "token_pool"), pool_rows, pool_cols,
+        _dev(wb_rows, torch.int32, "wb_rows", B), _dev(wb_cols, torch.int64, "wb_cols", B),
+        _dev(status, torch.int32, "status", 1), workspace.data_ptr(), workspace.numel(),
+        _dev(cached_len, torch.int32, "cached_len", fb),
+        _dev(device_len, torch.int32, "device_len", fb),
+        _dev(table_idx, torch.int32, "table_idx", fb), fb, int(page_size),
+        _dev(free_slots, torch.int32, "free_slots"), free_slots.numel(),
+        _dev(page_table, torch.int32, "page_table"), page_table.shape[0], page_table.shape[1],
+        _dev(total_out, torch.int64, "total_out", 1), _stream(stream, logits.device))
     _check(rc)
     return out_tokens
 
