@@ -37,7 +37,8 @@ UNIT = "tokens/s"
 WORKLOAD = "mixed"
 KERNEL_SOURCES = ("paged_kv_gb300/csrc/sample_common.cuh", "paged_kv_gb300/csrc/sample_stream.cuh",
                   "paged_kv_gb300/csrc/sample_finish.cuh", "paged_kv_gb300/csrc/sample_launch.cuh",
-                  "paged_kv_gb300/csrc/device_common.cuh", "paged_kv_gb300/csrc/launch_config.h")
+                  "paged_kv_gb300/csrc/device_common.cuh", "paged_kv_gb300/csrc/launch_config.h",
+                  "paged_kv_gb300/csrc/page_fill.cuh")
 GRAPH_LEN = 20  # steps per captured CUDA graph
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sampler_mixed_traffic.json")
 
