@@ -348,11 +348,12 @@ __device__ __forceinline__ unsigned long long mul_fx(unsigned long long z, float
   return q + ((up && frac) ? 1ull : 0ull);
 }
 
-// ceil(rem / w) for w > 0 and a quotient below 2^21, by bisection on
-// j * w >= rem (integer multiplies only).
+// ceil(rem / w) for w > 0 and a quotient at most `bound` (< 2^21), by
+// bisection on j * w >= rem (integer multiplies only).
 __device__ __forceinline__ unsigned long long ceil_div_small(unsigned long long rem,
-                                                             unsigned long long w) {
-  unsigned long long lo = 0, hi = 1ull << 21;
+                                                             unsigned long long w,
+                                                             unsigned long long bound) {
+  unsigned long long lo = 0, hi = bound;
   while (lo < hi) {
     const unsigned long long mid = (lo + hi) >> 1;
     if (mid * w >= rem) hi = mid;
@@ -774,7 +775,7 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
     unsigned long long rem;
     tp = row_select<BF16, true>(P, row, in_k, wfx, target, sm, c, &rem);
     const unsigned long long wt = mass_fx(weight(tp, m, c2));
-    const unsigned long long rp = wt == 0 ? ~0ull : ceil_div_small(rem, wt);
+    const unsigned long long rp = wt == 0 ? ~0ull : ceil_div_small(rem, wt, 1ull << 21);
     const float tpv = tp;
     cp = row_tie_cut<BF16>(P, row, [&](float x, int e) { return x == tpv && in_k(x, e); }, rp, sm,
                            c);

@@ -478,19 +478,21 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     }
     if (target < 1) target = 1;
     int cand = INT_MAX;
-    unsigned long long run = before, rem = 0, wc = 0;
+    unsigned long long run = before, rem = 0, wc = 0, nc = 0;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       if (run < target && run + mk[jj] >= target) {
         cand = 4 * tid + jj;
         rem = target - run;
         wc = wfx[jj];
+        nc = cnt[jj];
       }
       run += mk[jj];
     }
     if (cand != INT_MAX) {
-      // Members j of the cut key are kept iff run + j * w < target (one owner).
-      unsigned long long need = wc == 0 ? ~0ull : ceil_div_small(rem, wc);
+      // Members j of the cut key are kept iff run + j * w < target (one
+      // owner); at most the key's count of them.
+      unsigned long long need = wc == 0 ? ~0ull : ceil_div_small(rem, wc, nc);
       if (cand == ik && need > rk) need = rk;
       sm.bl[1] = need;
     }

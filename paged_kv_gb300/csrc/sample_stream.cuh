@@ -246,6 +246,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       fence_mbar_init();
     }
   }
+  // Each producer claims its first kStages tickets at once, before the row
+  // order is built, so that the ticket round trip overlaps it.
+  uint32_t first_ticket = 0;
+  if (VEC && producer && (threadIdx.x & 31) == 0) {
+    first_ticket = atomicAdd(&hdr->ticket, static_cast<uint32_t>(kStages));
+  }
   const bool ordered = P.B <= kOrderRows;
   if (ordered) {
     build_order<BF16, NV>(P, order, order_sum);  // ends with a CTA barrier
@@ -274,7 +280,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             }
             if (!ok) break;  // the consumers stopped: issue nothing more
           }
-          const uint32_t t = atomicAdd(&hdr->ticket, 1u);
+          const uint32_t t = n < kStages ? first_ticket + static_cast<uint32_t>(n)
+                                         : atomicAdd(&hdr->ticket, 1u);
           const int q = static_cast<int>(t);
           if (t >= static_cast<uint32_t>(items)) {
             stage_item[group][s] = -1;
