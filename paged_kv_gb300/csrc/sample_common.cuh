@@ -136,8 +136,11 @@ static_assert(offsetof(ChunkSlot, tmax) % 16 == 0 && offsetof(ChunkSlot, hist) %
 __device__ __forceinline__ WorkspaceHeader* ws_header(const SampleParams& P) {
   return static_cast<WorkspaceHeader*>(P.workspace);
 }
+__device__ __forceinline__ uint16_t* ws_finish_order(const SampleParams& P) {
+  return reinterpret_cast<uint16_t*>(static_cast<char*>(P.workspace) + kWorkspaceHeaderBytes);
+}
 __device__ __forceinline__ ChunkSlot* ws_records(const SampleParams& P) {
-  return reinterpret_cast<ChunkSlot*>(static_cast<char*>(P.workspace) + kWorkspaceHeaderBytes);
+  return reinterpret_cast<ChunkSlot*>(static_cast<char*>(P.workspace) + kRecordsOffset);
 }
 
 // Barrier of the calling thread's group of kThreads threads (named barrier

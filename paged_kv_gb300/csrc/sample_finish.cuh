@@ -726,7 +726,6 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
                                   static_cast<int>(blockIdx.x) - P.B, P.fill_ctas);
     return;
   }
-  const int row = blockIdx.x;
   const int C = P.chunks;
   const int V = P.V;
   Ctx c;
@@ -742,6 +741,10 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
     fence_mbar_init();
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The row of this CTA: the stream kernel's placement for ordered batches
+  // (heavy and light rows alternate), else the CTA index.
+  const int row = P.B <= kOrderRows ? static_cast<int>(__ldcg(ws_finish_order(P) + blockIdx.x))
+                                    : static_cast<int>(blockIdx.x);
   // The row's records in one bulk copy (they are contiguous), completing on
   // rec_bar; the row parameters and write-back coordinates load meanwhile.
   const uint32_t rec_bytes = static_cast<uint32_t>(C) * static_cast<uint32_t>(kChunkSlotBytes);

@@ -23,6 +23,17 @@ struct WorkspaceHeader {
 constexpr size_t kWorkspaceHeaderBytes = 256;
 static_assert(sizeof(WorkspaceHeader) == kWorkspaceHeaderBytes, "header size");
 
+// After the header: the finish kernel's row for each CTA (16-bit, batches of
+// up to kOrderRows rows), then the records.
+constexpr int kOrderRows = 4096;
+constexpr size_t kFinishOrderBytes = static_cast<size_t>(kOrderRows) * 2;
+constexpr size_t kRecordsOffset = kWorkspaceHeaderBytes + kFinishOrderBytes;
+
+// Workspace bytes for B rows of `chunks` chunks.
+inline size_t sample_workspace_need(int B, int chunks) {
+  return kRecordsOffset + static_cast<size_t>(B) * chunks * kChunkSlotBytes;
+}
+
 struct SampleParams {
   const void* logits;        // [B, row_stride] fp32 or bf16
   int64_t row_stride;        // elements

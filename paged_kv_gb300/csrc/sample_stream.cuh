@@ -113,24 +113,25 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
 // producer warp per group.
 constexpr int kStreamThreads = kGroups * (kThreads + 32);
 
-// Largest batch whose rows the stream kernel orders by cost (one 16-bit
-// entry per row in shared memory); larger batches go in row order.
-constexpr int kOrderRows = 4096;
+// Batches of up to kOrderRows rows (sample_params.h) are ordered by cost (one
+// 16-bit entry per row in shared memory); larger batches go in row order.
 constexpr int kOrderPerThread = (kOrderRows + kStreamThreads - 1) / kStreamThreads;
 
-// Cost class of a row's items in the stream kernel: 0 for the count
-// histogram (top-p rows without a small top-k), 1 for plain rows (one exp
-// per element), 2 for the rest (a maximum and a few stores).
+// Cost class of a row: 0 for the count-histogram and fallback rows (the
+// most work in both kernels), 1 for top-k rows (long in the finish kernel),
+// 2 for plain rows (one exp per element in the stream kernel), 3 for greedy
+// rows.  Classes 0 and 1 are the finish kernel's heavy rows.
 template <bool BF16, int NV>
 __device__ __forceinline__ int row_cost_class(const SampleParams& P, int row) {
   const int kind = row_params<BF16, NV>(P, row, 0).kind;
-  return kind == kKindH ? 0 : (kind == kKindP ? 1 : 2);
+  return (kind == kKindH || kind == kKindF) ? 0 : (kind == kKindK ? 1 : (kind == kKindP ? 2 : 3));
 }
 
 // order[0 .. B) = the rows sorted by cost class, stable in row index.  All
-// threads of the CTA call it; it ends with a CTA barrier.  Thread t ranks
-// rows [t * kOrderPerThread, (t + 1) * kOrderPerThread): three 16-bit class
-// counts packed in a 64-bit word, one CTA-wide exclusive scan.
+// threads of the CTA call it; it ends with a CTA barrier, after which
+// wsum[kStreamThreads / 32] holds the four class counts.  Thread t ranks rows
+// [t * kOrderPerThread, (t + 1) * kOrderPerThread): four 16-bit class counts
+// packed in a 64-bit word, one CTA-wide exclusive scan.
 template <bool BF16, int NV>
 __device__ __forceinline__ void build_order(const SampleParams& P, uint16_t* order,
                                             unsigned long long* wsum) {
@@ -170,21 +171,43 @@ __device__ __forceinline__ void build_order(const SampleParams& P, uint16_t* ord
   __syncthreads();
   const unsigned long long before = wsum[w] + (incl - cnt);
   const unsigned long long total = wsum[kWarpsAll];
-  uint32_t pos[3];
-  pos[0] = static_cast<uint32_t>(before & 0xffffu);
-  pos[1] = static_cast<uint32_t>(total & 0xffffu) + static_cast<uint32_t>((before >> 16) & 0xffffu);
-  pos[2] = static_cast<uint32_t>(total & 0xffffu) + static_cast<uint32_t>((total >> 16) & 0xffffu) +
-           static_cast<uint32_t>((before >> 32) & 0xffffu);
+  uint32_t pos[4];
+  uint32_t base = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    pos[q] = base + static_cast<uint32_t>((before >> (16 * q)) & 0xffffu);
+    base += static_cast<uint32_t>((total >> (16 * q)) & 0xffffu);
+  }
 #pragma unroll
   for (int j = 0; j < kOrderPerThread; ++j) {
     const int r = r0 + j;
     if (r < P.B) {
       const uint32_t c = (cls >> (2 * j)) & 3u;
-      const uint32_t at = c == 0 ? pos[0]++ : (c == 1 ? pos[1]++ : pos[2]++);
+      const uint32_t at = pos[c]++;
       order[at] = static_cast<uint16_t>(r);
     }
   }
   __syncthreads();
+}
+
+// The finish kernel's row of each CTA: heavy rows (classes 0 and 1) and
+// light ones alternate, so that CTAs placed side by side on an SM are rarely
+// two heavy rows; the longer list continues alone.  Written by CTA 0 of the
+// stream kernel after build_order.
+__device__ __forceinline__ void write_finish_order(const uint16_t* order, int B,
+                                                   unsigned long long counts, uint16_t* out) {
+  const int nh = static_cast<int>((counts & 0xffffu) + ((counts >> 16) & 0xffffu));
+  const int nl = B - nh;
+  const int mn = nh < nl ? nh : nl;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    int p;
+    if (b < 2 * mn) {
+      p = (b & 1) ? nh + (b >> 1) : (b >> 1);
+    } else {
+      p = nh > nl ? mn + (b - 2 * mn) : nh + mn + (b - 2 * mn);
+    }
+    out[b] = order[p];
+  }
 }
 
 // Row and chunk of item rank q (rows in cost order when `ordered`).
@@ -255,6 +278,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   const bool ordered = P.B <= kOrderRows;
   if (ordered) {
     build_order<BF16, NV>(P, order, order_sum);  // ends with a CTA barrier
+    if (blockIdx.x == 0) {
+      write_finish_order(order, P.B, order_sum[kStreamThreads / 32], ws_finish_order(P));
+    }
   } else {
     __syncthreads();
   }
