@@ -15,10 +15,11 @@ constexpr size_t kChunkSlotBytes = 16 + 128 + 256 * 4 + 2048;
 // The workspace starts with this header; the records follow it.  It must be
 // zero before the first call; every call leaves it ready for the next one.
 struct WorkspaceHeader {
-  uint32_t ticket;  // next item rank to hand out (stream kernel)
-  uint32_t done;    // stream CTAs finished in this call
-  uint32_t calls;   // calls completed; records of call n carry n + 1
-  uint32_t pad[61];
+  uint32_t ticket;        // next ticket of the stream kernel's main queue
+  uint32_t done;          // stream CTAs finished in this call
+  uint32_t calls;         // calls completed; records of call n carry n + 1
+  uint32_t ticket_heavy;  // next ticket of the queue of count-histogram items
+  uint32_t pad[60];
 };
 constexpr size_t kWorkspaceHeaderBytes = 256;
 static_assert(sizeof(WorkspaceHeader) == kWorkspaceHeaderBytes, "header size");

@@ -1,8 +1,7 @@
 // Stream kernel of the batched sampler: persistent CTAs of kGroups groups of
 // kThreads threads.  The items (row, chunk) are ranked with the rows in
-// falling cost order (build_order) and dealt out in rounds, one rank per
-// group and round (item_rank); each group takes its rounds in an order
-// rotated by its index (group_round).  A chunk is kThreads * NV 16-byte
+// falling cost order (build_order) and handed out one at a time from ticket
+// counters in the workspace header.  A chunk is kThreads * NV 16-byte
 // vectors of one row.  Aligned rows arrive through a
 // per-group ring of kStages shared-memory stages filled by 1-D bulk copies
 // (cp.async.bulk, completion counted on an mbarrier), issued kStages items
@@ -219,7 +218,7 @@ __device__ __forceinline__ void item_of(int q, int C, bool ordered, const uint16
 }
 
 // Items are handed out one at a time from the workspace header's ticket
-// counter, so a group that meets an expensive item takes fewer of the
+// counters, so a group that meets an expensive item takes fewer of the
 // cheap ones.  The last CTA to finish resets the counters and advances the
 // call number, which every record of this call carries (wseq): the finish
 // kernel trusts a record only with the current number, so a record a group
@@ -269,15 +268,24 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       fence_mbar_init();
     }
   }
-  // Each producer claims its first kStages tickets at once, before the row
-  // order is built, so that the ticket round trip overlaps it.
+  // Two queues (aligned rows): ranks [0, heavy) are the items of the
+  // count-histogram rows, bound by shared-memory atomics, ranks [heavy,
+  // items) the rest, bound by HBM.  Group 0 of a CTA starts on the first
+  // queue and group 1 on the second; each moves to the other queue once its
+  // own is empty, so the histogram work overlaps the streaming instead of
+  // holding every group at once.  Each producer claims its first kStages
+  // tickets before the row order is built, so that the ticket round trip
+  // overlaps it.
   uint32_t first_ticket = 0;
   if (VEC && producer && (threadIdx.x & 31) == 0) {
-    first_ticket = atomicAdd(&hdr->ticket, static_cast<uint32_t>(kStages));
+    first_ticket = atomicAdd(group == 0 ? &hdr->ticket_heavy : &hdr->ticket,
+                             static_cast<uint32_t>(kStages));
   }
   const bool ordered = P.B <= kOrderRows;
+  uint32_t heavy = 0;  // items of class-0 rows, ranked first
   if (ordered) {
     build_order<BF16, NV>(P, order, order_sum);  // ends with a CTA barrier
+    heavy = static_cast<uint32_t>(order_sum[kStreamThreads / 32] & 0xffffu) * static_cast<uint32_t>(C);
     if (blockIdx.x == 0) {
       write_finish_order(order, P.B, order_sum[kStreamThreads / 32], ws_finish_order(P));
     }
@@ -295,6 +303,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         int sent = -1, last_copy[kStages];
 #pragma unroll
         for (int s = 0; s < kStages; ++s) last_copy[s] = -1;
+        int qi = group == 0 ? 0 : 1;  // the queue in use: 0 heavy, 1 the rest
+        bool moved = false;           // already moved to the other queue
+        const bool stagger = heavy > 0u;
         for (int n = 0;; ++n) {
           const int s = n % kStages;
           if (n >= kStages) {
@@ -305,11 +316,32 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
               if (globaltimer_ns() - t0 > kWaitNs) break;
             }
             if (!ok) break;  // the consumers stopped: issue nothing more
+          } else if (stagger && n > 0) {
+            // The count-histogram items start first: the second opening copy
+            // of each group waits (bounded) until group 0's first chunk has
+            // landed, so that chunk does not share the opening burst with
+            // every other stage.
+            const long long t0 = globaltimer_ns();
+            while (!mbar_try_wait(reinterpret_cast<uint64_t*>(&full[0][0]), 0u)) {
+              if (globaltimer_ns() - t0 > kWaitNs) break;
+            }
           }
-          const uint32_t t = n < kStages ? first_ticket + static_cast<uint32_t>(n)
-                                         : atomicAdd(&hdr->ticket, 1u);
-          const int q = static_cast<int>(t);
-          if (t >= static_cast<uint32_t>(items)) {
+          int q = -1;
+          for (;;) {
+            const uint32_t t = (!moved && n < kStages)
+                                   ? first_ticket + static_cast<uint32_t>(n)
+                                   : atomicAdd(qi == 0 ? &hdr->ticket_heavy : &hdr->ticket, 1u);
+            const uint32_t lo = qi == 0 ? 0u : heavy;
+            const uint32_t len = qi == 0 ? heavy : static_cast<uint32_t>(items) - heavy;
+            if (t < len) {
+              q = static_cast<int>(lo + t);
+              break;
+            }
+            if (moved) break;  // both queues are empty
+            moved = true;
+            qi ^= 1;
+          }
+          if (q < 0) {
             stage_item[group][s] = -1;
             mbar_arrive(&fullb[s]);
             sent = n;
@@ -426,6 +458,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0 && atomicAdd(&hdr->done, 1u) == gridDim.x - 1) {
     hdr->ticket = 0u;
+    hdr->ticket_heavy = 0u;
     hdr->done = 0u;
     hdr->calls = seq;
   }

@@ -194,8 +194,8 @@ def test_deterministic_across_calls():
 
 
 def test_workspace_header_is_checked_and_repaired():
-    # A workspace whose header was never initialised (here: a ticket counter
-    # past every item) hands out no chunks, so every row's records are stale:
+    # A workspace whose header was never initialised (here: both ticket
+    # counters past every item) hands out no chunks, so every row's records are stale:
     # every token is -1 with status bit 64 and nothing is written back.  The
     # call leaves the header reset, and the next call on it is exact.
     w = workloads.mixed(B=24, V=32768)
@@ -203,8 +203,9 @@ def test_workspace_header_is_checked_and_repaired():
     ws = torch.zeros(pkv.sample_workspace_bytes(B, V, w.logits.dtype), dtype=torch.uint8,
                      device=DEV)
     hdr = ws[:16].view(torch.int32)
-    hdr[0] = 0x7FFFFF00  # ticket
+    hdr[0] = 0x7FFFFF00  # ticket (main queue)
     hdr[2] = 7           # calls
+    hdr[3] = 0x7FFFFF00  # ticket (count-histogram queue)
     L = w.logits.to(DEV)
     args = (_d(w.temperature), _d(w.top_k), _d(w.top_p), _d(w.uniform))
     pool = torch.zeros((B, 64), dtype=torch.int32, device=DEV)
@@ -217,7 +218,7 @@ def test_workspace_header_is_checked_and_repaired():
     assert (tok.cpu().numpy() == -1).all()
     assert int(status.item()) & pkv.ST_TIMEOUT
     assert int(pool.abs().sum().item()) == 0
-    assert hdr.cpu().tolist()[:3] == [0, 0, 8]
+    assert hdr.cpu().tolist()[:4] == [0, 0, 8, 0]
     status.zero_()
     tok = pkv.sample_batch(L, *args, status=status, workspace=ws)
     torch.cuda.synchronize()
