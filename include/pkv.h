@@ -74,10 +74,10 @@ int pkv_version(void);
 /*
  * Device bytes of the workspace pkv_sample_batch needs for (B, V, dtype), or
  * 0 for invalid arguments.  The sampler runs as two kernels: the first splits
- * every row into chunks, hands the chunks out to its CTAs from a counter in
+ * every row into chunks, hands the chunks out to its CTAs from counters in
  * the workspace header and leaves one record per (row, chunk) in the
- * workspace (about 3 KB each); the second settles each row from its
- * records.  The caller owns the workspace.  Before its first use it must be
+ * workspace (about 3 KB each, plus 16 KB of per-slice counts for top-p
+ * rows); the second settles each row from its records.  The caller owns the workspace.  Before its first use it must be
  * initialised once, by pkv_sample_workspace_init or by zeroing it; every
  * call then leaves it ready for the next call on the same stream.  A
  * workspace must not be used by two calls that may run concurrently.
@@ -146,12 +146,12 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
  * pkv_sample_batch_noalloc -- pkv_sample_batch without a caller workspace.
  *
  * Same arguments, meaning and errors as pkv_sample_batch, minus the
- * workspace: the sampler's scratch is a 16 MiB device array inside the
+ * workspace: the sampler's scratch is a 64 MiB device array inside the
  * library (one per device, zero at load time, left ready by every call), so
  * the call allocates nothing anywhere.  Calls on one device share that array:
  * they must not run concurrently (on different streams without ordering).
  * Errors: those of pkv_sample_batch, plus PKV_EUNSUPPORTED when
- * pkv_sample_workspace_bytes(B, V, dt) exceeds 16 MiB (e.g. B=1024,
+ * pkv_sample_workspace_bytes(B, V, dt) exceeds 64 MiB (e.g. B=1024,
  * V=256000), and PKV_ECUDA when the array's address cannot be read.
  */
 int pkv_sample_batch_noalloc(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,

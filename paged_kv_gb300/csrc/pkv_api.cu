@@ -160,7 +160,7 @@ constexpr int kFusedFillCtas = 32;
 
 // Scratch of pkv_sample_batch_noalloc: a zero-initialised device array of
 // the library (one instance per device), used as the sampler workspace.
-constexpr size_t kStaticScratchBytes = static_cast<size_t>(16) << 20;
+constexpr size_t kStaticScratchBytes = static_cast<size_t>(64) << 20;
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 // The array's address on the current device, looked up once per device.

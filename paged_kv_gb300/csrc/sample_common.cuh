@@ -142,6 +142,14 @@ __device__ __forceinline__ uint16_t* ws_finish_order(const SampleParams& P) {
 __device__ __forceinline__ ChunkSlot* ws_records(const SampleParams& P) {
   return reinterpret_cast<ChunkSlot*>(static_cast<char*>(P.workspace) + kRecordsOffset);
 }
+// Slice histograms of (row, chunk): kWarps blocks of kHistWords words (two
+// 16-bit counts each), block w for consumer warp w's slice of the chunk.
+static_assert(kSliceHistBytes == static_cast<size_t>(kWarps) * kHistWords * 4,
+              "one histogram per consumer warp");
+__device__ __forceinline__ uint4* ws_slice_hist(const SampleParams& P, int row, int chunk) {
+  char* base = reinterpret_cast<char*>(ws_records(P) + static_cast<size_t>(P.B) * P.chunks);
+  return reinterpret_cast<uint4*>(base + (static_cast<size_t>(row) * P.chunks + chunk) * kSliceHistBytes);
+}
 
 // Barrier of the calling thread's group of kThreads threads (named barrier
 // 1 + group); a finish CTA is one group.

@@ -389,8 +389,9 @@ __device__ __forceinline__ bool finish_topk(const SampleParams& P, SampleSmem& s
 // The finisher settles top-k (by count) and top-p (by fixed-point mass)
 // exactly on the merged keys: keys i < is are wholly in the kept set S, the
 // first rs members (in index order) of key is are in it too.  It then picks
-// the chunk holding the draw from per-chunk masses of S, stages that chunk
-// and finds the token with one pass of per-vector sums.  Returns false,
+// the chunk holding the draw from per-chunk masses of S, the slice of that
+// chunk from the stream kernel's per-warp histograms, and the token from one
+// prefix over the slice's elements.  Returns false,
 // having emitted nothing, when a cut lies below the merged window; the
 // caller then runs the exact fallback.
 template <int NV, bool VEC>
@@ -535,6 +536,7 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     if (v) sm.cnt[lane] = static_cast<uint32_t>(kept);
     if (lane == cstar) {
       sm.bi[0] = cstar;
+      sm.bi[4] = static_cast<int>(A - static_cast<uint32_t>(recs[cstar].s.i0));
       sm.bl[3] = tdraw - (incl - mr);
       sm.bl[5] = zs;
     }
@@ -546,8 +548,7 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   const uint32_t kept_c = sm.cnt[cstar];
   // In a chunk, the mass of S before a position is the mass above the cut
   // key plus wcut * min(cut-key members so far, kept): the first kept
-  // members count, later ones do not.  The records are consumed: the chunk
-  // is staged over them.
+  // members count, later ones do not.
   auto above_and_ties = [&](const uint4 v4, int e0, unsigned long long* a, uint32_t* t) {
     const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
     unsigned long long s = 0;
@@ -562,76 +563,114 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     *a = s;
     *t = n;
   };
-  stage_own<true, NV, VEC>(P, row, cstar, stage, warp, lane);
-  // Per (warp, vector) sums; entry q = warp * NV + j is in index order.
+  // ---- the slice of the chunk holding the draw, from the stream kernel's
+  // per-warp histograms of the chunk (copied over the consumed records):
+  // slice w (NV vectors of 32 lanes, contiguous in index order) has mass
+  // a_w above the cut key and t_w cut-key members.
+  const uint32_t dc = static_cast<uint32_t>(sm.bi[4]);  // merged key i = slice key i - dc
+  {
+    const uint4* src = ws_slice_hist(P, row, cstar);
+    for (int k = tid; k < static_cast<int>(kSliceHistBytes / 16); k += kThreads) {
+      cp_async16(stage + k, src + k);
+    }
+    cp_async_wait_all();
+  }
+  group_sync();
+  {
+    const uint16_t* hw = reinterpret_cast<const uint16_t*>(stage) + warp * kHistKeys;
+    unsigned long long a = 0;
+    uint32_t t = 0;
 #pragma unroll 1
-  for (int j = 0; j < NV; ++j) {
-    unsigned long long a;
-    uint32_t t;
-    above_and_ties(stage[(warp * NV + j) * 32 + lane], vec_base<true, NV>(cstar, warp, lane, j),
-                   &a, &t);
+    for (int i0 = static_cast<int>(dc); i0 <= is; i0 += 128) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i <= is) {
+          const uint32_t n = hw[i - static_cast<int>(dc)];
+          if (i < is) {
+            a += n * table[i];
+          } else {
+            t = n;
+          }
+        }
+      }
+    }
     a = warp_sum_u64(a);
     t = __reduce_add_sync(kFull, t);
     if (lane == 0) {
-      sm.scan[warp * NV + j] = a;
-      sm.hlo[warp * NV + j] = t;
+      sm.scan[warp] = a;
+      sm.hlo[warp] = t;
     }
   }
   group_sync();
-  if (warp == 0) {
-    constexpr int nq = kWarps * NV;
-    unsigned long long carry_a = 0;
-    uint32_t carry_t = 0;
-    int qstar = -1;
-    unsigned long long a_before = 0;
-    uint32_t t_before = 0;
-#pragma unroll 1
-    for (int base = 0; base < nq; base += 32) {
-      const int q = base + lane;
-      const unsigned long long a = q < nq ? sm.scan[q] : 0ull;
-      const uint32_t t = q < nq ? sm.hlo[q] : 0u;
-      const unsigned long long ai = warp_inclusive_scan(a, lane) + carry_a;
-      const uint32_t ti = warp_inclusive_scan(t, lane) + carry_t;
-      const unsigned long long pi = ai + wcut * min(static_cast<unsigned long long>(ti),
-                                                    static_cast<unsigned long long>(kept_c));
-      const unsigned bal = __ballot_sync(kFull, q < nq && tau < pi);
-      if (qstar < 0 && bal) {
-        const int ls = __ffs(bal) - 1;
-        qstar = base + ls;
-        a_before = __shfl_sync(kFull, ai - a, ls);
-        t_before = __shfl_sync(kFull, ti - t, ls);
-      }
-      carry_a = __shfl_sync(kFull, ai, 31);
-      carry_t = __shfl_sync(kFull, ti, 31);
-    }
-    if (lane == 0) {
-      sm.bi[2] = qstar;
-      sm.bl[6] = a_before;
-      sm.bi[3] = static_cast<int32_t>(t_before);
-    }
-  }
-  group_sync();
-  const int qstar = sm.bi[2];
-  if (qstar >= 0 && warp == qstar / NV) {
-    const int jstar = qstar % NV;
-    const uint4 v4 = stage[(warp * NV + jstar) * 32 + lane];
-    const int e0 = vec_base<true, NV>(cstar, warp, lane, jstar);
-    unsigned long long a;
-    uint32_t t;
-    above_and_ties(v4, e0, &a, &t);
-    const unsigned long long ai = warp_inclusive_scan(a, lane) + sm.bl[6];
-    const uint32_t ti = warp_inclusive_scan(t, lane) + static_cast<uint32_t>(sm.bi[3]);
+  // Every warp finds the draw's slice (lanes 0 .. kWarps - 1 hold the slices).
+  int wstar;
+  unsigned long long a_w;  // mass of S in the chunk before that slice without
+  uint32_t t_w;            // the cut key, and the cut-key members before it
+  {
+    const unsigned long long a = lane < kWarps ? sm.scan[lane] : 0ull;
+    const uint32_t t = lane < kWarps ? sm.hlo[lane] : 0u;
+    const unsigned long long ai = warp_inclusive_scan(a, lane);
+    const uint32_t ti = warp_inclusive_scan(t, lane);
     const unsigned long long pi =
         ai + wcut * min(static_cast<unsigned long long>(ti), static_cast<unsigned long long>(kept_c));
-    const unsigned bal = __ballot_sync(kFull, tau < pi);
-    const int ls = bal ? __ffs(bal) - 1 : 31;
-    int sel = -1;
-    if (lane == ls) {
-      // Walk the lane's elements with the mass of S before each.
-      unsigned long long above = ai - a;
-      uint32_t tc = ti - t;
-      int last = -1;
-      for_vec_c<true>(v4, e0, [&](float x, int e) {
+    const unsigned bal = __ballot_sync(kFull, lane < kWarps && tau < pi);
+    wstar = bal ? __ffs(bal) - 1 : -1;
+    const int from = wstar < 0 ? 0 : wstar;
+    a_w = __shfl_sync(kFull, ai - a, from);
+    t_w = __shfl_sync(kFull, ti - t, from);
+  }
+  // ---- the slice's NV * 32 vectors, two consecutive ones per thread (L2
+  // reads), one prefix over the CTA, and the element in the thread whose
+  // range holds tau.
+  const bool active = wstar >= 0 && tid < NV * 16;
+  uint32_t v[2][4];
+  int e0[2];
+  unsigned long long a = 0;
+  uint32_t t = 0;
+  if (active) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      e0[k] = cstar * (kThreads * NV * 8) + (wstar * NV * 32 + 2 * tid + k) * 8;
+      load_vec<true, NV, VEC>(P, row, e0[k], v[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      unsigned long long ak;
+      uint32_t tk;
+      above_and_ties(make_uint4(v[k][0], v[k][1], v[k][2], v[k][3]), e0[k], &ak, &tk);
+      a += ak;
+      t += tk;
+    }
+  }
+  const unsigned long long ai = warp_inclusive_scan(a, lane);
+  const uint32_t ti = warp_inclusive_scan(t, lane);
+  if (lane == 31) {
+    sm.wl[warp] = ai;
+    sm.wu[warp] = ti;
+  }
+  group_sync();
+  unsigned long long ab = a_w;
+  uint32_t tb = t_w;
+  for (int w = 0; w < warp; ++w) {
+    ab += sm.wl[w];
+    tb += sm.wu[w];
+  }
+  const unsigned long long a_in = ab + ai, a_ex = a_in - a;
+  const uint32_t t_in = tb + ti, t_ex = t_in - t;
+  const unsigned long long p_in =
+      a_in + wcut * min(static_cast<unsigned long long>(t_in), static_cast<unsigned long long>(kept_c));
+  const unsigned long long p_ex =
+      a_ex + wcut * min(static_cast<unsigned long long>(t_ex), static_cast<unsigned long long>(kept_c));
+  const bool mine = active && tau >= p_ex && tau < p_in;
+  if (mine) {
+    // Walk the thread's elements with the mass of S before each.
+    unsigned long long above = a_ex;
+    uint32_t tc = t_ex;
+    int sel = -1, last = -1;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      for_vec_c<true>(make_uint4(v[k][0], v[k][1], v[k][2], v[k][3]), e0[k], [&](float x, int e) {
         if (e < V) {
           const uint32_t i = A - key16(x);
           const unsigned long long pb =
@@ -651,12 +690,12 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
           }
         }
       });
-      if (sel < 0) sel = last;
     }
-    const int tok = __shfl_sync(kFull, sel, ls);
-    if (lane == 0) emit(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
+    if (sel < 0) sel = last;
+    emit(P, row, sel, sel < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
   }
-  if (qstar < 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
+  // No thread's range holds tau only when the masses are not finite.
+  if (__syncthreads_or(mine) == 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
   if (q_row != nullptr) {
     // Debug output: q over every chunk; a cut-key member is kept when its
     // rank among the chunk's members is below kept_r.

@@ -25,14 +25,18 @@ constexpr size_t kWorkspaceHeaderBytes = 256;
 static_assert(sizeof(WorkspaceHeader) == kWorkspaceHeaderBytes, "header size");
 
 // After the header: the finish kernel's row for each CTA (16-bit, batches of
-// up to kOrderRows rows), then the records.
+// up to kOrderRows rows), then the records, then one block of slice
+// histograms per (row, chunk): for each of the stream kernel's 8 consumer
+// warps, the 16-bit counts of the 1024 keys below the chunk maximum over
+// that warp's slice of the chunk (written for count-histogram rows only).
 constexpr int kOrderRows = 4096;
 constexpr size_t kFinishOrderBytes = static_cast<size_t>(kOrderRows) * 2;
 constexpr size_t kRecordsOffset = kWorkspaceHeaderBytes + kFinishOrderBytes;
+constexpr size_t kSliceHistBytes = 8 * 1024 * 2;
 
 // Workspace bytes for B rows of `chunks` chunks.
 inline size_t sample_workspace_need(int B, int chunks) {
-  return kRecordsOffset + static_cast<size_t>(B) * chunks * kChunkSlotBytes;
+  return kRecordsOffset + static_cast<size_t>(B) * chunks * (kChunkSlotBytes + kSliceHistBytes);
 }
 
 struct SampleParams {

@@ -27,13 +27,13 @@ constexpr int stream_stage_bytes() {
 
 template <int NV>
 constexpr int stream_dyn_bytes() {
-  return kGroups * stream_stages<NV>() * stream_stage_bytes<NV>() + kGroups * kHistWords * 4;
+  return kGroups * stream_stages<NV>() * stream_stage_bytes<NV>() + kGroups * kWarps * kHistWords * 4;
 }
 
 // Reduces one chunk (registers d, the kernel's layout) to its workspace
 // record.  All threads of the group call it.  Every warp records its maximum;
 // plain rows add the warp's mass, greedy and top-k rows the thread maxima,
-// top-p rows a count histogram of the chunk.
+// top-p rows a count histogram of the chunk and one of each warp's slice.
 template <bool BF16, int NV, bool VEC>
 __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& sm, const Ctx& c,
                                              uint32_t* hist, ChunkSlot* slot, int row, int chunk,
@@ -79,10 +79,14 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
   if constexpr (BF16) {
     if (rp.kind == kKindH) {
       // ---- counts per 16-bit key over the window [a - kHistKeys + 1, a],
-      // a the key of the chunk maximum.
+      // a the key of the chunk maximum: one histogram per warp (its slice of
+      // NV vectors), summed into the chunk's.  hist holds kWarps blocks of
+      // kHistWords words.
       if (lane == 0) sm.wf[warp] = wmax;
-      hist[tid] = 0u;
-      hist[tid + kThreads] = 0u;
+      uint4* h4 = reinterpret_cast<uint4*>(hist);
+      constexpr int kH4 = kWarps * kHistWords / 4;  // 16-byte words of all blocks
+#pragma unroll
+      for (int k = 0; k < kH4 / kThreads; ++k) h4[tid + k * kThreads] = make_uint4(0u, 0u, 0u, 0u);
       group_sync();
       float cm = sm.wf[0];
 #pragma unroll
@@ -93,12 +97,23 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
         for_regs<true, NV>(d, chunk, warp, lane, [&](float x, int e) {
           const uint32_t idx = a - key16(x);
           if (idx < static_cast<uint32_t>(kHistKeys) && (!has_pad || e < V)) {
-            atomicAdd(&hist[idx >> 1], 1u << ((idx & 1u) * 16u));
+            atomicAdd(&hist[warp * kHistWords + (idx >> 1)], 1u << ((idx & 1u) * 16u));
           }
         });
       }
       group_sync();
-      reinterpret_cast<uint2*>(slot->hist)[tid] = make_uint2(hist[2 * tid], hist[2 * tid + 1]);
+      // Sums of packed counts: a key's chunk count is at most the chunk's
+      // length (< 65536), so the 16-bit halves never carry.
+      uint32_t s0 = 0u, s1 = 0u;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        s0 += hist[w * kHistWords + 2 * tid];
+        s1 += hist[w * kHistWords + 2 * tid + 1];
+      }
+      reinterpret_cast<uint2*>(slot->hist)[tid] = make_uint2(s0, s1);
+      uint4* sh = ws_slice_hist(P, row, chunk);
+#pragma unroll
+      for (int k = 0; k < kH4 / kThreads; ++k) sh[tid + k * kThreads] = h4[tid + k * kThreads];
       if (tid == 0) {
         Summary s = {};
         s.i0 = static_cast<int32_t>(a);
@@ -387,7 +402,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     c.csize = static_cast<uint32_t>(C);
     SampleSmem& sm = smg[group];
     uint32_t* hist =
-        reinterpret_cast<uint32_t*>(dyn + kGroups * kStages * kStageBytes) + group * kHistWords;
+        reinterpret_cast<uint32_t*>(dyn + kGroups * kStages * kStageBytes) + group * kWarps * kHistWords;
     ChunkSlot* ws = ws_records(P);
     bool trusted = true;  // this warp has seen every copy land
     for (int n = 0;; ++n) {

@@ -21,7 +21,8 @@ DEV = "cuda"
 def test_noalloc_rejects_batches_beyond_its_scratch():
     lib = pkv.load()
     p = ctypes.c_void_p(256)
-    # B=1024, V=256000 bf16 needs about 53 MB of records; the scratch holds 16 MiB.
+    # B=1024, V=256000 bf16 needs about 320 MB of records and slice histograms;
+    # the scratch holds 64 MiB.
     rc = lib.pkv_sample_batch_noalloc(p, pkv.PKV_BF16, 1024, 256000, 256000, None, None, None,
                                       None, p, None, 0, 0, None, None, None, None, None)
     assert rc == pkv.PKV_EUNSUPPORTED
