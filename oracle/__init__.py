@@ -58,6 +58,11 @@ def _load():
             lib.oracle_fill_page_table.argtypes = [vp, vp, vp, i32, i32, vp, i64,
                                                    vp, i64, i64, vp, vp]
             lib.oracle_fill_page_table.restype = i32
+            lib.oracle_free_pages.argtypes = [vp, vp, vp, i32, i32, vp, i64, i64, vp, i64,
+                                              i64, vp, vp]
+            lib.oracle_free_pages.restype = i32
+            lib.oracle_check_free_list.argtypes = [vp, i64, i32, i64, i64]
+            lib.oracle_check_free_list.restype = i32
             _lib = lib
     return _lib
 
@@ -175,3 +180,33 @@ def fill_page_table(cached_len, device_len, table_idx, page_size: int, free_slot
                                     _ptr(fs), len(fs), _ptr(page_table), R, C,
                                     _ptr(total), _ptr(status))
     return {"rc": int(rc), "total": int(total[0]), "status": int(status[0])}
+
+
+def free_pages(table_idx, begin, end, page_size: int, page_table: np.ndarray, free_slots,
+               free_count: int) -> dict:
+    """Batched lazy free: append page_table[t, b:e:ps] of every request to the
+    free list.  ``free_slots`` is an int32 array of the list's capacity whose
+    first ``free_count`` entries are live; it is updated in place."""
+    lib = _load()
+    t = _np(table_idx, np.int32)
+    b = _np(begin, np.int32)
+    e = _np(end, np.int32)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    if not isinstance(free_slots, np.ndarray) or free_slots.dtype != np.int32 \
+            or not free_slots.flags.c_contiguous:
+        raise TypeError("free_slots must be a C-contiguous int32 array")
+    R, C = pt.shape
+    total = np.zeros(1, np.int64)
+    status = np.zeros(1, np.int32)
+    rc = lib.oracle_free_pages(_ptr(t), _ptr(b), _ptr(e), len(t), int(page_size), _ptr(pt), R, C,
+                               _ptr(free_slots), int(free_count), len(free_slots),
+                               _ptr(total), _ptr(status))
+    return {"rc": int(rc), "total": int(total[0]), "status": int(status[0])}
+
+
+def check_free_list(free_slots, page_size: int, num_pages: int, cache_pages: int) -> int:
+    """Integrity bits of a free list: 1 count, 2 alignment, 4 range, 8 duplicate."""
+    lib = _load()
+    fs = _np(free_slots, np.int32)
+    return int(lib.oracle_check_free_list(_ptr(fs), len(fs), int(page_size), int(num_pages),
+                                          int(cache_pages)))

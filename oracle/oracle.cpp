@@ -14,7 +14,9 @@
 //     batch" (_make_write_tuple, Scheduler._forward);
 //   * "CacheManager: allocation, release and admission control" -- sections
 //     "The free-page list", "Allocating pages for this step's tokens"
-//     (allocate_paged, _write_page_table) and the self-test answer 4.
+//     (allocate_paged, _write_page_table), the self-test answer 4, "Freeing,
+//     and freeing lazily" (lazy_free_region) and "The integrity check"
+//     (check_integrity).
 //
 // Arithmetic is fp64 throughout.  Sorting uses std::sort with a total order,
 // which is a library primitive used as one step.  Readings of points the pages
@@ -347,6 +349,78 @@ int oracle_fill_page_table(const int32_t* cached_len, const int32_t* device_len,
     }
   }
   return 0;
+}
+
+// Batched lazy free, lazy_free_region: inside the region every freed index
+// tensor contributes indices[::ps] -- its first element and every ps-th one
+// after it -- and on exit the contributions are concatenated onto the end of
+// the free list in the order they were freed.  The freed indices of request
+// i are the slice page_table[table_idx[i], begin[i] : end[i]] of its table
+// row (cache_req frees slices of page_table[table_idx, :cached_len]).
+// READING: requests are freed in batch order; an empty or reversed range
+// (end <= begin) frees nothing; a range whose row lies outside the table or
+// whose bounds lie outside [0, pt_cols] is flagged (status 4 or 8) and frees
+// nothing; when the free list's capacity cannot take the whole batch, nothing
+// is appended (status 32, return -2).  *total = the number of entries
+// appended.  free_slots holds free_count entries and room for capacity.
+int oracle_free_pages(const int32_t* table_idx, const int32_t* begin, const int32_t* end,
+                      int B, int page_size, const int32_t* page_table, int64_t pt_rows,
+                      int64_t pt_cols, int32_t* free_slots, int64_t free_count,
+                      int64_t capacity, int64_t* total, int32_t* status) {
+  *status = 0;
+  *total = 0;
+  std::vector<int32_t> appended;
+  for (int i = 0; i < B; ++i) {
+    const int64_t b = begin[i], e = end[i];
+    if (e <= b) continue;
+    const int64_t t = table_idx[i];
+    if (t < 0 || t >= pt_rows) {
+      *status |= kRowOOB;
+      continue;
+    }
+    if (b < 0 || e > pt_cols) {
+      *status |= kColOOB;
+      continue;
+    }
+    for (int64_t col = b; col < e; col += page_size) {
+      appended.push_back(page_table[t * pt_cols + col]);
+    }
+  }
+  if (free_count + static_cast<int64_t>(appended.size()) > capacity) {
+    *status |= 32;
+    return -2;
+  }
+  for (size_t g = 0; g < appended.size(); ++g) free_slots[free_count + g] = appended[g];
+  *total = static_cast<int64_t>(appended.size());
+  return 0;
+}
+
+// The integrity check, check_integrity: the free pages and the pages the
+// prefix cache holds add up to the pool (bit 1 when they do not), and with
+// ps > 1 every free entry is a page start, a multiple of ps (bit 2).
+// READING, two more bits for what the pages say the check is for ("anything
+// forgotten, or freed twice"): an entry that is not the start of a pool page
+// [0, num_pages * ps) (bit 4), and a page listed more than once (bit 8).
+int oracle_check_free_list(const int32_t* free_slots, int64_t free_count, int page_size,
+                           int64_t num_pages, int64_t cache_pages) {
+  int bits = 0;
+  if (free_count + cache_pages != num_pages) bits |= 1;
+  std::vector<char> seen(static_cast<size_t>(num_pages > 0 ? num_pages : 0), 0);
+  for (int64_t g = 0; g < free_count; ++g) {
+    const int64_t slot = free_slots[g];
+    if (page_size > 1 && slot % page_size != 0) {
+      bits |= 2;
+      continue;
+    }
+    if (slot < 0 || slot >= num_pages * page_size) {
+      bits |= 4;
+      continue;
+    }
+    const int64_t page = slot / page_size;
+    if (seen[page]) bits |= 8;
+    seen[page] = 1;
+  }
+  return bits;
 }
 
 }  // extern "C"

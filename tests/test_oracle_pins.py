@@ -335,3 +335,78 @@ def test_pages_disjoint_aligned_and_enospc():
     out = oracle.fill_page_table(w.cached_len, w.device_len, w.table_idx, w.page_size,
                                  free[: N - 1], pt2)
     assert out["rc"] == -2 and (pt2 == -1).all()
+
+
+# ---------------------------------------------------------------- golden + brute force: free path
+
+
+def test_pages_free_roundtrip():
+    g = _golden("pages_free_roundtrip.json")
+    ps, n, t = g["page_size"], g["num_pages"], g["table_idx"]
+    free = np.arange(n, dtype=np.int32) * ps
+    pt = np.zeros((4, 32), np.int32)
+    for c, d in g["alloc_steps"]:
+        out = oracle.fill_page_table([c], [d], [t], ps, free, pt)
+        assert out["rc"] == 0
+        free = free[out["total"]:]
+    cap = np.full(n, -1, np.int32)
+    cap[: len(free)] = free
+    out = oracle.free_pages([t], [g["free_begin"]], [g["free_end"]], ps, pt, cap, len(free))
+    assert out["rc"] == 0 and out["status"] == 0 and out["total"] == 3
+    assert cap.tolist() == g["expected_free_list"]
+    assert oracle.check_free_list(cap, ps, n, 0) == g["expected_integrity_bits"]
+
+
+def test_pages_integrity_detects_leak():
+    g = _golden("pages_integrity_leak.json")
+    n, ps = g["num_pages"], g["page_size"]
+    free = np.arange(n, dtype=np.int32) * ps
+    assert oracle.check_free_list(free, ps, n, 0) == g["expected_bits_fresh"]
+    assert oracle.check_free_list(free[g["leaked"]:], ps, n, 0) == g["expected_bits_after_leak"]
+
+
+def test_integrity_bits_by_hand():
+    # 4 pages of 4 tokens: a full list in any order passes; each fault sets its bit.
+    assert oracle.check_free_list([12, 0, 8, 4], 4, 4, 0) == 0
+    assert oracle.check_free_list([12, 0], 4, 4, 2) == 0      # two pages held by the cache
+    assert oracle.check_free_list([12, 0], 4, 4, 1) == 1      # one page missing
+    assert oracle.check_free_list([12, 1, 8, 4], 4, 4, 0) == 2  # not a page start
+    assert oracle.check_free_list([12, 16, 8, 4], 4, 4, 0) == 4  # past the pool
+    assert oracle.check_free_list([12, 4, 8, 4], 4, 4, 0) == 8   # page 1 twice (page 0 lost)
+    assert oracle.check_free_list([-4, 0, 8, 4], 4, 4, 0) == 4   # negative start
+    assert oracle.check_free_list([3, 0, 1, 2], 1, 4, 0) == 0    # ps=1: every slot is a start
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_free_matches_the_pages_slicing(seed):
+    # The pages' own expression, free_slots = cat([free_slots] + [row[b:e][::ps] ...]),
+    # evaluated with numpy slicing on random tables, ragged and unaligned ranges.
+    rng = np.random.default_rng(seed)
+    ps = int(rng.choice([1, 2, 4, 16]))
+    R, C, B = 6, 40, int(rng.integers(0, 9))
+    pt = rng.integers(0, 1000, size=(R, C)).astype(np.int32)
+    t = rng.integers(0, R, size=B).astype(np.int32)
+    b = rng.integers(0, C, size=B).astype(np.int32)
+    e = np.minimum(C, b + rng.integers(-3, 30, size=B)).astype(np.int32)
+    base = rng.integers(0, 1000, size=int(rng.integers(0, 5))).astype(np.int32)
+    want = np.concatenate([base] + [pt[t[i], b[i]:e[i]][::ps] for i in range(B)]).astype(np.int32)
+    cap = np.full(len(want) + 3, -7, np.int32)
+    cap[: len(base)] = base
+    out = oracle.free_pages(t, b, e, ps, pt, cap, len(base))
+    assert out["rc"] == 0 and out["status"] == 0 and out["total"] == len(want) - len(base)
+    assert cap[: len(want)].tolist() == want.tolist()
+    assert (cap[len(want):] == -7).all()
+
+
+def test_free_errors_write_nothing_or_skip():
+    pt = np.arange(24, dtype=np.int32).reshape(3, 8)
+    cap = np.full(4, -1, np.int32)
+    # Capacity: 2 + 3 entries do not fit in 4: nothing is appended.
+    cap[:2] = [100, 101]
+    out = oracle.free_pages([0], [0], [5], 2, pt, cap, 2)
+    assert out["rc"] == -2 and out["status"] == 32 and out["total"] == 0
+    assert cap.tolist() == [100, 101, -1, -1]
+    # A row outside the table and a range past its end are flagged and skipped.
+    out = oracle.free_pages([5, 1, 2], [0, 6, 0], [2, 9, 3], 2, pt, cap, 2)
+    assert out["rc"] == 0 and out["status"] == 4 | 8 and out["total"] == 2
+    assert cap.tolist() == [100, 101, 16, 18]
