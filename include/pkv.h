@@ -245,6 +245,67 @@ int pkv_fill_page_table(const int32_t* cached_len, const int32_t* device_len,
                         int64_t pt_rows, int64_t pt_cols, int64_t* total_out,
                         int32_t* status, pkv_stream_t stream);
 
+/*
+ * pkv_free_pages -- batched lazy free ("CacheManager: allocation, release
+ * and admission control", section "Freeing, and freeing lazily":
+ * lazy_free_region appends indices[::page_size] of every freed index tensor
+ * and concatenates the lot onto free_slots once).
+ *
+ * The freed indices of request i are the slice
+ * page_table[table_idx[i], begin[i] : end[i]] of its table row (cache_req,
+ * section "Handing the KV to the prefix cache", frees slices of
+ * page_table[table_idx, :cached_len]).  On device, in batch order, every
+ * page_size-th entry of each slice starting at its first,
+ *   page_table[table_idx[i], begin[i] + j * page_size],
+ *   j < ceil((end[i] - begin[i]) / page_size),
+ * is appended at free_slots[free_count ...].  A range with end <= begin frees
+ * nothing.  A range whose row lies outside the table sets PKV_ST_ROW_OOB,
+ * one with begin < 0 or end > pt_cols sets PKV_ST_COL_OOB; either frees
+ * nothing.  If free_count plus the entries to append exceeds free_capacity,
+ * PKV_ST_NOSPC is set, *total_out is 0 and nothing is written.
+ *   table_idx, begin, end [B] int32 (device); page_table [pt_rows, pt_cols]
+ *   int32 (device, read only); free_slots [free_capacity] int32 (device),
+ *   entries [0, free_count) live; total_out device int64 or NULL (receives
+ *   the number of entries appended; the caller's new count is free_count
+ *   plus it); status device int32 or NULL.
+ * Errors: PKV_EINVAL (NULL pointer, B < 0, B > PKV_MAX_FILL_BATCH,
+ * page_size < 1, free_count or free_capacity outside [0, 2^31) or
+ * free_count > free_capacity, empty table), PKV_ECUDA.  B == 0 writes
+ * *total_out = 0.
+ */
+int pkv_free_pages(const int32_t* table_idx, const int32_t* begin, const int32_t* end, int B,
+                   int page_size, const int32_t* page_table, int64_t pt_rows, int64_t pt_cols,
+                   int32_t* free_slots, int64_t free_count, int64_t free_capacity,
+                   int64_t* total_out, int32_t* status, pkv_stream_t stream);
+
+/* Bits of pkv_check_free_list's result. */
+#define PKV_FL_COUNT 1      /* free pages + cached pages != pool pages          */
+#define PKV_FL_ALIGN 2      /* an entry is not a multiple of page_size (ps > 1) */
+#define PKV_FL_RANGE 4      /* an entry outside [0, num_pages * page_size)      */
+#define PKV_FL_DUPLICATE 8  /* a page listed more than once                     */
+
+/*
+ * pkv_check_free_list -- the free-list integrity check as a device reduction
+ * (same page, section "The integrity check": check_integrity requires
+ * len(free_slots) + cache_pages == num_pages and, for page_size > 1, every
+ * entry a multiple of page_size).  Two more checks serve what the section
+ * says the check is for (a page forgotten or freed twice): every entry is the
+ * start of a pool page, and no page is listed twice.
+ *
+ * Enqueues the zeroing of *result and of the bitmap, then one kernel that
+ * ORs PKV_FL_* bits into *result.  An entry failing the alignment check is
+ * not checked further; one outside the pool is not checked for duplicates.
+ *   free_slots [free_count] int32 (device); num_pages, cache_pages >= 0;
+ *   bitmap [bitmap_words] uint32 device scratch, bitmap_words >=
+ *   ceil(num_pages / 32); result device int32.
+ * Errors: PKV_EINVAL (NULL pointer, free_count outside [0, 2^31), page_size
+ * < 1, num_pages or cache_pages < 0, num_pages * page_size >= 2^31, bitmap
+ * too small), PKV_ECUDA.
+ */
+int pkv_check_free_list(const int32_t* free_slots, int64_t free_count, int page_size,
+                        int64_t num_pages, int64_t cache_pages, uint32_t* bitmap,
+                        int64_t bitmap_words, int32_t* result, pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

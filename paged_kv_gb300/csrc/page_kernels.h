@@ -25,6 +25,29 @@ struct FillParams {
   bool vec4;                   // 16-byte stores are aligned (ps % 4 == 0, pt_cols % 4 == 0)
 };
 
+// Batched lazy free (free_kernels.cu).
+struct FreeParams {
+  const int32_t* table_idx;    // [B]
+  const int32_t* begin;        // [B] first freed column of the row
+  const int32_t* end;          // [B] one past the last freed column
+  int B;
+  int page_size;
+  const int32_t* page_table;   // [pt_rows, pt_cols]
+  int64_t pt_rows;
+  int64_t pt_cols;
+  int32_t* free_slots;         // [capacity], entries [0, free_count) live
+  int64_t free_count;
+  int64_t capacity;
+  int64_t* total_out;          // device, or nullptr
+  int32_t* status;             // device, or nullptr
+};
+
+size_t free_smem_bytes(int B);
+cudaError_t launch_free_pages(const FreeParams& F, int num_sms, cudaStream_t stream);
+cudaError_t launch_check_free_list(const int32_t* free_slots, int64_t free_count, int page_size,
+                                   int64_t num_pages, int64_t cache_pages, uint32_t* bitmap,
+                                   int32_t* result, int num_sms, cudaStream_t stream);
+
 size_t fill_smem_bytes(int B);
 cudaError_t launch_fill_page_table(const FillParams& F, int num_sms, cudaStream_t stream);
 cudaError_t launch_writeback(const int32_t* tokens, const int32_t* rows, const int64_t* cols,

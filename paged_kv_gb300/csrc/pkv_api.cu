@@ -375,4 +375,73 @@ int pkv_decode_tail(const void* logits, pkv_dtype dt, int B, int V, int64_t row_
                        status, workspace, workspace_bytes, stream, &F);
 }
 
+int pkv_free_pages(const int32_t* table_idx, const int32_t* begin, const int32_t* end, int B,
+                   int page_size, const int32_t* page_table, int64_t pt_rows, int64_t pt_cols,
+                   int32_t* free_slots, int64_t free_count, int64_t free_capacity,
+                   int64_t* total_out, int32_t* status, pkv_stream_t stream) {
+  if (B < 0 || B > PKV_MAX_FILL_BATCH)
+    return fail(PKV_EINVAL, "B=%d outside [0, %d]", B, PKV_MAX_FILL_BATCH);
+  if (page_size < 1) return fail(PKV_EINVAL, "page_size=%d < 1", page_size);
+  if (free_count < 0 || free_capacity < 0 || free_capacity > INT32_MAX || free_count > free_capacity)
+    return fail(PKV_EINVAL, "free_count=%lld, free_capacity=%lld: need 0 <= count <= capacity < 2^31",
+                (long long)free_count, (long long)free_capacity);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0) {
+    if (total_out != nullptr) {
+      const cudaError_t e = cudaMemsetAsync(total_out, 0, sizeof(int64_t), s);
+      if (e != cudaSuccess) return cuda_fail(e, "total_out reset");
+    }
+    return ok();
+  }
+  if (table_idx == nullptr || begin == nullptr || end == nullptr || page_table == nullptr ||
+      free_slots == nullptr)
+    return fail(PKV_EINVAL, "NULL pointer argument");
+  if (pt_rows < 1 || pt_cols < 1) return fail(PKV_EINVAL, "empty page table");
+  pkv::FreeParams F;
+  F.table_idx = table_idx;
+  F.begin = begin;
+  F.end = end;
+  F.B = B;
+  F.page_size = page_size;
+  F.page_table = page_table;
+  F.pt_rows = pt_rows;
+  F.pt_cols = pt_cols;
+  F.free_slots = free_slots;
+  F.free_count = free_count;
+  F.capacity = free_capacity;
+  F.total_out = total_out;
+  F.status = status;
+  const cudaError_t e = pkv::launch_free_pages(F, num_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "free launch");
+  return ok();
+}
+
+int pkv_check_free_list(const int32_t* free_slots, int64_t free_count, int page_size,
+                        int64_t num_pages, int64_t cache_pages, uint32_t* bitmap,
+                        int64_t bitmap_words, int32_t* result, pkv_stream_t stream) {
+  if (result == nullptr || bitmap == nullptr || (free_slots == nullptr && free_count > 0))
+    return fail(PKV_EINVAL, "NULL pointer argument");
+  if (free_count < 0 || free_count > INT32_MAX)
+    return fail(PKV_EINVAL, "free_count=%lld outside [0, 2^31)", (long long)free_count);
+  if (page_size < 1) return fail(PKV_EINVAL, "page_size=%d < 1", page_size);
+  if (num_pages < 0 || cache_pages < 0)
+    return fail(PKV_EINVAL, "num_pages=%lld, cache_pages=%lld: need >= 0", (long long)num_pages,
+                (long long)cache_pages);
+  if (num_pages > INT32_MAX / page_size)
+    return fail(PKV_EINVAL, "num_pages * page_size = %lld * %d is not below 2^31",
+                (long long)num_pages, page_size);
+  const int64_t words = (num_pages + 31) / 32;
+  if (bitmap_words < words)
+    return fail(PKV_EINVAL, "bitmap of %lld words, %lld needed", (long long)bitmap_words,
+                (long long)words);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(result, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess && words > 0) e = cudaMemsetAsync(bitmap, 0, static_cast<size_t>(words) * 4, s);
+  if (e != cudaSuccess) return cuda_fail(e, "integrity scratch reset");
+  e = pkv::launch_check_free_list(free_slots, free_count, page_size, num_pages, cache_pages, bitmap,
+                                  result, num_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "integrity launch");
+  return ok();
+}
+
 }  // extern "C"

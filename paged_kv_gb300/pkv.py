@@ -24,6 +24,7 @@ PKV_OK, PKV_EINVAL, PKV_ENOSPC, PKV_ECUDA, PKV_EUNSUPPORTED = 0, -1, -2, -3, -4
 PKV_FP32, PKV_BF16 = 0, 1
 ST_NONFINITE, ST_ALL_NEG_INF, ST_ROW_OOB, ST_COL_OOB, ST_BAD_UNIFORM, ST_NOSPC = 1, 2, 4, 8, 16, 32
 ST_TIMEOUT = 64
+FL_COUNT, FL_ALIGN, FL_RANGE, FL_DUPLICATE = 1, 2, 4, 8
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +71,11 @@ def load() -> ctypes.CDLL:
             lib.pkv_fill_page_table.restype = i32
             lib.pkv_fill_page_table.argtypes = [vp, vp, vp, i32, i32, vp, i64, vp, i64, i64,
                                                 vp, vp, vp]
+            lib.pkv_free_pages.restype = i32
+            lib.pkv_free_pages.argtypes = [vp, vp, vp, i32, i32, vp, i64, i64, vp, i64, i64,
+                                           vp, vp, vp]
+            lib.pkv_check_free_list.restype = i32
+            lib.pkv_check_free_list.argtypes = [vp, i64, i32, i64, i64, vp, i64, vp, vp]
             _lib = lib
     return _lib
 
@@ -328,4 +334,37 @@ def fill_page_table(cached_len: torch.Tensor, device_len: torch.Tensor, table_id
         _dev(page_table, torch.int32, "page_table"), R, C,
         _dev(total_out, torch.int64, "total_out", 1), _dev(status, torch.int32, "status", 1),
         _stream(stream, page_table.device))
+    _check(rc)
+
+
+def free_pages(table_idx: torch.Tensor, begin: torch.Tensor, end: torch.Tensor, page_size: int,
+               page_table: torch.Tensor, free_slots: torch.Tensor, free_count: int,
+               total_out: Optional[torch.Tensor] = None,
+               status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """pkv_free_pages: append page_table[t, b:e:ps] of every request after the
+    ``free_count`` live entries of ``free_slots`` (whose length is the capacity)."""
+    lib = load()
+    B = table_idx.numel()
+    R, C = page_table.shape
+    rc = lib.pkv_free_pages(
+        _dev(table_idx, torch.int32, "table_idx", B), _dev(begin, torch.int32, "begin", B),
+        _dev(end, torch.int32, "end", B), B, int(page_size),
+        _dev(page_table, torch.int32, "page_table"), R, C,
+        _dev(free_slots, torch.int32, "free_slots"), int(free_count), free_slots.numel(),
+        _dev(total_out, torch.int64, "total_out", 1), _dev(status, torch.int32, "status", 1),
+        _stream(stream, page_table.device))
+    _check(rc)
+
+
+def check_free_list(free_slots: torch.Tensor, free_count: int, page_size: int, num_pages: int,
+                    cache_pages: int, bitmap: torch.Tensor, result: torch.Tensor,
+                    stream=None) -> None:
+    """pkv_check_free_list: OR the FL_* bits of the first ``free_count`` entries
+    into ``result`` (zeroed first); ``bitmap`` is int32 scratch of
+    ceil(num_pages / 32) words."""
+    lib = load()
+    rc = lib.pkv_check_free_list(
+        _dev(free_slots, torch.int32, "free_slots"), int(free_count), int(page_size),
+        int(num_pages), int(cache_pages), _dev(bitmap, torch.int32, "bitmap"), bitmap.numel(),
+        _dev(result, torch.int32, "result", 1), _stream(stream, result.device))
     _check(rc)

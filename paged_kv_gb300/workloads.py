@@ -216,3 +216,32 @@ def random_params(B: int, seed: int, greedy_frac: float = 0.3,
     p = pv[torch.randint(0, len(p_values), (B,), generator=g)]
     u = torch.rand(B, generator=g)
     return t, k, p, u
+
+
+def release_batch(B: int, page_size: int, num_pages: int, seed: int, max_len: int = 2512,
+                  ragged: bool = True):
+    """Seeded inputs of a batched release of finished requests.
+
+    Every request first owns ``device_len`` tokens from position 0 (allocated
+    from ``free_slots``, a permutation of the pool's page starts); then the
+    slice ``[begin, end)`` of its table row is freed.  ``ragged`` mixes whole
+    rows (begin 0), unaligned begins, empty and reversed ranges; otherwise
+    every request frees [0, device_len).  Returns a dict of CPU tensors and
+    the page-table shape.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    device_len = torch.randint(1, max_len + 1, (B,), generator=g).to(torch.int32)
+    table_idx = torch.randperm(B + 1, generator=g)[:B].to(torch.int32)
+    free_slots = (torch.randperm(num_pages, generator=g) * page_size).to(torch.int32)
+    if ragged:
+        begin = torch.randint(0, 2 * page_size + 1, (B,), generator=g).to(torch.int32)
+        end = (device_len - torch.randint(0, 3, (B,), generator=g).to(torch.int32))
+        begin[torch.rand(B, generator=g) < 0.5] = 0
+        end[torch.rand(B, generator=g) < 0.1] = 0  # empty or reversed
+    else:
+        begin = torch.zeros(B, dtype=torch.int32)
+        end = device_len.clone()
+    width = _align_up_32(max_len)
+    return {"device_len": device_len, "table_idx": table_idx, "free_slots": free_slots,
+            "begin": begin, "end": end.to(torch.int32), "pt_shape": (B + 1, width)}

@@ -104,6 +104,28 @@ def test_host_validation_launches_nothing():
     assert rc == pkv.PKV_EINVAL
 
 
+def test_free_path_host_validation_launches_nothing():
+    lib = pkv.load()
+    d = ctypes.c_void_p(16)
+    # B outside [0, 4096], page_size < 1, count above capacity, NULL pointers.
+    assert lib.pkv_free_pages(d, d, d, -1, 4, d, 4, 4, d, 0, 8, None, None, None) == pkv.PKV_EINVAL
+    assert lib.pkv_free_pages(d, d, d, 5000, 4, d, 4, 4, d, 0, 8, None, None, None) == pkv.PKV_EINVAL
+    assert lib.pkv_free_pages(d, d, d, 2, 0, d, 4, 4, d, 0, 8, None, None, None) == pkv.PKV_EINVAL
+    assert "page_size" in pkv.last_error()
+    assert lib.pkv_free_pages(d, d, d, 2, 4, d, 4, 4, d, 9, 8, None, None, None) == pkv.PKV_EINVAL
+    assert "capacity" in pkv.last_error()
+    assert lib.pkv_free_pages(d, None, d, 2, 4, d, 4, 4, d, 0, 8, None, None, None) == pkv.PKV_EINVAL
+    assert lib.pkv_free_pages(d, d, d, 2, 4, d, 0, 4, d, 0, 8, None, None, None) == pkv.PKV_EINVAL
+    # The integrity check: NULL result, pool above 2^31 entries, bitmap too small.
+    assert lib.pkv_check_free_list(d, 4, 4, 4, 0, d, 1, None, None) == pkv.PKV_EINVAL
+    assert lib.pkv_check_free_list(d, 4, 64, 1 << 26, 0, d, 1 << 21, d, None) == pkv.PKV_EINVAL
+    assert "2^31" in pkv.last_error()
+    assert lib.pkv_check_free_list(d, 4, 4, 100, 0, d, 3, d, None) == pkv.PKV_EINVAL
+    assert "bitmap" in pkv.last_error()
+    assert lib.pkv_check_free_list(d, -1, 4, 4, 0, d, 1, d, None) == pkv.PKV_EINVAL
+    assert lib.pkv_check_free_list(d, 4, 4, -4, 0, d, 1, d, None) == pkv.PKV_EINVAL
+
+
 @pytest.mark.parametrize("name", ["pr1", "mixed", "nucleus", "large"])
 def test_host_alloc_pages_matches_oracle(name):
     w = workloads.make(name) if name in ("pr1",) else workloads.make(name, B=64, V=64)
