@@ -34,29 +34,33 @@ __device__ __forceinline__ int64_t div_ceil_len(int32_t a, int32_t b) {
   return (static_cast<int64_t>(a) + b - 1) / b;
 }
 
-// Dynamic shared memory of page_fill_cta: off[B + 1], first[B], row[B].
+// Shared memory of page_fill_cta: 64 words of warp totals and flags, then
+// off[B + 1], first[B], row[B].
+constexpr int kFillHeadWords = 64;
 __host__ __device__ constexpr size_t smem_bytes(int B) {
-  return static_cast<size_t>(3 * B + 1) * sizeof(int32_t);
+  return static_cast<size_t>(kFillHeadWords + 3 * B + 1) * sizeof(int32_t);
 }
 
-// Run by all kT threads of CTA `cta` of `ncta` fill CTAs.
-template <int kT>
+// Run by the kT threads (index tid) of CTA `cta` of `ncta` fill CTAs.
+// sync() is the barrier of those kT threads; smem holds smem_bytes(F.B).
+template <int kT, class Sync>
 __device__ __forceinline__ void page_fill_cta(const FillParams& F, int32_t* smem, int cta,
-                                              int ncta) {
+                                              int ncta, int tid, Sync sync) {
   constexpr int kW = kT / 32;
-  __shared__ int32_t s_warp[kW];
-  __shared__ int s_bad;
+  static_assert(kW < kFillHeadWords, "warp totals fit the head");
+  int32_t* s_warp = smem;
+  int* s_bad = smem + kW;
   const int B = F.B;
-  int32_t* s_off = smem;             // B + 1 exclusive offsets
-  int32_t* s_first = s_off + B + 1;  // first page per request
-  int32_t* s_row = s_first + B;      // table row, or -1 for "skip"
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* s_off = smem + kFillHeadWords;  // B + 1 exclusive offsets
+  int32_t* s_first = s_off + B + 1;        // first page per request
+  int32_t* s_row = s_first + B;            // table row, or -1 for "skip"
+  const int lane = tid & 31, warp = tid >> 5;
   const int ps = F.page_size;
   // Per-thread contiguous run of requests, so the scan keeps batch order.
   const int per = (B + kT - 1) / kT;
   const int i0 = min(B, tid * per);
   const int i1 = min(B, i0 + per);
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) *s_bad = 0;
   int32_t run = 0;
   int bad = 0;
   for (int i = i0; i < i1; ++i) {
@@ -86,9 +90,10 @@ __device__ __forceinline__ void page_fill_cta(const FillParams& F, int32_t* smem
     const int32_t y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
+  sync();  // s_bad is zero before any thread ORs into it
+  if (bad) atomicOr(s_bad, bad);
   if (lane == 31) s_warp[warp] = incl;
-  if (bad) atomicOr(&s_bad, bad);
-  __syncthreads();
+  sync();
   int32_t wbase = 0, total32 = 0;
 #pragma unroll
   for (int w = 0; w < kW; ++w) {
@@ -104,12 +109,12 @@ __device__ __forceinline__ void page_fill_cta(const FillParams& F, int32_t* smem
   }
   const int64_t total = total32;
   if (tid == 0) s_off[B] = total32;
-  __syncthreads();
+  sync();
 
   const bool nospc = total > F.free_count;
   if (cta == 0 && tid == 0) {
     if (F.total_out != nullptr) *F.total_out = nospc ? 0 : total;
-    const int st = (nospc ? kStNoSpc : 0) | s_bad;
+    const int st = (nospc ? kStNoSpc : 0) | *s_bad;
     if (st != 0 && F.status != nullptr) atomicOr(F.status, st);
   }
   if (nospc || total == 0) return;

@@ -23,7 +23,8 @@ constexpr int kStColOOB = 8;
 
 __global__ void __launch_bounds__(kFillThreads) fill_page_table_kernel(const FillParams F) {
   extern __shared__ int32_t smem[];
-  fill::page_fill_cta<kFillThreads>(F, smem, blockIdx.x, gridDim.x);
+  fill::page_fill_cta<kFillThreads>(F, smem, blockIdx.x, gridDim.x, threadIdx.x,
+                                    []() { __syncthreads(); });
 }
 
 __global__ void writeback_kernel(const int32_t* __restrict__ tokens,

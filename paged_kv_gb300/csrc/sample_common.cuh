@@ -70,7 +70,7 @@ constexpr int kFinishDynBytes = kFinOffTable + kHistKeys * 8;
 static_assert(kFinRecBytes % 16 == 0, "aligned regions");
 static_assert(kThreads * 16 * 16 <= kFinOffTable, "a staged chunk (NV <= 16) below the mass table");
 static_assert(kFinListCap * 2 >= kMaxChunks * kThreads, "the thread maxima fit the list region");
-static_assert(kFinishDynBytes >= static_cast<int>((3 * kMaxFillBatch + 1) * 4),
+static_assert(kFinishDynBytes >= static_cast<int>((64 + 3 * kMaxFillBatch + 1) * 4),
               "a fused page-fill CTA's scan fits the finish kernel's shared memory");
 constexpr float kMassScale = 1099511627776.0f;  // 2^40: fixed-point unit of probability mass
 constexpr long long kWaitNs = 500000000ll;      // bound of every wait on a bulk copy (0.5 s)

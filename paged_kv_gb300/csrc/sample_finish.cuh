@@ -762,7 +762,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
     // Fused page allocation and table fill: independent of the stream
     // kernel's output, so these CTAs start at once (no griddepcontrol.wait).
     fill::page_fill_cta<kThreads>(P.fill, reinterpret_cast<int32_t*>(dyn),
-                                  static_cast<int>(blockIdx.x) - P.B, P.fill_ctas);
+                                  static_cast<int>(blockIdx.x) - P.B, P.fill_ctas, threadIdx.x,
+                                  []() { __syncthreads(); });
     return;
   }
   const int C = P.chunks;

@@ -119,6 +119,9 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
         s.i0 = static_cast<int32_t>(a);
         slot->s = s;
       }
+      // Every warp has read the histograms before the group's next item
+      // clears them (there is no group barrier between items otherwise).
+      group_sync();
     }
   }
 }
