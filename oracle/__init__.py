@@ -63,6 +63,9 @@ def _load():
             lib.oracle_free_pages.restype = i32
             lib.oracle_check_free_list.argtypes = [vp, i64, i32, i64, i64]
             lib.oracle_check_free_list.restype = i32
+            lib.oracle_prepare_step.argtypes = [vp, vp, vp, i32, i32, vp, i64, vp, i64, i64,
+                                                vp, i64, i64, vp, vp, vp, i64, vp, vp, vp]
+            lib.oracle_prepare_step.restype = i32
             _lib = lib
     return _lib
 
@@ -210,3 +213,37 @@ def check_free_list(free_slots, page_size: int, num_pages: int, cache_pages: int
     fs = _np(free_slots, np.int32)
     return int(lib.oracle_check_free_list(_ptr(fs), len(fs), int(page_size), int(num_pages),
                                           int(cache_pages)))
+
+
+def prepare_step(cached_len, device_len, table_idx, page_size: int, free_slots,
+                 page_table: np.ndarray, token_pool, max_tokens: int) -> dict:
+    """The step before the model: allocate and fill the new pages of every
+    request in ``page_table`` (in place), then pack the positions
+    [cached_len, device_len) in batch order and gather ``input_ids`` from the
+    token pool and ``out_loc`` from the page table at (table_idx, position).
+    Returns the three packed int32 arrays (length = the token count when it
+    is at most ``max_tokens``, else empty), the totals, status bits and rc."""
+    lib = _load()
+    c = _np(cached_len, np.int32)
+    d = _np(device_len, np.int32)
+    t = _np(table_idx, np.int32)
+    fs = _np(free_slots, np.int32)
+    pool = _np(token_pool, np.int32)
+    if page_table.dtype != np.int32 or not page_table.flags.c_contiguous:
+        raise TypeError("page_table must be a C-contiguous int32 array")
+    R, C = page_table.shape
+    PR, PC = pool.shape
+    cap = max(int(max_tokens), 0)
+    pos = np.full(cap, -7, np.int32)
+    ids = np.full(cap, -7, np.int32)
+    loc = np.full(cap, -7, np.int32)
+    pages = np.zeros(1, np.int64)
+    ntok = np.zeros(1, np.int64)
+    status = np.zeros(1, np.int32)
+    rc = lib.oracle_prepare_step(_ptr(c), _ptr(d), _ptr(t), len(c), int(page_size), _ptr(fs),
+                                 len(fs), _ptr(page_table), R, C, _ptr(pool), PR, PC, _ptr(pos),
+                                 _ptr(ids), _ptr(loc), int(max_tokens), _ptr(pages), _ptr(ntok),
+                                 _ptr(status))
+    n = int(ntok[0]) if rc == 0 else 0
+    return {"rc": int(rc), "positions": pos[:n], "input_ids": ids[:n], "out_loc": loc[:n],
+            "total_pages": int(pages[0]), "total_tokens": int(ntok[0]), "status": int(status[0])}

@@ -11,7 +11,7 @@
 //   * "The engine and the sampler" -- sections "The sampler" (Sampler.prepare,
 //     Sampler.sample, sample_torch) and "Tests" (test_sampler_greedy_and_filters);
 //   * "The scheduler skeleton and the offline interface" -- section "Preparing a
-//     batch" (_make_write_tuple, Scheduler._forward);
+//     batch" (_prepare_batch, _make_write_tuple, Scheduler._forward);
 //   * "CacheManager: allocation, release and admission control" -- sections
 //     "The free-page list", "Allocating pages for this step's tokens"
 //     (allocate_paged, _write_page_table), the self-test answer 4, "Freeing,
@@ -421,6 +421,77 @@ int oracle_check_free_list(const int32_t* free_slots, int64_t free_count, int pa
     seen[page] = 1;
   }
   return bits;
+}
+
+// The step before the model, Scheduler._prepare_batch and Scheduler._forward
+// ("The scheduler skeleton and the offline interface", section "Preparing a
+// batch"), in their order:
+//   1. allocate_paged: the new pages of every request are taken from the
+//      free list and written into the page table (oracle_fill_page_table);
+//   2. _make_positions: the positions [cached_len, device_len) of every
+//      request, packed into one array in batch order;
+//   3. the input tuple (table_idx, position) of each packed token gathers
+//      input_ids = token_pool[input tuple] and out_loc = page_table[input
+//      tuple], the latter after step 1.
+// READINGS: a request with device_len <= cached_len has no tokens.  The token
+// count is checked before anything is written: above max_tokens, status bit
+// 128, return -3, nothing written.  When the pages do not fit (status 32,
+// return -2) nothing is written either and *total_pages is 0.  A request
+// whose gathers would leave the token pool or the page table (a table row
+// outside either, cached_len < 0, device_len past either's columns, or new
+// pages that the fill skipped) still gets its positions, its input_ids and
+// out_loc entries are -1, and status bit 4 (row) or 8 (column) is set.
+// *total_tokens is always the step's token count.
+int oracle_prepare_step(const int32_t* cached_len, const int32_t* device_len,
+                        const int32_t* table_idx, int B, int page_size,
+                        const int32_t* free_slots, int64_t free_count, int32_t* page_table,
+                        int64_t pt_rows, int64_t pt_cols, const int32_t* token_pool,
+                        int64_t pool_rows, int64_t pool_cols, int32_t* positions,
+                        int32_t* input_ids, int32_t* out_loc, int64_t max_tokens,
+                        int64_t* total_pages, int64_t* total_tokens, int32_t* status) {
+  *status = 0;
+  *total_pages = 0;
+  int64_t ntok = 0;
+  for (int i = 0; i < B; ++i) {
+    if (device_len[i] > cached_len[i]) ntok += static_cast<int64_t>(device_len[i]) - cached_len[i];
+  }
+  *total_tokens = ntok;
+  if (ntok > max_tokens) {
+    *status = 128;
+    return -3;
+  }
+  // 1. pages.
+  int32_t fill_status = 0;
+  int64_t pages = 0;
+  const int rc = oracle_fill_page_table(cached_len, device_len, table_idx, B, page_size,
+                                        free_slots, free_count, page_table, pt_rows, pt_cols,
+                                        &pages, &fill_status);
+  *status |= fill_status;
+  if (rc != 0) return rc;
+  *total_pages = pages;
+  // 2. and 3. positions and the two gathers, request by request.
+  int64_t j = 0;
+  for (int i = 0; i < B; ++i) {
+    const int64_t c = cached_len[i], d = device_len[i];
+    if (d <= c) continue;
+    const int64_t first = div_ceil(c, page_size), last = div_ceil(d, page_size);
+    const int64_t t = table_idx[i];
+    bool ok = true;
+    if (t < 0 || t >= pt_rows || t >= pool_rows) {
+      *status |= kRowOOB;
+      ok = false;
+    } else if (c < 0 || d > pt_cols || d > pool_cols ||
+               (last > first && last * page_size > pt_cols)) {
+      *status |= kColOOB;
+      ok = false;
+    }
+    for (int64_t pos = c; pos < d; ++pos, ++j) {
+      positions[j] = static_cast<int32_t>(pos);
+      input_ids[j] = ok ? token_pool[t * pool_cols + pos] : -1;
+      out_loc[j] = ok ? page_table[t * pt_cols + pos] : -1;
+    }
+  }
+  return 0;
 }
 
 }  // extern "C"

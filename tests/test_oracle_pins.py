@@ -410,3 +410,111 @@ def test_free_errors_write_nothing_or_skip():
     out = oracle.free_pages([5, 1, 2], [0, 6, 0], [2, 9, 3], 2, pt, cap, 2)
     assert out["rc"] == 0 and out["status"] == 4 | 8 and out["total"] == 2
     assert cap.tolist() == [100, 101, 16, 18]
+
+
+# ---------------------------------------------------------------- golden + second statement: the step before the model
+
+
+def test_prepare_selftest_example():
+    # The pages' self-test 4 numbers run through _prepare_batch by hand.
+    g = _golden("prepare_selftest.json")
+    pt = np.zeros(g["pt_shape"], np.int32)
+    pt[1, :8] = g["pt_row1_prefix"]
+    pool = np.zeros((2, 16), np.int32)
+    pool[1] = g["pool_row1"]
+    r = oracle.prepare_step(g["cached_len"], g["device_len"], g["table_idx"], g["page_size"],
+                            g["free_slots"], pt, pool, 16)
+    assert r["rc"] == 0 and r["status"] == 0
+    assert r["positions"].tolist() == g["expected_positions"]
+    assert r["input_ids"].tolist() == g["expected_input_ids"]
+    assert r["out_loc"].tolist() == g["expected_out_loc"]
+    assert pt[1].tolist() == g["expected_row1"]
+    assert (r["total_pages"], r["total_tokens"]) == (g["expected_total_pages"],
+                                                     g["expected_total_tokens"])
+
+
+def _batch4_state(g):
+    ps = g["page_size"]
+    pt = np.zeros(g["pt_shape"], np.int32)
+    for i, (c, t) in enumerate(zip(g["cached_len"], g["table_idx"])):
+        first = -(-c // ps)
+        pt[t, :first * ps] = 1000 * (t + 1) + np.arange(first * ps)
+    pool = (100 * np.arange(g["pool_shape"][0])[:, None] + np.arange(g["pool_shape"][1])[None, :])
+    free = np.arange(g["num_free_pages"], dtype=np.int32) * ps
+    return pt, pool.astype(np.int32), free
+
+
+def test_prepare_batch_hand_example():
+    g = _golden("prepare_batch4.json")
+    pt, pool, free = _batch4_state(g)
+    r = oracle.prepare_step(g["cached_len"], g["device_len"], g["table_idx"], g["page_size"],
+                            free, pt, pool, 64)
+    assert r["rc"] == 0 and r["status"] == 0
+    assert r["positions"].tolist() == g["expected_positions"]
+    assert r["input_ids"].tolist() == g["expected_input_ids"]
+    assert r["out_loc"].tolist() == g["expected_out_loc"]
+    assert (r["total_pages"], r["total_tokens"]) == (g["expected_total_pages"],
+                                                     g["expected_total_tokens"])
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prepare_matches_the_offline_slices(seed):
+    # The offline example on the same page builds the same three arrays from
+    # slices: positions = cat(arange(cached, device)), the inputs =
+    # cat(token row[cached:device]), out_loc = cat(page_table[row,
+    # cached:device]).  The oracle gathers token by token through the input
+    # tuple; the two statements must agree (page table taken after the fill).
+    rng = np.random.default_rng(100 + seed)
+    B, ps = 12, int(rng.choice([1, 4, 16]))
+    cached = rng.integers(0, 60, B).astype(np.int32)
+    device = (cached + rng.integers(0, 40, B)).astype(np.int32)
+    tidx = rng.permutation(B + 3)[:B].astype(np.int32)
+    cols = ((int(device.max()) + ps - 1) // ps) * ps
+    pt = rng.integers(0, 1 << 20, (B + 3, cols)).astype(np.int32)
+    pool = rng.integers(0, 1 << 17, (B + 3, cols + 5)).astype(np.int32)
+    free = (rng.permutation(4096) * ps).astype(np.int32)
+    pt_after = pt.copy()
+    fill = oracle.fill_page_table(cached, device, tidx, ps, free, pt_after)
+    assert fill["rc"] == 0
+    r = oracle.prepare_step(cached, device, tidx, ps, free, pt, pool, 1 << 14)
+    assert r["rc"] == 0 and r["status"] == 0
+    np.testing.assert_array_equal(pt, pt_after)
+    want_pos = np.concatenate([np.arange(c, d) for c, d in zip(cached, device)]).astype(np.int32)
+    want_ids = np.concatenate([pool[t, c:d] for t, c, d in zip(tidx, cached, device)])
+    want_loc = np.concatenate([pt_after[t, c:d] for t, c, d in zip(tidx, cached, device)])
+    np.testing.assert_array_equal(r["positions"], want_pos)
+    np.testing.assert_array_equal(r["input_ids"], want_ids)
+    np.testing.assert_array_equal(r["out_loc"], want_loc)
+    assert r["total_tokens"] == int((device - cached).sum())
+    # Page-aligned free list: every position in a new page lands at the same
+    # offset inside its page ("writes page-aligned token positions"), and the
+    # new pages are the free list's first entries in batch order.
+    first = np.concatenate([np.full(d - c, -(-c // ps)) for c, d in zip(cached, device)])
+    new = r["positions"] // ps >= first
+    assert ((r["out_loc"][new] - r["positions"][new]) % ps == 0).all()
+    starts = r["out_loc"][new] - r["positions"][new] % ps
+    assert list(dict.fromkeys(starts.tolist())) == free[:r["total_pages"]].tolist()
+
+
+def test_prepare_errors_write_nothing_or_skip():
+    g = _golden("prepare_batch4.json")
+    pt, pool, free = _batch4_state(g)
+    # Above the token capacity: nothing written, the count still reported.
+    pt0 = pt.copy()
+    r = oracle.prepare_step(g["cached_len"], g["device_len"], g["table_idx"], 4, free, pt, pool, 11)
+    assert r["rc"] == -3 and r["status"] == 128 and r["total_tokens"] == 12
+    np.testing.assert_array_equal(pt, pt0)
+    # Not enough free pages: nothing written.
+    r = oracle.prepare_step(g["cached_len"], g["device_len"], g["table_idx"], 4, free[:3], pt,
+                            pool, 64)
+    assert r["rc"] == -2 and r["status"] == 32 and r["total_pages"] == 0
+    np.testing.assert_array_equal(pt, pt0)
+    # A request in a row outside the pool keeps its positions, gathers -1.
+    small_pool = pool[:3].copy()
+    r = oracle.prepare_step(g["cached_len"], g["device_len"], g["table_idx"], 4, free, pt,
+                            small_pool, 64)
+    assert r["rc"] == 0 and r["status"] == 4
+    assert r["positions"].tolist() == g["expected_positions"]
+    assert r["input_ids"].tolist()[-3:] == [-1, -1, -1]
+    assert r["out_loc"].tolist()[-3:] == [-1, -1, -1]
+    assert r["out_loc"].tolist()[:-3] == g["expected_out_loc"][:-3]
