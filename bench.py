@@ -355,6 +355,17 @@ def run_ours(args):
     alg = algorithmic_bytes(w)
     achieved = alg / (us_k * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
+    # The step before the model on the same batch (pages, positions and the
+    # input_ids / out_loc gathers of every token in [cached_len, device_len)).
+    n_tok = int((w.device_len - w.cached_len).clamp(min=0).sum())
+    prep_pool = torch.zeros(w.pool_shape, dtype=torch.int32, device=device)
+    prep_out = [torch.empty(n_tok, dtype=torch.int32, device=device) for _ in range(3)]
+    prep_tot = [torch.zeros(1, dtype=torch.int64, device=device) for _ in range(2)]
+    ms_p = timed_graph_steps(lambda i: pkv.prepare_step(cached, dev_len, tidx, w.page_size, free,
+                                                        pt, prep_pool, n_tok, *prep_out,
+                                                        *prep_tot, status),
+                             n_k, args.warmup, dist_mod, device)
+    prep_bytes = n_tok * (3 * 4 + 4 + 4) + 12 * w.B
     ms_f = timed_graph_steps(lambda i: pkv.fill_page_table(cached, dev_len, tidx, w.page_size,
                                                            free, pt, total, status),
                              n_k, args.warmup, dist_mod, device)
@@ -406,6 +417,8 @@ def run_ours(args):
                        "l2": f"logits rotate over {nbuf} buffers ({nbuf * logit_bytes >> 20} MiB > 2x L2)"},
             "logits_gbs": round(world * logit_bytes / (ms_per_step * 1e-3) / 1e9, 1),
             "page_fill_us": round(ms_f / n_k * 1e3, 3),
+            "prepare_step": {"us": round(ms_p / n_k * 1e3, 3), "tokens": n_tok,
+                             "gbs": round(prep_bytes / (ms_p / n_k * 1e-3) / 1e9, 1)},
             "roofline": {"bound": "hbm", "kernel": "pkv_sample_batch (stream_kernel + finish_kernel)",
                          "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

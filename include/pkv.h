@@ -58,6 +58,7 @@ typedef enum { PKV_FP32 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_ST_TIMEOUT 64      /* a row's records are missing or untrusted (a
                                   copy did not land in time, or the workspace
                                   was not initialised); the token is -1       */
+#define PKV_ST_TOKEN_CAP 128   /* prepare step: more tokens than max_tokens    */
 
 /* Largest vocabulary the sampler handles for each dtype. */
 #define PKV_MAX_VOCAB_BF16 524288
@@ -277,6 +278,44 @@ int pkv_free_pages(const int32_t* table_idx, const int32_t* begin, const int32_t
                    int page_size, const int32_t* page_table, int64_t pt_rows, int64_t pt_cols,
                    int32_t* free_slots, int64_t free_count, int64_t free_capacity,
                    int64_t* total_out, int32_t* status, pkv_stream_t stream);
+
+/*
+ * pkv_prepare_step -- the step before the model, in one launch ("The
+ * scheduler skeleton and the offline interface", section "Preparing a batch":
+ * Scheduler._prepare_batch, then the input gather of Scheduler._forward):
+ *   1. the page allocation and table fill of pkv_fill_page_table (same
+ *      arguments, same rules, *total_pages_out = pages taken from the front
+ *      of free_slots);
+ *   2. positions = the positions [cached_len[i], device_len[i]) of every
+ *      request, packed in batch order (a request with device_len <=
+ *      cached_len has none);
+ *   3. for packed entry j of request i at position p:
+ *        input_ids[j] = token_pool[table_idx[i], p],
+ *        out_loc[j]   = page_table[table_idx[i], p]  (after step 1).
+ * *total_tokens_out = the step's token count N (always written).  If N >
+ * max_tokens, PKV_ST_TOKEN_CAP is set and nothing else is written; if the
+ * pages do not fit, PKV_ST_NOSPC is set and nothing else is written.  A
+ * request whose gathers would leave the pool or the table (row outside
+ * either: PKV_ST_ROW_OOB; cached_len < 0, device_len past either's columns,
+ * or new pages the fill skipped: PKV_ST_COL_OOB) keeps its positions and gets
+ * -1 in input_ids and out_loc.
+ *   cached_len, device_len, table_idx [B] int32 (device); free_slots
+ *   [free_count] int32 (device); page_table [pt_rows, pt_cols] int32
+ *   (device, written); token_pool [pool_rows, pool_cols] int32 (device, read
+ *   only); positions, input_ids, out_loc [max_tokens] int32 (device,
+ *   written); total_pages_out, total_tokens_out device int64 or NULL; status
+ *   device int32 or NULL.  The caller advances free_slots by the page total.
+ * Errors: those of pkv_fill_page_table, plus PKV_EINVAL for max_tokens
+ * outside [0, 2^31), a NULL or empty token pool, or a NULL output array when
+ * max_tokens > 0; PKV_ECUDA.  B == 0 writes both totals as 0.
+ */
+int pkv_prepare_step(const int32_t* cached_len, const int32_t* device_len,
+                     const int32_t* table_idx, int B, int page_size, const int32_t* free_slots,
+                     int64_t free_count, int32_t* page_table, int64_t pt_rows, int64_t pt_cols,
+                     const int32_t* token_pool, int64_t pool_rows, int64_t pool_cols,
+                     int32_t* positions, int32_t* input_ids, int32_t* out_loc, int64_t max_tokens,
+                     int64_t* total_pages_out, int64_t* total_tokens_out, int32_t* status,
+                     pkv_stream_t stream);
 
 /* Bits of pkv_check_free_list's result. */
 #define PKV_FL_COUNT 1      /* free pages + cached pages != pool pages          */

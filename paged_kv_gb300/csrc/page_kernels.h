@@ -48,6 +48,23 @@ cudaError_t launch_check_free_list(const int32_t* free_slots, int64_t free_count
                                    int64_t num_pages, int64_t cache_pages, uint32_t* bitmap,
                                    int32_t* result, int num_sms, cudaStream_t stream);
 
+// The step before the model (prepare_kernels.cu): the page fill of `fill`
+// plus the packed positions and the two gathers.
+struct PrepareParams {
+  FillParams fill;             // total_out receives the pages allocated
+  const int32_t* token_pool;   // [pool_rows, pool_cols]
+  int64_t pool_rows;
+  int64_t pool_cols;
+  int32_t* positions;          // [max_tokens]
+  int32_t* input_ids;          // [max_tokens]
+  int32_t* out_loc;            // [max_tokens]
+  int64_t max_tokens;
+  int64_t* tokens_out;         // device, or nullptr: the step's token count
+};
+
+size_t prepare_smem_bytes(int B);
+cudaError_t launch_prepare_step(const PrepareParams& Q, int num_sms, cudaStream_t stream);
+
 size_t fill_smem_bytes(int B);
 cudaError_t launch_fill_page_table(const FillParams& F, int num_sms, cudaStream_t stream);
 cudaError_t launch_writeback(const int32_t* tokens, const int32_t* rows, const int64_t* cols,

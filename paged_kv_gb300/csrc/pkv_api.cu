@@ -375,6 +375,46 @@ int pkv_decode_tail(const void* logits, pkv_dtype dt, int B, int V, int64_t row_
                        status, workspace, workspace_bytes, stream, &F);
 }
 
+int pkv_prepare_step(const int32_t* cached_len, const int32_t* device_len,
+                     const int32_t* table_idx, int B, int page_size, const int32_t* free_slots,
+                     int64_t free_count, int32_t* page_table, int64_t pt_rows, int64_t pt_cols,
+                     const int32_t* token_pool, int64_t pool_rows, int64_t pool_cols,
+                     int32_t* positions, int32_t* input_ids, int32_t* out_loc, int64_t max_tokens,
+                     int64_t* total_pages_out, int64_t* total_tokens_out, int32_t* status,
+                     pkv_stream_t stream) {
+  pkv::PrepareParams Q;
+  const int bad = fill_args(cached_len, device_len, table_idx, B, page_size, free_slots,
+                            free_count, page_table, pt_rows, pt_cols, total_pages_out, status,
+                            &Q.fill);
+  if (bad != PKV_OK) return bad;
+  if (max_tokens < 0 || max_tokens > INT32_MAX)
+    return fail(PKV_EINVAL, "max_tokens=%lld outside [0, 2^31)", (long long)max_tokens);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (B == 0) {
+    for (int64_t* out : {total_pages_out, total_tokens_out}) {
+      if (out == nullptr) continue;
+      const cudaError_t e = cudaMemsetAsync(out, 0, sizeof(int64_t), s);
+      if (e != cudaSuccess) return cuda_fail(e, "total reset");
+    }
+    return ok();
+  }
+  if (token_pool == nullptr) return fail(PKV_EINVAL, "token_pool is NULL");
+  if (pool_rows < 1 || pool_cols < 1) return fail(PKV_EINVAL, "empty token pool");
+  if (max_tokens > 0 && (positions == nullptr || input_ids == nullptr || out_loc == nullptr))
+    return fail(PKV_EINVAL, "NULL output array");
+  Q.token_pool = token_pool;
+  Q.pool_rows = pool_rows;
+  Q.pool_cols = pool_cols;
+  Q.positions = positions;
+  Q.input_ids = input_ids;
+  Q.out_loc = out_loc;
+  Q.max_tokens = max_tokens;
+  Q.tokens_out = total_tokens_out;
+  const cudaError_t e = pkv::launch_prepare_step(Q, num_sms(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "prepare launch");
+  return ok();
+}
+
 int pkv_free_pages(const int32_t* table_idx, const int32_t* begin, const int32_t* end, int B,
                    int page_size, const int32_t* page_table, int64_t pt_rows, int64_t pt_cols,
                    int32_t* free_slots, int64_t free_count, int64_t free_capacity,

@@ -24,6 +24,7 @@ PKV_OK, PKV_EINVAL, PKV_ENOSPC, PKV_ECUDA, PKV_EUNSUPPORTED = 0, -1, -2, -3, -4
 PKV_FP32, PKV_BF16 = 0, 1
 ST_NONFINITE, ST_ALL_NEG_INF, ST_ROW_OOB, ST_COL_OOB, ST_BAD_UNIFORM, ST_NOSPC = 1, 2, 4, 8, 16, 32
 ST_TIMEOUT = 64
+ST_TOKEN_CAP = 128
 FL_COUNT, FL_ALIGN, FL_RANGE, FL_DUPLICATE = 1, 2, 4, 8
 
 _lock = threading.Lock()
@@ -74,6 +75,9 @@ def load() -> ctypes.CDLL:
             lib.pkv_free_pages.restype = i32
             lib.pkv_free_pages.argtypes = [vp, vp, vp, i32, i32, vp, i64, i64, vp, i64, i64,
                                            vp, vp, vp]
+            lib.pkv_prepare_step.restype = i32
+            lib.pkv_prepare_step.argtypes = [vp, vp, vp, i32, i32, vp, i64, vp, i64, i64, vp,
+                                             i64, i64, vp, vp, vp, i64, vp, vp, vp, vp]
             lib.pkv_check_free_list.restype = i32
             lib.pkv_check_free_list.argtypes = [vp, i64, i32, i64, i64, vp, i64, vp, vp]
             _lib = lib
@@ -335,6 +339,50 @@ def fill_page_table(cached_len: torch.Tensor, device_len: torch.Tensor, table_id
         _dev(total_out, torch.int64, "total_out", 1), _dev(status, torch.int32, "status", 1),
         _stream(stream, page_table.device))
     _check(rc)
+
+
+def prepare_step(cached_len: torch.Tensor, device_len: torch.Tensor, table_idx: torch.Tensor,
+                 page_size: int, free_slots: torch.Tensor, page_table: torch.Tensor,
+                 token_pool: torch.Tensor, max_tokens: int,
+                 positions: Optional[torch.Tensor] = None,
+                 input_ids: Optional[torch.Tensor] = None,
+                 out_loc: Optional[torch.Tensor] = None,
+                 total_pages: Optional[torch.Tensor] = None,
+                 total_tokens: Optional[torch.Tensor] = None,
+                 status: Optional[torch.Tensor] = None, stream=None):
+    """pkv_prepare_step: allocate and fill this step's pages, pack the
+    positions [cached_len, device_len) and gather input_ids / out_loc at
+    (table_idx, position).  Returns (positions, input_ids, out_loc,
+    total_pages, total_tokens) as device tensors; the first three hold
+    ``max_tokens`` entries, of which the first total_tokens are the step's."""
+    lib = load()
+    B = cached_len.numel()
+    dev = page_table.device
+    R, C = page_table.shape
+    PR, PC = token_pool.shape
+    n = int(max_tokens)
+
+    def out(t, dtype, k):
+        return t if t is not None else torch.empty(k, dtype=dtype, device=dev)
+
+    positions = out(positions, torch.int32, n)
+    input_ids = out(input_ids, torch.int32, n)
+    out_loc = out(out_loc, torch.int32, n)
+    total_pages = out(total_pages, torch.int64, 1)
+    total_tokens = out(total_tokens, torch.int64, 1)
+    rc = lib.pkv_prepare_step(
+        _dev(cached_len, torch.int32, "cached_len", B), _dev(device_len, torch.int32, "device_len", B),
+        _dev(table_idx, torch.int32, "table_idx", B), B, int(page_size),
+        _dev(free_slots, torch.int32, "free_slots"), free_slots.numel(),
+        _dev(page_table, torch.int32, "page_table"), R, C,
+        _dev(token_pool, torch.int32, "token_pool"), PR, PC,
+        _dev(positions, torch.int32, "positions", n), _dev(input_ids, torch.int32, "input_ids", n),
+        _dev(out_loc, torch.int32, "out_loc", n), n,
+        _dev(total_pages, torch.int64, "total_pages", 1),
+        _dev(total_tokens, torch.int64, "total_tokens", 1),
+        _dev(status, torch.int32, "status", 1), _stream(stream, dev))
+    _check(rc)
+    return positions, input_ids, out_loc, total_pages, total_tokens
 
 
 def free_pages(table_idx: torch.Tensor, begin: torch.Tensor, end: torch.Tensor, page_size: int,

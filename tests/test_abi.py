@@ -126,6 +126,31 @@ def test_free_path_host_validation_launches_nothing():
     assert lib.pkv_check_free_list(d, 4, 4, -4, 0, d, 1, d, None) == pkv.PKV_EINVAL
 
 
+def test_prepare_step_host_validation_launches_nothing():
+    lib = pkv.load()
+    d = ctypes.c_void_p(16)
+    f = lib.pkv_prepare_step
+    ok = dict(cached=d, device=d, table=d, B=2, ps=4, free=d, nfree=8, pt=d, ptr=4, ptc=16,
+              pool=d, pr=4, pc=16, pos=d, ids=d, loc=d, cap=32)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["cached"], a["device"], a["table"], a["B"], a["ps"], a["free"], a["nfree"],
+                 a["pt"], a["ptr"], a["ptc"], a["pool"], a["pr"], a["pc"], a["pos"], a["ids"],
+                 a["loc"], a["cap"], None, None, None, None)
+
+    assert call(B=-1) == pkv.PKV_EINVAL
+    assert call(B=5000) == pkv.PKV_EINVAL
+    assert call(ps=0) == pkv.PKV_EINVAL and "page_size" in pkv.last_error()
+    assert call(cap=-1) == pkv.PKV_EINVAL and "max_tokens" in pkv.last_error()
+    assert call(cap=1 << 31) == pkv.PKV_EINVAL
+    assert call(pool=None) == pkv.PKV_EINVAL and "token_pool" in pkv.last_error()
+    assert call(pr=0) == pkv.PKV_EINVAL
+    assert call(loc=None) == pkv.PKV_EINVAL and "output" in pkv.last_error()
+    assert call(table=None) == pkv.PKV_EINVAL
+    assert call(ptc=0) == pkv.PKV_EINVAL
+
+
 @pytest.mark.parametrize("name", ["pr1", "mixed", "nucleus", "large"])
 def test_host_alloc_pages_matches_oracle(name):
     w = workloads.make(name) if name in ("pr1",) else workloads.make(name, B=64, V=64)
