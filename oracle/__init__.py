@@ -63,6 +63,10 @@ def _load():
             lib.oracle_free_pages.restype = i32
             lib.oracle_check_free_list.argtypes = [vp, i64, i32, i64, i64]
             lib.oracle_check_free_list.restype = i32
+            lib.oracle_philox4x64.argtypes = [vp, vp, vp]
+            lib.oracle_philox4x64.restype = None
+            lib.oracle_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint64, i32, vp]
+            lib.oracle_uniforms.restype = None
             lib.oracle_prepare_step.argtypes = [vp, vp, vp, i32, i32, vp, i64, vp, i64, i64,
                                                 vp, i64, i64, vp, vp, vp, i64, vp, vp, vp]
             lib.oracle_prepare_step.restype = i32
@@ -247,3 +251,22 @@ def prepare_step(cached_len, device_len, table_idx, page_size: int, free_slots,
     n = int(ntok[0]) if rc == 0 else 0
     return {"rc": int(rc), "positions": pos[:n], "input_ids": ids[:n], "out_loc": loc[:n],
             "total_pages": int(pages[0]), "total_tokens": int(ntok[0]), "status": int(status[0])}
+
+
+def philox4x64(counter, key) -> np.ndarray:
+    """One Philox-4x64-10 block: four 64-bit words for a 4-word counter and a
+    2-word key."""
+    lib = _load()
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint64))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64))
+    out = np.empty(4, np.uint64)
+    lib.oracle_philox4x64(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniforms(seed: int, offset: int, B: int) -> np.ndarray:
+    """The B float32 uniforms of call ``offset`` under ``seed`` (one per row)."""
+    lib = _load()
+    u = np.empty(B, np.float32)
+    lib.oracle_uniforms(int(seed) & ((1 << 64) - 1), int(offset) & ((1 << 64) - 1), int(B), _ptr(u))
+    return u

@@ -423,6 +423,56 @@ int oracle_check_free_list(const int32_t* free_slots, int64_t free_count, int pa
   return bits;
 }
 
+// Counter-based uniforms for the draw.  The pages seed one generator per
+// engine (torch.manual_seed(42) in Engine) and rely on every rank making the
+// same random calls in the same order ("The scheduler's IO and multi-rank
+// synchronization", section "Sending results"); a counter-based generator
+// gives each (call, row) its own number with no state to keep in step.
+// Philox-4x64 with 10 rounds, from its published definition (Salmon, Moraes,
+// Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011):
+// each round multiplies words 0 and 2 by two odd constants, takes the high
+// and low halves, and mixes them with words 1 and 3 and the round key; the
+// key is bumped by two Weyl increments (the golden ratio and sqrt(3) - 1,
+// scaled to 64 bits) between rounds.
+void oracle_philox4x64(const uint64_t* ctr, const uint64_t* key, uint64_t* out) {
+  const uint64_t m0 = 0xD2E7470EE14C6C93ull, m1 = 0xCA5A826395121157ull;
+  const uint64_t w0 = 0x9E3779B97F4A7C15ull, w1 = 0xBB67AE8584CAA73Bull;
+  uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint64_t k0 = key[0], k1 = key[1];
+  for (int round = 0; round < 10; ++round) {
+    const unsigned __int128 p0 = static_cast<unsigned __int128>(m0) * x0;
+    const unsigned __int128 p1 = static_cast<unsigned __int128>(m1) * x2;
+    const uint64_t hi0 = static_cast<uint64_t>(p0 >> 64), lo0 = static_cast<uint64_t>(p0);
+    const uint64_t hi1 = static_cast<uint64_t>(p1 >> 64), lo1 = static_cast<uint64_t>(p1);
+    const uint64_t y0 = hi1 ^ x1 ^ k0, y1 = lo1, y2 = hi0 ^ x3 ^ k1, y3 = lo0;
+    x0 = y0;
+    x1 = y1;
+    x2 = y2;
+    x3 = y3;
+    k0 += w0;
+    k1 += w1;
+  }
+  out[0] = x0;
+  out[1] = x1;
+  out[2] = x2;
+  out[3] = x3;
+}
+
+// The uniform of row b in call `offset` under `seed`: the first word of the
+// Philox block at counter (b, offset, 0, 0) with key (seed, 0), its top 24
+// bits scaled by 2^-24 (exact in fp32, in [0, 1)).  READING: the pages fix
+// only the seed; the counter layout and the 24-bit conversion are this
+// library's choices.
+void oracle_uniforms(uint64_t seed, uint64_t offset, int B, float* u) {
+  const uint64_t key[2] = {seed, 0};
+  for (int b = 0; b < B; ++b) {
+    const uint64_t ctr[4] = {static_cast<uint64_t>(b), offset, 0, 0};
+    uint64_t out[4];
+    oracle_philox4x64(ctr, key, out);
+    u[b] = static_cast<float>(static_cast<double>(out[0] >> 40) * (1.0 / 16777216.0));
+  }
+}
+
 // The step before the model, Scheduler._prepare_batch and Scheduler._forward
 // ("The scheduler skeleton and the offline interface", section "Preparing a
 // batch"), in their order:

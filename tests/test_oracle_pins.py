@@ -518,3 +518,47 @@ def test_prepare_errors_write_nothing_or_skip():
     assert r["input_ids"].tolist()[-3:] == [-1, -1, -1]
     assert r["out_loc"].tolist()[-3:] == [-1, -1, -1]
     assert r["out_loc"].tolist()[:-3] == g["expected_out_loc"][:-3]
+
+
+
+# ---------------------------------------------------------------- library routine: the counter-based uniforms
+
+
+def _numpy_block(counter, key):
+    # numpy's Philox advances its counter before producing a block, so the
+    # block of counter c comes out of a generator whose counter is c - 1.
+    c = [int(x) for x in counter]
+    i = 0
+    while c[i] == 0:
+        c[i] = (1 << 64) - 1
+        i += 1
+    c[i] -= 1
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=np.array(c, dtype=np.uint64))
+    return bg.random_raw(4).astype(np.uint64)
+
+
+@pytest.mark.parametrize("counter,key", [
+    ((1, 0, 0, 0), (0, 0)),
+    ((5, 42, 0, 0), (42, 0)),
+    ((0, 3, 0, 0), (7, 9)),                      # a borrow into the second word
+    ((2**64 - 1, 2**64 - 1, 5, 1), (2**64 - 1, 2**64 - 1)),
+    ((123456789, 987654321, 2**40, 2**63), (0xDEADBEEF, 0xC0FFEE)),
+])
+def test_philox_block_matches_numpy(counter, key):
+    np.testing.assert_array_equal(oracle.philox4x64(counter, key), _numpy_block(counter, key))
+
+
+def test_uniforms_are_the_top_24_bits_of_word_0():
+    seed, offset, B = 42, 17, 300
+    u = oracle.uniforms(seed, offset, B)
+    assert u.dtype == np.float32 and ((u >= 0) & (u < 1)).all()
+    for b in (0, 1, 2, 299):
+        x0 = int(_numpy_block((b, offset, 0, 0), (seed, 0))[0])
+        assert u[b] == np.float32((x0 >> 40) / 2**24)
+    # Closed form of the conversion at its ends: 24-bit values k map to k / 2^24.
+    k = (u.astype(np.float64) * 2**24)
+    np.testing.assert_array_equal(k, np.floor(k))
+    # Calls and seeds give different streams; the same (seed, call) repeats.
+    assert not np.array_equal(u, oracle.uniforms(seed, offset + 1, B))
+    assert not np.array_equal(u, oracle.uniforms(seed + 1, offset, B))
+    np.testing.assert_array_equal(u, oracle.uniforms(seed, offset, B))
