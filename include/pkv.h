@@ -317,6 +317,26 @@ int pkv_prepare_step(const int32_t* cached_len, const int32_t* device_len,
                      int64_t* total_pages_out, int64_t* total_tokens_out, int32_t* status,
                      pkv_stream_t stream);
 
+/*
+ * pkv_philox_uniforms -- the uniforms of one sampler call, generated on the
+ * device so the draw needs no host input.  The pages seed one generator per
+ * engine (torch.manual_seed(42) in Engine) and rely on every tensor-parallel
+ * rank making the same random calls ("The scheduler's IO and multi-rank
+ * synchronization", section "Sending results"); a counter-based generator
+ * gives each (call, row) its own number, so ranks that pass the same seed and
+ * call number agree by construction.
+ *
+ * uniform[b] = (word 0 of Philox-4x64-10(counter = (b, offset, 0, 0),
+ * key = (seed, 0))) >> 40, times 2^-24: in [0, 1), exact in fp32.  Philox
+ * as published by Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+ * easy as 1, 2, 3" (SC 2011).  `offset` is the caller's call number (e.g.
+ * the decode step).
+ *   uniform [B] float (device, written); B in [0, 65535].
+ * Errors: PKV_EINVAL (B out of range, NULL uniform with B > 0), PKV_ECUDA.
+ */
+int pkv_philox_uniforms(uint64_t seed, uint64_t offset, int B, float* uniform,
+                        pkv_stream_t stream);
+
 /* Bits of pkv_check_free_list's result. */
 #define PKV_FL_COUNT 1      /* free pages + cached pages != pool pages          */
 #define PKV_FL_ALIGN 2      /* an entry is not a multiple of page_size (ps > 1) */

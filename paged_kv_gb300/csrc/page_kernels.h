@@ -65,6 +65,9 @@ struct PrepareParams {
 size_t prepare_smem_bytes(int B);
 cudaError_t launch_prepare_step(const PrepareParams& Q, int num_sms, cudaStream_t stream);
 
+// Counter-based uniforms of one sampler call (philox_kernels.cu).
+cudaError_t launch_uniforms(uint64_t seed, uint64_t offset, int B, float* u, cudaStream_t stream);
+
 size_t fill_smem_bytes(int B);
 cudaError_t launch_fill_page_table(const FillParams& F, int num_sms, cudaStream_t stream);
 cudaError_t launch_writeback(const int32_t* tokens, const int32_t* rows, const int64_t* cols,

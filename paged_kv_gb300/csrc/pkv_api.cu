@@ -415,6 +415,17 @@ int pkv_prepare_step(const int32_t* cached_len, const int32_t* device_len,
   return ok();
 }
 
+int pkv_philox_uniforms(uint64_t seed, uint64_t offset, int B, float* uniform,
+                        pkv_stream_t stream) {
+  if (B < 0 || B > 65535) return fail(PKV_EINVAL, "B=%d outside [0, 65535]", B);
+  if (B == 0) return ok();
+  if (uniform == nullptr) return fail(PKV_EINVAL, "uniform is NULL");
+  const cudaError_t e =
+      pkv::launch_uniforms(seed, offset, B, uniform, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "uniforms launch");
+  return ok();
+}
+
 int pkv_free_pages(const int32_t* table_idx, const int32_t* begin, const int32_t* end, int B,
                    int page_size, const int32_t* page_table, int64_t pt_rows, int64_t pt_cols,
                    int32_t* free_slots, int64_t free_count, int64_t free_capacity,

@@ -78,6 +78,8 @@ def load() -> ctypes.CDLL:
             lib.pkv_prepare_step.restype = i32
             lib.pkv_prepare_step.argtypes = [vp, vp, vp, i32, i32, vp, i64, vp, i64, i64, vp,
                                              i64, i64, vp, vp, vp, i64, vp, vp, vp, vp]
+            lib.pkv_philox_uniforms.restype = i32
+            lib.pkv_philox_uniforms.argtypes = [ctypes.c_uint64, ctypes.c_uint64, i32, vp, vp]
             lib.pkv_check_free_list.restype = i32
             lib.pkv_check_free_list.argtypes = [vp, i64, i32, i64, i64, vp, i64, vp, vp]
             _lib = lib
@@ -383,6 +385,20 @@ def prepare_step(cached_len: torch.Tensor, device_len: torch.Tensor, table_idx: 
         _dev(status, torch.int32, "status", 1), _stream(stream, dev))
     _check(rc)
     return positions, input_ids, out_loc, total_pages, total_tokens
+
+
+def philox_uniforms(seed: int, offset: int, B: int, out: Optional[torch.Tensor] = None,
+                    device=None, stream=None) -> torch.Tensor:
+    """pkv_philox_uniforms: the B float32 uniforms of call ``offset`` under
+    ``seed``, generated on the device."""
+    if out is None:
+        out = torch.empty(int(B), dtype=torch.float32,
+                          device=device if device is not None else "cuda")
+    rc = load().pkv_philox_uniforms(int(seed) & ((1 << 64) - 1), int(offset) & ((1 << 64) - 1),
+                                    int(B), _dev(out, torch.float32, "out", int(B)),
+                                    _stream(stream, out.device))
+    _check(rc)
+    return out
 
 
 def free_pages(table_idx: torch.Tensor, begin: torch.Tensor, end: torch.Tensor, page_size: int,

@@ -151,6 +151,15 @@ def test_prepare_step_host_validation_launches_nothing():
     assert call(ptc=0) == pkv.PKV_EINVAL
 
 
+def test_philox_uniforms_host_validation_launches_nothing():
+    lib = pkv.load()
+    d = ctypes.c_void_p(16)
+    assert lib.pkv_philox_uniforms(42, 0, -1, d, None) == pkv.PKV_EINVAL
+    assert lib.pkv_philox_uniforms(42, 0, 65536, d, None) == pkv.PKV_EINVAL
+    assert lib.pkv_philox_uniforms(42, 0, 4, None, None) == pkv.PKV_EINVAL
+    assert lib.pkv_philox_uniforms(42, 0, 0, None, None) == pkv.PKV_OK
+
+
 @pytest.mark.parametrize("name", ["pr1", "mixed", "nucleus", "large"])
 def test_host_alloc_pages_matches_oracle(name):
     w = workloads.make(name) if name in ("pr1",) else workloads.make(name, B=64, V=64)
