@@ -51,6 +51,9 @@ def _load():
             lib.oracle_sample.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp,
                                           vp, vp, vp, vp, vp, vp, i32]
             lib.oracle_sample.restype = i32
+            lib.oracle_sample_ex.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp,
+                                             vp, vp, vp, vp, vp, vp, vp, i32]
+            lib.oracle_sample_ex.restype = i32
             lib.oracle_writeback.argtypes = [vp, vp, vp, i32, vp, i64, i64]
             lib.oracle_writeback.restype = i32
             lib.oracle_alloc_pages.argtypes = [vp, vp, i32, i32, i64, vp, vp, vp, vp]
@@ -110,13 +113,14 @@ def logits_bits(logits):
 
 
 def sample(logits, temperature=None, top_k=None, top_p=None, uniform=None,
-           want_probs: bool = False, threads: int = 1) -> dict:
+           want_probs: bool = False, threads: int = 1, min_p=None) -> dict:
     """Sample one token per row of ``logits`` [B, V] (fp32 or bf16).
 
     ``temperature=None`` is the all-greedy batch; rows with temperature <= 0
-    are greedy.  ``top_k`` / ``top_p`` None mean "off".  Returns a dict with
-    ``tokens`` (int32), ``probs`` (fp64 [B, V] or None), ``topp_margin``,
-    ``cdf_margin``, ``kept`` and ``row_status``.
+    are greedy.  ``top_k`` / ``top_p`` / ``min_p`` None mean "off".  Returns a
+    dict with ``tokens`` (int32), ``probs`` (fp64 [B, V] or None),
+    ``topp_margin``, ``cdf_margin``, ``minp_margin``, ``kept`` and
+    ``row_status``.
     """
     lib = _load()
     bits, dcode = logits_bits(logits)
@@ -135,11 +139,13 @@ def sample(logits, temperature=None, top_k=None, top_p=None, uniform=None,
     cm = np.empty(B, np.float64)
     kept = np.empty(B, np.int32)
     st = np.empty(B, np.int32)
-    lib.oracle_sample(_ptr(bits), dcode, B, V, V, _ptr(t), _ptr(k), _ptr(p), _ptr(u),
-                      _ptr(tokens), _ptr(probs), _ptr(tm), _ptr(cm), _ptr(kept),
-                      _ptr(st), int(threads))
+    mp = _np(min_p, np.float32)
+    mm = np.empty(B, np.float64)
+    lib.oracle_sample_ex(_ptr(bits), dcode, B, V, V, _ptr(t), _ptr(k), _ptr(p), _ptr(mp),
+                         _ptr(u), _ptr(tokens), _ptr(probs), _ptr(tm), _ptr(cm), _ptr(mm),
+                         _ptr(kept), _ptr(st), int(threads))
     return {"tokens": tokens, "probs": probs, "topp_margin": tm, "cdf_margin": cm,
-            "kept": kept, "row_status": st}
+            "minp_margin": mm, "kept": kept, "row_status": st}
 
 
 def writeback(tokens, rows, cols, pool: np.ndarray) -> int:

@@ -60,6 +60,7 @@ struct RowResult {
   int32_t status = 0;
   double topp_margin = INFINITY;  // min over K of |before_i / Z_k - p|
   double cdf_margin = INFINITY;   // min over S of |u - c_i|
+  double minp_margin = INFINITY;  // min over S (before min_p) of |w_i / min_p - 1|
 };
 
 // Greedy decoding: the page's all-greedy path is torch.argmax.  READING: ties
@@ -92,8 +93,12 @@ RowResult greedy_row(const std::vector<double>& l, double* q_row) {
 //      probability mass before it is >= p                    (before = cumsum - p)
 //   5. renormalise what is left and draw by inverse CDF in vocab order
 //      (the probabilities are scattered back to vocab order before drawing).
+// With min_p > 0 (exercise 2 of the same page and its answer), step 4b drops
+// from S every token whose probability is below min_p times the largest
+// probability: a mask on the full tempered distribution, intersected with
+// the top-k / top-p set.
 RowResult sampled_row(const std::vector<double>& l, double T, int k, double p,
-                      double u, double* q_row) {
+                      double min_p, double u, double* q_row) {
   RowResult r;
   const int V = static_cast<int>(l.size());
   bool any_finite = false;
@@ -153,6 +158,17 @@ RowResult sampled_row(const std::vector<double>& l, double T, int k, double p,
     for (int i = 0; i < V; ++i) in_s[i] = in_k[i];
   }
 
+  // Step 4b: p_i / p_max = exp((l_i - m) / T) = w_i, since m is the row
+  // maximum.  READING: the mask is intersected with S as computed above (top-p
+  // is not recomputed on the masked distribution).
+  if (min_p > 0.0) {
+    for (int i = 0; i < V; ++i) {
+      if (!in_s[i]) continue;
+      r.minp_margin = std::min(r.minp_margin, std::fabs(w[i] / min_p - 1.0));
+      if (w[i] < min_p) in_s[i] = 0;
+    }
+  }
+
   // Step 5: renormalise over S and scan S in ascending vocab index.
   double zs = 0.0;
   int kept = 0;
@@ -184,10 +200,10 @@ RowResult sampled_row(const std::vector<double>& l, double T, int k, double p,
 
 void sample_rows(const void* logits, int dtype, int V, int64_t row_stride,
                  const float* temperature, const int32_t* top_k,
-                 const float* top_p, const float* uniform, int row_begin,
-                 int row_end, int32_t* tokens, double* probs,
-                 double* topp_margin, double* cdf_margin, int32_t* kept,
-                 int32_t* row_status) {
+                 const float* top_p, const float* min_p, const float* uniform,
+                 int row_begin, int row_end, int32_t* tokens, double* probs,
+                 double* topp_margin, double* cdf_margin, double* minp_margin,
+                 int32_t* kept, int32_t* row_status) {
   std::vector<double> l(V);
   for (int b = row_begin; b < row_end; ++b) {
     for (int i = 0; i < V; ++i) l[i] = load_logit(logits, dtype, b * row_stride + i);
@@ -210,12 +226,16 @@ void sample_rows(const void* logits, int dtype, int V, int64_t row_stride,
       if (top_p != nullptr) {
         p = std::min(std::max(static_cast<double>(top_p[b]), 1e-6), 1.0);
       }
+      // READING: min_p NULL, <= 0 or NaN is off; above 1 it is 1.
+      double mp = 0.0;
+      if (min_p != nullptr && min_p[b] > 0.0f) mp = std::min(static_cast<double>(min_p[b]), 1.0);
       const double u = static_cast<double>(uniform[b]);
-      r = sampled_row(l, T, k, p, u, q_row);
+      r = sampled_row(l, T, k, p, mp, u, q_row);
     }
     tokens[b] = r.token;
     if (topp_margin) topp_margin[b] = r.topp_margin;
     if (cdf_margin) cdf_margin[b] = r.cdf_margin;
+    if (minp_margin) minp_margin[b] = r.minp_margin;
     if (kept) kept[b] = r.kept;
     if (row_status) row_status[b] = r.status;
   }
@@ -234,19 +254,19 @@ extern "C" {
 // optional dense probabilities q [B, V] (fp64), the top-p and CDF margins,
 // |S| and the row status bits.  n_threads > 1 splits rows over std::threads.
 // Returns the OR of all row status bits.
-int oracle_sample(const void* logits, int dtype, int B, int V, int64_t row_stride,
-                  const float* temperature, const int32_t* top_k,
-                  const float* top_p, const float* uniform, int32_t* tokens,
-                  double* probs, double* topp_margin, double* cdf_margin,
-                  int32_t* kept, int32_t* row_status, int n_threads) {
+int oracle_sample_ex(const void* logits, int dtype, int B, int V, int64_t row_stride,
+                     const float* temperature, const int32_t* top_k,
+                     const float* top_p, const float* min_p, const float* uniform,
+                     int32_t* tokens, double* probs, double* topp_margin, double* cdf_margin,
+                     double* minp_margin, int32_t* kept, int32_t* row_status, int n_threads) {
   std::vector<int32_t> local_status;
   if (row_status == nullptr) {
     local_status.assign(B, 0);
     row_status = local_status.data();
   }
   if (n_threads <= 1 || B <= 1) {
-    sample_rows(logits, dtype, V, row_stride, temperature, top_k, top_p, uniform,
-                0, B, tokens, probs, topp_margin, cdf_margin, kept, row_status);
+    sample_rows(logits, dtype, V, row_stride, temperature, top_k, top_p, min_p, uniform,
+                0, B, tokens, probs, topp_margin, cdf_margin, minp_margin, kept, row_status);
   } else {
     const int nt = std::min(n_threads, B);
     std::vector<std::thread> pool;
@@ -254,14 +274,25 @@ int oracle_sample(const void* logits, int dtype, int B, int V, int64_t row_strid
       const int b0 = static_cast<int>(static_cast<int64_t>(B) * t / nt);
       const int b1 = static_cast<int>(static_cast<int64_t>(B) * (t + 1) / nt);
       pool.emplace_back(sample_rows, logits, dtype, V, row_stride, temperature,
-                        top_k, top_p, uniform, b0, b1, tokens, probs,
-                        topp_margin, cdf_margin, kept, row_status);
+                        top_k, top_p, min_p, uniform, b0, b1, tokens, probs,
+                        topp_margin, cdf_margin, minp_margin, kept, row_status);
     }
     for (auto& th : pool) th.join();
   }
   int all = 0;
   for (int b = 0; b < B; ++b) all |= row_status[b];
   return all;
+}
+
+// oracle_sample_ex with min_p off for every row.
+int oracle_sample(const void* logits, int dtype, int B, int V, int64_t row_stride,
+                  const float* temperature, const int32_t* top_k,
+                  const float* top_p, const float* uniform, int32_t* tokens,
+                  double* probs, double* topp_margin, double* cdf_margin,
+                  int32_t* kept, int32_t* row_status, int n_threads) {
+  return oracle_sample_ex(logits, dtype, B, V, row_stride, temperature, top_k, top_p, nullptr,
+                          uniform, tokens, probs, topp_margin, cdf_margin, nullptr, kept,
+                          row_status, n_threads);
 }
 
 // Token write-back, Scheduler._forward: token_pool[rows[b], cols[b]] = tok[b].

@@ -20,8 +20,10 @@ def rank_of(l, i):
     return sum(1 for j in range(len(l)) if l[j] > l[i] or (l[j] == l[i] and j < i))
 
 
-def kept_probabilities(l, T, k, p):
-    """{token: q} over the kept set S of one sampled row."""
+def kept_probabilities(l, T, k, p, min_p=0.0):
+    """{token: q} over the kept set S of one sampled row.  min_p > 0 keeps
+    only the tokens whose probability is at least min_p times the largest
+    (exercise 2 of the same page), intersected with the top-k / top-p set."""
     V = len(l)
     if k < 1 or k >= V:
         k = V
@@ -35,6 +37,9 @@ def kept_probabilities(l, T, k, p):
              if sum(w[j] for j in K if ranks[j] < ranks[i]) / zk < p]
     else:
         S = K
+    if min_p > 0.0:
+        pmax = max(math.exp((l[j] - m) / T) for j in range(V))  # 1 at the maximum
+        S = [i for i in S if w[i] / pmax >= min(min_p, 1.0)]
     zs = sum(w[i] for i in S)
     return {i: w[i] / zs for i in S}
 
@@ -49,5 +54,5 @@ def draw(q, u):
     return max(i for i in q if q[i] > 0)
 
 
-def sample_row(l, T, k, p, u):
-    return draw(kept_probabilities(l, T, k, p), u)
+def sample_row(l, T, k, p, u, min_p=0.0):
+    return draw(kept_probabilities(l, T, k, p, min_p), u)

@@ -562,3 +562,69 @@ def test_uniforms_are_the_top_24_bits_of_word_0():
     assert not np.array_equal(u, oracle.uniforms(seed, offset + 1, B))
     assert not np.array_equal(u, oracle.uniforms(seed + 1, offset, B))
     np.testing.assert_array_equal(u, oracle.uniforms(seed, offset, B))
+
+
+# ---------------------------------------------------------------- closed forms + brute force: min_p
+
+
+def _sample_minp(values, T, min_p, k=-1, p=1.0, u=0.5):
+    return oracle.sample(_row(values), torch.tensor([T]), torch.tensor([k], dtype=torch.int32),
+                         torch.tensor([p]), torch.tensor([u]), want_probs=True,
+                         min_p=torch.tensor([min_p]))
+
+
+def test_min_p_page_example_closed_forms():
+    # The pages' test row [5, 4, 3, 0, 0, 0] at T = 1: probabilities relative
+    # to the largest are 1, e^-1 = 0.368, e^-2 = 0.135, e^-5 = 0.0067.
+    l = [5.0, 4.0, 3.0, 0.0, 0.0, 0.0]
+    q = _sample_minp(l, 1.0, 0.3)["probs"][0]  # keeps tokens 0 and 1
+    assert np.count_nonzero(q) == 2
+    assert abs(q[0] - math.e ** 5 / (math.e ** 5 + math.e ** 4)) < 1e-12  # 0.73106
+    assert np.count_nonzero(_sample_minp(l, 1.0, 0.5)["probs"][0]) == 1
+    q = _sample_minp(l, 1.0, 0.1)["probs"][0]  # e^-2 >= 0.1 > e^-5
+    z = math.e ** 5 + math.e ** 4 + math.e ** 3
+    np.testing.assert_allclose(q[:3], [math.e ** 5 / z, math.e ** 4 / z, math.e ** 3 / z],
+                               atol=1e-12)
+    assert not q[3:].any()
+    # Temperature scales the threshold: at T = 2, e^(-1/2) = 0.61 >= 0.5.
+    assert np.count_nonzero(_sample_minp(l, 2.0, 0.5)["probs"][0]) == 2
+
+
+def test_min_p_intersects_with_top_k_and_top_p():
+    l = [5.0, 4.0, 3.0, 0.0, 0.0, 0.0]
+    # top_k = 2 keeps {0, 1}; min_p = 0.1 alone keeps {0, 1, 2}: the intersection.
+    assert set(np.nonzero(_sample_minp(l, 1.0, 0.1, k=2)["probs"][0])[0]) == {0, 1}
+    # top_p = 0.5 keeps {0}; min_p = 0.3 keeps {0, 1}.
+    assert set(np.nonzero(_sample_minp(l, 1.0, 0.3, p=0.5)["probs"][0])[0]) == {0}
+    # min_p = 1 keeps the maximum only (tie-free row): the argmax.
+    rng = np.random.default_rng(4)
+    row = rng.normal(0, 3, 500).astype(np.float32)
+    r = _sample_minp(row.tolist(), 0.8, 1.0, u=0.77)
+    assert r["tokens"][0] == int(np.argmax(row)) and np.count_nonzero(r["probs"][0]) == 1
+    # Off (0 or negative) and tiny values change nothing on a narrow row.
+    narrow = (rng.random(200) * 2).astype(np.float32).tolist()
+    base = _sample1(narrow, 1.0, u=0.3)["probs"][0]
+    for mp in (0.0, -1.0, 1e-30):
+        np.testing.assert_array_equal(_sample_minp(narrow, 1.0, mp, u=0.3)["probs"][0], base)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_min_p_brute_force_tiny_vocab(seed):
+    rng = np.random.default_rng(300 + seed)
+    for _ in range(40):
+        V = int(rng.integers(1, 17))
+        l = np.asarray(rng.normal(0, 2, V), np.float32).astype(np.float64).tolist()
+        T = float(np.float32(rng.choice([0.3, 0.7, 1.0, 1.8])))
+        k = int(rng.choice([-1, 2, 3, V]))
+        p = float(np.float32(rng.choice([1.0, 0.9, 0.5])))
+        mp = float(np.float32(rng.choice([0.01, 0.1, 0.4, 0.9])))
+        u = float(np.float32(rng.random()))
+        res = _sample_minp(l, T, mp, k=k, p=p, u=u)
+        q_bf = brute_force.kept_probabilities(l, T, k, p, mp)
+        q = res["probs"][0]
+        if res["minp_margin"][0] > 1e-9 and res["topp_margin"][0] > 1e-9:
+            assert set(np.nonzero(q)[0].tolist()) == set(i for i in q_bf if q_bf[i] > 0)
+            for i, qi in q_bf.items():
+                assert abs(q[i] - qi) < 1e-12
+            if res["cdf_margin"][0] > 1e-9:
+                assert res["tokens"][0] == brute_force.sample_row(l, T, k, p, u, mp)
