@@ -355,6 +355,14 @@ def run_ours(args):
     alg = algorithmic_bytes(w)
     achieved = alg / (us_k * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
+    # The same batch with min_p = 0.05 on every row (sampled rows then take
+    # the exact path).
+    minp = torch.full((w.B,), 0.05, dtype=torch.float32, device=device)
+    ms_m = timed_graph_steps(lambda i: pkv.sample_batch(bufs[i % nbuf], t, k, p, u,
+                                                        out_tokens=out, status=status,
+                                                        min_p=minp),
+                             max(50, n_k // 4), args.warmup, dist_mod, device)
+    us_m = ms_m / max(50, n_k // 4) * 1e3
     # The step before the model on the same batch (pages, positions and the
     # input_ids / out_loc gathers of every token in [cached_len, device_len)).
     n_tok = int((w.device_len - w.cached_len).clamp(min=0).sum())
@@ -417,6 +425,7 @@ def run_ours(args):
                        "l2": f"logits rotate over {nbuf} buffers ({nbuf * logit_bytes >> 20} MiB > 2x L2)"},
             "logits_gbs": round(world * logit_bytes / (ms_per_step * 1e-3) / 1e9, 1),
             "page_fill_us": round(ms_f / n_k * 1e3, 3),
+            "minp_us": round(us_m, 3),
             "prepare_step": {"us": round(ms_p / n_k * 1e3, 3), "tokens": n_tok,
                              "gbs": round(prep_bytes / (ms_p / n_k * 1e-3) / 1e9, 1)},
             "roofline": {"bound": "hbm", "kernel": "pkv_sample_batch (stream_kernel + finish_kernel)",

@@ -144,6 +144,26 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
                      void* workspace, size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * pkv_sample_batch_ex -- pkv_sample_batch with a min_p filter ("The engine and
+ * the sampler", exercise 2 and its answer): in a sampled row, a token stays
+ * only if its probability is at least min_p[b] times the row's largest
+ * probability (on the full distribution after temperature scaling), a mask
+ * intersected with the top-k / top-p set before the renormalisation and the
+ * draw.  min_p [B] float (device) or NULL (off for every row); a value <= 0
+ * or NaN is off, above 1 is 1.  Greedy rows ignore it.  Rows with min_p on
+ * take the exact path (selects over the row in global memory), slower than
+ * the other rows.  All other arguments, the meaning and the errors are those
+ * of pkv_sample_batch, which equals this call with min_p NULL.
+ */
+int pkv_sample_batch_ex(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                        const float* temperature, const int32_t* top_k, const float* top_p,
+                        const float* min_p, const float* uniform, int32_t* out_tokens,
+                        int32_t* token_pool, int64_t pool_rows, int64_t pool_cols,
+                        const int32_t* wb_rows, const int64_t* wb_cols, float* probs_out,
+                        int32_t* status, void* workspace, size_t workspace_bytes,
+                        pkv_stream_t stream);
+
+/*
  * pkv_sample_batch_noalloc -- pkv_sample_batch without a caller workspace.
  *
  * Same arguments, meaning and errors as pkv_sample_batch, minus the

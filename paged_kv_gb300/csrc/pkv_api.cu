@@ -192,7 +192,7 @@ namespace {
 // pkv_sample_batch, with an optional page fill run by extra finish CTAs.
 int sample_launch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
                   const float* temperature, const int32_t* top_k, const float* top_p,
-                  const float* uniform, int32_t* out_tokens, int32_t* token_pool,
+                  const float* min_p, const float* uniform, int32_t* out_tokens, int32_t* token_pool,
                   int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
                   const int64_t* wb_cols, float* probs_out, int32_t* status, void* workspace,
                   size_t workspace_bytes, pkv_stream_t stream, const pkv::FillParams* fill) {
@@ -224,6 +224,7 @@ int sample_launch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_st
   P.temperature = temperature;
   P.top_k = top_k;
   P.top_p = top_p;
+  P.min_p = min_p;
   P.uniform = uniform;
   P.out_tokens = out_tokens;
   P.token_pool = token_pool;
@@ -255,9 +256,21 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
                      int64_t pool_rows, int64_t pool_cols, const int32_t* wb_rows,
                      const int64_t* wb_cols, float* probs_out, int32_t* status,
                      void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
-  return sample_launch(logits, dt, B, V, row_stride, temperature, top_k, top_p, uniform,
-                       out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols, probs_out,
-                       status, workspace, workspace_bytes, stream, nullptr);
+  return sample_launch(logits, dt, B, V, row_stride, temperature, top_k, top_p, nullptr,
+                       uniform, out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols,
+                       probs_out, status, workspace, workspace_bytes, stream, nullptr);
+}
+
+int pkv_sample_batch_ex(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
+                        const float* temperature, const int32_t* top_k, const float* top_p,
+                        const float* min_p, const float* uniform, int32_t* out_tokens,
+                        int32_t* token_pool, int64_t pool_rows, int64_t pool_cols,
+                        const int32_t* wb_rows, const int64_t* wb_cols, float* probs_out,
+                        int32_t* status, void* workspace, size_t workspace_bytes,
+                        pkv_stream_t stream) {
+  return sample_launch(logits, dt, B, V, row_stride, temperature, top_k, top_p, min_p,
+                       uniform, out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols,
+                       probs_out, status, workspace, workspace_bytes, stream, nullptr);
 }
 
 int pkv_sample_batch_noalloc(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
@@ -370,9 +383,9 @@ int pkv_decode_tail(const void* logits, pkv_dtype dt, int B, int V, int64_t row_
         cudaMemsetAsync(total_out, 0, sizeof(int64_t), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "total_out reset");
   }
-  return sample_launch(logits, dt, B, V, row_stride, temperature, top_k, top_p, uniform,
-                       out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols, nullptr,
-                       status, workspace, workspace_bytes, stream, &F);
+  return sample_launch(logits, dt, B, V, row_stride, temperature, top_k, top_p, nullptr,
+                       uniform, out_tokens, token_pool, pool_rows, pool_cols, wb_rows, wb_cols,
+                       nullptr, status, workspace, workspace_bytes, stream, &F);
 }
 
 int pkv_prepare_step(const int32_t* cached_len, const int32_t* device_len,

@@ -751,8 +751,8 @@ __device__ __forceinline__ float row_select(const SampleParams& P, int row, K&& 
 
 template <bool BF16>
 __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& sm, const Ctx& c,
-                                             int row, int k, bool use_p, float p, float u,
-                                             float m, float c2, int st, float* q_row) {
+                                             int row, int k, bool use_p, float p, float minp,
+                                             float u, float m, float c2, int st, float* q_row) {
   const int V = P.V;
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   // ---- top-k: the k-th key by count, ties cut by index.
@@ -794,7 +794,13 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
   }
   const float tpf = tp;
   const int cpf = cp;
-  auto in_s = [&](float x, int e) { return in_k(x, e) && (x > tpf || (x == tpf && e < cpf)); };
+  // min_p: a token stays when its probability is at least minp times the
+  // largest one, weight(x) = 2^((x - m) * c2) >= minp (the row maximum m has
+  // weight 1, so the set never empties).
+  auto in_s = [&](float x, int e) {
+    return in_k(x, e) && (x > tpf || (x == tpf && e < cpf)) &&
+           (minp <= 0.0f || weight(x, m, c2) >= minp);
+  };
   // ---- draw in index order over contiguous segments.
   const int per = (V + kThreads - 1) / kThreads;
   const int i0 = min(V, tid * per);
@@ -849,6 +855,7 @@ __device__ __noinline__ void leader_fallback(const SampleParams& P, SampleSmem& 
 // decision in both kernels).
 struct RowParams {
   float T, p, u, c2;
+  float minp;  // 0 when min_p is off, else in (0, 1]
   int k;     // V when top-k is off
   int st;    // status bits found so far (a bad uniform)
   int kind;
@@ -866,6 +873,7 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
   r.k = V;
   r.st = 0;
   r.kind = kKindG;
+  r.minp = 0.0f;
   const bool greedy = P.temperature == nullptr || !(P.temperature[row] > 0.0f);
   if (!greedy) {
     r.T = fmaxf(P.temperature[row], 1e-6f);
@@ -883,7 +891,12 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
     // at least k threads whose elements all lie inside the row.
     const int full_threads = V / (NV * L::VW);
     (void)C;
-    if (k < V && k <= kMaxK && full_threads >= k) {
+    // min_p (off when <= 0 or NaN, at most 1): its rows take the exact path.
+    const float mp = P.min_p != nullptr ? P.min_p[row] : 0.0f;
+    r.minp = mp > 0.0f ? fminf(mp, 1.0f) : 0.0f;
+    if (r.minp > 0.0f) {
+      r.kind = kKindF;
+    } else if (k < V && k <= kMaxK && full_threads >= k) {
       r.kind = kKindK;
     } else if (k == V && !(r.p < 1.0f)) {
       r.kind = kKindP;

@@ -876,7 +876,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
       group_sync();
     }
   }
-  leader_fallback<BF16>(P, sm, c, row, rp.k, rp.use_p, rp.p, rp.u, m, rp.c2, rp.st, q_row);
+  leader_fallback<BF16>(P, sm, c, row, rp.k, rp.use_p, rp.p, rp.minp, rp.u, m, rp.c2, rp.st,
+                        q_row);
 }
 
 }  // namespace pkv

@@ -47,6 +47,7 @@ struct SampleParams {
   const float* temperature;  // [B] or nullptr (all greedy)
   const int32_t* top_k;      // [B] or nullptr
   const float* top_p;        // [B] or nullptr
+  const float* min_p;        // [B] or nullptr (off)
   const float* uniform;      // [B] (sampled rows)
   int32_t* out_tokens;       // [B]
   int32_t* token_pool;       // [pool_rows, pool_cols] or nullptr

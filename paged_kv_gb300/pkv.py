@@ -62,6 +62,9 @@ def load() -> ctypes.CDLL:
                                             i64, vp, i64, i64, vp, vp]
             lib.pkv_sample_workspace_init.restype = i32
             lib.pkv_sample_workspace_init.argtypes = [vp, sz, vp]
+            lib.pkv_sample_batch_ex.restype = i32
+            lib.pkv_sample_batch_ex.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp,
+                                                vp, i64, i64, vp, vp, vp, vp, vp, sz, vp]
             lib.pkv_sample_batch.restype = i32
             lib.pkv_sample_batch.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp, vp, vp,
                                              i64, i64, vp, vp, vp, vp, vp, sz, vp]
@@ -158,8 +161,10 @@ def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = Non
                  token_pool: Optional[torch.Tensor] = None,
                  wb_rows: Optional[torch.Tensor] = None, wb_cols: Optional[torch.Tensor] = None,
                  probs_out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                 workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """pkv_sample_batch: one int32 token per row of ``logits`` [B, V].
+                 workspace: Optional[torch.Tensor] = None, stream=None,
+                 min_p: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """pkv_sample_batch: one int32 token per row of ``logits`` [B, V]
+    (pkv_sample_batch_ex when ``min_p`` is given).
 
     ``logits`` is fp32 or bf16 with unit column stride (any row stride).
     ``workspace`` (a uint8 CUDA tensor, initialised once with
@@ -190,10 +195,15 @@ def sample_batch(logits: torch.Tensor, temperature: Optional[torch.Tensor] = Non
         workspace = _workspace(logits.device, need)
     if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
         raise TypeError("workspace must be a contiguous uint8 CUDA tensor")
-    rc = lib.pkv_sample_batch(
-        logits.data_ptr(), dcode, B, V, logits.stride(0),
-        _dev(temperature, torch.float32, "temperature", B),
-        _dev(top_k, torch.int32, "top_k", B), _dev(top_p, torch.float32, "top_p", B),
+    head = (logits.data_ptr(), dcode, B, V, logits.stride(0),
+            _dev(temperature, torch.float32, "temperature", B),
+            _dev(top_k, torch.int32, "top_k", B), _dev(top_p, torch.float32, "top_p", B))
+    if min_p is not None:
+        call = lambda *rest: lib.pkv_sample_batch_ex(  # noqa: E731
+            *head, _dev(min_p, torch.float32, "min_p", B), *rest)
+    else:
+        call = lambda *rest: lib.pkv_sample_batch(*head, *rest)  # noqa: E731
+    rc = call(
         _dev(uniform, torch.float32, "uniform", B), _dev(out_tokens, torch.int32, "out_tokens", B),
         _dev(token_pool, torch.int32, "token_pool"), pool_rows, pool_cols,
         _dev(wb_rows, torch.int32, "wb_rows", B), _dev(wb_cols, torch.int64, "wb_cols", B),

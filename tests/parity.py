@@ -41,13 +41,16 @@ def _as_np(x):
 
 
 def check_sampler(logits: torch.Tensor, temperature, top_k, top_p, uniform,
-                  gpu_tokens, gpu_probs=None, ores=None) -> dict:
-    """Asserts parity; returns counts of checked / excused rows."""
+                  gpu_tokens, gpu_probs=None, ores=None, min_p=None) -> dict:
+    """Asserts parity; returns counts of checked / excused rows.  Rows whose
+    min_p boundary lies within TOL of a kept token's relative probability are
+    excused like the top-p boundary rows (and only counted)."""
     logits = logits.detach().cpu()
     B, V = logits.shape
     if ores is None:
         ores = oracle.sample(logits, temperature, top_k, top_p, uniform,
-                             want_probs=gpu_probs is not None, threads=8)
+                             want_probs=gpu_probs is not None, threads=8, min_p=min_p)
+    mp = _as_np(min_p)
     t = _as_np(temperature)
     k = _as_np(top_k)
     p = _as_np(top_p)
@@ -55,7 +58,8 @@ def check_sampler(logits: torch.Tensor, temperature, top_k, top_p, uniform,
     gt = _as_np(gpu_tokens).astype(np.int64)
     gq = _as_np(gpu_probs)
     lf = logits.double().numpy()
-    stats = {"greedy": 0, "exact": 0, "excused_cdf": 0, "excused_topp": 0, "probs_checked": 0}
+    stats = {"greedy": 0, "exact": 0, "excused_cdf": 0, "excused_topp": 0, "excused_minp": 0,
+             "probs_checked": 0}
     for b in range(B):
         ot = int(ores["tokens"][b])
         greedy = t is None or not (t[b] > 0)
@@ -65,8 +69,14 @@ def check_sampler(logits: torch.Tensor, temperature, top_k, top_p, uniform,
             if gq is not None and ot >= 0:
                 assert gq[b, ot] == 1.0 and np.count_nonzero(gq[b]) == 1
             continue
+        if ores["minp_margin"][b] < TOL:
+            stats["excused_minp"] += 1
+            continue
         topp_ok = ores["topp_margin"][b] >= TOL
         cdf_ok = ores["cdf_margin"][b] >= TOL
+        if not topp_ok and mp is not None and mp[b] > 0:
+            stats["excused_topp"] += 1
+            continue
         if topp_ok and cdf_ok:
             assert gt[b] == ot, (f"row {b}: gpu token {gt[b]} oracle {ot} "
                                  f"(margins topp {ores['topp_margin'][b]:.3g}, "
