@@ -150,10 +150,10 @@ int pkv_sample_batch(const void* logits, pkv_dtype dt, int B, int V, int64_t row
  * probability (on the full distribution after temperature scaling), a mask
  * intersected with the top-k / top-p set before the renormalisation and the
  * draw.  min_p [B] float (device) or NULL (off for every row); a value <= 0
- * or NaN is off, above 1 is 1.  Greedy rows ignore it.  Rows with min_p on
- * take the exact path (selects over the row in global memory), slower than
- * the other rows.  All other arguments, the meaning and the errors are those
- * of pkv_sample_batch, which equals this call with min_p NULL.
+ * or NaN is off, above 1 is 1.  Greedy rows ignore it.  A sampled row with
+ * no other filter becomes a filtered row (slower than a plain one).  All
+ * other arguments, the meaning and the errors are those of
+ * pkv_sample_batch, which equals this call with min_p NULL.
  */
 int pkv_sample_batch_ex(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,
                         const float* temperature, const int32_t* top_k, const float* top_p,

@@ -891,14 +891,13 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
     // at least k threads whose elements all lie inside the row.
     const int full_threads = V / (NV * L::VW);
     (void)C;
-    // min_p (off when <= 0 or NaN, at most 1): its rows take the exact path.
+    // min_p (off when <= 0 or NaN, at most 1) is one more cut on the kept
+    // set of every filtered kind; a row with no other filter is filtered.
     const float mp = P.min_p != nullptr ? P.min_p[row] : 0.0f;
     r.minp = mp > 0.0f ? fminf(mp, 1.0f) : 0.0f;
-    if (r.minp > 0.0f) {
-      r.kind = kKindF;
-    } else if (k < V && k <= kMaxK && full_threads >= k) {
+    if (k < V && k <= kMaxK && full_threads >= k) {
       r.kind = kKindK;
-    } else if (k == V && !(r.p < 1.0f)) {
+    } else if (k == V && !(r.p < 1.0f) && !(r.minp > 0.0f)) {
       r.kind = kKindP;
     } else {
       r.kind = BF16 ? kKindH : kKindF;

@@ -341,7 +341,8 @@ __device__ __forceinline__ bool finish_topk(const SampleParams& P, SampleSmem& s
     if (target < 1ull) target = 1ull;
     if (target > zk) target = zk;
   }
-  const bool kept = in_k && before < target;
+  // min_p: weights fall with the rank, so the cut keeps S a prefix.
+  const bool kept = in_k && before < target && (rp.minp <= 0.0f || wf >= rp.minp);
   const int s = block_max_int(kept ? tid + 1 : 0, sm.wi, lane, warp);  // S = the first s of the order
   // ---- draw in index order over S: entry t goes to position pos_t.
   unsigned long long* wpos = sm.scan;  // the candidate ids are consumed
@@ -500,7 +501,22 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     is = block_min_int(cand, sm.wi, lane, warp);
     rs = sm.bl[1];
   }
-  if (is >= kHistKeys) return false;  // unreachable when the masses add up
+  if (rp.minp > 0.0f) {
+    // min_p: the first key whose weight is below minp ends the kept set (key
+    // 0, the row maximum, weighs 1).
+    int cut = INT_MAX;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int i = 4 * tid + jj;
+      if (weight(key16_float(A - static_cast<uint32_t>(i)), m, rp.c2) < rp.minp) cut = min(cut, i);
+    }
+    cut = block_min_int(cut, sm.wi, lane, warp);
+    if (cut <= is) {
+      is = cut;
+      rs = 0;
+    }
+  }
+  if (is >= kHistKeys) return false;  // a cut below the window: the exact path
   const unsigned long long wcut = table[is];
   // ---- per-chunk mass of S above the cut key and the cut key's members.
   for (int r = warp; r < C; r += kWarps) {

@@ -68,3 +68,19 @@ def test_minp_off_equals_the_plain_call_and_one_is_argmax():
     check_sampler(w.logits, w.temperature, w.top_k, w.top_p, w.uniform, one, min_p=ones)
     lf = w.logits.float()
     assert (lf[torch.arange(w.B), torch.as_tensor(one, dtype=torch.long)] == lf.max(dim=1).values).all()
+
+
+def test_minp_on_large_topk_histogram_rows():
+    # top_k = 1024 then top_p = 0.95 (bf16 histogram rows with a top-k), plus min_p.
+    w = workloads.large(B=24, V=65536)
+    mp = _minp(w.B, 3, frac=0.7, lo=0.01, hi=0.6)
+    B, V = w.logits.shape
+    probs = torch.empty((B, V), dtype=torch.float32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tok = pkv.sample_batch(_d(w.logits), _d(w.temperature), _d(w.top_k), _d(w.top_p),
+                           _d(w.uniform), probs_out=probs, status=status, min_p=_d(mp))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    st = check_sampler(w.logits, w.temperature, w.top_k, w.top_p, w.uniform, tok.cpu().numpy(),
+                       gpu_probs=probs.cpu().numpy(), min_p=mp)
+    assert st["exact"] + st["excused_cdf"] >= 12
