@@ -640,8 +640,8 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   // reads), one prefix over the CTA, and the element in the thread whose
   // range holds tau.
   const bool active = wstar >= 0 && tid < NV * 16;
-  uint32_t v[2][4];
-  int e0[2];
+  uint32_t v[2][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+  int e0[2] = {0, 0};
   unsigned long long a = 0;
   uint32_t t = 0;
   if (active) {
@@ -679,36 +679,45 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   const unsigned long long p_ex =
       a_ex + wcut * min(static_cast<unsigned long long>(t_ex), static_cast<unsigned long long>(kept_c));
   const bool mine = active && tau >= p_ex && tau < p_in;
-  if (mine) {
-    // Walk the thread's elements with the mass of S before each.
-    unsigned long long above = a_ex;
-    uint32_t tc = t_ex;
-    int sel = -1, last = -1;
+  // The owner of tau (at most one thread) hands its 16 elements to lanes
+  // 0..15 of its warp, in index order; two warp scans give each element the
+  // mass of S before it, and the first element whose interval holds tau is
+  // the token (else the last one that carries mass).
+  const unsigned own = __ballot_sync(kFull, mine);
+  if (own != 0u) {
+    const int ol = __ffs(own) - 1;
+    const int j = lane & 15;
+    const int want = (j >> 3) * 4 + ((j & 7) >> 1);  // word of element j
+    uint32_t word = 0u;
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      for_vec_c<true>(make_uint4(v[k][0], v[k][1], v[k][2], v[k][3]), e0[k], [&](float x, int e) {
-        if (e < V) {
-          const uint32_t i = A - key16(x);
-          const unsigned long long pb =
-              above + wcut * min(static_cast<unsigned long long>(tc),
-                                 static_cast<unsigned long long>(kept_c));
-          unsigned long long w = 0;
-          if (i < static_cast<uint32_t>(is)) {
-            w = table[i];
-            above += w;
-          } else if (i == static_cast<uint32_t>(is)) {
-            w = tc < kept_c ? wcut : 0ull;
-            ++tc;
-          }
-          if (w > 0) {
-            last = e;
-            if (sel < 0 && tau < pb + w) sel = e;
-          }
-        }
-      });
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t x = __shfl_sync(kFull, q < 4 ? v[0][q] : v[1][q - 4], ol);
+      if (q == want) word = x;
     }
-    if (sel < 0) sel = last;
-    emit(P, row, sel, sel < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
+    const int e = __shfl_sync(kFull, e0[0], ol) + j;  // e0[1] = e0[0] + 8
+    const unsigned long long aex = __shfl_sync(kFull, a_ex, ol);
+    const uint32_t tex = __shfl_sync(kFull, t_ex, ol);
+    const float x = elem<true>(word, j & 1);
+    const bool valid = lane < 16 && e < V;
+    const uint32_t i = A - key16(x);
+    const bool above = valid && i < static_cast<uint32_t>(is);
+    const bool tie = valid && i == static_cast<uint32_t>(is);
+    const unsigned long long wa = above ? table[i] : 0ull;
+    const uint32_t ti1 = tie ? 1u : 0u;
+    const unsigned long long abefore = aex + warp_inclusive_scan(wa, lane) - wa;
+    const uint32_t tc = tex + warp_inclusive_scan(ti1, lane) - ti1;
+    const unsigned long long pb =
+        abefore + wcut * min(static_cast<unsigned long long>(tc),
+                             static_cast<unsigned long long>(kept_c));
+    const unsigned long long w = above ? wa : ((tie && tc < kept_c) ? wcut : 0ull);
+    const unsigned hit = __ballot_sync(kFull, w > 0 && tau < pb + w);
+    const unsigned pos = __ballot_sync(kFull, w > 0);
+    const int src = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+    const int sel = __shfl_sync(kFull, e, src < 0 ? 0 : src);
+    if (lane == 0) {
+      const int tok = src < 0 ? -1 : sel;
+      emit(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
+    }
   }
   // No thread's range holds tau only when the masses are not finite.
   if (__syncthreads_or(mine) == 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
