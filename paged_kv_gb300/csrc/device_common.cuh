@@ -256,10 +256,12 @@ __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v)
          lo;
 }
 
-// Inclusive prefix over lanes: lane l gets v_0 + ... + v_l.
+// Inclusive prefix over lanes: lane l gets v_0 + ... + v_l.  Used by code
+// that runs once per row, where instruction fetch sets the pace: a loop
+// keeps one copy of the step's code.
 template <typename T>
 __device__ __forceinline__ T warp_inclusive_scan(T v, int lane) {
-#pragma unroll
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     const T n = __shfl_up_sync(kFull, v, o);
     if (lane >= o) v += n;
@@ -270,7 +272,7 @@ __device__ __forceinline__ T warp_inclusive_scan(T v, int lane) {
 // Inclusive suffix over lanes: lane l gets v_l + ... + v_31.
 template <typename T>
 __device__ __forceinline__ T warp_suffix_scan(T v, int lane) {
-#pragma unroll
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     const T n = __shfl_down_sync(kFull, v, o);
     if (lane + o < 32) v += n;

@@ -379,12 +379,16 @@ __device__ __forceinline__ unsigned long long pick4(const unsigned long long (&a
 
 // ----------------------------------------------------------------- block helpers
 
+// These run once per row in the finish paths, where instruction fetch sets
+// the pace: their loops stay rolled (one copy of the body's code).
+
 template <typename T>
 __device__ __forceinline__ T block_suffix_scan(T v, T* s_w, int lane, int warp) {
   v = warp_suffix_scan(v, lane);
   if (lane == 0) s_w[warp] = v;
   group_sync();
   T add = 0;
+#pragma unroll 1
   for (int w = warp + 1; w < kWarps; ++w) add += s_w[w];
   group_sync();
   return v + add;
@@ -397,6 +401,7 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* s_w, int lane, int war
   if (lane == 31) s_w[warp] = incl;
   group_sync();
   T before = 0, all = 0;
+#pragma unroll 1
   for (int w = 0; w < kWarps; ++w) {
     if (w < warp) before += s_w[w];
     all += s_w[w];
@@ -412,6 +417,7 @@ __device__ __forceinline__ T block_sum(T v, T* s_w, int lane, int warp) {
   if (lane == 0) s_w[warp] = v;
   group_sync();
   T r = 0;
+#pragma unroll 1
   for (int w = 0; w < kWarps; ++w) r += s_w[w];
   group_sync();
   return r;
@@ -422,7 +428,7 @@ __device__ __forceinline__ int block_max_int(int v, int32_t* s_w, int lane, int 
   if (lane == 0) s_w[warp] = v;
   group_sync();
   int r = s_w[0];
-#pragma unroll
+#pragma unroll 1
   for (int w = 1; w < kWarps; ++w) r = max(r, s_w[w]);
   group_sync();
   return r;
@@ -433,7 +439,7 @@ __device__ __forceinline__ int block_min_int(int v, int32_t* s_w, int lane, int 
   if (lane == 0) s_w[warp] = v;
   group_sync();
   int r = s_w[0];
-#pragma unroll
+#pragma unroll 1
   for (int w = 1; w < kWarps; ++w) r = min(r, s_w[w]);
   group_sync();
   return r;
