@@ -181,7 +181,8 @@ __device__ __forceinline__ void finish_plain(const SampleParams& P, SampleSmem& 
       if (lane == ls) {
         float run = incl - sj;
         int lastv = -1;
-        for_vec<BF16>(v4, vec_base<BF16, NV>(r, warp, lane, jstar), [&](float x, int e) {
+        for_vec_c<BF16>(make_uint4(v4[0], v4[1], v4[2], v4[3]),
+                        vec_base<BF16, NV>(r, warp, lane, jstar), [&](float x, int e) {
           const float w = e < V ? weight(x, m, rp.c2) : 0.0f;
           run += w;
           if (w > 0.0f) {
@@ -566,10 +567,9 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   // key plus wcut * min(cut-key members so far, kept): the first kept
   // members count, later ones do not.
   auto above_and_ties = [&](const uint4 v4, int e0, unsigned long long* a, uint32_t* t) {
-    const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
     unsigned long long s = 0;
     uint32_t n = 0;
-    for_vec<true>(w4, e0, [&](float x, int e) {
+    for_vec_c<true>(v4, e0, [&](float x, int e) {
       if (e < V) {
         const uint32_t i = A - key16(x);
         if (i < static_cast<uint32_t>(is)) s += table[i];
