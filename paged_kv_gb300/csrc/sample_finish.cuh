@@ -524,6 +524,7 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     const uint32_t delta = A - static_cast<uint32_t>(recs[r].s.i0);
     const uint16_t* h16 = reinterpret_cast<const uint16_t*>(recs[r].hist);
     unsigned long long part = 0;
+#pragma unroll 1
     for (int i = lane; i < is; i += 32) {
       if (static_cast<uint32_t>(i) >= delta) part += h16[i - delta] * table[i];
     }
@@ -597,18 +598,12 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     unsigned long long a = 0;
     uint32_t t = 0;
 #pragma unroll 1
-    for (int i0 = static_cast<int>(dc); i0 <= is; i0 += 128) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * 32 + lane;
-        if (i <= is) {
-          const uint32_t n = hw[i - static_cast<int>(dc)];
-          if (i < is) {
-            a += n * table[i];
-          } else {
-            t = n;
-          }
-        }
+    for (int i = static_cast<int>(dc) + lane; i <= is; i += 32) {
+      const uint32_t n = hw[i - static_cast<int>(dc)];
+      if (i < is) {
+        a += n * table[i];
+      } else {
+        t = n;
       }
     }
     a = warp_sum_u64(a);
