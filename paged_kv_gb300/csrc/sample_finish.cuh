@@ -429,13 +429,14 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
       if (i >= delta) cnt[jj] += h16[i - delta];
     }
   }
-  unsigned long long wfx[4];
-#pragma unroll
+  // Every key's weight, empty keys included (they only ever meet a zero
+  // count); one rolled loop, read back from the table below.
+#pragma unroll 1
   for (int jj = 0; jj < 4; ++jj) {
     const uint32_t i = static_cast<uint32_t>(4 * tid + jj);
-    wfx[jj] = cnt[jj] ? mass_fx(weight(key16_float(A - i), m, rp.c2)) : 0ull;
-    table[i] = wfx[jj];
+    table[i] = A >= i ? mass_fx(weight(key16_float(A - i), m, rp.c2)) : 0ull;
   }
+  const unsigned long long* wfx = table + 4 * tid;  // this thread's four keys
   // ---- top-k by count: keys i < ik are wholly in K, key ik keeps rk members.
   int ik = kHistKeys;
   unsigned long long rk = 0;
@@ -587,6 +588,7 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   const uint32_t dc = static_cast<uint32_t>(sm.bi[4]);  // merged key i = slice key i - dc
   {
     const uint4* src = ws_slice_hist(P, row, cstar);
+#pragma unroll 1
     for (int k = tid; k < static_cast<int>(kSliceHistBytes / 16); k += kThreads) {
       cp_async16(stage + k, src + k);
     }
@@ -663,6 +665,7 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   group_sync();
   unsigned long long ab = a_w;
   uint32_t tb = t_w;
+#pragma unroll 1
   for (int w = 0; w < warp; ++w) {
     ab += sm.wl[w];
     tb += sm.wu[w];
