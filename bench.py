@@ -479,9 +479,25 @@ def cpu_baseline(w, budget_s: float = 12.0, rows: int = 64) -> dict:
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
+    # The same sample on one thread (a shorter run: 16 rows per pass).
+    one_rows, one_done, t1 = 16, 0, time.perf_counter()
+    one_logits = w.logits[:one_rows].contiguous()
+    one_args = tuple(None if x is None else x[:one_rows] for x in (w.temperature, w.top_k,
+                                                                   w.top_p, w.uniform))
+    while True:
+        oracle.sample(one_logits, *one_args, threads=1)
+        pt = np.zeros(w.pt_shape, np.int32)
+        oracle.fill_page_table(w.cached_len, w.device_len, w.table_idx, w.page_size,
+                               w.free_slots, pt)
+        one_done += one_rows
+        if time.perf_counter() - t1 >= budget_s / 4:
+            break
+    dt1 = time.perf_counter() - t1
     return {"value": round(done / dt, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1_thread": round(one_done / dt1, 2),
             "sample": f"{done} rows of the mixed batch ({rows} per pass, with the full page fill) "
-                      f"in {dt:.1f} s, fp64, {cores} threads"}
+                      f"in {dt:.1f} s, fp64, {cores} threads; one thread: {one_done} rows in "
+                      f"{dt1:.1f} s"}
 
 
 def run_reference(args):
