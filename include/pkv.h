@@ -1,17 +1,22 @@
 /*
  * pkv.h -- C ABI of the decode-step tail: batched per-request sampling with
- * fused token write-back, and paged-KV page allocation / page-table fill.
+ * fused token write-back, and paged-KV page allocation / page-table fill;
+ * plus the step before the model, device uniforms, min_p and the free path.
  *
  * The operations follow "mini-sglang from Scratch":
  *   - sampling: page "The engine and the sampler", section "The sampler"
- *     (Sampler.prepare, Sampler.sample, sample_torch);
- *   - token write-back: page "The scheduler skeleton and the offline
- *     interface", section "Preparing a batch" (_make_write_tuple,
- *     Scheduler._forward);
- *   - page allocation and page-table fill: page "CacheManager: allocation,
- *     release and admission control", sections "The free-page list",
- *     "Allocating pages for this step's tokens" (_allocate, allocate_paged,
- *     _write_page_table).
+ *     (Sampler.prepare, Sampler.sample, sample_torch), and its exercise 2
+ *     (min_p);
+ *   - token write-back and the step before the model: page "The scheduler
+ *     skeleton and the offline interface", section "Preparing a batch"
+ *     (_prepare_batch, _make_write_tuple, Scheduler._forward);
+ *   - page allocation, page-table fill and the free path: page
+ *     "CacheManager: allocation, release and admission control", sections
+ *     "The free-page list", "Allocating pages for this step's tokens"
+ *     (_allocate, allocate_paged, _write_page_table), "Freeing, and freeing
+ *     lazily", "The integrity check";
+ *   - device uniforms: page "The scheduler's IO and multi-rank
+ *     synchronization", section "Sending results" (one seed for every rank).
  *
  * Conventions for every entry point:
  *   - Pointers are DEVICE pointers owned by the caller unless the comment says

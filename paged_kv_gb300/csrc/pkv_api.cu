@@ -67,7 +67,7 @@ extern "C" {
 
 const char* pkv_last_error(void) { return g_err; }
 
-int pkv_version(void) { return 300; }
+int pkv_version(void) { return 310; }
 
 size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt) {
   if (B < 1 || V < 1 || (dt != PKV_FP32 && dt != PKV_BF16)) return 0;

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_workspace():
     lib = pkv.load()
-    assert pkv.version() == 300
+    assert pkv.version() == 310
     # A 256-byte header, 8 KB of finish placement, then per (row, chunk) one
     # 3216-byte record and 16 KB of slice histograms (8 warps x 1024 16-bit
     # counts); the mixed batch's rows are 8 chunks of 20480 bf16.
