@@ -21,6 +21,9 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.cpp")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
+# A prebuilt oracle library to load instead (the mutant test of
+# tests/test_oracle_mutants.py loads copies with one planted mistake each).
+_LIB_OVERRIDE = os.environ.get("PKV_ORACLE_LIB")
 _lock = threading.Lock()
 _lib = None
 
@@ -45,8 +48,11 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            lib = ctypes.CDLL(_LIB_PATH)
+            if _LIB_OVERRIDE:
+                lib = ctypes.CDLL(_LIB_OVERRIDE)
+            else:
+                build()
+                lib = ctypes.CDLL(_LIB_PATH)
             vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
             lib.oracle_sample.argtypes = [vp, i32, i32, i32, i64, vp, vp, vp, vp,
                                           vp, vp, vp, vp, vp, vp, i32]
