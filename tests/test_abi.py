@@ -126,6 +126,23 @@ def test_free_path_host_validation_launches_nothing():
     assert lib.pkv_check_free_list(d, 4, 4, -4, 0, d, 1, d, None) == pkv.PKV_EINVAL
 
 
+def test_sample_batch_ex_validates_like_the_plain_call():
+    lib = pkv.load()
+    d = ctypes.c_void_p(16)
+    # (logits, dt, B, V, stride, T, k, p, min_p, u, out, pool, rows, cols, wb_rows, wb_cols,
+    #  probs, status, workspace, workspace_bytes, stream)
+    f = lib.pkv_sample_batch_ex
+    assert f(None, 1, 4, 100, 100, None, None, None, d, None, d, None, 0, 0, None, None, None,
+             None, None, 0, None) == pkv.PKV_EINVAL and "logits" in pkv.last_error()
+    assert f(d, 1, 4, 100, 99, None, None, None, d, None, d, None, 0, 0, None, None, None, None,
+             None, 0, None) == pkv.PKV_EINVAL and "row_stride" in pkv.last_error()
+    assert f(d, 1, 4, 100, 100, d, None, None, d, None, d, None, 0, 0, None, None, None, None,
+             None, 0, None) == pkv.PKV_EINVAL and "uniform" in pkv.last_error()
+    # A valid call without a workspace is refused before any launch.
+    assert f(d, 1, 4, 100, 100, None, None, None, d, None, d, None, 0, 0, None, None, None, None,
+             None, 0, None) == pkv.PKV_EINVAL and "workspace" in pkv.last_error()
+
+
 def test_prepare_step_host_validation_launches_nothing():
     lib = pkv.load()
     d = ctypes.c_void_p(16)
