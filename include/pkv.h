@@ -170,12 +170,23 @@ int pkv_sample_batch_ex(const void* logits, pkv_dtype dt, int B, int V, int64_t 
 
 /*
  * pkv_sample_batch_noalloc -- pkv_sample_batch without a caller workspace.
+ * The source pages have no counterpart: this entry point exists for callers
+ * that cannot allocate device memory at the point where they sample.  Such
+ * callers include a decode loop that must never stall (cudaMalloc can
+ * synchronise the device and has no latency bound), code running while a
+ * stream is being captured into a CUDA graph (allocation is not allowed
+ * there), host callbacks enqueued on a stream (they may not call CUDA at
+ * all), and engines that handed nearly all free memory to the KV pool at
+ * start-up and have no headroom left.
  *
  * Same arguments, meaning and errors as pkv_sample_batch, minus the
  * workspace: the sampler's scratch is a 64 MiB device array inside the
  * library (one per device, zero at load time, left ready by every call), so
- * the call allocates nothing anywhere.  Calls on one device share that array:
- * they must not run concurrently (on different streams without ordering).
+ * the call allocates nothing anywhere.  The first call on a device looks up
+ * that array's device address (cudaGetSymbolAddress) and caches it, so make
+ * that first call before any stream capture.  Calls on one device share the
+ * array: calls that overlap on the GPU (different streams without ordering)
+ * race on it and must be avoided.
  * Errors: those of pkv_sample_batch, plus PKV_EUNSUPPORTED when
  * pkv_sample_workspace_bytes(B, V, dt) exceeds 64 MiB (e.g. B=1024,
  * V=256000), and PKV_ECUDA when the array's address cannot be read.

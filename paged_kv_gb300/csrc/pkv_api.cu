@@ -158,12 +158,20 @@ int fill_args(const int32_t* cached_len, const int32_t* device_len, const int32_
 // Page-fill CTAs appended to the finish kernel by pkv_decode_tail.
 constexpr int kFusedFillCtas = 32;
 
-// Scratch of pkv_sample_batch_noalloc: a zero-initialised device array of
-// the library (one instance per device), used as the sampler workspace.
+// Scratch of pkv_sample_batch_noalloc, for callers that cannot allocate
+// device memory when they sample (a decode loop that must not stall on
+// cudaMalloc, a stream under graph capture, a host callback, an engine whose
+// memory went to the KV pool): a zero-initialised device array of the
+// library (one instance per device, held until the process exits), used as
+// the sampler workspace.  Every call leaves it ready for the next; calls
+// that overlap on the GPU race on it.
 constexpr size_t kStaticScratchBytes = static_cast<size_t>(64) << 20;
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// The array's address on the current device, looked up once per device.
+// The array's address on the current device: in host code the array's name
+// is only a host-side stand-in, so the device address is looked up (with
+// that device current) on the first call on each device and cached.  That
+// first call should come before any stream capture.
 cudaError_t static_scratch(void** out) {
   static void* cache[64] = {nullptr};
   int dev = 0;

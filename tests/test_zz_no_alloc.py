@@ -1,5 +1,13 @@
 """pkv_sample_batch_noalloc: the sampler with the library's static scratch.
 
+This entry point serves callers that cannot allocate device memory where
+they sample: a decode loop that must not stall on cudaMalloc (it can
+synchronise the device), code inside a CUDA-graph stream capture, host
+callbacks on a stream, and engines that gave their free memory to the KV
+pool.  The source pages have no counterpart.  This file is collected last
+so that a failure here comes after every other test has run; it also passes
+alone in a fresh process.
+
 CPU: the size limit and the argument checks answer before any CUDA call.
 GPU: the tokens equal the oracle's (parity bar of tests/parity.py), equal
 those of pkv_sample_batch with a caller workspace, and no device memory is
