@@ -60,21 +60,26 @@ def test_noalloc_matches_oracle_and_workspace_path_without_allocating():
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     pool = torch.zeros(w.pool_shape, dtype=torch.int32, device=DEV)
     rows, cols = w.wb_rows.to(DEV), w.wb_cols.to(DEV)
+    saved = torch.empty((3, B), dtype=torch.int32, device=DEV)  # each call's tokens
     # Warm up (library load, symbol lookup), then count allocations over calls.
     pkv.sample_batch_noalloc(L, *args, out_tokens=out, status=status)
     torch.cuda.synchronize()
     before = torch.cuda.memory_stats(DEV).get("allocation.all.allocated", 0)
-    for _ in range(3):
+    for i in range(3):
         pkv.sample_batch_noalloc(L, *args, out_tokens=out, token_pool=pool, wb_rows=rows,
                                  wb_cols=cols, status=status)
+        saved[i].copy_(out)
     torch.cuda.synchronize()
     after = torch.cuda.memory_stats(DEV).get("allocation.all.allocated", 0)
     assert after == before
     assert int(status.item()) == 0
-    tok = out.cpu().numpy()
-    check_sampler(w.logits, w.temperature, w.top_k, w.top_p, w.uniform, tok)
+    # Two calls in a row each equal the workspace entry point's tokens (and so
+    # the oracle's, within the parity bar): the shared scratch is left ready.
     ref = pkv.sample_batch(L, *args).cpu().numpy()
-    np.testing.assert_array_equal(tok, ref)
+    for i in (1, 2):
+        tok = saved[i].cpu().numpy()
+        np.testing.assert_array_equal(tok, ref)
+        check_sampler(w.logits, w.temperature, w.top_k, w.top_p, w.uniform, tok)
     # The fused write-back went through as well.
     got = pool.cpu().numpy()
     r, c = w.wb_rows.numpy(), w.wb_cols.numpy()
