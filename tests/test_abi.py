@@ -30,6 +30,16 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, name), f"{name} is declared in pkv.h but not exported"
 
 
+def test_binding_types_every_declared_function():
+    # The ctypes binding declares argument and result types for every entry
+    # point of pkv.h (an untyped call would pass 64-bit values as int).
+    lib = pkv.load()
+    for name in declared_functions():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, f"{name}: no argtypes in paged_kv_gb300/pkv.py"
+        assert fn.restype is not None, f"{name}: no restype in paged_kv_gb300/pkv.py"
+
+
 def test_version_and_workspace():
     lib = pkv.load()
     assert pkv.version() == 310
