@@ -39,7 +39,11 @@ KERNEL_SOURCES = ("paged_kv_gb300/csrc/sample_common.cuh", "paged_kv_gb300/csrc/
                   "paged_kv_gb300/csrc/sample_finish.cuh", "paged_kv_gb300/csrc/sample_launch.cuh",
                   "paged_kv_gb300/csrc/device_common.cuh", "paged_kv_gb300/csrc/launch_config.h",
                   "paged_kv_gb300/csrc/page_fill.cuh")
-GRAPH_LEN = 20  # steps per captured CUDA graph
+GRAPH_LEN = 20  # steps per captured CUDA graph (at most)
+MIN_REPLAYS = 5  # graph replays per timed region (at least, when there are enough steps)
+# The workloads of every configuration the method is measured on; the
+# headline value is the mixed batch.
+CONFIG_WORKLOADS = ("pr1", "greedy", "mixed", "nucleus", "large")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sampler_mixed_traffic.json")
 
 
@@ -154,14 +158,18 @@ def make_graph(fn, n: int, device):
     return g
 
 
-def timed_graph_steps(fn, steps: int, warmup: int, dist_mod, device) -> float:
-    """Times exactly `steps` calls of fn, replayed from CUDA graphs of
-    GRAPH_LEN calls (plus one graph for the remainder) so that host launch
-    cost does not enter; at least `warmup` untimed calls first.  Barriers,
-    synchronisation and the max over ranks as in timed_steps."""
+def timed_graph_steps(fn, steps: int, warmup: int, dist_mod, device, spread=None) -> float:
+    """Times exactly `steps` calls of fn, replayed from CUDA graphs (so that
+    host launch cost does not enter): graphs of up to GRAPH_LEN calls, short
+    enough that there are at least MIN_REPLAYS replays, plus one graph for
+    the remainder; at least `warmup` untimed calls first.  Barriers,
+    synchronisation and the max over ranks as in timed_steps.  Returns the
+    milliseconds of the whole region; if `spread` is a dict it receives the
+    per-replay microseconds per call (median, min, max, replays), from events
+    recorded between the replays inside the same region."""
     import torch
 
-    glen = max(1, min(GRAPH_LEN, steps))
+    glen = max(1, min(GRAPH_LEN, steps // MIN_REPLAYS if steps >= MIN_REPLAYS else steps))
     full = make_graph(fn, glen, device)
     rem = steps % glen
     tail = make_graph(fn, rem, device) if rem else None
@@ -170,17 +178,22 @@ def timed_graph_steps(fn, steps: int, warmup: int, dist_mod, device) -> float:
     torch.cuda.synchronize(device)
     barrier(dist_mod, device)
     torch.cuda.synchronize(device)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps // glen):
+    n_full = steps // glen
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_full + 2)]
+    ev[0].record()
+    for i in range(n_full):
         full.replay()
+        ev[i + 1].record()
     if tail is not None:
         tail.replay()
-    end.record()
+    ev[-1].record()
     torch.cuda.synchronize(device)
-    ms = start.elapsed_time(end)
+    ms = ev[0].elapsed_time(ev[-1])
     barrier(dist_mod, device)
+    if spread is not None and n_full > 0:
+        us = sorted(ev[i].elapsed_time(ev[i + 1]) * 1e3 / glen for i in range(n_full))
+        spread.update({"median_us": round(us[len(us) // 2], 3), "min_us": round(us[0], 3),
+                       "max_us": round(us[-1], 3), "replays": n_full, "calls_per_replay": glen})
     return max_over_ranks(ms, dist_mod, device)
 
 
@@ -303,6 +316,46 @@ def algorithmic_bytes(w) -> int:
 # ----------------------------------------------------------------- our arm
 
 
+def measure_config(name: str, device, dist_mod, peak: float, warmup: int, calls: int) -> dict:
+    """One workload's pkv_sample_batch (fused write-back, no debug output),
+    graph-replayed with the logits rotating over enough buffers to exceed
+    twice the L2 size: median and range of the per-replay time per call,
+    sampled tokens/s, logits GB/s and the fraction of the HBM peak."""
+    import torch
+
+    from paged_kv_gb300 import pkv, workloads
+
+    w = workloads.make(name)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+    logit_bytes = w.B * w.V * w.elt
+    nbuf = min(600, max(4, -(-2 * l2 // logit_bytes) + 1))
+    base = w.logits.to(device)
+    bufs = [base] + [base.clone() for _ in range(nbuf - 1)]
+    d = lambda x: None if x is None else x.to(device)  # noqa: E731
+    t, k, p, u = d(w.temperature), d(w.top_k), d(w.top_p), d(w.uniform)
+    pool = torch.zeros(w.pool_shape, dtype=torch.int32, device=device)
+    rows, cols = d(w.wb_rows), d(w.wb_cols)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    out = torch.empty(w.B, dtype=torch.int32, device=device)
+    spread = {}
+    timed_graph_steps(lambda i: pkv.sample_batch(bufs[i % nbuf], t, k, p, u, out_tokens=out,
+                                                 token_pool=pool, wb_rows=rows, wb_cols=cols,
+                                                 status=status),
+                      calls, warmup, dist_mod, device, spread)
+    torch.cuda.synchronize(device)
+    us = spread["median_us"]
+    gbs = logit_bytes / (us * 1e-6) / 1e9
+    res = {"B": w.B, "V": w.V, "dtype": "bf16" if w.elt == 2 else "fp32", "us": us,
+           "min_us": spread["min_us"], "max_us": spread["max_us"],
+           "replays": spread["replays"], "calls_per_replay": spread["calls_per_replay"],
+           "tokens_per_s": round(w.B / (us * 1e-6), 1), "logits_gbs": round(gbs, 1),
+           "frac": round(gbs / peak, 4), "status": int(status.item()), "buffers": nbuf}
+    del bufs, base
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
 
@@ -335,26 +388,26 @@ def run_ours(args):
         pkv.decode_tail(bufs[i % nbuf], t, k, p, u, out, pool, rows, cols, cached, dev_len, tidx,
                         w.page_size, free, pt, total, status)
 
+    step_spread = {}
     with ClockSampler(physical_gpu_index(local_rank)) as clocks:
-        ms = timed_graph_steps(step, args.steps, args.warmup, dist_mod, device)
+        ms = timed_graph_steps(step, args.steps, args.warmup, dist_mod, device, step_spread)
     torch.cuda.synchronize(device)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status word {int(status.item())} after the timed run")
     ms_per_step = ms / args.steps
     value = world * w.B / (ms_per_step * 1e-3)
 
-    # The dominant operation (one pkv_sample_batch: stream + finish kernel)
-    # alone, replayed from graphs and timed with events on the replay stream.
-    n_k = max(200, min(args.steps, 5000))
-    ms_k = timed_graph_steps(lambda i: pkv.sample_batch(bufs[i % nbuf], t, k, p, u,
-                                                        out_tokens=out, token_pool=pool,
-                                                        wb_rows=rows, wb_cols=cols,
-                                                        status=status),
-                             n_k, args.warmup, dist_mod, device)
-    us_k = ms_k / n_k * 1e3
+    # Every configuration: one pkv_sample_batch per call (with the fused
+    # write-back), graph-replayed, median and spread over the replays.  The
+    # mixed batch's entry is the dominant operation of the step and gives
+    # the roofline.
+    peak, peak_kind = measured_peaks()
+    n_k = max(MIN_REPLAYS * GRAPH_LEN, min(args.steps, 2000))
+    configs = {name: measure_config(name, device, dist_mod, peak, args.warmup, n_k)
+               for name in CONFIG_WORKLOADS}
+    us_k = configs[WORKLOAD]["us"]
     alg = algorithmic_bytes(w)
     achieved = alg / (us_k * 1e-6) / 1e9
-    peak, peak_kind = measured_peaks()
     # The same batch with min_p = 0.05 on every row (sampled rows then take
     # the exact path).
     minp = torch.full((w.B,), 0.05, dtype=torch.float32, device=device)
@@ -446,6 +499,8 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}",
                        "l2": f"logits rotate over {nbuf} buffers ({nbuf * logit_bytes >> 20} MiB > 2x L2)"},
             "logits_gbs": round(world * logit_bytes / (ms_per_step * 1e-3) / 1e9, 1),
+            "step_spread": step_spread,
+            "configs": configs,
             "page_fill_us": round(ms_f / n_k * 1e3, 3),
             "minp_us": round(us_m, 3),
             "prepare_step": {"us": round(ms_p / n_k * 1e3, 3), "tokens": n_tok,
@@ -454,7 +509,11 @@ def run_ours(args):
                          "achieved": round(achieved, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
-                         "algorithmic_bytes": alg, "us_per_launch": round(us_k, 3)},
+                         "algorithmic_bytes": alg, "us_per_launch": round(us_k, 3),
+                         "us_per_launch_spread": [configs[WORKLOAD]["min_us"],
+                                                  configs[WORKLOAD]["max_us"]],
+                         "timing": "median over graph replays of the mixed batch's "
+                                   "pkv_sample_batch, logits rotating past L2"},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "pipelined": "step i+1's inputs copied on a second stream during step i"},

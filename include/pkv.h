@@ -175,9 +175,10 @@ int pkv_sample_batch_ex(const void* logits, pkv_dtype dt, int B, int V, int64_t 
  * callers include a decode loop that must never stall (cudaMalloc can
  * synchronise the device and has no latency bound), code running while a
  * stream is being captured into a CUDA graph (allocation is not allowed
- * there), host callbacks enqueued on a stream (they may not call CUDA at
- * all), and engines that handed nearly all free memory to the KV pool at
- * start-up and have no headroom left.
+ * there), and engines that handed nearly all free memory to the KV pool at
+ * start-up and have no headroom left.  The call itself uses the CUDA runtime
+ * (it looks up the array and launches kernels), so it is made from ordinary
+ * host code, never from inside a host callback on a stream.
  *
  * Same arguments, meaning and errors as pkv_sample_batch, minus the
  * workspace: the sampler's scratch is a 64 MiB device array inside the

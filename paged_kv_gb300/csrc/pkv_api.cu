@@ -160,8 +160,8 @@ constexpr int kFusedFillCtas = 32;
 
 // Scratch of pkv_sample_batch_noalloc, for callers that cannot allocate
 // device memory when they sample (a decode loop that must not stall on
-// cudaMalloc, a stream under graph capture, a host callback, an engine whose
-// memory went to the KV pool): a zero-initialised device array of the
+// cudaMalloc, a stream under graph capture, an engine whose memory went to
+// the KV pool): a zero-initialised device array of the
 // library (one instance per device, held until the process exits), used as
 // the sampler workspace.  Every call leaves it ready for the next; calls
 // that overlap on the GPU race on it.

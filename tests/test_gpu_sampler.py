@@ -277,6 +277,13 @@ def _full(name, rows_checked=None, probs_rows=32):
     return stats
 
 
+def _every_row_checked(stats, B):
+    # Every row is either exact (greedy or sampled) or excused and validated.
+    assert stats["greedy"] + stats["exact"] + stats["validated"] == B, stats
+    assert stats["validated"] == (stats["excused_cdf"] + stats["excused_topp"]
+                                  + stats["excused_minp"]), stats
+
+
 def test_full_greedy():
     stats = _full("greedy")
     assert stats["greedy"] == 64
@@ -284,14 +291,17 @@ def test_full_greedy():
 
 def test_full_mixed():
     stats = _full("mixed")
+    _every_row_checked(stats, 256)
     assert stats["exact"] + stats["greedy"] >= 200, stats
 
 
 def test_full_nucleus():
     stats = _full("nucleus")
+    _every_row_checked(stats, 256)
     assert stats["exact"] >= 200, stats
 
 
-def test_full_large_sampled_rows():
-    stats = _full("large", rows_checked=np.arange(0, 1024, 16), probs_rows=16)
-    assert stats["exact"] >= 48, stats
+def test_full_large_every_row():
+    stats = _full("large", probs_rows=16)
+    _every_row_checked(stats, 1024)
+    assert stats["exact"] >= 900, stats

@@ -2,11 +2,12 @@
 
 This entry point serves callers that cannot allocate device memory where
 they sample: a decode loop that must not stall on cudaMalloc (it can
-synchronise the device), code inside a CUDA-graph stream capture, host
-callbacks on a stream, and engines that gave their free memory to the KV
-pool.  The source pages have no counterpart.  This file is collected last
-so that a failure here comes after every other test has run; it also passes
-alone in a fresh process.
+synchronise the device), code inside a CUDA-graph stream capture, and
+engines that gave their free memory to the KV pool.  The call uses the CUDA
+runtime itself, so it is made from ordinary host code, not from a host
+callback.  The source pages have no counterpart.  This file is collected
+last so that a failure here comes after every other test has run; it also
+passes alone in a fresh process.
 
 CPU: the size limit and the argument checks answer before any CUDA call.
 GPU: the tokens equal the oracle's (parity bar of tests/parity.py), equal
@@ -73,10 +74,11 @@ def test_noalloc_matches_oracle_and_workspace_path_without_allocating():
     after = torch.cuda.memory_stats(DEV).get("allocation.all.allocated", 0)
     assert after == before
     assert int(status.item()) == 0
-    # Two calls in a row each equal the workspace entry point's tokens (and so
-    # the oracle's, within the parity bar): the shared scratch is left ready.
+    # Every call after the warm-up (three in a row) equals the workspace entry
+    # point's tokens, and so the oracle's within the parity bar: the shared
+    # scratch is left ready by each call.
     ref = pkv.sample_batch(L, *args).cpu().numpy()
-    for i in (1, 2):
+    for i in range(3):
         tok = saved[i].cpu().numpy()
         np.testing.assert_array_equal(tok, ref)
         check_sampler(w.logits, w.temperature, w.top_k, w.top_p, w.uniform, tok)
