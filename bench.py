@@ -38,7 +38,7 @@ WORKLOAD = "mixed"
 KERNEL_SOURCES = ("paged_kv_gb300/csrc/sample_common.cuh", "paged_kv_gb300/csrc/sample_stream.cuh",
                   "paged_kv_gb300/csrc/sample_finish.cuh", "paged_kv_gb300/csrc/sample_launch.cuh",
                   "paged_kv_gb300/csrc/device_common.cuh", "paged_kv_gb300/csrc/launch_config.h",
-                  "paged_kv_gb300/csrc/page_fill.cuh")
+                  "paged_kv_gb300/csrc/sample_params.h", "paged_kv_gb300/csrc/page_fill.cuh")
 GRAPH_LEN = 20  # steps per captured CUDA graph (at most)
 MIN_REPLAYS = 5  # graph replays per timed region (at least, when there are enough steps)
 # The workloads of every configuration the method is measured on; the
@@ -517,7 +517,7 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "pipelined": "step i+1's inputs copied on a second stream during step i"},
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 2 * args.steps,  # per step: stream_kernel and finish_kernel
             "timing": f"device value and roofline: CUDA graphs of {GRAPH_LEN} steps replayed; "
                       "e2e: host-launched calls",
             "clocks": clocks.summary(),

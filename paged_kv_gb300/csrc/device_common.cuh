@@ -1,6 +1,6 @@
-// Device helpers shared by the sm_103a kernels: thread-block-cluster and
-// distributed-shared-memory primitives (inline PTX), streaming loads, the
-// order-preserving float key, and warp-level scans.
+// Device helpers shared by the sm_103a kernels: mbarrier and bulk-copy
+// primitives (inline PTX), streaming loads, the order-preserving float key,
+// and warp-level scans.
 #pragma once
 
 #include <cstdint>
@@ -9,87 +9,6 @@
 namespace pkv {
 
 constexpr unsigned kFull = 0xffffffffu;
-
-// ----------------------------------------------------------------- cluster
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-// Full cluster barrier.  Release/acquire at cluster scope: shared-memory
-// writes made before it by any thread of any CTA in the cluster are visible
-// to every thread of the cluster after it.  Every thread must call it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Split form of the cluster barrier: arrive (release) now, wait (acquire)
-// later.  A CTA that has arrived may exit without waiting; waiting CTAs then
-// see everything it wrote before arriving.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Arrive without memory ordering (a start-up barrier that only says "this
-// CTA is running"; orderings it needs come from a fence before it).
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-// Shared-window address of `p` (a __shared__ object of this CTA) as seen in
-// CTA `rank` of the same cluster.
-__device__ __forceinline__ uint32_t dsmem(const void* p, uint32_t rank) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ unsigned long long ld_dsmem_u64(uint32_t addr) {
-  unsigned long long v;
-  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_dsmem_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
-               :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 // ----------------------------------------------------------------- mbarrier
 
@@ -129,12 +48,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
-// Orders this thread's earlier generic-proxy shared-memory accesses before
-// later asynchronous-proxy (bulk copy) writes to the same memory.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Tests phase `parity` of this CTA's mbarrier (acquire at CTA scope).  May
 // suspend briefly; true once the phase is complete.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -142,27 +55,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
-
-// Arrives (count 1) on an mbarrier of another CTA of the cluster, given its
-// shared::cluster address (dsmem).  Release at cluster scope: this thread's
-// earlier writes, and those ordered before them by a CTA barrier, are
-// visible to a thread that observes the phase with an acquire wait.
-__device__ __forceinline__ void mbar_remote_arrive(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
-               :: "r"(cluster_addr) : "memory");
-}
-
-// Tests phase `parity` of this CTA's mbarrier with acquire at cluster scope
-// (pairs with mbar_remote_arrive).  May suspend briefly; true once complete.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
   return ok != 0;

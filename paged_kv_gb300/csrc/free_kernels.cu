@@ -12,9 +12,11 @@
 //   range of every entry, duplicates through a bitmap of the pool's pages, and
 //   the count equation; one OR into the result per CTA.
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "device_attr.h"
 #include "page_kernels.h"
 
 namespace pkv {
@@ -150,14 +152,10 @@ __global__ void __launch_bounds__(kCheckThreads) check_free_list_kernel(
 size_t free_smem_bytes(int B) { return static_cast<size_t>(3 * B + 1) * sizeof(int32_t); }
 
 cudaError_t launch_free_pages(const FreeParams& F, int num_sms, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(free_pages_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(free_smem_bytes(kMaxFillBatch)));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0ull};
+  const cudaError_t e = set_smem_limit_once(smem_set, free_pages_kernel,
+                                            static_cast<int>(free_smem_bytes(kMaxFillBatch)));
+  if (e != cudaSuccess) return e;
   // One CTA per SM; each recomputes the (cheap) scan.
   const int grid = num_sms > 0 ? num_sms : 1;
   free_pages_kernel<<<grid, kFreeThreads, free_smem_bytes(F.B), stream>>>(F);

@@ -10,6 +10,9 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
+#include "device_attr.h"
 #include "page_fill.cuh"
 #include "page_kernels.h"
 
@@ -54,14 +57,10 @@ size_t fill_smem_bytes(int B) { return fill::smem_bytes(B); }
 
 cudaError_t launch_fill_page_table(const FillParams& F, int num_sms, cudaStream_t stream) {
   const size_t smem = fill_smem_bytes(F.B);
-  static bool attr_done = false;
-  if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        fill_page_table_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        static_cast<int>(fill_smem_bytes(kMaxFillBatch)));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0ull};
+  const cudaError_t e = set_smem_limit_once(smem_set, fill_page_table_kernel,
+                                            static_cast<int>(fill_smem_bytes(kMaxFillBatch)));
+  if (e != cudaSuccess) return e;
   // Enough CTAs to cover the device; each recomputes the (cheap) scan.
   const int grid = num_sms > 0 ? num_sms : 1;
   fill_page_table_kernel<<<grid, kFillThreads, smem, stream>>>(F);

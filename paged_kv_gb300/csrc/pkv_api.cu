@@ -11,6 +11,7 @@
 #include <cstring>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/pkv.h"
 #include "launch_config.h"
@@ -45,15 +46,19 @@ int cuda_fail(cudaError_t e, const char* what) {
   return fail(PKV_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// SM count of the current device (cached per device).
+// SM count of the current device (cached per device; threads that race on
+// the first call store the same value).
 int num_sms() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 1;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 1;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -173,29 +178,24 @@ __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 // that device current) on the first call on each device and cached.  That
 // first call should come before any stream capture.
 cudaError_t static_scratch(void** out) {
-  static void* cache[64] = {nullptr};
+  static std::atomic<void*> cache[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && cache[dev] != nullptr) {
-    *out = cache[dev];
-    return cudaSuccess;
+  if (dev >= 0 && dev < 64) {
+    void* c = cache[dev].load(std::memory_order_acquire);
+    if (c != nullptr) {
+      *out = c;
+      return cudaSuccess;
+    }
   }
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_static_scratch);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) cache[dev] = p;
+  if (dev >= 0 && dev < 64) cache[dev].store(p, std::memory_order_release);
   *out = p;
   return cudaSuccess;
 }
-
-}  // namespace
-
-extern "C" {
-
-}  // extern "C"
-
-namespace {
 
 // pkv_sample_batch, with an optional page fill run by extra finish CTAs.
 int sample_launch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_stride,

@@ -19,9 +19,11 @@
 // does not write there; consecutive threads write consecutive packed
 // entries and read consecutive pool and table columns of one request.
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "device_attr.h"
 #include "page_fill.cuh"
 #include "page_kernels.h"
 
@@ -214,14 +216,10 @@ __global__ void __launch_bounds__(kPrepThreads) prepare_step_kernel(const Prepar
 size_t prepare_smem_bytes(int B) { return prep_smem_bytes(B); }
 
 cudaError_t launch_prepare_step(const PrepareParams& Q, int num_sms, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        prepare_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        static_cast<int>(prep_smem_bytes(kMaxFillBatch)));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> smem_set{0ull};
+  const cudaError_t e = set_smem_limit_once(smem_set, prepare_step_kernel,
+                                            static_cast<int>(prep_smem_bytes(kMaxFillBatch)));
+  if (e != cudaSuccess) return e;
   const int grid = num_sms > 0 ? num_sms : 1;
   prepare_step_kernel<<<grid, kPrepThreads, prep_smem_bytes(Q.fill.B), stream>>>(Q);
   return cudaGetLastError();

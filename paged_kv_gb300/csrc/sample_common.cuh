@@ -284,30 +284,6 @@ __device__ __forceinline__ float regs_max(const uint32_t (&d)[NV][4]) {
   }
 }
 
-// Maximum of one 16-bit-element vector (NaN-propagating).
-template <bool BF16>
-__device__ __forceinline__ float vec_max(const uint32_t (&w)[4]) {
-  if constexpr (BF16) {
-    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(w[0], w[1]), bf16x2_max_nan(w[2], w[3]));
-    return fmax_nan(elem<true>(m2, 0), elem<true>(m2, 1));
-  } else {
-    return fmax_nan(fmax_nan(__uint_as_float(w[0]), __uint_as_float(w[1])),
-                    fmax_nan(__uint_as_float(w[2]), __uint_as_float(w[3])));
-  }
-}
-
-// x.lo >= t and x.hi >= t for the two bf16 values of a word (t2 holds t in
-// both halves; NaN compares false, -0 equals +0): bit 0 and bit 1.
-__device__ __forceinline__ uint32_t bf16x2_ge(uint32_t x, uint32_t t2) {
-  uint32_t r;
-  asm("{\n\t.reg .pred p, q;\n\t"
-      "setp.ge.bf16x2 p|q, %1, %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t"
-      "@q or.b32 %0, %0, 2;\n\t}"
-      : "=r"(r) : "r"(x), "r"(t2));
-  return r;
-}
-
 // 16-bit order-preserving key of a bf16 value held as a float (-0 folded).
 __device__ __forceinline__ uint32_t key16(float x) { return float_key(x) >> 16; }
 
@@ -371,10 +347,6 @@ __device__ __forceinline__ unsigned long long ceil_div_small(unsigned long long 
     else lo = mid + 1;
   }
   return lo;
-}
-
-__device__ __forceinline__ unsigned long long pick4(const unsigned long long (&a)[4], int j) {
-  return j == 0 ? a[0] : (j == 1 ? a[1] : (j == 2 ? a[2] : a[3]));
 }
 
 // ----------------------------------------------------------------- block helpers
@@ -496,8 +468,6 @@ __device__ __forceinline__ void emit_token(const SampleParams& P, int row, int t
   if (st != 0 && P.status != nullptr) atomicOr(P.status, st);
 }
 
-// ----------------------------------------------------------------- warp helpers
-
 // ----------------------------------------------------------------- chunk search
 //
 // These re-read a chunk from global memory (an L2 hit: the chunk was just
@@ -560,20 +530,6 @@ __device__ __forceinline__ void stage_own(const SampleParams& P, int row, int ch
     }
   }
   cp_async_wait_all();
-}
-
-// f(x, e) for every element the thread owns in chunk `chunk`, index order
-// within the thread.
-template <bool BF16, int NV, bool VEC, typename F>
-__device__ __forceinline__ void for_chunk(const SampleParams& P, int row, int chunk, int warp,
-                                          int lane, F&& f) {
-#pragma unroll 1
-  for (int j = 0; j < NV; ++j) {
-    const int e0 = vec_base<BF16, NV>(chunk, warp, lane, j);
-    uint32_t w[4];
-    load_vec<BF16, NV, VEC>(P, row, e0, w);
-    for_vec<BF16>(w, e0, f);
-  }
 }
 
 // ----------------------------------------------------------------- list selects

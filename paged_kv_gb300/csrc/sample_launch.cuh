@@ -7,7 +7,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
+#include "device_attr.h"
 #include "launch_config.h"
 #include "sample_finish.cuh"
 #include "sample_stream.cuh"
@@ -20,15 +22,12 @@ cudaError_t launch_pair(const SampleParams& P, int num_sms, cudaStream_t stream)
   auto fkern = finish_kernel<BF16, NV, VEC>;
   constexpr int kStreamDyn = stream_dyn_bytes<NV>();
   constexpr int kFinishDyn = kFinishDynBytes;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(skern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kStreamDyn);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fkern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFinishDyn);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // The shared-memory limits are per device: set once on each device.
+  static std::atomic<unsigned long long> stream_set{0ull}, finish_set{0ull};
+  cudaError_t e = set_smem_limit_once(stream_set, skern, kStreamDyn);
+  if (e != cudaSuccess) return e;
+  e = set_smem_limit_once(finish_set, fkern, kFinishDyn);
+  if (e != cudaSuccess) return e;
   const int items = P.B * P.chunks;
   const int ctas = std::min(num_sms, (items + kGroups - 1) / kGroups);
   cudaLaunchConfig_t cfg = {};
@@ -36,7 +35,7 @@ cudaError_t launch_pair(const SampleParams& P, int num_sms, cudaStream_t stream)
   cfg.blockDim = dim3(kStreamThreads, 1, 1);
   cfg.dynamicSmemBytes = kStreamDyn;
   cfg.stream = stream;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, skern, P);
+  e = cudaLaunchKernelEx(&cfg, skern, P);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t fcfg = {};
   fcfg.gridDim = dim3(static_cast<unsigned>(P.B + P.fill_ctas), 1, 1);
