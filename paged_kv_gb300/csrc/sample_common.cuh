@@ -32,8 +32,15 @@
 //      value share one weight, so exact counts per value give exact masses;
 //      each chunk counts its elements per value over the 1024 values below
 //      its maximum.
-//   F  whatever the above cannot settle (a cut below the window; fp32 rows
-//      with top-p or k > 256): radix passes over the row in global memory.
+//   T  top-p (or min_p) without top-k on fp32 rows: each chunk lists its
+//      elements at or above a bound below which at least 64 of its thread
+//      maxima lie; the lists hold every element above the largest bound, and
+//      when the top-p cut falls there the finisher settles the row from the
+//      lists alone (two weighted selects: the cut by value, the draw by
+//      index).
+//   F  whatever the above cannot settle (a cut below the window or the
+//      lists; fp32 rows with k > 256): radix passes over the row in global
+//      memory.
 // No tensor cores (nothing here is a contraction); exp is MUFU.EX2.
 #pragma once
 
@@ -82,13 +89,19 @@ constexpr int kStColOOB = 8;
 constexpr int kStBadUniform = 16;
 constexpr int kStTimeout = 64;
 
-enum RowKind { kKindG = 0, kKindK = 1, kKindP = 2, kKindH = 3, kKindF = 4 };
+enum RowKind { kKindG = 0, kKindK = 1, kKindP = 2, kKindH = 3, kKindF = 4, kKindT = 5 };
+
+// T rows: a chunk's bound leaves at least kCandMin of its thread maxima at
+// or above it; its list of (order key, index) entries takes the space of
+// the thread maxima and the histogram (kCandCap entries).
+constexpr int kCandMin = 64;
 
 // One chunk's summary.
 struct __align__(16) Summary {
-  float f0;     // unused
+  float f0;     // T: the chunk's bound (every element at or above it is listed)
   float f1;     // unused
-  int32_t i0;   // H: 16-bit key of the chunk maximum (the histogram's anchor)
+  int32_t i0;   // H: 16-bit key of the chunk maximum (the histogram's anchor); T: list
+                // length, -1 when the list overflowed
   uint32_t u0;  // unused
 };
 
@@ -106,6 +119,16 @@ struct __align__(16) ChunkSlot {
   float tmax[kThreads];
   uint32_t hist[kHistWords];
 };
+// T rows: the candidate list over tmax and hist (contiguous).
+static_assert(offsetof(ChunkSlot, hist) == offsetof(ChunkSlot, tmax) + sizeof(float) * kThreads,
+              "the candidate list spans tmax and hist");
+constexpr int kCandCap = static_cast<int>((sizeof(float) * kThreads + 4 * kHistWords) / 8);
+__device__ __forceinline__ unsigned long long* slot_cands(ChunkSlot* s) {
+  return reinterpret_cast<unsigned long long*>(s->tmax);
+}
+__device__ __forceinline__ const unsigned long long* slot_cands(const ChunkSlot* s) {
+  return reinterpret_cast<const unsigned long long*>(s->tmax);
+}
 
 struct SampleSmem {
   Summary gather[kMaxChunks];
@@ -537,19 +560,20 @@ __device__ __forceinline__ void stage_own(const SampleParams& P, int row, int ch
 // The leader's list holds n entries (value, row index) in ascending index
 // order.  These run in one CTA with __syncthreads only.
 
-// Radix select over the list: the key t such that the weight of entries with
-// key > t is < target <= the weight with key >= t.  weight_of(i) is 1 (count)
-// or a fixed-point mass; entries with keep(i) false weigh nothing.  Returns t
-// and the weight still needed from the entries equal to t in *rem.  Only the
-// key bits on which the kept entries differ are examined, 8 at a time.
-template <bool MASS, typename K, typename W>
-__device__ __forceinline__ float list_select(const float* val, int n, K&& keep, W&& weight_of,
-                                             unsigned long long target, SampleSmem& sm,
-                                             const Ctx& c, unsigned long long* rem_out) {
+// Radix select over a list of n entries with 32-bit keys key_of(i): the key
+// t such that the weight of entries with key > t is < target <= the weight
+// with key >= t.  weight_of(i) is 1 (count) or a fixed-point mass; entries
+// with keep(i) false weigh nothing.  Returns t and the weight still needed
+// from the entries equal to t in *rem.  Only the key bits on which the kept
+// entries differ are examined, 8 at a time.  Runs on one group.
+template <bool MASS, typename KeyOf, typename K, typename W>
+__device__ __forceinline__ uint32_t list_select_key(KeyOf&& key_of, int n, K&& keep, W&& weight_of,
+                                                    unsigned long long target, SampleSmem& sm,
+                                                    const Ctx& c, unsigned long long* rem_out) {
   uint32_t kand = 0xffffffffu, kor = 0u;
   for (int i = c.tid; i < n; i += kThreads) {
     if (keep(i)) {
-      const uint32_t k = float_key(val[i]);
+      const uint32_t k = key_of(i);
       kand &= k;
       kor |= k;
     }
@@ -572,7 +596,7 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
   if (diff == 0u) {
     group_sync();
     *rem_out = rem;
-    return key_float(a);
+    return a;
   }
   const int top = 31 - __clz(diff);
   const int bottom = __ffs(diff) - 1;
@@ -588,7 +612,7 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
     group_sync();
     for (int i = c.tid; i < n; i += kThreads) {
       if (!keep(i)) continue;
-      const uint32_t key = float_key(val[i]);
+      const uint32_t key = key_of(i);
       if ((key & amask) != (prefix & amask)) continue;
       const uint32_t dg = (key >> lo) & dmask;
       if constexpr (MASS) {
@@ -618,7 +642,17 @@ __device__ __forceinline__ float list_select(const float* val, int n, K&& keep, 
   }
   group_sync();
   *rem_out = rem;
-  return key_float(prefix);
+  return prefix;
+}
+
+// list_select_key over the order keys of float values val[0 .. n): returns
+// the value of the selected key.
+template <bool MASS, typename K, typename W>
+__device__ __forceinline__ float list_select(const float* val, int n, K&& keep, W&& weight_of,
+                                             unsigned long long target, SampleSmem& sm,
+                                             const Ctx& c, unsigned long long* rem_out) {
+  return key_float(list_select_key<MASS>([&](int i) { return float_key(val[i]); }, n, keep,
+                                         weight_of, target, sm, c, rem_out));
 }
 
 // ----------------------------------------------------------------- exact fallback (F)
@@ -861,8 +895,10 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
       r.kind = kKindK;
     } else if (k == V && !(r.p < 1.0f) && !(r.minp > 0.0f)) {
       r.kind = kKindP;
+    } else if (BF16) {
+      r.kind = kKindH;
     } else {
-      r.kind = BF16 ? kKindH : kKindF;
+      r.kind = k == V ? kKindT : kKindF;
     }
   }
   r.use_p = r.p < 1.0f;

@@ -766,6 +766,123 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   return true;
 }
 
+// ----------------------------------------------------------------- candidate finish (T)
+
+// The chunks' candidate lists, gathered (value, index) into l_val / l_idx,
+// hold every element of the row at or above thr, the largest of the chunks'
+// bounds.  When the top-p cut lies there (the mass at or above thr reaches
+// p * Z), S is settled from the lists alone: a weighted select by value gives
+// the cut value and the mass still needed from its ties, a count select by
+// index the last kept tie, and a weighted select by index (keys in falling
+// index order) the drawn token.  Returns false, having emitted nothing, when
+// a list overflowed or the cut lies below thr; the caller then runs the
+// exact fallback.
+template <bool BF16, int NV, bool VEC>
+__device__ __forceinline__ bool finish_cand(const SampleParams& P, SampleSmem& sm, const Ctx& c,
+                                            const ChunkSlot* recs, float* l_val, int32_t* l_idx,
+                                            int row, const RowParams& rp, float m,
+                                            const WriteBack& wb, float* q_row) {
+  const int tid = c.tid, lane = c.lane, warp = c.warp;
+  const int C = static_cast<int>(c.csize);
+  // ---- the row's total mass from the warp records.
+  float mw = 0.0f;
+  if (tid < C * kWarps) {
+    const float wmax = recs[tid / kWarps].wm[tid % kWarps];
+    if (wmax > -INFINITY) mw = recs[tid / kWarps].wz[tid % kWarps] * ex2((wmax - m) * rp.c2);
+  }
+  const float zrow = block_sum<float>(mw, sm.wt, lane, warp);
+  // ---- list offsets, the largest bound, overflow (warp 0; C <= 32).
+  if (warp == 0) {
+    const bool v = lane < C;
+    const int n = v ? recs[lane].s.i0 : 0;
+    float th = v ? recs[lane].s.f0 : -INFINITY;
+    const bool over = __any_sync(kFull, v && n < 0);
+    const int nn = n < 0 ? 0 : n;
+    const int incl = warp_inclusive_scan(nn, lane);
+    const int total = __shfl_sync(kFull, incl, 31);
+    if (v) sm.cnt[lane] = static_cast<uint32_t>(incl - nn);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) th = fmaxf(th, __shfl_xor_sync(kFull, th, o));
+    if (lane == 0) {
+      sm.bi[0] = over ? -1 : total;
+      sm.bf4[0] = th;
+    }
+  }
+  group_sync();
+  const int total = sm.bi[0];
+  const float thr = sm.bf4[0];
+  if (total < 0 || total > kFinListCap) return false;
+#pragma unroll 1
+  for (int r = 0; r < C; ++r) {
+    const int n = recs[r].s.i0;
+    const int off = static_cast<int>(sm.cnt[r]);
+    const unsigned long long* cand = slot_cands(&recs[r]);
+    for (int i = tid; i < n; i += kThreads) {
+      const unsigned long long e = cand[i];
+      l_val[off + i] = key_float(static_cast<uint32_t>(e >> 32));
+      l_idx[off + i] = static_cast<int32_t>(static_cast<uint32_t>(e));
+    }
+  }
+  group_sync();
+  auto keep = [&](int i) { return l_val[i] >= thr; };
+  auto wfx = [&](int i) { return mass_fx(weight(l_val[i], m, rp.c2)); };
+  // ---- the top-p cut inside the complete part of the lists.
+  float tp = -INFINITY;
+  int ci = INT_MAX;  // ties of tp with an index below ci are kept
+  if (rp.use_p) {
+    unsigned long long zc = 0;
+    for (int i = tid; i < total; i += kThreads) zc += keep(i) ? wfx(i) : 0ull;
+    zc = block_sum<unsigned long long>(zc, sm.wl, lane, warp);
+    unsigned long long target = mul_fx(fx40(zrow), rp.p, true);
+    if (target < 1ull) target = 1ull;
+    if (zc < target) return false;  // the cut lies below the lists' bound
+    unsigned long long rem;
+    tp = list_select<true>(l_val, total, keep, wfx, target, sm, c, &rem);
+    // Ties of tp: the first ceil(rem / w(tp)) of them in index order.
+    uint32_t nt = 0;
+    for (int i = tid; i < total; i += kThreads) nt += (keep(i) && l_val[i] == tp) ? 1u : 0u;
+    nt = block_sum<uint32_t>(nt, sm.wu, lane, warp);
+    const unsigned long long wt = mass_fx(weight(tp, m, rp.c2));
+    const unsigned long long need = wt == 0 ? ~0ull : ceil_div_small(rem, wt, nt);
+    if (need < nt) {
+      unsigned long long r2;
+      const uint32_t kc = list_select_key<false>(
+          [&](int i) { return ~static_cast<uint32_t>(l_idx[i]); }, total,
+          [&](int i) { return keep(i) && l_val[i] == tp; }, [](int) { return 1ull; }, need, sm, c,
+          &r2);
+      ci = static_cast<int>(~kc) + 1;  // the need-th smallest index of the ties, plus one
+    }
+  } else if (thr > -INFINITY && weight(thr, m, rp.c2) >= rp.minp) {
+    return false;  // min_p alone keeps elements below the lists' bound
+  }
+  const float tpf = tp;
+  const int cif = ci;
+  auto in_s = [&](int i) {
+    const float x = l_val[i];
+    return keep(i) && (x > tpf || (x == tpf && l_idx[i] < cif)) &&
+           (rp.minp <= 0.0f || weight(x, m, rp.c2) >= rp.minp);
+  };
+  // ---- the draw in index order: the first token whose cumulative mass
+  // exceeds floor(u * Z_S), a weighted select on keys falling with the index.
+  unsigned long long zs = 0;
+  for (int i = tid; i < total; i += kThreads) zs += in_s(i) ? wfx(i) : 0ull;
+  zs = block_sum<unsigned long long>(zs, sm.wl, lane, warp);
+  unsigned long long tdraw = mul_fx(zs, rp.u, false);
+  if (tdraw >= zs) tdraw = zs - 1ull;  // zs >= the row maximum's own weight > 0
+  unsigned long long r3;
+  const uint32_t kt = list_select_key<true>([&](int i) { return ~static_cast<uint32_t>(l_idx[i]); },
+                                            total, in_s, wfx, tdraw + 1ull, sm, c, &r3);
+  const int tok = static_cast<int>(~kt);
+  if (tid == 0) emit(P, row, tok, rp.st, wb);
+  if (q_row != nullptr) {
+    const float inv = 1.0f / (static_cast<float>(zs) / kMassScale);
+    for (int i = tid; i < total; i += kThreads) {
+      if (in_s(i)) q_row[l_idx[i]] = weight(l_val[i], m, rp.c2) * inv;
+    }
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------- the finish kernel
 
 // One CTA of kThreads threads per row.  Launched as a programmatic dependent
@@ -888,6 +1005,10 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
   }
   if (rp.kind == kKindK) {
     if (finish_topk<BF16, NV, VEC>(P, sm, c, recs, l_val, l_idx, row, rp, m, wb, q_row)) return;
+    group_sync();
+  }
+  if (rp.kind == kKindT) {
+    if (finish_cand<BF16, NV, VEC>(P, sm, c, recs, l_val, l_idx, row, rp, m, wb, q_row)) return;
     group_sync();
   }
   if constexpr (BF16) {

@@ -57,9 +57,9 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
   const float tmax = regs_max<BF16, NV>(d);
   const float wmax = warp_max_nan(tmax);
   if (lane == 0) slot->wm[warp] = wmax;
-  if (tid == 0 && rp.kind != kKindH) slot->s = Summary{};
+  if (tid == 0 && rp.kind != kKindH && rp.kind != kKindT) slot->s = Summary{};
 
-  if (rp.kind == kKindP || (rp.kind == kKindH && k == V)) {
+  if (rp.kind == kKindP || rp.kind == kKindT || (rp.kind == kKindH && k == V)) {
     // ---- the warp's mass relative to its maximum (online: each thread
     // relative to its own maximum, then rescaled).  (x - tmax) * c2, not an
     // fma with tmax * c2: for large c2 (T -> 0) the rounding of tmax * c2
@@ -75,6 +75,71 @@ __device__ __forceinline__ void reduce_chunk(const SampleParams& P, SampleSmem& 
     // value by the k-th largest of them and re-reads the few threads above.
     // Greedy: the finisher re-reads the threads holding the row maximum.
     slot->tmax[tid] = tmax;
+  }
+  if (rp.kind == kKindT) {
+    // ---- the chunk's candidate list: a bound theta with at least kCandMin
+    // thread maxima at or above it, then every element >= theta.  The thread
+    // maxima are counted in 256 buckets of 1/8 logit below the chunk maximum
+    // (the last one open); theta is the smallest thread maximum in the
+    // buckets that first hold kCandMin of them.  The finisher trusts the list
+    // for the elements at or above the largest bound of the row's chunks.
+    if (lane == 0) sm.wf[warp] = wmax;
+    uint32_t* bucket = hist;                  // 256 counts, then the list length
+    bucket[tid] = 0u;
+    if (tid == 0) bucket[kBuckets] = 0u;
+    group_sync();
+    float cm = sm.wf[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) cm = fmax_nan(cm, sm.wf[w]);
+    const bool finite = cm == cm && cm != INFINITY && cm != -INFINITY;
+    int b = kBuckets;  // no bucket
+    if (finite && tmax > -INFINITY) {
+      const float dist = cm - tmax;  // >= 0
+      b = dist < 32.0f ? min(static_cast<int>(dist * 8.0f), kBuckets - 1) : kBuckets - 1;
+      atomicAdd(&bucket[b], 1u);
+    }
+    group_sync();
+    {
+      const uint32_t h = bucket[tid];
+      uint32_t tot;
+      const uint32_t before = block_exclusive_scan<uint32_t>(h, sm.wu, lane, warp, &tot);
+      if (tid == 0) sm.bi[6] = kBuckets - 1;
+      group_sync();
+      if (tid < kBuckets - 1 && before < static_cast<uint32_t>(kCandMin) &&
+          before + h >= static_cast<uint32_t>(kCandMin)) {
+        sm.bi[6] = tid;
+      }
+      group_sync();
+    }
+    const int bk = sm.bi[6];
+    uint32_t kmin = __reduce_min_sync(kFull, b <= bk ? float_key(tmax) : 0xffffffffu);
+    if (lane == 0) sm.wu[warp] = kmin;
+    group_sync();
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) kmin = min(kmin, sm.wu[w]);
+    const float theta = (finite && kmin != 0xffffffffu) ? key_float(kmin) : -INFINITY;
+    unsigned long long* cand = slot_cands(slot);
+    if (cm == cm) {
+      for_regs<BF16, NV>(d, chunk, warp, lane, [&](float x, int e) {
+        if (x >= theta && (!has_pad || e < V)) {
+          const uint32_t at = atomicAdd(&bucket[kBuckets], 1u);
+          if (at < static_cast<uint32_t>(kCandCap)) {
+            cand[at] = (static_cast<unsigned long long>(float_key(x)) << 32) |
+                       static_cast<unsigned long long>(static_cast<uint32_t>(e));
+          }
+        }
+      });
+    }
+    group_sync();
+    if (tid == 0) {
+      const uint32_t n = bucket[kBuckets];
+      Summary sm0 = {};
+      sm0.f0 = theta;
+      sm0.i0 = (cm == cm && n <= static_cast<uint32_t>(kCandCap)) ? static_cast<int32_t>(n) : -1;
+      slot->s = sm0;
+    }
+    // Every thread has read the counts before the group's next item clears them.
+    group_sync();
   }
   if constexpr (BF16) {
     if (rp.kind == kKindH) {
@@ -141,7 +206,9 @@ constexpr int kOrderPerThread = (kOrderRows + kStreamThreads - 1) / kStreamThrea
 template <bool BF16, int NV>
 __device__ __forceinline__ int row_cost_class(const SampleParams& P, int row) {
   const int kind = row_params<BF16, NV>(P, row, 0).kind;
-  return (kind == kKindH || kind == kKindF) ? 0 : (kind == kKindK ? 1 : (kind == kKindP ? 2 : 3));
+  return (kind == kKindH || kind == kKindF || kind == kKindT)
+             ? 0
+             : (kind == kKindK ? 1 : (kind == kKindP ? 2 : 3));
 }
 
 // order[0 .. B) = the rows sorted by cost class, stable in row index.  All
