@@ -82,8 +82,8 @@ int pkv_version(void);
  * 0 for invalid arguments.  The sampler runs as two kernels: the first splits
  * every row into chunks, hands the chunks out to its CTAs from counters in
  * the workspace header and leaves one record per (row, chunk) in the
- * workspace (about 3 KB each, plus 16 KB of per-slice counts for top-p
- * rows); the second settles each row from its records.  The caller owns the workspace.  Before its first use it must be
+ * workspace (about 3 KB each, plus 16 KB of per-slice counts on bf16 rows
+ * for top-p); the second settles each row from its records.  The caller owns the workspace.  Before its first use it must be
  * initialised once, by pkv_sample_workspace_init or by zeroing it; every
  * call then leaves it ready for the next call on the same stream.  A
  * workspace must not be used by two calls that may run concurrently.

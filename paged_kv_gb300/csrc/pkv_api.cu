@@ -84,7 +84,7 @@ size_t pkv_sample_workspace_bytes(int B, int V, pkv_dtype dt) {
       chunks = std::max(chunks, static_cast<size_t>(cfg.chunks));
     }
   }
-  return pkv::sample_workspace_need(B, static_cast<int>(chunks));
+  return pkv::sample_workspace_need(B, static_cast<int>(chunks), dt == PKV_BF16);
 }
 
 int pkv_sample_workspace_init(void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
@@ -218,7 +218,7 @@ int sample_launch(const void* logits, pkv_dtype dt, int B, int V, int64_t row_st
     return fail(PKV_EUNSUPPORTED, "no launch shape covers V=%d", V);
   if (static_cast<int64_t>(cfg.chunks - 1) * cfg.chunk >= V)
     return fail(PKV_EUNSUPPORTED, "launch shape with an empty chunk (V=%d)", V);
-  const size_t need = pkv::sample_workspace_need(B, cfg.chunks);
+  const size_t need = pkv::sample_workspace_need(B, cfg.chunks, bf16);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(PKV_EINVAL, "workspace of %zu bytes needed (pkv_sample_workspace_bytes), got %zu",
                 need, workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);

@@ -28,15 +28,17 @@ static_assert(sizeof(WorkspaceHeader) == kWorkspaceHeaderBytes, "header size");
 // up to kOrderRows rows), then the records, then one block of slice
 // histograms per (row, chunk): for each of the stream kernel's 8 consumer
 // warps, the 16-bit counts of the 1024 keys below the chunk maximum over
-// that warp's slice of the chunk (written for count-histogram rows only).
+// that warp's slice of the chunk (written for count-histogram rows only,
+// which are bf16 rows: fp32 workspaces have no slice histograms).
 constexpr int kOrderRows = 4096;
 constexpr size_t kFinishOrderBytes = static_cast<size_t>(kOrderRows) * 2;
 constexpr size_t kRecordsOffset = kWorkspaceHeaderBytes + kFinishOrderBytes;
 constexpr size_t kSliceHistBytes = 8 * 1024 * 2;
 
-// Workspace bytes for B rows of `chunks` chunks.
-inline size_t sample_workspace_need(int B, int chunks) {
-  return kRecordsOffset + static_cast<size_t>(B) * chunks * (kChunkSlotBytes + kSliceHistBytes);
+// Workspace bytes for B rows of `chunks` chunks of bf16 or fp32 logits.
+inline size_t sample_workspace_need(int B, int chunks, bool bf16) {
+  return kRecordsOffset +
+         static_cast<size_t>(B) * chunks * (kChunkSlotBytes + (bf16 ? kSliceHistBytes : 0));
 }
 
 struct SampleParams {

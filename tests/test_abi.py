@@ -50,6 +50,9 @@ def test_version_and_workspace():
     per = 3216 + 8 * 1024 * 2
     assert lib.pkv_sample_workspace_bytes(256, 151936, 1) == fixed + 256 * 8 * per
     assert lib.pkv_sample_workspace_bytes(1024, 256000, 1) == fixed + 1024 * 16 * per
+    # fp32 rows have no count-histogram items, so no slice histograms: the
+    # nucleus batch's rows are 15 chunks of 10240 fp32.
+    assert lib.pkv_sample_workspace_bytes(256, 151936, 0) == fixed + 256 * 15 * 3216
     assert lib.pkv_sample_workspace_bytes(0, 100, 1) == 0
     assert lib.pkv_sample_workspace_bytes(4, 0, 1) == 0
     assert lib.pkv_sample_workspace_bytes(4, 100, 7) == 0

@@ -38,6 +38,15 @@ def test_noalloc_rejects_batches_beyond_its_scratch():
     assert "static scratch" in pkv.last_error()
 
 
+def test_noalloc_scratch_holds_the_benchmark_batches():
+    # The mixed bf16 batch and the fp32 full-vocabulary nucleus batch (both
+    # B=256, V=151936) fit the 64 MiB scratch; the large bf16 one does not.
+    lib = pkv.load()
+    assert lib.pkv_sample_workspace_bytes(256, 151936, pkv.PKV_BF16) <= 64 << 20
+    assert lib.pkv_sample_workspace_bytes(256, 151936, pkv.PKV_FP32) <= 64 << 20
+    assert lib.pkv_sample_workspace_bytes(1024, 256000, pkv.PKV_BF16) > 64 << 20
+
+
 def test_noalloc_checks_arguments_first():
     lib = pkv.load()
     rc = lib.pkv_sample_batch_noalloc(None, pkv.PKV_BF16, 4, 100, 100, None, None, None, None,
