@@ -4,7 +4,9 @@
 sampler calls on the mixed workload's logits (B=256, V=151936 bf16, four
 rotating buffers) with the parameters of one case: ``greedy`` (temperature
 0), ``plain`` (T=1), ``topk50``, ``topp`` (p=0.9, no top-k), ``topk50_topp``
-or ``mixed`` (the benchmark's own parameters).  Needs a GPU and the built
+or ``mixed`` (the benchmark's own parameters); or on one of the other
+workloads with its own parameters: ``pr1``, ``greedy_batch`` (B=64, V=128256
+bf16, all greedy), ``nucleus`` (fp32) or ``large``.  Needs a GPU and the built
 library.
 """
 
@@ -30,15 +32,22 @@ def params(case: str, w):
     return table[case]
 
 
+WORKLOADS = {"pr1": "pr1", "greedy_batch": "greedy", "nucleus": "nucleus", "large": "large"}
+
+
 def main(argv=None) -> None:
     argv = sys.argv[1:] if argv is None else argv
     case = argv[0] if argv else "mixed"
     calls = int(argv[1]) if len(argv) > 1 else 6
     dev = torch.device("cuda")
-    w = workloads.mixed()
+    if case in WORKLOADS:
+        w = workloads.make(WORKLOADS[case])
+        t, k, p = (None if x is None else x.to(dev) for x in (w.temperature, w.top_k, w.top_p))
+    else:
+        w = workloads.mixed()
+        t, k, p = (None if x is None else x.to(dev) for x in params(case, w))
     base = w.logits.to(dev)
-    bufs = [base] + [base.clone() for _ in range(3)]
-    t, k, p = (None if x is None else x.to(dev) for x in params(case, w))
+    bufs = [base] + [base.clone() for _ in range(3 if w.B * w.V * w.elt < (1 << 30) else 0)]
     u = w.uniform.to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     for i in range(calls):

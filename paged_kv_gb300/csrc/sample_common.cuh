@@ -159,9 +159,6 @@ static_assert(offsetof(ChunkSlot, tmax) % 16 == 0 && offsetof(ChunkSlot, hist) %
 __device__ __forceinline__ WorkspaceHeader* ws_header(const SampleParams& P) {
   return static_cast<WorkspaceHeader*>(P.workspace);
 }
-__device__ __forceinline__ uint16_t* ws_finish_order(const SampleParams& P) {
-  return reinterpret_cast<uint16_t*>(static_cast<char*>(P.workspace) + kWorkspaceHeaderBytes);
-}
 __device__ __forceinline__ ChunkSlot* ws_records(const SampleParams& P) {
   return reinterpret_cast<ChunkSlot*>(static_cast<char*>(P.workspace) + kRecordsOffset);
 }
@@ -858,10 +855,26 @@ struct RowParams {
   bool use_p;
 };
 
+// A row's raw parameters.  All five loads are issued at once (none depends
+// on another), so a thread that ranks several rows pays one round trip.
+struct RowInputs {
+  float t, p, u, mp;
+  int k;
+};
+
+__device__ __forceinline__ RowInputs load_row_inputs(const SampleParams& P, int row) {
+  RowInputs in;
+  in.t = P.temperature != nullptr ? P.temperature[row] : 0.0f;
+  in.k = P.top_k != nullptr ? P.top_k[row] : -1;
+  in.p = P.top_p != nullptr ? P.top_p[row] : 1.0f;
+  in.u = P.uniform != nullptr ? P.uniform[row] : 0.0f;
+  in.mp = P.min_p != nullptr ? P.min_p[row] : 0.0f;
+  return in;
+}
+
 template <bool BF16, int NV>
-__device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, int C) {
+__device__ __forceinline__ RowParams row_params_of(const RowInputs& in, int V) {
   using L = Layout<BF16>;
-  const int V = P.V;
   RowParams r;
   r.T = 1.0f;
   r.p = 1.0f;
@@ -870,14 +883,14 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
   r.st = 0;
   r.kind = kKindG;
   r.minp = 0.0f;
-  const bool greedy = P.temperature == nullptr || !(P.temperature[row] > 0.0f);
+  const bool greedy = !(in.t > 0.0f);  // no temperature tensor reads as 0
   if (!greedy) {
-    r.T = fmaxf(P.temperature[row], 1e-6f);
-    int k = P.top_k != nullptr ? P.top_k[row] : -1;
+    r.T = fmaxf(in.t, 1e-6f);
+    int k = in.k;
     if (k < 1 || k >= V) k = V;
     r.k = k;
-    r.p = P.top_p != nullptr ? fminf(fmaxf(P.top_p[row], 1e-6f), 1.0f) : 1.0f;
-    float u = P.uniform[row];
+    r.p = fminf(fmaxf(in.p, 1e-6f), 1.0f);
+    float u = in.u;
     if (!(u >= 0.0f && u < 1.0f)) {
       r.st |= kStBadUniform;
       u = (u != u) ? 0.0f : fminf(fmaxf(u, 0.0f), 0x1.fffffep-1f);
@@ -886,11 +899,9 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
     // K bounds the k-th value by the k-th largest thread maximum: it needs
     // at least k threads whose elements all lie inside the row.
     const int full_threads = V / (NV * L::VW);
-    (void)C;
     // min_p (off when <= 0 or NaN, at most 1) is one more cut on the kept
     // set of every filtered kind; a row with no other filter is filtered.
-    const float mp = P.min_p != nullptr ? P.min_p[row] : 0.0f;
-    r.minp = mp > 0.0f ? fminf(mp, 1.0f) : 0.0f;
+    r.minp = in.mp > 0.0f ? fminf(in.mp, 1.0f) : 0.0f;
     if (k < V && k <= kMaxK && full_threads >= k) {
       r.kind = kKindK;
     } else if (k == V && !(r.p < 1.0f) && !(r.minp > 0.0f)) {
@@ -904,6 +915,12 @@ __device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, 
   r.use_p = r.p < 1.0f;
   r.c2 = 1.4426950408889634f / r.T;  // log2(e) / T
   return r;
+}
+
+template <bool BF16, int NV>
+__device__ __forceinline__ RowParams row_params(const SampleParams& P, int row, int C) {
+  (void)C;
+  return row_params_of<BF16, NV>(load_row_inputs(P, row), P.V);
 }
 
 }  // namespace pkv

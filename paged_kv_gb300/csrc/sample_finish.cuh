@@ -920,13 +920,14 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
     mbar_init(bar, 1);
     fence_mbar_init();
   }
+  // The row's parameters and write-back coordinates are inputs, not the
+  // stream kernel's output: they load before the wait.
+  const int row = static_cast<int>(blockIdx.x);
+  const RowParams rp = row_params<BF16, NV>(P, row, C);
+  const WriteBack wb = load_write_back(P, row);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The row of this CTA: the stream kernel's placement for ordered batches
-  // (heavy and light rows alternate), else the CTA index.
-  const int row = P.B <= kOrderRows ? static_cast<int>(__ldcg(ws_finish_order(P) + blockIdx.x))
-                                    : static_cast<int>(blockIdx.x);
   // The row's records in one bulk copy (they are contiguous), completing on
-  // rec_bar; the row parameters and write-back coordinates load meanwhile.
+  // rec_bar.
   const uint32_t rec_bytes = static_cast<uint32_t>(C) * static_cast<uint32_t>(kChunkSlotBytes);
   if (tid == 0) {
     const char* src = reinterpret_cast<const char*>(ws_records(P) + static_cast<size_t>(row) * C);
@@ -935,8 +936,6 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
       bulk_copy_g2s(dyn + off, src + off, min(16384u, rec_bytes - off), bar);
     }
   }
-  const RowParams rp = row_params<BF16, NV>(P, row, C);
-  const WriteBack wb = load_write_back(P, row);
   const uint32_t seq = __ldcg(&ws_header(P)->calls);  // the stream kernel's call number
   float* q_row = P.probs_out != nullptr ? P.probs_out + static_cast<size_t>(row) * V : nullptr;
   group_sync();  // the barrier's initialisation is visible to every waiter

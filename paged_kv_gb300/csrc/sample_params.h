@@ -24,15 +24,15 @@ struct WorkspaceHeader {
 constexpr size_t kWorkspaceHeaderBytes = 256;
 static_assert(sizeof(WorkspaceHeader) == kWorkspaceHeaderBytes, "header size");
 
-// After the header: the finish kernel's row for each CTA (16-bit, batches of
-// up to kOrderRows rows), then the records, then one block of slice
-// histograms per (row, chunk): for each of the stream kernel's 8 consumer
-// warps, the 16-bit counts of the 1024 keys below the chunk maximum over
-// that warp's slice of the chunk (written for count-histogram rows only,
-// which are bf16 rows: fp32 workspaces have no slice histograms).
+// After the header: the records, then one block of slice histograms per
+// (row, chunk): for each of the stream kernel's 8 consumer warps, the 16-bit
+// counts of the 1024 keys below the chunk maximum over that warp's slice of
+// the chunk (written for count-histogram rows only, which are bf16 rows:
+// fp32 workspaces have no slice histograms).  Batches of up to kOrderRows
+// rows are streamed in cost order (the order lives in the stream kernel's
+// shared memory).
 constexpr int kOrderRows = 4096;
-constexpr size_t kFinishOrderBytes = static_cast<size_t>(kOrderRows) * 2;
-constexpr size_t kRecordsOffset = kWorkspaceHeaderBytes + kFinishOrderBytes;
+constexpr size_t kRecordsOffset = kWorkspaceHeaderBytes;
 constexpr size_t kSliceHistBytes = 8 * 1024 * 2;
 
 // Workspace bytes for B rows of `chunks` chunks of bf16 or fp32 logits.

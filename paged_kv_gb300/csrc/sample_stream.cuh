@@ -199,37 +199,49 @@ constexpr int kStreamThreads = kGroups * (kThreads + 32);
 // 16-bit entry per row in shared memory); larger batches go in row order.
 constexpr int kOrderPerThread = (kOrderRows + kStreamThreads - 1) / kStreamThreads;
 
-// Cost class of a row: 0 for the count-histogram and fallback rows (the
-// most work in both kernels), 1 for top-k rows (long in the finish kernel),
-// 2 for plain rows (one exp per element in the stream kernel), 3 for greedy
-// rows.  Classes 0 and 1 are the finish kernel's heavy rows.
+// Cost class of a row's parameters: 0 for the count-histogram, candidate
+// and fallback rows (the most work in both kernels), 1 for top-k rows (long
+// in the finish kernel), 2 for plain rows (one exp per element in the
+// stream kernel), 3 for greedy rows.  Classes 0 and 1 are the finish
+// kernel's heavy rows.
 template <bool BF16, int NV>
-__device__ __forceinline__ int row_cost_class(const SampleParams& P, int row) {
-  const int kind = row_params<BF16, NV>(P, row, 0).kind;
+__device__ __forceinline__ int row_cost_class(const RowInputs& in, int V) {
+  const int kind = row_params_of<BF16, NV>(in, V).kind;
   return (kind == kKindH || kind == kKindF || kind == kKindT)
              ? 0
              : (kind == kKindK ? 1 : (kind == kKindP ? 2 : 3));
 }
 
-// order[0 .. B) = the rows sorted by cost class, stable in row index.  All
-// threads of the CTA call it; it ends with a CTA barrier, after which
-// wsum[kStreamThreads / 32] holds the four class counts.  Thread t ranks rows
-// [t * kOrderPerThread, (t + 1) * kOrderPerThread): four 16-bit class counts
-// packed in a 64-bit word, one CTA-wide exclusive scan.
+// order[0 .. n): the rows the queues hand out, sorted by cost class, stable
+// in row index: every row except the light rows below r_early (those are
+// streamed as early items, see the kernel).  All threads of the CTA call it;
+// it ends with a CTA barrier, after which wsum[kStreamThreads / 32] holds the
+// four class counts of the rows placed.  Thread t ranks the `per` rows
+// [t * per, (t + 1) * per), per = ceil(B / kStreamThreads) (so every thread
+// has work and the parameter loads of all rows are in flight at once): four
+// 16-bit class counts packed in a 64-bit word, one CTA-wide exclusive scan.
 template <bool BF16, int NV>
-__device__ __forceinline__ void build_order(const SampleParams& P, uint16_t* order,
+__device__ __forceinline__ void build_order(const SampleParams& P, int r_early, uint16_t* order,
                                             unsigned long long* wsum) {
   constexpr int kWarpsAll = kStreamThreads / 32;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  const int r0 = t * kOrderPerThread;
-  uint32_t cls = 0;
+  const int per = (P.B + kStreamThreads - 1) / kStreamThreads;  // <= kOrderPerThread
+  const int r0 = t * per;
+  RowInputs in[kOrderPerThread];
+#pragma unroll
+  for (int j = 0; j < kOrderPerThread; ++j) {
+    if (j < per && r0 + j < P.B) in[j] = load_row_inputs(P, r0 + j);
+  }
+  uint32_t cls = 0, placed = 0;
   unsigned long long cnt = 0;
 #pragma unroll
   for (int j = 0; j < kOrderPerThread; ++j) {
     const int r = r0 + j;
-    if (r < P.B) {
-      const int c = row_cost_class<BF16, NV>(P, r);
+    if (j < per && r < P.B) {
+      const int c = row_cost_class<BF16, NV>(in[j], P.V);
+      if (r < r_early && c != 0) continue;  // an early row
       cls |= static_cast<uint32_t>(c) << (2 * j);
+      placed |= 1u << j;
       cnt += 1ull << (16 * c);
     }
   }
@@ -265,7 +277,7 @@ __device__ __forceinline__ void build_order(const SampleParams& P, uint16_t* ord
 #pragma unroll
   for (int j = 0; j < kOrderPerThread; ++j) {
     const int r = r0 + j;
-    if (r < P.B) {
+    if ((placed >> j) & 1u) {
       const uint32_t c = (cls >> (2 * j)) & 3u;
       const uint32_t at = pos[c]++;
       order[at] = static_cast<uint16_t>(r);
@@ -274,32 +286,19 @@ __device__ __forceinline__ void build_order(const SampleParams& P, uint16_t* ord
   __syncthreads();
 }
 
-// The finish kernel's row of each CTA: heavy rows (classes 0 and 1) and
-// light ones alternate, so that CTAs placed side by side on an SM are rarely
-// two heavy rows; the longer list continues alone.  Written by CTA 0 of the
-// stream kernel after build_order.
-__device__ __forceinline__ void write_finish_order(const uint16_t* order, int B,
-                                                   unsigned long long counts, uint16_t* out) {
-  const int nh = static_cast<int>((counts & 0xffffu) + ((counts >> 16) & 0xffffu));
-  const int nl = B - nh;
-  const int mn = nh < nl ? nh : nl;
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    int p;
-    if (b < 2 * mn) {
-      p = (b & 1) ? nh + (b >> 1) : (b >> 1);
-    } else {
-      p = nh > nl ? mn + (b - 2 * mn) : nh + mn + (b - 2 * mn);
-    }
-    out[b] = order[p];
+// Row and chunk of item rank q: ranks [0, e0) are the early items in row
+// order (item e is chunk e % C of row e / C), the others map through the
+// cost order when `ordered`.
+__device__ __forceinline__ void item_of(int q, int C, int e0, bool ordered, const uint16_t* order,
+                                        int* row, int* chunk) {
+  if (q < e0) {
+    *row = q / C;
+    *chunk = q - (q / C) * C;
+    return;
   }
-}
-
-// Row and chunk of item rank q (rows in cost order when `ordered`).
-__device__ __forceinline__ void item_of(int q, int C, bool ordered, const uint16_t* order, int* row,
-                                        int* chunk) {
-  const int r = q / C;
+  const int r = (q - e0) / C;
   *row = ordered ? static_cast<int>(order[r]) : r;
-  *chunk = q - r * C;
+  *chunk = (q - e0) - r * C;
 }
 
 // Items are handed out one at a time from the workspace header's ticket
@@ -339,41 +338,66 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   unsigned char* ring = dyn + group * kStages * kStageBytes;
   uint64_t* fullb = reinterpret_cast<uint64_t*>(full[group]);
   uint64_t* emptyb = reinterpret_cast<uint64_t*>(empty[group]);
+  // Early items (aligned, ordered batches): producer (CTA b, group g) owns
+  // item e = 2b + g of the rows [0, early_rows) in row order (chunk e % C of
+  // row e / C).  If that row is light (not a count-histogram, candidate or
+  // fallback row), its first stage takes the item at the kernel's start:
+  // one read of the row's parameters, no ticket and no cost order needed.
+  // The queues hand out every other row: the heavy rows first (early range
+  // included), then the light rows from early_rows on.
+  const bool ordered = P.B <= kOrderRows;
+  const int early_rows =
+      (VEC && ordered) ? min(P.B, static_cast<int>(gridDim.x) * kGroups / C) : 0;
+  const uint32_t early = static_cast<uint32_t>(early_rows * C);  // rank offset of the queues
 
-  if constexpr (VEC) {
+  // Two queues (aligned rows): ranks [early, early + heavy) are the items of
+  // the count-histogram and candidate rows, bound by shared-memory work,
+  // ranks [early + heavy, items) the rest, bound by HBM.  Group 0 of a CTA
+  // starts on the first queue and group 1 on the second; each moves to the
+  // other queue once its own is empty, so the heavy work overlaps the
+  // streaming instead of holding every group at once.  Each producer claims
+  // its next tickets before the row order is built, so that the ticket round
+  // trip overlaps it.
+  uint32_t first_ticket = 0;
+  int first_item = -1;  // this producer's early item
+  if (VEC && producer && (threadIdx.x & 31) == 0) {
     // full[s]: the producer's arrival (with the copy's bytes) completes it;
     // empty[s]: one arrival per consumer warp once its vectors are loaded.
-    if (threadIdx.x == 0) {
-      for (int g = 0; g < kGroups; ++g) {
-        for (int s = 0; s < kStages; ++s) {
-          mbar_init(reinterpret_cast<uint64_t*>(&full[g][s]), 1);
-          mbar_init(reinterpret_cast<uint64_t*>(&empty[g][s]), kWarps);
-        }
+    // Each producer initialises its own group's barriers (the consumers
+    // first use them after the CTA barrier that ends build_order).
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&fullb[s], 1);
+      mbar_init(&emptyb[s], kWarps);
+    }
+    fence_mbar_init();
+    const int e = static_cast<int>(blockIdx.x) * kGroups + group;
+    if (e < static_cast<int>(early) &&
+        row_cost_class<BF16, NV>(load_row_inputs(P, e / C), V) != 0) {
+      first_item = e;
+      const int r = e / C, ch = e - (e / C) * C;
+      const int e0 = ch * CHUNK;
+      const uint32_t bytes = static_cast<uint32_t>(max(0, min(CHUNK, V - e0))) * L::ELT;
+      const char* src = static_cast<const char*>(P.logits) +
+                        (static_cast<size_t>(r) * static_cast<size_t>(P.row_stride) +
+                         static_cast<size_t>(e0)) * L::ELT;
+      stage_item[group][0] = e;
+      mbar_arrive_expect_tx(&fullb[0], bytes);
+      for (uint32_t off = 0; off < bytes; off += 16384u) {
+        bulk_copy_g2s(ring + off, src + off, min(16384u, bytes - off), &fullb[0]);
       }
-      fence_mbar_init();
     }
-  }
-  // Two queues (aligned rows): ranks [0, heavy) are the items of the
-  // count-histogram rows, bound by shared-memory atomics, ranks [heavy,
-  // items) the rest, bound by HBM.  Group 0 of a CTA starts on the first
-  // queue and group 1 on the second; each moves to the other queue once its
-  // own is empty, so the histogram work overlaps the streaming instead of
-  // holding every group at once.  Each producer claims its first kStages
-  // tickets before the row order is built, so that the ticket round trip
-  // overlaps it.
-  uint32_t first_ticket = 0;
-  if (VEC && producer && (threadIdx.x & 31) == 0) {
     first_ticket = atomicAdd(group == 0 ? &hdr->ticket_heavy : &hdr->ticket,
-                             static_cast<uint32_t>(kStages));
+                             static_cast<uint32_t>(kStages - (first_item >= 0 ? 1 : 0)));
   }
-  const bool ordered = P.B <= kOrderRows;
   uint32_t heavy = 0;  // items of class-0 rows, ranked first
+  uint32_t queued = static_cast<uint32_t>(items);  // ranks [early, queued) are the queues'
   if (ordered) {
-    build_order<BF16, NV>(P, order, order_sum);  // ends with a CTA barrier
-    heavy = static_cast<uint32_t>(order_sum[kStreamThreads / 32] & 0xffffu) * static_cast<uint32_t>(C);
-    if (blockIdx.x == 0) {
-      write_finish_order(order, P.B, order_sum[kStreamThreads / 32], ws_finish_order(P));
-    }
+    build_order<BF16, NV>(P, early_rows, order, order_sum);  // ends with a CTA barrier
+    const unsigned long long cls = order_sum[kStreamThreads / 32];
+    heavy = static_cast<uint32_t>(cls & 0xffffu) * static_cast<uint32_t>(C);
+    const uint32_t placed = static_cast<uint32_t>((cls & 0xffffu) + ((cls >> 16) & 0xffffu) +
+                                                  ((cls >> 32) & 0xffffu) + (cls >> 48));
+    queued = early + placed * static_cast<uint32_t>(C);
   } else {
     __syncthreads();
   }
@@ -391,7 +415,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         int qi = group == 0 ? 0 : 1;  // the queue in use: 0 heavy, 1 the rest
         bool moved = false;           // already moved to the other queue
         const bool stagger = heavy > 0u;
-        for (int n = 0;; ++n) {
+        const int n0 = first_item >= 0 ? 1 : 0;  // stage 0 already holds the early item
+        if (n0 == 1) last_copy[0] = 0;
+        for (int n = n0;; ++n) {
           const int s = n % kStages;
           if (n >= kStages) {
             const uint32_t parity = static_cast<uint32_t>(n / kStages - 1) & 1u;
@@ -414,10 +440,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           int q = -1;
           for (;;) {
             const uint32_t t = (!moved && n < kStages)
-                                   ? first_ticket + static_cast<uint32_t>(n)
+                                   ? first_ticket + static_cast<uint32_t>(n - n0)
                                    : atomicAdd(qi == 0 ? &hdr->ticket_heavy : &hdr->ticket, 1u);
-            const uint32_t lo = qi == 0 ? 0u : heavy;
-            const uint32_t len = qi == 0 ? heavy : static_cast<uint32_t>(items) - heavy;
+            const uint32_t lo = qi == 0 ? early : early + heavy;
+            const uint32_t len = qi == 0 ? heavy : queued - early - heavy;
             if (t < len) {
               q = static_cast<int>(lo + t);
               break;
@@ -433,7 +459,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             break;
           }
           int r, ch;
-          item_of(q, C, ordered, order, &r, &ch);
+          item_of(q, C, static_cast<int>(early), ordered, order, &r, &ch);
           const int e0 = ch * CHUNK;
           // Every chunk starts inside the row (the launch never makes an empty one).
           const uint32_t bytes = static_cast<uint32_t>(max(0, min(CHUNK, V - e0))) * L::ELT;
@@ -497,7 +523,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         q = *static_cast<volatile int*>(&stage_item[group][s]);
         if (q < 0) break;
         int row, chunk;
-        item_of(q, C, ordered, order, &row, &chunk);
+        item_of(q, C, static_cast<int>(early), ordered, order, &row, &chunk);
         const uint4* sv = reinterpret_cast<const uint4*>(ring + s * kStageBytes);
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
@@ -526,11 +552,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         group_sync();
         if (q >= items) break;
         int row, chunk;
-        item_of(q, C, ordered, order, &row, &chunk);
+        item_of(q, C, static_cast<int>(early), ordered, order, &row, &chunk);
         load_chunk<BF16, NV, false>(P, row, chunk, c.warp, c.lane, d);
       }
       int row, chunk;
-      item_of(q, C, ordered, order, &row, &chunk);
+      item_of(q, C, static_cast<int>(early), ordered, order, &row, &chunk);
       c.crank = static_cast<uint32_t>(chunk);
       ChunkSlot* slot = ws + (static_cast<size_t>(row) * C + chunk);
       const RowParams rp = row_params<BF16, NV>(P, row, C);

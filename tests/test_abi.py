@@ -43,10 +43,10 @@ def test_binding_types_every_declared_function():
 def test_version_and_workspace():
     lib = pkv.load()
     assert pkv.version() == 310
-    # A 256-byte header, 8 KB of finish placement, then per (row, chunk) one
+    # A 256-byte header, then per (row, chunk) one
     # 3216-byte record and 16 KB of slice histograms (8 warps x 1024 16-bit
     # counts); the mixed batch's rows are 8 chunks of 20480 bf16.
-    fixed = 256 + 8192
+    fixed = 256
     per = 3216 + 8 * 1024 * 2
     assert lib.pkv_sample_workspace_bytes(256, 151936, 1) == fixed + 256 * 8 * per
     assert lib.pkv_sample_workspace_bytes(1024, 256000, 1) == fixed + 1024 * 16 * per

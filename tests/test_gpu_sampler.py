@@ -195,10 +195,13 @@ def test_deterministic_across_calls():
 
 def test_workspace_header_is_checked_and_repaired():
     # A workspace whose header was never initialised (here: both ticket
-    # counters past every item) hands out no chunks, so every row's records are stale:
-    # every token is -1 with status bit 64 and nothing is written back.  The
-    # call leaves the header reset, and the next call on it is exact.
-    w = workloads.mixed(B=24, V=32768)
+    # counters past every item) hands out no queued item, so the rows those
+    # items belong to have stale records: their tokens are -1 with status bit
+    # 64 and nothing is written back for them.  Rows the kernel starts on
+    # without a ticket (the first item of every producer) may still be
+    # settled, and then exactly.  The call leaves the header reset, and the
+    # next call on it is exact.
+    w = workloads.mixed(B=400, V=32768)
     B, V = w.logits.shape
     ws = torch.zeros(pkv.sample_workspace_bytes(B, V, w.logits.dtype), dtype=torch.uint8,
                      device=DEV)
@@ -215,9 +218,17 @@ def test_workspace_header_is_checked_and_repaired():
     tok = pkv.sample_batch(L, *args, token_pool=pool, wb_rows=_d(rows), wb_cols=_d(cols),
                            status=status, workspace=ws)
     torch.cuda.synchronize()
-    assert (tok.cpu().numpy() == -1).all()
+    tok = tok.cpu().numpy()
+    failed = tok == -1
+    assert failed.any()
     assert int(status.item()) & pkv.ST_TIMEOUT
-    assert int(pool.abs().sum().item()) == 0
+    written = pool.cpu().numpy()[:, 0]
+    assert (written[failed] == 0).all()
+    ok = np.nonzero(~failed)[0]
+    if len(ok):
+        sub = lambda x: None if x is None else x[ok]  # noqa: E731
+        check_sampler(w.logits[ok], sub(w.temperature), sub(w.top_k), sub(w.top_p),
+                      sub(w.uniform), tok[ok])
     assert hdr.cpu().tolist()[:4] == [0, 0, 8, 0]
     status.zero_()
     tok = pkv.sample_batch(L, *args, status=status, workspace=ws)
