@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK, PKV_EINVAL, PKV_ENOSPC, PKV_ECUDA, PKV_EUNSUPPORTED = 0, -1, -2, -3, -4
 PKV_FP32, PKV_BF16 = 0, 1
+PKV_MAX_VOCAB_FP32, PKV_MAX_VOCAB_BF16 = 262144, 524288
 ST_NONFINITE, ST_ALL_NEG_INF, ST_ROW_OOB, ST_COL_OOB, ST_BAD_UNIFORM, ST_NOSPC = 1, 2, 4, 8, 16, 32
 ST_TIMEOUT = 64
 ST_TOKEN_CAP = 128

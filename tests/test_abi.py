@@ -40,6 +40,13 @@ def test_binding_types_every_declared_function():
         assert fn.restype is not None, f"{name}: no restype in paged_kv_gb300/pkv.py"
 
 
+def test_binding_constants_match_the_header():
+    text = open(HEADER).read()
+    for name in ("PKV_MAX_VOCAB_FP32", "PKV_MAX_VOCAB_BF16"):
+        m = re.search(r"#define\s+%s\s+(\d+)" % name, text)
+        assert m is not None and int(m.group(1)) == getattr(pkv, name), name
+
+
 def test_version_and_workspace():
     lib = pkv.load()
     assert pkv.version() == 310

@@ -95,6 +95,47 @@ def test_every_row_kind_in_one_batch(dtype):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_batch_beyond_the_cost_order(dtype):
+    # More rows than the stream kernel orders by cost (4096): items are then
+    # taken in row order from one queue.
+    B, V = 5000, 4096
+    seed = 31 + (1 if dtype == torch.bfloat16 else 0)
+    logits = workloads.random_rows(B, V, dtype, seed=seed)
+    t, k, p, u = workloads.random_params(B, seed=seed + 2, k_values=(-1, 1, 20, 300, V),
+                                         p_values=(1.0, 0.5, 0.9, 0.95))
+    tok, _, st = gpu_sample(logits, t, k, p, u)
+    assert st == 0
+    stats = check_sampler(logits, t, k, p, u, tok, None)
+    _every_row_checked(stats, B)
+
+
+def test_maximum_batch():
+    B, V = 65535, 40
+    logits = workloads.random_rows(B, V, torch.bfloat16, seed=41, discrete=True)
+    t, k, p, u = workloads.random_params(B, seed=42, k_values=(-1, 1, 5, V),
+                                         p_values=(1.0, 0.5, 0.9))
+    tok, _, st = gpu_sample(logits, t, k, p, u)
+    assert st == 0
+    stats = check_sampler(logits, t, k, p, u, tok, None)
+    _every_row_checked(stats, B)
+
+
+@pytest.mark.parametrize("dtype,V", [(torch.float32, pkv.PKV_MAX_VOCAB_FP32),
+                                     (torch.bfloat16, pkv.PKV_MAX_VOCAB_BF16)])
+def test_rows_at_the_vocab_limit(dtype, V):
+    # Greedy, top-k, top-p, top-k with top-p, and plain rows at the largest V.
+    logits = workloads.random_rows(5, V, dtype, seed=51, scale=2.0)
+    t = torch.tensor([0.0, 0.9, 1.1, 0.7, 1.0])
+    k = torch.tensor([-1, 40, -1, 500, -1], dtype=torch.int32)
+    p = torch.tensor([1.0, 1.0, 0.9, 0.8, 1.0])
+    u = torch.rand(5, generator=torch.Generator().manual_seed(52))
+    tok, q, st = gpu_sample(logits, t, k, p, u, probs=True)
+    assert st == 0
+    stats = check_sampler(logits, t, k, p, u, tok, q)
+    _every_row_checked(stats, 5)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_unaligned_rows_take_the_scalar_path(dtype):
     B, V = 6, 3001
     base = workloads.random_rows(B, V + 1, dtype, seed=21)
