@@ -99,105 +99,145 @@ __device__ __forceinline__ void emit(const SampleParams& P, int row, int tok, in
 
 // ----------------------------------------------------------------- plain finish (P)
 
-// No filter: the draw is over the whole row.  The record masses (warp w of
-// chunk r: wz relative to its maximum wm) are scanned in index order to find
-// the (chunk, warp) holding u * Z; that warp re-reads its slice and finds the
-// token with per-vector sums.
+// Inclusive prefix over the CTA's threads in tid order, with each thread's
+// exclusive prefix taken as its predecessor's inclusive one (not incl - v):
+// the intervals [before, incl) of threads with mass then tile [0, total)
+// without gaps or overlaps, so at most one thread owns a point of it.
+__device__ __forceinline__ float block_incl_scan_f(float v, float* s_w, int lane, int warp,
+                                                   float* before, float* total) {
+  const float wincl = warp_inclusive_scan(v, lane);
+  if (lane == 31) s_w[warp] = wincl;
+  group_sync();
+  float off = 0.0f, all = 0.0f;
+#pragma unroll 1
+  for (int w = 0; w < kWarps; ++w) {
+    if (w == warp) off = all;
+    all += s_w[w];
+  }
+  group_sync();
+  const float incl = off + wincl;
+  const float prev = __shfl_up_sync(kFull, incl, 1);
+  *before = lane == 0 ? off : prev;
+  *total = all;
+  return incl;
+}
+
+// No filter: the draw is over the whole row.  Warp 0 scans the record masses
+// (warp w of chunk r: wz relative to its maximum wm) in index order to find
+// the (chunk, warp) holding u * Z; the CTA re-reads that warp's slice (an L2
+// hit; two consecutive vectors per thread), one prefix over the CTA finds the
+// thread holding the rest of the draw, and that thread the token.
 template <bool BF16, int NV, bool VEC>
 __device__ __forceinline__ void finish_plain(const SampleParams& P, SampleSmem& sm, const Ctx& c,
                                              const ChunkSlot* recs, int row, const RowParams& rp,
                                              float m, const WriteBack& wb, float* q_row) {
+  using L = Layout<BF16>;
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   const int C = static_cast<int>(c.csize);
   const int V = P.V;
-  const int nrec = C * kWarps;
-  float mw = 0.0f;
-  if (tid < nrec) {
-    const float wmax = recs[tid / kWarps].wm[tid % kWarps];
-    if (wmax > -INFINITY) mw = recs[tid / kWarps].wz[tid % kWarps] * ex2((wmax - m) * rp.c2);
-  }
-  float zrow;
-  const float before = block_exclusive_scan<float>(mw, sm.wt, lane, warp, &zrow);
-  float target = rp.u * zrow;
-  if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
-  // The entry whose interval holds target; rounding can leave none: then
-  // the last entry with mass.
-  const int hit = block_min_int(
-      (mw > 0.0f && target >= before && target < before + mw) ? tid : INT_MAX, sm.wi, lane, warp);
-  const int lastm = block_max_int(mw > 0.0f ? tid : -1, sm.wi, lane, warp);
-  const int estar = hit != INT_MAX ? hit : lastm;
-  if (tid == estar) sm.bf4[0] = hit != INT_MAX ? target - before : INFINITY;
-  group_sync();
-  const float tau = sm.bf4[0];
-  if (estar >= 0 && warp == estar % kWarps) {
-    const int r = estar / kWarps;
-    uint32_t d[NV][4];
-    load_chunk<BF16, NV, VEC>(P, row, r, warp, lane, d);
-    // Per-vector lane sums, then the vector holding tau, the lane, the element.
-    float s[NV];
-    int lastl = -1;
+  if (warp == 0) {
+    // Lane l holds entries 4l .. 4l + 3 (entry chunk * kWarps + warp; C * kWarps <= 128).
+    float mw[4];
+    float s = 0.0f;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      float sj = 0.0f;
-      for_vec<BF16>(d[j], vec_base<BF16, NV>(r, warp, lane, j), [&](float x, int e) {
-        const float w = e < V ? weight(x, m, rp.c2) : 0.0f;
-        sj += w;
-        if (w > 0.0f) lastl = e;
-      });
-      s[j] = sj;
-    }
-    float tot[NV];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) tot[j] = warp_sum(s[j]);
-    int jstar = -1;
-    float a = 0.0f, abefore = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-      if (jstar < 0 && tot[j] > 0.0f && tau < a + tot[j]) {
-        jstar = j;
-        abefore = a;
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * lane + j;
+      mw[j] = 0.0f;
+      if (e < C * kWarps) {
+        const float wmax = recs[e / kWarps].wm[e % kWarps];
+        if (wmax > -INFINITY) mw[j] = recs[e / kWarps].wz[e % kWarps] * ex2((wmax - m) * rp.c2);
       }
-      a += tot[j];
+      s += mw[j];
     }
-    const int lastw = __reduce_max_sync(kFull, lastl);  // the slice's last element with mass
-    int tok = lastw;
-    if (jstar >= 0) {
-      float sj = 0.0f;
-      uint32_t v4[4] = {0u, 0u, 0u, 0u};
+    const float incl = warp_inclusive_scan(s, lane);
+    const float zrow = __shfl_sync(kFull, incl, 31);
+    float target = rp.u * zrow;
+    if (!(target < zrow)) target = nextafterf(zrow, 0.0f);
+    // The lane whose interval holds target; rounding can leave none: then
+    // the last lane with mass, at the end of its last entry with mass.
+    const unsigned hit = __ballot_sync(kFull, s > 0.0f && target < incl);
+    const unsigned pos = __ballot_sync(kFull, s > 0.0f);
+    const int l = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    if (lane == l) {
+      float run = incl - s;
+      int estar = -1, elast = -1;
+      float tau = INFINITY;
 #pragma unroll
-      for (int j = 0; j < NV; ++j) {
-        if (j == jstar) {
-          sj = s[j];
-          v4[0] = d[j][0];
-          v4[1] = d[j][1];
-          v4[2] = d[j][2];
-          v4[3] = d[j][3];
+      for (int j = 0; j < 4; ++j) {
+        if (mw[j] > 0.0f) {
+          elast = 4 * lane + j;
+          if (estar < 0 && hit != 0u && target < run + mw[j]) {
+            estar = elast;
+            tau = fmaxf(target - run, 0.0f);
+          }
+          run += mw[j];
         }
       }
-      const float incl = warp_inclusive_scan(sj, lane) + abefore;
-      const unsigned bal = __ballot_sync(kFull, tau < incl);
-      const int ls = bal ? __ffs(bal) - 1 : 31;
-      int sel = -1;
-      if (lane == ls) {
-        float run = incl - sj;
-        int lastv = -1;
-        for_vec_c<BF16>(make_uint4(v4[0], v4[1], v4[2], v4[3]),
-                        vec_base<BF16, NV>(r, warp, lane, jstar), [&](float x, int e) {
-          const float w = e < V ? weight(x, m, rp.c2) : 0.0f;
-          run += w;
-          if (w > 0.0f) {
-            lastv = e;
-            if (sel < 0 && tau < run) sel = e;
-          }
-        });
-        if (sel < 0) sel = lastv;
+      if (estar < 0) {
+        estar = elast;
+        tau = INFINITY;
       }
-      const int found = __shfl_sync(kFull, sel, ls);
-      if (found >= 0) tok = found;
+      sm.bi[0] = pos ? estar : -1;
+      sm.bf4[0] = tau;
+      sm.bf4[1] = zrow;
     }
-    if (lane == 0) emit(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
   }
-  if (estar < 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
+  group_sync();
+  const int estar = sm.bi[0];
+  const float tau = sm.bf4[0];
+  const float zrow = sm.bf4[1];
+  if (estar < 0) {
+    if (tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
+  } else {
+    // Vectors 2t and 2t + 1 of the slice (vector j * 32 + l of the stream
+    // layout): 2 * VW consecutive elements from e0.
+    const int r = estar / kWarps, w = estar % kWarps;
+    const bool active = tid < NV * 16;
+    const int e0 = vec_base<BF16, NV>(r, w, (2 * tid) % 32, (2 * tid) / 32);
+    uint4 v[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    if (active) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint32_t q[4];
+        load_vec<BF16, NV, VEC>(P, row, e0 + k * L::VW, q);
+        v[k] = make_uint4(q[0], q[1], q[2], q[3]);
+      }
+    }
+    float s = 0.0f;
+    int last = -1;
+    if (active) {
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {
+        for_vec_c<BF16>(k == 0 ? v[0] : v[1], e0 + k * L::VW, [&](float x, int e) {
+          const float wt = e < V ? weight(x, m, rp.c2) : 0.0f;
+          s += wt;
+          if (wt > 0.0f) last = e;
+        });
+      }
+    }
+    float before, total;
+    const float incl = block_incl_scan_f(s, sm.wt, lane, warp, &before, &total);
+    const bool mine = s > 0.0f && tau >= before && tau < incl;
+    if (mine) {
+      float run = before;
+      int sel = -1;
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {
+        for_vec_c<BF16>(k == 0 ? v[0] : v[1], e0 + k * L::VW, [&](float x, int e) {
+          const float wt = e < V ? weight(x, m, rp.c2) : 0.0f;
+          if (sel < 0 && wt > 0.0f && tau < run + wt) sel = e;
+          run += wt;
+        });
+      }
+      emit(P, row, sel >= 0 ? sel : last, rp.st, wb);
+    }
+    if (!(tau < total)) {
+      // The rest of the draw lies past the slice's own mass (rounding): its
+      // last element with mass.
+      const int lastall = block_max_int(last, sm.wi, lane, warp);
+      if (tid == 0) emit(P, row, lastall, lastall < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
+    }
+  }
   if (q_row != nullptr) {
     const float inv = 1.0f / zrow;
     for (int r = 0; r < C; ++r) {
@@ -344,35 +384,25 @@ __device__ __forceinline__ bool finish_topk(const SampleParams& P, SampleSmem& s
   }
   // min_p: weights fall with the rank, so the cut keeps S a prefix.
   const bool kept = in_k && before < target && (rp.minp <= 0.0f || wf >= rp.minp);
-  const int s = block_max_int(kept ? tid + 1 : 0, sm.wi, lane, warp);  // S = the first s of the order
-  // ---- draw in index order over S: entry t goes to position pos_t.
-  unsigned long long* wpos = sm.scan;  // the candidate ids are consumed
-  int32_t* ipos = reinterpret_cast<int32_t*>(sm.hhi);
-  int32_t* korder = reinterpret_cast<int32_t*>(sm.hlo);  // sorted[] is consumed
-  group_sync();
-  if (kept) korder[tid] = xi;
-  group_sync();
-  if (kept) {
-    int pos = 0;
+  // ---- draw in index order over S = the first s of the order: entry t
+  // owns [c_t, c_t + w_t) with c_t the mass of the kept entries of smaller
+  // index; the intervals tile [0, Z_S) exactly (fixed point).
+  int32_t* kidx = reinterpret_cast<int32_t*>(sm.hhi);
+  unsigned long long* kw = sm.scan;  // the candidate ids are consumed
+  kidx[tid] = kept ? xi : INT_MAX;
+  kw[tid] = kept ? w : 0ull;
+  const int s = block_max_int(kept ? tid + 1 : 0, sm.wi, lane, warp);  // its barriers publish kidx, kw
+  unsigned long long cum = 0, zs = 0;
 #pragma unroll 4
-    for (int u = 0; u < s; ++u) pos += korder[u] < xi ? 1 : 0;
-    wpos[pos] = w;
-    ipos[pos] = xi;
+  for (int t = 0; t < s; ++t) {
+    const unsigned long long wt = kw[t];
+    zs += wt;
+    cum += kidx[t] < xi ? wt : 0ull;
   }
-  group_sync();
-  const unsigned long long wp = tid < s ? wpos[tid] : 0ull;
-  unsigned long long zs;
-  const unsigned long long bp =
-      block_exclusive_scan<unsigned long long>(wp, sm.wl, lane, warp, &zs);
   const unsigned long long tdraw = mul_fx(zs, rp.u, false);
-  const int hit = block_min_int(
-      (tid < s && wp > 0 && tdraw >= bp && tdraw < bp + wp) ? tid : INT_MAX, sm.wi, lane, warp);
-  const int lastw = block_max_int((tid < s && wp > 0) ? tid : -1, sm.wi, lane, warp);
-  const int pstar = hit != INT_MAX ? hit : lastw;
-  if (tid == 0) {
-    const int tok = pstar >= 0 ? ipos[pstar] : -1;
-    emit(P, row, tok, tok < 0 ? (rp.st | kStNonFinite) : rp.st, wb);
-  }
+  const bool owner = kept && w > 0ull && tdraw >= cum && tdraw < cum + w;
+  if (owner) emit(P, row, xi, rp.st, wb);
+  if (__syncthreads_or(owner) == 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
   if (q_row != nullptr) {
     const float zf = block_sum<float>(kept ? wf : 0.0f, sm.wt, lane, warp);
     if (kept) q_row[xi] = wf / zf;

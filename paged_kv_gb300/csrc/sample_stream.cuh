@@ -320,6 +320,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   __shared__ __align__(8) unsigned long long empty[kGroups][kStages];
   __shared__ int stage_item[kGroups][kStages];  // rank copied into the stage, -1: no more
   __shared__ int group_item[kGroups];           // rank of the group's item (element-load path)
+  __shared__ int early_taken[kGroups];          // 1: the group's stage 0 holds an early item
+  __shared__ int lent_seen;                     // 1: group 1 saw group 0's stage 0 land
   __shared__ uint16_t order[kOrderRows];
   __shared__ unsigned long long order_sum[kStreamThreads / 32 + 1];
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -353,11 +355,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   // Two queues (aligned rows): ranks [early, early + heavy) are the items of
   // the count-histogram and candidate rows, bound by shared-memory work,
   // ranks [early + heavy, items) the rest, bound by HBM.  Group 0 of a CTA
-  // starts on the first queue and group 1 on the second; each moves to the
-  // other queue once its own is empty, so the heavy work overlaps the
-  // streaming instead of holding every group at once.  Each producer claims
-  // its next tickets before the row order is built, so that the ticket round
-  // trip overlaps it.
+  // starts on the first queue and group 1 on the second; a group that took
+  // no heavy item moves to the heavy queue once its own is empty, so the
+  // heavy work overlaps the streaming instead of holding every group at
+  // once.  Each producer claims its next tickets before the row order is
+  // built, so that the ticket round trip overlaps it.
   uint32_t first_ticket = 0;
   int first_item = -1;  // this producer's early item
   if (VEC && producer && (threadIdx.x & 31) == 0) {
@@ -386,6 +388,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         bulk_copy_g2s(ring + off, src + off, min(16384u, bytes - off), &fullb[0]);
       }
     }
+    early_taken[group] = first_item >= 0 ? 1 : 0;  // read by the consumers after build_order
+    if (group == 0) lent_seen = 0;
     first_ticket = atomicAdd(group == 0 ? &hdr->ticket_heavy : &hdr->ticket,
                              static_cast<uint32_t>(kStages - (first_item >= 0 ? 1 : 0)));
   }
@@ -414,6 +418,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         for (int s = 0; s < kStages; ++s) last_copy[s] = -1;
         int qi = group == 0 ? 0 : 1;  // the queue in use: 0 heavy, 1 the rest
         bool moved = false;           // already moved to the other queue
+        bool took_heavy = false;      // has taken items of the heavy queue
         const bool stagger = heavy > 0u;
         const int n0 = first_item >= 0 ? 1 : 0;  // stage 0 already holds the early item
         if (n0 == 1) last_copy[0] = 0;
@@ -446,9 +451,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             const uint32_t len = qi == 0 ? heavy : queued - early - heavy;
             if (t < len) {
               q = static_cast<int>(lo + t);
+              took_heavy = took_heavy || qi == 0;
               break;
             }
-            if (moved) break;  // both queues are empty
+            // Both queues are empty, or this group did heavy work: light
+            // items it took now would wait in its ring behind a heavy one
+            // while the other groups drain the light queue.
+            if (moved || took_heavy) break;
             moved = true;
             qi ^= 1;
           }
@@ -501,30 +510,54 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         reinterpret_cast<uint32_t*>(dyn + kGroups * kStages * kStageBytes) + group * kWarps * kHistWords;
     ChunkSlot* ws = ws_records(P);
     bool trusted = true;  // this warp has seen every copy land
+    // When there is heavy work, group 1 consumes the early item in group 0's
+    // first stage (before its own items), and group 0 starts on its first
+    // ticketed item, a heavy one: the long items start first while group 0's
+    // producer still keeps two stages ahead.  A stage's barriers count its
+    // consumers' arrivals, not which group's warps make them.
+    bool lend = false;
+    if constexpr (VEC) lend = kStages >= 2 && heavy > 0u && early_taken[0] != 0;
     for (int n = 0;; ++n) {
       uint32_t d[NV][4];
       int q;
+      // The stage consumed n-th: group sg's item m.
+      const int sg = (lend && group == 1 && n == 0) ? 0 : group;
+      const int m = lend ? (group == 0 ? n + 1 : (n == 0 ? 0 : n - 1)) : n;
       if constexpr (VEC) {
         // Each warp waits for the stage on its own (bounded), reads the rank,
         // loads its vectors and signals the producer; no group-wide barrier
         // on the data path.  After a timeout the warp still reads the rank
         // (written long before) and goes on, so that the group's barriers
         // stay matched, but its records are marked untrusted.
-        const int s = n % kStages;
-        const uint32_t parity = static_cast<uint32_t>(n / kStages) & 1u;
-        bool ok = mbar_try_wait(&fullb[s], parity);
+        const int s = m % kStages;
+        const uint32_t parity = static_cast<uint32_t>(m / kStages) & 1u;
+        uint64_t* full_s = reinterpret_cast<uint64_t*>(&full[sg][s]);
+        if (lend && group == 0 && m == kStages) {
+          // The first phase of this stage went to group 1: a parity test for
+          // the second is only meaningful once the first has completed.
+          const long long t0 = globaltimer_ns();
+          while (*static_cast<volatile int*>(&lent_seen) == 0) {
+            if (globaltimer_ns() - t0 > kWaitNs) {
+              trusted = false;
+              break;
+            }
+          }
+        }
+        bool ok = mbar_try_wait(full_s, parity);
         if (!ok) {
           const long long t0 = globaltimer_ns();
-          while (!(ok = mbar_try_wait(&fullb[s], parity))) {
+          while (!(ok = mbar_try_wait(full_s, parity))) {
             if (globaltimer_ns() - t0 > kWaitNs) break;
           }
         }
         if (!ok) trusted = false;
-        q = *static_cast<volatile int*>(&stage_item[group][s]);
+        if (sg != group && ok && c.lane == 0) *static_cast<volatile int*>(&lent_seen) = 1;
+        q = *static_cast<volatile int*>(&stage_item[sg][s]);
         if (q < 0) break;
         int row, chunk;
         item_of(q, C, static_cast<int>(early), ordered, order, &row, &chunk);
-        const uint4* sv = reinterpret_cast<const uint4*>(ring + s * kStageBytes);
+        const uint4* sv =
+            reinterpret_cast<const uint4*>(dyn + (sg * kStages + s) * kStageBytes);
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
           const int e0 = vec_base<BF16, NV>(chunk, c.warp, c.lane, j);
@@ -540,7 +573,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
           }
         }
         __syncwarp();
-        if (c.lane == 0) mbar_arrive(&emptyb[s]);
+        if (c.lane == 0) mbar_arrive(reinterpret_cast<uint64_t*>(&empty[sg][s]));
       } else {
         // Element loads: thread 0 of the group takes the ticket.
         if (c.tid == 0) {
