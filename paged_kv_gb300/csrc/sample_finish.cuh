@@ -437,15 +437,21 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
   const int k = rp.k;
   const bool topk = k < V;
   const uint32_t A = key16(m);
-  // The row's total mass (for top-p without top-k), from the warp records.
-  float zrow = 0.0f;
-  if (!topk) {
-    float mw = 0.0f;
-    if (tid < C * kWarps) {
-      const float wmax = recs[tid / kWarps].wm[tid % kWarps];
-      if (wmax > -INFINITY) mw = recs[tid / kWarps].wz[tid % kWarps] * ex2((wmax - m) * rp.c2);
+  // The row's total mass (for top-p without top-k), from the warp records:
+  // warp 0 alone (lane l: entries 4l .. 4l + 3), published by the barriers
+  // of the scans below.
+  if (!topk && warp == 0) {
+    float z = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * lane + j;
+      if (e < C * kWarps) {
+        const float wmax = recs[e / kWarps].wm[e % kWarps];
+        if (wmax > -INFINITY) z += recs[e / kWarps].wz[e % kWarps] * ex2((wmax - m) * rp.c2);
+      }
     }
-    zrow = block_sum<float>(mw, sm.wt, lane, warp);
+    z = warp_sum(z);
+    if (lane == 0) sm.bf4[2] = z;
   }
   // ---- merged counts and fixed-point weights; thread t holds keys 4t .. 4t + 3.
   uint32_t cnt[4] = {0u, 0u, 0u, 0u};
@@ -467,6 +473,12 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     table[i] = A >= i ? mass_fx(weight(key16_float(A - i), m, rp.c2)) : 0ull;
   }
   const unsigned long long* wfx = table + 4 * tid;  // this thread's four keys
+  // No owner below leaves a cut at kHistKeys (the barriers of the scans
+  // order these before the owners' writes).
+  if (tid == 0) {
+    sm.bi[6] = kHistKeys;
+    sm.bi[7] = kHistKeys;
+  }
   // ---- top-k by count: keys i < ik are wholly in K, key ik keeps rk members.
   int ik = kHistKeys;
   unsigned long long rk = 0;
@@ -475,17 +487,18 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
     uint32_t total;
     const uint32_t before = block_exclusive_scan<uint32_t>(local, sm.wu, lane, warp, &total);
     if (total < static_cast<uint32_t>(k)) return false;  // the k-th value lies below the window
-    int cand = INT_MAX;
+    // Exactly one key brings the count from below k to k or more.
     uint32_t run = before;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       if (run < static_cast<uint32_t>(k) && run + cnt[jj] >= static_cast<uint32_t>(k)) {
-        cand = 4 * tid + jj;
-        sm.bl[0] = static_cast<unsigned long long>(k) - run;  // one owner
+        sm.bi[6] = 4 * tid + jj;
+        sm.bl[0] = static_cast<unsigned long long>(k) - run;
       }
       run += cnt[jj];
     }
-    ik = block_min_int(cand, sm.wi, lane, warp);
+    group_sync();
+    ik = sm.bi[6];
     rk = sm.bl[0];
   }
   // ---- top-p inside K by mass: keys i < is wholly in S, key is keeps rs.
@@ -507,10 +520,12 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
       target = mul_fx(zk, rp.p, true);
       if (target > zk) target = zk;
     } else {
-      target = mul_fx(fx40(zrow), rp.p, true);
+      target = mul_fx(fx40(sm.bf4[2]), rp.p, true);
       if (zk < target) return false;  // the top-p cut lies below the window
     }
     if (target < 1) target = 1;
+    // Exactly one key brings the mass from below target to target or more
+    // (1 <= target <= zk).
     int cand = INT_MAX;
     unsigned long long run = before, rem = 0, wc = 0, nc = 0;
 #pragma unroll
@@ -524,13 +539,15 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
       run += mk[jj];
     }
     if (cand != INT_MAX) {
-      // Members j of the cut key are kept iff run + j * w < target (one
-      // owner); at most the key's count of them.
+      // Members j of the cut key are kept iff run + j * w < target; at most
+      // the key's count of them.
       unsigned long long need = wc == 0 ? ~0ull : ceil_div_small(rem, wc, nc);
       if (cand == ik && need > rk) need = rk;
       sm.bl[1] = need;
+      sm.bi[7] = cand;
     }
-    is = block_min_int(cand, sm.wi, lane, warp);
+    group_sync();
+    is = sm.bi[7];
     rs = sm.bl[1];
   }
   if (rp.minp > 0.0f) {
@@ -956,14 +973,32 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
   const RowParams rp = row_params<BF16, NV>(P, row, C);
   const WriteBack wb = load_write_back(P, row);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // The row's records in one bulk copy (they are contiguous), completing on
-  // rec_bar.
-  const uint32_t rec_bytes = static_cast<uint32_t>(C) * static_cast<uint32_t>(kChunkSlotBytes);
-  if (tid == 0) {
-    const char* src = reinterpret_cast<const char*>(ws_records(P) + static_cast<size_t>(row) * C);
-    mbar_arrive_expect_tx(bar, rec_bytes);
-    for (uint32_t off = 0; off < rec_bytes; off += 16384u) {
-      bulk_copy_g2s(dyn + off, src + off, min(16384u, rec_bytes - off), bar);
+  // The parts of the row's records that its kind reads, one bulk copy per
+  // (chunk, part), issued by the lanes of warp 0 and completing on rec_bar:
+  // the header (summary and warp words) always, the thread maxima for
+  // greedy and top-k rows, the count histogram for count-histogram rows and
+  // the whole record (the candidate list) for candidate rows.
+  {
+    constexpr uint32_t kHead = static_cast<uint32_t>(offsetof(ChunkSlot, tmax));
+    constexpr uint32_t kHistOff = static_cast<uint32_t>(offsetof(ChunkSlot, hist));
+    uint32_t len0 = kHead, len1 = 0;  // [0, len0) and [kHistOff, kHistOff + len1)
+    if (rp.kind == kKindG || rp.kind == kKindK) {
+      len0 = kHistOff;
+    } else if (rp.kind == kKindH) {
+      len1 = static_cast<uint32_t>(kChunkSlotBytes) - kHistOff;
+    } else if (rp.kind == kKindT) {
+      len0 = static_cast<uint32_t>(kChunkSlotBytes);
+    }
+    if (c.warp == 0) {
+      if (c.lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(C) * (len0 + len1));
+      __syncwarp();
+      if (c.lane < C) {
+        const char* src = reinterpret_cast<const char*>(ws_records(P) +
+                                                        static_cast<size_t>(row) * C + c.lane);
+        unsigned char* dst = dyn + static_cast<size_t>(c.lane) * kChunkSlotBytes;
+        bulk_copy_g2s(dst, src, len0, bar);
+        if (len1 != 0u) bulk_copy_g2s(dst + kHistOff, src + kHistOff, len1, bar);
+      }
     }
   }
   const uint32_t seq = __ldcg(&ws_header(P)->calls);  // the stream kernel's call number
