@@ -815,116 +815,278 @@ __device__ __forceinline__ bool finish_hist(const SampleParams& P, SampleSmem& s
 
 // ----------------------------------------------------------------- candidate finish (T)
 
-// The chunks' candidate lists, gathered (value, index) into l_val / l_idx,
-// hold every element of the row at or above thr, the largest of the chunks'
-// bounds.  When the top-p cut lies there (the mass at or above thr reaches
-// p * Z), S is settled from the lists alone: a weighted select by value gives
-// the cut value and the mass still needed from its ties, a count select by
-// index the last kept tie, and a weighted select by index (keys in falling
-// index order) the drawn token.  Returns false, having emitted nothing, when
-// a list overflowed or the cut lies below thr; the caller then runs the
-// exact fallback.
+// The chunks' candidate lists hold every element of the row at or above
+// thr, the largest of the chunks' bounds.  The entries at or above thr are
+// gathered from the workspace as packed keys (order key of the value above,
+// the complement of the index below: a larger key comes first in (value
+// desc, index asc)).  When the top-p cut lies among them (their mass
+// reaches p * Z), S_p is a prefix of that order.  Its end is found without
+// sorting: the entries' masses are summed in 256 buckets of equal width
+// over the values [thr, m] (a bucket index that never falls as the value
+// rises), a suffix scan over the buckets finds the one holding the cut, and
+// only that bucket's entries are ranked exactly, so the tied members of the
+// cut value enter in index order.  S is S_p less the weights below min_p.
+// The draw is in index order: the mass of S per index bucket (256 over
+// [0, V)) and one prefix find the bucket holding floor(u * Z_S); inside it
+// entry t owns [c_t, c_t + w_t), c_t the mass of the bucket's entries of S
+// with a smaller index, so the intervals tile [0, Z_S) exactly.  Returns
+// false, having emitted nothing, when a list overflowed, the gathered
+// entries exceed the capacity, the cut lies below thr or a resolved bucket
+// holds more than kBuckets entries; the caller then runs the exact fallback.
 template <bool BF16, int NV, bool VEC>
 __device__ __forceinline__ bool finish_cand(const SampleParams& P, SampleSmem& sm, const Ctx& c,
-                                            const ChunkSlot* recs, float* l_val, int32_t* l_idx,
-                                            int row, const RowParams& rp, float m,
-                                            const WriteBack& wb, float* q_row) {
+                                            unsigned char* scratch, const ChunkSlot* recs,
+                                            unsigned long long* keys, int row,
+                                            const RowParams& rp, float m, const WriteBack& wb,
+                                            float* q_row) {
   const int tid = c.tid, lane = c.lane, warp = c.warp;
   const int C = static_cast<int>(c.csize);
-  // ---- the row's total mass from the warp records.
-  float mw = 0.0f;
-  if (tid < C * kWarps) {
-    const float wmax = recs[tid / kWarps].wm[tid % kWarps];
-    if (wmax > -INFINITY) mw = recs[tid / kWarps].wz[tid % kWarps] * ex2((wmax - m) * rp.c2);
-  }
-  const float zrow = block_sum<float>(mw, sm.wt, lane, warp);
-  // ---- list offsets, the largest bound, overflow (warp 0; C <= 32).
+  const int V = P.V;
+  // ---- warp 0: the row's total mass from the warp records, the list
+  // offsets (sm.cnt), their total, the largest bound and overflow (C <= 32).
   if (warp == 0) {
+    float z = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * lane + j;
+      if (e < C * kWarps) {
+        const float wmax = recs[e / kWarps].wm[e % kWarps];
+        if (wmax > -INFINITY) z += recs[e / kWarps].wz[e % kWarps] * ex2((wmax - m) * rp.c2);
+      }
+    }
+    z = warp_sum(z);
     const bool v = lane < C;
     const int n = v ? recs[lane].s.i0 : 0;
     float th = v ? recs[lane].s.f0 : -INFINITY;
     const bool over = __any_sync(kFull, v && n < 0);
     const int nn = n < 0 ? 0 : n;
     const int incl = warp_inclusive_scan(nn, lane);
-    const int total = __shfl_sync(kFull, incl, 31);
+    const int all_n = __shfl_sync(kFull, incl, 31);
     if (v) sm.cnt[lane] = static_cast<uint32_t>(incl - nn);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) th = fmaxf(th, __shfl_xor_sync(kFull, th, o));
     if (lane == 0) {
-      sm.bi[0] = over ? -1 : total;
+      sm.bi[0] = over ? -1 : all_n;
+      sm.bi[1] = 0;   // entries gathered
+      sm.bi[3] = -1;  // the cut's value bucket (none: all of the entries)
+      sm.bi[4] = -1;  // the draw's index bucket
+      sm.bi[5] = 0;   // entries of a resolved bucket
       sm.bf4[0] = th;
+      sm.bf4[2] = z;
     }
   }
+  unsigned long long* hmass = sm.scan;  // per bucket (kBuckets == kThreads)
+  hmass[tid] = 0ull;
   group_sync();
   const int total = sm.bi[0];
   const float thr = sm.bf4[0];
-  if (total < 0 || total > kFinListCap) return false;
-#pragma unroll 1
-  for (int r = 0; r < C; ++r) {
-    const int n = recs[r].s.i0;
-    const int off = static_cast<int>(sm.cnt[r]);
-    const unsigned long long* cand = slot_cands(&recs[r]);
-    for (int i = tid; i < n; i += kThreads) {
-      const unsigned long long e = cand[i];
-      l_val[off + i] = key_float(static_cast<uint32_t>(e >> 32));
-      l_idx[off + i] = static_cast<int32_t>(static_cast<uint32_t>(e));
+  const float zrow = sm.bf4[2];
+  if (total < 0) return false;
+  if (!rp.use_p && thr > -INFINITY && weight(thr, m, rp.c2) >= rp.minp) {
+    return false;  // min_p alone keeps elements below the lists' bound
+  }
+  // ---- gather the entries >= thr from the workspace: flat position f of
+  // the concatenated lists, four loads in flight per thread, appends
+  // aggregated per warp.
+  const uint32_t kthr = thr > -INFINITY ? float_key(thr) : 0u;
+  const ChunkSlot* wrec = ws_records(P) + static_cast<size_t>(row) * C;
+  auto entry_at = [&](int f) {
+    int r = 0;  // the last list starting at or before f (C <= 16)
+#pragma unroll
+    for (int step = kMaxChunks / 2; step > 0; step >>= 1) {
+      if (r + step < C && static_cast<int>(sm.cnt[r + step]) <= f) r += step;
+    }
+    return __ldcg(slot_cands(const_cast<ChunkSlot*>(wrec + r)) + (f - static_cast<int>(sm.cnt[r])));
+  };
+  for (int f0 = 0; f0 < total; f0 += 4 * kThreads) {
+    unsigned long long e[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int f = f0 + q * kThreads + tid;
+      e[q] = f < total ? entry_at(f) : 0ull;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int f = f0 + q * kThreads + tid;
+      const uint32_t kx = static_cast<uint32_t>(e[q] >> 32);
+      const bool take = f < total && kx >= kthr;
+      const unsigned bal = __ballot_sync(kFull, take);
+      int at0 = 0;
+      if (lane == 0 && bal != 0u) at0 = atomicAdd(&sm.bi[1], __popc(bal));
+      const int at = __shfl_sync(kFull, at0, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (take && at < kFinListCap) {
+        keys[at] = (static_cast<unsigned long long>(kx) << 32) |
+                   static_cast<unsigned long long>(0xffffffffu - static_cast<uint32_t>(e[q]));
+      }
     }
   }
   group_sync();
-  auto keep = [&](int i) { return l_val[i] >= thr; };
-  auto wfx = [&](int i) { return mass_fx(weight(l_val[i], m, rp.c2)); };
-  // ---- the top-p cut inside the complete part of the lists.
-  float tp = -INFINITY;
-  int ci = INT_MAX;  // ties of tp with an index below ci are kept
+  const int n = sm.bi[1];
+  if (n < 1 || n > kFinListCap) return false;
+  // ---- per entry: mass, value bucket; per value bucket: mass.  The records
+  // are consumed, so their space holds the per-entry arrays.
+  unsigned long long* sw = reinterpret_cast<unsigned long long*>(scratch);          // [kFinListCap]
+  uint8_t* vb = scratch + kFinListCap * 8;                                          // [kFinListCap]
+  uint8_t* in_cut = vb + kFinListCap;  // kept members of the cut bucket              [kFinListCap]
+  const float span = m - thr;
+  const float scale = (thr > -INFINITY && span > 0.0f) ? static_cast<float>(kBuckets) / span : 0.0f;
+  auto vbucket = [&](float x) {
+    const float b = (x - thr) * scale;  // >= 0, non-decreasing in x
+    return b < static_cast<float>(kBuckets - 1) ? static_cast<int>(b) : kBuckets - 1;
+  };
+  for (int t = tid; t < n; t += kThreads) {
+    const float x = key_float(static_cast<uint32_t>(keys[t] >> 32));
+    const unsigned long long w = mass_fx(weight(x, m, rp.c2));
+    const int b = vbucket(x);
+    sw[t] = w;
+    vb[t] = static_cast<uint8_t>(b);
+    in_cut[t] = 0;
+    atomicAdd(&hmass[b], w);
+  }
+  group_sync();
+  // ---- the bucket holding the top-p cut: the mass of the buckets above
+  // it is below target, with it target or more (one owner).
+  int bc = -1;
+  unsigned long long rem = 0;
   if (rp.use_p) {
-    unsigned long long zc = 0;
-    for (int i = tid; i < total; i += kThreads) zc += keep(i) ? wfx(i) : 0ull;
-    zc = block_sum<unsigned long long>(zc, sm.wl, lane, warp);
     unsigned long long target = mul_fx(fx40(zrow), rp.p, true);
     if (target < 1ull) target = 1ull;
-    if (zc < target) return false;  // the cut lies below the lists' bound
-    unsigned long long rem;
-    tp = list_select<true>(l_val, total, keep, wfx, target, sm, c, &rem);
-    // Ties of tp: the first ceil(rem / w(tp)) of them in index order.
-    uint32_t nt = 0;
-    for (int i = tid; i < total; i += kThreads) nt += (keep(i) && l_val[i] == tp) ? 1u : 0u;
-    nt = block_sum<uint32_t>(nt, sm.wu, lane, warp);
-    const unsigned long long wt = mass_fx(weight(tp, m, rp.c2));
-    const unsigned long long need = wt == 0 ? ~0ull : ceil_div_small(rem, wt, nt);
-    if (need < nt) {
-      unsigned long long r2;
-      const uint32_t kc = list_select_key<false>(
-          [&](int i) { return ~static_cast<uint32_t>(l_idx[i]); }, total,
-          [&](int i) { return keep(i) && l_val[i] == tp; }, [](int) { return 1ull; }, need, sm, c,
-          &r2);
-      ci = static_cast<int>(~kc) + 1;  // the need-th smallest index of the ties, plus one
+    const unsigned long long hm = hmass[tid];
+    const unsigned long long incl = block_suffix_scan<unsigned long long>(hm, sm.wl, lane, warp);
+    unsigned long long all = 0;  // the warps' totals stay in sm.wl after the scan
+#pragma unroll 1
+    for (int w = 0; w < kWarps; ++w) all += sm.wl[w];
+    if (all < target) return false;  // the cut lies below the lists' bound
+    const unsigned long long above = incl - hm;
+    if (above < target && incl >= target) {
+      sm.bi[3] = tid;
+      sm.bl[6] = target - above;
     }
-  } else if (thr > -INFINITY && weight(thr, m, rp.c2) >= rp.minp) {
-    return false;  // min_p alone keeps elements below the lists' bound
+    group_sync();
+    bc = sm.bi[3];
+    rem = sm.bl[6];
   }
-  const float tpf = tp;
-  const int cif = ci;
-  auto in_s = [&](int i) {
-    const float x = l_val[i];
-    return keep(i) && (x > tpf || (x == tpf && l_idx[i] < cif)) &&
-           (rp.minp <= 0.0f || weight(x, m, rp.c2) >= rp.minp);
+  // ---- rank the cut bucket's entries; the first j of them (mass from
+  // below rem to rem or more) are kept.
+  uint32_t* memb = sm.hlo;  // entry positions, then ranks in sm.hhi
+  if (bc >= 0) {
+    for (int t0b = warp * 32; t0b < n; t0b += kWarps * 32) {
+      const int t = t0b + lane;
+      const bool in = t < n && vb[t] == bc;
+      const unsigned bal = __ballot_sync(kFull, in);
+      int at0 = 0;
+      if (lane == 0 && bal != 0u) at0 = atomicAdd(&sm.bi[5], __popc(bal));
+      const int at = __shfl_sync(kFull, at0, 0) + __popc(bal & ((1u << lane) - 1u));
+      if (in && at < kBuckets) memb[at] = static_cast<uint32_t>(t);
+    }
+    group_sync();
+    const int nb = sm.bi[5];
+    if (nb > kBuckets) return false;
+    unsigned long long* rw = sm.scan;  // masses in rank order (the bucket masses are consumed)
+    int rank = -1;
+    if (tid < nb) {
+      const unsigned long long ki = keys[memb[tid]];
+      rank = 0;
+#pragma unroll 1
+      for (int q = 0; q < nb; ++q) rank += keys[memb[q]] > ki ? 1 : 0;
+      sm.hhi[tid] = static_cast<uint32_t>(rank);
+    }
+    group_sync();
+    if (tid < nb) rw[rank] = sw[memb[tid]];
+    if (tid == 0) {
+      sm.bi[5] = 0;
+      sm.bi[6] = nb;  // kept members (all, should the sums not reach rem)
+    }
+    group_sync();
+    const unsigned long long wr = tid < nb ? rw[tid] : 0ull;
+    unsigned long long tot;
+    const unsigned long long bef = block_exclusive_scan<unsigned long long>(wr, sm.wl, lane, warp, &tot);
+    if (tid < nb && bef < rem && bef + wr >= rem) sm.bi[6] = tid + 1;
+    group_sync();
+    const int jkeep = sm.bi[6];
+    if (tid < nb && static_cast<int>(sm.hhi[tid]) < jkeep) in_cut[memb[tid]] = 1;
+    group_sync();
+  }
+  auto in_s = [&](int t) {
+    const int b = vb[t];
+    if (bc >= 0 && (b < bc || (b == bc && in_cut[t] == 0))) return false;
+    return rp.minp <= 0.0f ||
+           weight(key_float(static_cast<uint32_t>(keys[t] >> 32)), m, rp.c2) >= rp.minp;
   };
-  // ---- the draw in index order: the first token whose cumulative mass
-  // exceeds floor(u * Z_S), a weighted select on keys falling with the index.
-  unsigned long long zs = 0;
-  for (int i = tid; i < total; i += kThreads) zs += in_s(i) ? wfx(i) : 0ull;
-  zs = block_sum<unsigned long long>(zs, sm.wl, lane, warp);
+  // ---- the draw: the mass of S per index bucket, the bucket holding it.
+  auto ibucket = [&](int idx) {
+    return static_cast<int>((static_cast<unsigned long long>(idx) * kBuckets) /
+                            static_cast<unsigned long long>(V));
+  };
+  unsigned long long* bmass = sm.scan;
+  bmass[tid] = 0ull;
+  group_sync();
+  for (int t = tid; t < n; t += kThreads) {
+    if (in_s(t)) {
+      atomicAdd(&bmass[ibucket(static_cast<int>(0xffffffffu - static_cast<uint32_t>(keys[t])))],
+                sw[t]);
+    }
+  }
+  group_sync();
+  const unsigned long long mb = bmass[tid];
+  unsigned long long zs;
+  const unsigned long long bb = block_exclusive_scan<unsigned long long>(mb, sm.wl, lane, warp, &zs);
+  if (zs == 0ull) {
+    if (tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
+    return true;
+  }
   unsigned long long tdraw = mul_fx(zs, rp.u, false);
-  if (tdraw >= zs) tdraw = zs - 1ull;  // zs >= the row maximum's own weight > 0
-  unsigned long long r3;
-  const uint32_t kt = list_select_key<true>([&](int i) { return ~static_cast<uint32_t>(l_idx[i]); },
-                                            total, in_s, wfx, tdraw + 1ull, sm, c, &r3);
-  const int tok = static_cast<int>(~kt);
-  if (tid == 0) emit(P, row, tok, rp.st, wb);
+  if (tdraw >= zs) tdraw = zs - 1ull;
+  if (mb > 0ull && tdraw >= bb && tdraw < bb + mb) {
+    sm.bi[4] = tid;
+    sm.bl[7] = tdraw - bb;
+  }
+  group_sync();
+  const int bstar = sm.bi[4];
+  const unsigned long long rest = sm.bl[7];
+  // ---- the drawn bucket's entries of S (aggregated appends), then the owner.
+  for (int t0b = warp * 32; t0b < n; t0b += kWarps * 32) {
+    const int t = t0b + lane;
+    bool in = false;
+    if (t < n) {
+      const int xi = static_cast<int>(0xffffffffu - static_cast<uint32_t>(keys[t]));
+      in = ibucket(xi) == bstar && in_s(t);
+    }
+    const unsigned bal = __ballot_sync(kFull, in);
+    int at0 = 0;
+    if (lane == 0 && bal != 0u) at0 = atomicAdd(&sm.bi[5], __popc(bal));
+    const int at = __shfl_sync(kFull, at0, 0) + __popc(bal & ((1u << lane) - 1u));
+    if (in && at < kBuckets) memb[at] = static_cast<uint32_t>(t);
+  }
+  group_sync();
+  const int nm = sm.bi[5];
+  if (nm > kBuckets) return false;
+  bool owner = false;
+  if (tid < nm) {
+    const int t = static_cast<int>(memb[tid]);
+    const int xi = static_cast<int>(0xffffffffu - static_cast<uint32_t>(keys[t]));
+    const unsigned long long w = sw[t];
+    unsigned long long cum = 0;
+#pragma unroll 1
+    for (int q = 0; q < nm; ++q) {
+      const int tq = static_cast<int>(memb[q]);
+      const int xq = static_cast<int>(0xffffffffu - static_cast<uint32_t>(keys[tq]));
+      cum += xq < xi ? sw[tq] : 0ull;
+    }
+    if (w > 0ull && rest >= cum && rest < cum + w) {
+      owner = true;
+      emit(P, row, xi, rp.st, wb);
+    }
+  }
+  if (__syncthreads_or(owner) == 0 && tid == 0) emit(P, row, -1, rp.st | kStNonFinite, wb);
   if (q_row != nullptr) {
     const float inv = 1.0f / (static_cast<float>(zs) / kMassScale);
-    for (int i = tid; i < total; i += kThreads) {
-      if (in_s(i)) q_row[l_idx[i]] = weight(l_val[i], m, rp.c2) * inv;
+    for (int t = tid; t < n; t += kThreads) {
+      if (in_s(t)) {
+        const unsigned long long kk = keys[t];
+        q_row[0xffffffffu - static_cast<uint32_t>(kk)] =
+            weight(key_float(static_cast<uint32_t>(kk >> 32)), m, rp.c2) * inv;
+      }
     }
   }
   return true;
@@ -976,8 +1138,8 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
   // The parts of the row's records that its kind reads, one bulk copy per
   // (chunk, part), issued by the lanes of warp 0 and completing on rec_bar:
   // the header (summary and warp words) always, the thread maxima for
-  // greedy and top-k rows, the count histogram for count-histogram rows and
-  // the whole record (the candidate list) for candidate rows.
+  // greedy and top-k rows and the count histogram for count-histogram rows
+  // (candidate rows read their lists from the workspace directly).
   {
     constexpr uint32_t kHead = static_cast<uint32_t>(offsetof(ChunkSlot, tmax));
     constexpr uint32_t kHistOff = static_cast<uint32_t>(offsetof(ChunkSlot, hist));
@@ -986,8 +1148,6 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
       len0 = kHistOff;
     } else if (rp.kind == kKindH) {
       len1 = static_cast<uint32_t>(kChunkSlotBytes) - kHistOff;
-    } else if (rp.kind == kKindT) {
-      len0 = static_cast<uint32_t>(kChunkSlotBytes);
     }
     if (c.warp == 0) {
       if (c.lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(C) * (len0 + len1));
@@ -1072,7 +1232,10 @@ __global__ void __launch_bounds__(kThreads, 2) finish_kernel(const __grid_consta
     group_sync();
   }
   if (rp.kind == kKindT) {
-    if (finish_cand<BF16, NV, VEC>(P, sm, c, recs, l_val, l_idx, row, rp, m, wb, q_row)) return;
+    if (finish_cand<BF16, NV, VEC>(P, sm, c, dyn, recs, reinterpret_cast<unsigned long long*>(l_val),
+                                   row, rp, m, wb, q_row)) {
+      return;
+    }
     group_sync();
   }
   if constexpr (BF16) {
