@@ -17,15 +17,17 @@
 //     through its (row, chunk) items, fed by a ring of 1-D bulk copies
 //     (cp.async.bulk + mbarrier) from global into shared memory, so the next
 //     chunk is in flight while the current one is reduced.  Each item leaves
-//     a small record in the workspace: a summary, per-warp masses (plain
-//     rows), a candidate list (top-k rows) or a count histogram (top-p rows).
+//     a small record in the workspace: a summary and per-warp maxima, with
+//     per-warp masses (plain and top-p rows), the thread maxima (greedy and
+//     top-k rows), a count histogram (bf16 top-p rows) or a candidate list
+//     (fp32 top-p rows).
 //   * finish: one CTA per row (programmatic dependent launch) reads the
 //     records of its row and settles the token exactly.
 // Row kinds:
 //   G  greedy: (max, first index) per chunk.
-//   K  top-k with k <= 256: a chunk-local lower bound theta_c on the row's
-//      k-th value (a chunk holding k elements >= theta_c cannot miss any of
-//      the row's top-k) selects candidates with no global information.
+//   K  top-k with k <= 256: the chunk's thread maxima; the finisher bounds
+//      the row's k-th value by the k-th largest of the row's thread maxima
+//      and re-reads the few threads at or above it.
 //   P  plain (no filter): chunk and per-warp (max, mass); the finisher picks
 //      the warp of the draw and re-reads that warp's slice.
 //   H  top-p, or top-k with k > 256, on bf16 rows: all elements with one bf16
@@ -36,8 +38,8 @@
 //      elements at or above a bound below which at least 64 of its thread
 //      maxima lie; the lists hold every element above the largest bound, and
 //      when the top-p cut falls there the finisher settles the row from the
-//      lists alone (two weighted selects: the cut by value, the draw by
-//      index).
+//      lists alone (masses per value bucket for the cut and per index bucket
+//      for the draw, each resolved exactly inside one bucket).
 //   F  whatever the above cannot settle (a cut below the window or the
 //      lists; fp32 rows with k > 256): radix passes over the row in global
 //      memory.
@@ -66,9 +68,10 @@ static_assert(kHistWords == 2 * kThreads, "two histogram words per thread");
 
 
 // Dynamic shared memory of the finish kernel (offsets 16-byte aligned): the
-// row's records (one bulk copy), the K rows' candidate list (values, then
-// indices) and the H rows' fixed-point mass per merged key.  An H row stages
-// its draw chunk from offset 0 once the records are consumed.
+// parts of the row's records its kind reads, the K rows' candidate list (T
+// rows: their gathered sort keys) and the H rows' fixed-point mass per
+// merged key.  Once the records are consumed, an H row stages its draw
+// slice histograms and a T row its per-entry masses from offset 0.
 constexpr int kFinListCap = 2048;
 constexpr int kFinRecBytes = kMaxChunks * static_cast<int>(kChunkSlotBytes);
 constexpr int kFinOffList = kFinRecBytes;

@@ -3,9 +3,10 @@
 // sample_common.cuh for the row kinds).
 //
 // Every phase here runs once per row, so the kernel is built for latency:
-// the records arrive in one bulk copy, per-record work is spread over the
-// threads and combined by warp reductions (no thread walks the C * 8 warp
-// records alone), and the write-back coordinates are loaded at the start.
+// the record parts a row reads arrive in bulk copies issued together,
+// per-record work is spread over the threads and combined by warp
+// reductions (no thread walks the C * 8 warp records alone), and the
+// write-back coordinates are loaded at the start.
 #pragma once
 
 #include "page_fill.cuh"
