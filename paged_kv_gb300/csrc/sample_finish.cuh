@@ -929,8 +929,11 @@ __device__ __forceinline__ bool finish_cand(const SampleParams& P, SampleSmem& s
   unsigned long long* sw = reinterpret_cast<unsigned long long*>(scratch);          // [kFinListCap]
   uint8_t* vb = scratch + kFinListCap * 8;                                          // [kFinListCap]
   uint8_t* in_cut = vb + kFinListCap;  // kept members of the cut bucket              [kFinListCap]
+  // A span too small for a finite scale puts every entry in bucket 0 (they
+  // are then ranked exactly, or the row takes the exact path).
   const float span = m - thr;
-  const float scale = (thr > -INFINITY && span > 0.0f) ? static_cast<float>(kBuckets) / span : 0.0f;
+  const float scale =
+      (thr > -INFINITY && span > 1e-30f) ? static_cast<float>(kBuckets) / span : 0.0f;
   auto vbucket = [&](float x) {
     const float b = (x - thr) * scale;  // >= 0, non-decreasing in x
     return b < static_cast<float>(kBuckets - 1) ? static_cast<int>(b) : kBuckets - 1;

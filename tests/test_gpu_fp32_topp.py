@@ -59,3 +59,25 @@ def test_fp32_topp_sweep(shape, V):
     stats = check_sampler(logits, t, None, p, u, tok.cpu().numpy(), gpu_probs=probs.cpu().numpy(),
                           min_p=mp)
     assert stats["greedy"] + stats["exact"] + stats["validated"] == B, stats
+
+
+def test_fp32_topp_near_zero_spread():
+    # About one element in 40 takes a value in [0, 1e-38] over a floor of
+    # -10: most threads' maxima are such values, so the lists' bound lies
+    # among them and the span up to the row maximum is far too small for a
+    # finite bucket scale.  Small p puts the cut among the listed entries,
+    # and equal weights make it a count in (value desc, index asc) order.
+    B, V = 4, 20480
+    g = torch.Generator().manual_seed(77)
+    logits = torch.full((B, V), -10.0)
+    hot = torch.rand(B, V, generator=g) < 1.0 / 40.0
+    logits[hot] = 1e-38 * torch.rand(int(hot.sum()), generator=g)
+    t = torch.ones(B)
+    p = torch.tensor([0.05, 0.1, 0.03, 0.08])
+    u = torch.rand(B, generator=g)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tok = pkv.sample_batch(logits.to(DEV), t.to(DEV), None, p.to(DEV), u.to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    stats = check_sampler(logits, t, None, p, u, tok.cpu().numpy(), None)
+    assert stats["greedy"] + stats["exact"] + stats["validated"] == B, stats
