@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
             bool ok = false;
             while (!(ok = mbar_try_wait(&emptyb[s], parity))) {
               if (globaltimer_ns() - t0 > kWaitNs) break;
-              __nanosleep(128);  // leave the issue slots to the consumers
+              __nanosleep(512);  // leave the issue slots to the consumers
             }
             if (!ok) break;  // the consumers stopped: issue nothing more
           } else if (stagger && n > 0) {
